@@ -1,0 +1,242 @@
+"""ctypes front-end of the fp64 CPU oracle (TEST INFRASTRUCTURE ONLY).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package.  The product path (the CUDA library and its
+Python binding) never imports it, and the oracle never imports the product.
+
+Each wrapper below mirrors one C function of ``moe_oracle.cpp``; the C source
+documents the definition it follows.  Inputs are torch tensors or numpy
+arrays; bf16 tensors are passed as their raw bit patterns and widened exactly
+inside the oracle.  Results are float64 / int32 numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+import threading
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libmoe_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (OpenMP, -O2, no fast-math) if needed."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_BUILD)
+    os.close(fd)
+    cmd = ["g++", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c++17",
+           "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            vp = ctypes.c_void_p
+            ci, cl, cd = ctypes.c_int, ctypes.c_long, ctypes.c_double
+            sig = {
+                "oracle_num_threads": ([], ci),
+                "oracle_set_num_threads": ([ci], ci),
+                "oracle_bf16_value": ([ctypes.c_uint16], cd),
+                "oracle_route_topk": ([ci, ci, ci, ci, vp, vp, vp], ci),
+                "oracle_permute": ([ci, ci, ci, vp, vp, vp, vp, vp], ci),
+                "oracle_gather_rows": ([cl, ci, vp, vp, vp], ci),
+                "oracle_gemm1_swiglu": ([cl, ci, ci, ci, ci, cd, vp, vp, vp, vp], ci),
+                "oracle_gemm2": ([cl, ci, ci, ci, vp, vp, vp, vp], ci),
+                "oracle_unpermute_combine": ([ci, ci, ci, vp, vp, vp, vp], ci),
+                "oracle_moe_forward": ([ci, ci, ci, ci, ci, ci, ci, cd, vp, vp, vp, vp,
+                                        vp, vp, vp, vp], ci),
+                "oracle_dense_bruteforce": ([ci, ci, ci, ci, ci, ci, cd, vp, vp, vp, vp,
+                                             vp, vp], ci),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+# ---------------------------------------------------------------- helpers
+
+def _np(a, dtype) -> np.ndarray:
+    """Contiguous numpy copy/view of a torch tensor or array with ``dtype``."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu()
+            if a.dtype == torch.bfloat16:
+                a = a.contiguous().view(torch.int16).numpy().view(np.uint16)
+            else:
+                a = a.contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.dtype(dtype):
+        if np.dtype(dtype) == np.uint16:
+            raise TypeError("bf16 operands must be passed as bf16 tensors or uint16 bits")
+        a = np.ascontiguousarray(a.astype(dtype))
+    return a
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _expert_ptrs(ws: Sequence[Optional[np.ndarray]]):
+    arr = (ctypes.c_void_p * len(ws))()
+    for i, w in enumerate(ws):
+        arr[i] = None if w is None else w.ctypes.data
+    return arr
+
+
+def _experts(w, E: int):
+    """Per-expert bf16 bit arrays from a [E, ...] tensor or a list (None = unused)."""
+    if isinstance(w, (list, tuple)):
+        assert len(w) == E
+        return [None if m is None else _np(m, np.uint16) for m in w]
+    a = _np(w, np.uint16)
+    return [a[e] for e in range(E)]
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        raise ValueError(f"{name} rejected its arguments (code {rc})")
+
+
+# ---------------------------------------------------------------- API
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> int:
+    return _load().oracle_set_num_threads(int(n))
+
+
+def bf16_value(bits: int) -> float:
+    return _load().oracle_bf16_value(int(bits))
+
+
+def route_topk(logits, k: int, renormalize: bool = True):
+    lg = _np(logits, np.float32)
+    T, E = lg.shape
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    _check(_load().oracle_route_topk(T, E, k, int(renormalize), _p(lg), _p(idx), _p(w)),
+           "oracle_route_topk")
+    return idx, w
+
+
+def permute(topk_idx, E: int) -> Dict[str, np.ndarray]:
+    ix = _np(topk_idx, np.int32)
+    T, k = ix.shape
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    rmap = np.empty((T, k), np.int32)
+    ptok = np.empty(T * k, np.int32)
+    _check(_load().oracle_permute(T, E, k, _p(ix), _p(counts), _p(offsets), _p(rmap), _p(ptok)),
+           "oracle_permute")
+    return {"tokens_per_expert": counts, "expert_offsets": offsets,
+            "row_id_map": rmap, "permuted_token": ptok}
+
+
+def gather_rows(x, permuted_token) -> np.ndarray:
+    xb = _np(x, np.uint16)
+    pt = _np(permuted_token, np.int32)
+    R, H = pt.shape[0], xb.shape[1]
+    out = np.empty((R, H), np.uint16)
+    _load().oracle_gather_rows(R, H, _p(xb), _p(pt), _p(out))
+    return out
+
+
+def gemm1_swiglu(x_perm, expert_offsets, w1, F: int, interleave: int = 0,
+                 clamp: float = 0.0) -> np.ndarray:
+    xp = _np(x_perm, np.uint16)
+    off = _np(expert_offsets, np.int32)
+    E = off.shape[0] - 1
+    R, H = xp.shape
+    ws = _experts(w1, E)
+    ptrs = _expert_ptrs(ws)
+    h = np.empty((R, F), np.float64)
+    _check(_load().oracle_gemm1_swiglu(R, H, F, E, interleave, float(clamp), _p(off), _p(xp),
+                                       ptrs, _p(h)), "oracle_gemm1_swiglu")
+    return h
+
+
+def gemm2(h, expert_offsets, w2, H: int) -> np.ndarray:
+    hh = _np(h, np.float64)
+    off = _np(expert_offsets, np.int32)
+    E = off.shape[0] - 1
+    R, F = hh.shape
+    ws = _experts(w2, E)
+    ptrs = _expert_ptrs(ws)
+    y = np.empty((R, H), np.float64)
+    _check(_load().oracle_gemm2(R, H, F, E, _p(off), _p(hh), ptrs, _p(y)), "oracle_gemm2")
+    return y
+
+
+def unpermute_combine(y, row_id_map, topk_w) -> np.ndarray:
+    yy = _np(y, np.float64)
+    rm = _np(row_id_map, np.int32)
+    ww = _np(topk_w, np.float64)
+    T, k = rm.shape
+    H = yy.shape[1]
+    out = np.empty((T, H), np.float64)
+    _load().oracle_unpermute_combine(T, H, k, _p(yy), _p(rm), _p(ww), _p(out))
+    return out
+
+
+def moe_forward(x, logits, w1, w2, k: int, renormalize: bool = True, interleave: int = 0,
+                clamp: float = 0.0) -> Dict[str, np.ndarray]:
+    """The whole layer on the given tokens.  ``w1``/``w2`` are [E, ...] tensors or
+    per-expert lists where unused experts may be None."""
+    xb = _np(x, np.uint16)
+    lg = _np(logits, np.float32)
+    T, H = xb.shape
+    E = lg.shape[1]
+    w1s, w2s = _experts(w1, E), _experts(w2, E)
+    F = next(m for m in w2s if m is not None).shape[1]
+    out = np.empty((T, H), np.float64)
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    counts = np.empty(E, np.int32)
+    _check(_load().oracle_moe_forward(T, H, F, E, k, int(renormalize), interleave, float(clamp),
+                                      _p(lg), _p(xb), _expert_ptrs(w1s), _expert_ptrs(w2s),
+                                      _p(out), _p(idx), _p(w), _p(counts)),
+           "oracle_moe_forward")
+    return {"out": out, "topk_idx": idx, "topk_w": w, "tokens_per_expert": counts}
+
+
+def dense_bruteforce(x, topk_idx, topk_w, w1, w2, interleave: int = 0,
+                     clamp: float = 0.0) -> np.ndarray:
+    xb = _np(x, np.uint16)
+    ix = _np(topk_idx, np.int32)
+    ww = _np(topk_w, np.float64)
+    T, H = xb.shape
+    k = ix.shape[1]
+    w2a = _np(w2, np.uint16)
+    E, _, F = w2a.shape
+    w1s, w2s = _experts(w1, E), [w2a[e] for e in range(E)]
+    out = np.empty((T, H), np.float64)
+    _check(_load().oracle_dense_bruteforce(T, H, F, E, k, interleave, float(clamp), _p(ix),
+                                           _p(ww), _p(xb), _expert_ptrs(w1s),
+                                           _expert_ptrs(w2s), _p(out)),
+           "oracle_dense_bruteforce")
+    return out

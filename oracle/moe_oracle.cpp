@@ -1,0 +1,342 @@
+// CPU ORACLE for the single-GPU MoE expert-FFN forward -- TEST INFRASTRUCTURE.
+//
+// Plain, slow, fp64 C++ written straight from the definitions of the layer.
+// Only tests, the package's smoke check and the benchmark's CPU-baseline leg
+// may load this library; the product path never calls it.  It shares no code,
+// header, table or constant with the CUDA path.
+//
+// Sources for what each step computes (page titles and sections):
+//   * "[SM90] Add W4A8 MegaMoE support" (FlashInfer), description + Usage:
+//     the layer is routing -> two expert GEMMs -> clamped SwiGLU -> top-k
+//     reduction; routes are expert indices with -1 masking a route, routing
+//     weights are fp32, activation scales are fp32 per 128 channels, NVFP4
+//     weight scales are E4M3 per 16 values.
+//   * "add permute fusion into hybrid ep" (Megatron-LM), PR description:
+//     permute = reorder token rows into expert-contiguous order, unpermute =
+//     the inverse reorder that feeds the combine.
+//   * "Support GEMM + Swiglu fused MLP" (Megatron-LM), description and the
+//     review thread on moe_mlp_glu_interleave_size: fc1 produces gate and up
+//     and SwiGLU consumes them; the interleave option reorders W1's rows.
+//
+// Readings where the pages are silent (each is also listed in the design
+// notes): selection on raw fp32 logits with ties to the lowest expert id;
+// weights = softmax over the k selected logits (renormalize=1) or the full
+// softmax probabilities (renormalize=0); stable (token-ascending) order inside
+// an expert; interleave I = alternating blocks of I gate rows and I up rows;
+// clamp c: silu(min(g, c)) * clamp(u, -c, c).
+//
+// Pins: every function here is checked by the CPU test-suite against brute
+// force, closed forms, library routines (numpy / torch) and invariants.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+// bf16 is the top half of an IEEE binary32; widening is exact.
+inline double bf16_value(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+// Row of W1 holding gate (resp. up) output column f.
+//   interleave 0: W1 = [gate rows 0..F-1 | up rows 0..F-1]
+//   interleave I: blocks of I gate rows followed by I up rows, repeated.
+inline long gate_row(long f, long F, long I) {
+  if (I <= 0) return f;
+  return (f / I) * 2 * I + f % I;
+}
+inline long up_row(long f, long F, long I) {
+  if (I <= 0) return F + f;
+  return gate_row(f, F, I) + I;
+}
+
+inline double silu(double z) { return z / (1.0 + std::exp(-z)); }
+
+// clamp <= 0 or non-finite means "no clamp".
+inline double swiglu(double g, double u, double c) {
+  if (c > 0 && std::isfinite(c)) {
+    g = std::fmin(g, c);
+    u = std::fmax(std::fmin(u, c), -c);
+  }
+  return silu(g) * u;
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+int oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}
+
+double oracle_bf16_value(uint16_t bits) { return bf16_value(bits); }
+
+// ---------------------------------------------------------------------------
+// Step 1: top-k routing.
+// For token t the selected set is the k experts with the largest logits,
+// listed by (logit descending, expert id ascending).  Comparisons are exact
+// fp32 comparisons (+0 == -0).  Weights, in fp64:
+//   renormalize = 1: softmax over the k selected logits;
+//   renormalize = 0: the full softmax probability of each selected expert.
+// Returns 0, or -1 on bad sizes.
+int oracle_route_topk(int T, int E, int k, int renormalize, const float* logits,
+                      int32_t* topk_idx, double* topk_w) {
+  if (T < 0 || E < 1 || k < 1 || k > E) return -1;
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + static_cast<long>(t) * E;
+    std::vector<char> taken(E, 0);
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || l[e] > l[best]) best = e;  // strict: ties keep the lower id
+      }
+      taken[best] = 1;
+      topk_idx[static_cast<long>(t) * k + j] = best;
+    }
+    const double lmax = l[topk_idx[static_cast<long>(t) * k]];
+    double denom = 0.0;
+    if (renormalize) {
+      for (int j = 0; j < k; ++j)
+        denom += std::exp(static_cast<double>(l[topk_idx[static_cast<long>(t) * k + j]]) - lmax);
+    } else {
+      for (int e = 0; e < E; ++e) denom += std::exp(static_cast<double>(l[e]) - lmax);
+    }
+    for (int j = 0; j < k; ++j) {
+      double v = std::exp(static_cast<double>(l[topk_idx[static_cast<long>(t) * k + j]]) - lmax);
+      topk_w[static_cast<long>(t) * k + j] = v / denom;
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Step 2: permute bookkeeping.
+//   tokens_per_expert[e] = number of routes (t, j) with topk_idx[t][j] == e
+//   expert_offsets       = exclusive prefix sum (E + 1 entries)
+//   rows are handed out in (expert ascending, token ascending) order:
+//     row_id_map[t][j]    = the permuted row of route (t, j), -1 if masked
+//     permuted_token[row] = t, and -1 for the unused tail rows when some
+//                           routes are masked.
+// Returns 0, -1 on bad sizes, -2 on an index outside [-1, E), -3 when a token
+// lists the same expert twice.
+int oracle_permute(int T, int E, int k, const int32_t* topk_idx, int32_t* tokens_per_expert,
+                   int32_t* expert_offsets, int32_t* row_id_map, int32_t* permuted_token) {
+  if (T < 0 || E < 1 || k < 1) return -1;
+  const long R = static_cast<long>(T) * k;
+  for (long i = 0; i < R; ++i)
+    if (topk_idx[i] < -1 || topk_idx[i] >= E) return -2;
+  for (int t = 0; t < T; ++t)
+    for (int a = 0; a < k; ++a)
+      for (int b = a + 1; b < k; ++b) {
+        int32_t ea = topk_idx[static_cast<long>(t) * k + a];
+        if (ea >= 0 && ea == topk_idx[static_cast<long>(t) * k + b]) return -3;
+      }
+  for (int e = 0; e < E; ++e) tokens_per_expert[e] = 0;
+  for (long i = 0; i < R; ++i)
+    if (topk_idx[i] >= 0) tokens_per_expert[topk_idx[i]] += 1;
+  expert_offsets[0] = 0;
+  for (int e = 0; e < E; ++e) expert_offsets[e + 1] = expert_offsets[e] + tokens_per_expert[e];
+  for (long i = 0; i < R; ++i) row_id_map[i] = -1;
+  for (long r = 0; r < R; ++r) permuted_token[r] = -1;
+  for (int e = 0; e < E; ++e) {
+    int32_t next = expert_offsets[e];
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j)
+        if (topk_idx[static_cast<long>(t) * k + j] == e) {
+          row_id_map[static_cast<long>(t) * k + j] = next;
+          permuted_token[next] = t;
+          ++next;
+        }
+  }
+  return 0;
+}
+
+// Materialise the permuted activations: x_perm[r] = x[permuted_token[r]]
+// (rows with permuted_token = -1 are zero).
+int oracle_gather_rows(long R, int H, const uint16_t* x, const int32_t* permuted_token,
+                       uint16_t* x_perm) {
+  for (long r = 0; r < R; ++r) {
+    uint16_t* dst = x_perm + r * H;
+    if (permuted_token[r] < 0) {
+      std::memset(dst, 0, sizeof(uint16_t) * H);
+    } else {
+      std::memcpy(dst, x + static_cast<long>(permuted_token[r]) * H, sizeof(uint16_t) * H);
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Steps 3+4: GEMM1 and SwiGLU for the rows of each expert, in fp64.
+// For permuted row r in expert e's segment [expert_offsets[e], expert_offsets[e+1]):
+//   g_f = sum_h x_perm[r][h] * W1_e[gate_row(f)][h]
+//   u_f = sum_h x_perm[r][h] * W1_e[up_row(f)][h]
+//   h[r][f] = silu(min(g_f, c)) * clamp(u_f, -c, c)        (no clamp if c <= 0)
+// w1_experts[e] points at expert e's [2F, H] bf16 matrix (NULL allowed for an
+// expert with no rows).  Rows beyond expert_offsets[E] are set to 0.
+int oracle_gemm1_swiglu(long R, int H, int F, int E, int interleave, double clamp,
+                        const int32_t* expert_offsets, const uint16_t* x_perm,
+                        const uint16_t* const* w1_experts, double* h) {
+  if (interleave > 0 && F % interleave != 0) return -1;
+  for (int e = 0; e < E; ++e)
+    if (expert_offsets[e + 1] > expert_offsets[e] && w1_experts[e] == nullptr) return -2;
+  for (long r = expert_offsets[E]; r < R; ++r)
+    for (int f = 0; f < F; ++f) h[r * F + f] = 0.0;
+  for (int e = 0; e < E; ++e) {
+    const long r0 = expert_offsets[e], r1 = expert_offsets[e + 1];
+    if (r1 <= r0) continue;
+    const uint16_t* W = w1_experts[e];
+#pragma omp parallel for schedule(dynamic)
+    for (long r = r0; r < r1; ++r) {
+      std::vector<double> xr(H);
+      for (int c = 0; c < H; ++c) xr[c] = bf16_value(x_perm[r * H + c]);
+      for (int f = 0; f < F; ++f) {
+        const uint16_t* wg = W + gate_row(f, F, interleave) * static_cast<long>(H);
+        const uint16_t* wu = W + up_row(f, F, interleave) * static_cast<long>(H);
+        double g = 0.0, u = 0.0;
+        for (int c = 0; c < H; ++c) {
+          g += xr[c] * bf16_value(wg[c]);
+          u += xr[c] * bf16_value(wu[c]);
+        }
+        h[r * F + f] = swiglu(g, u, clamp);
+      }
+    }
+  }
+  return 0;
+}
+
+// Step 5: GEMM2, y[r][n] = sum_f h[r][f] * W2_e[n][f] (W2_e is [H, F]).
+int oracle_gemm2(long R, int H, int F, int E, const int32_t* expert_offsets, const double* h,
+                 const uint16_t* const* w2_experts, double* y) {
+  for (int e = 0; e < E; ++e)
+    if (expert_offsets[e + 1] > expert_offsets[e] && w2_experts[e] == nullptr) return -2;
+  for (long r = expert_offsets[E]; r < R; ++r)
+    for (int n = 0; n < H; ++n) y[r * H + n] = 0.0;
+  for (int e = 0; e < E; ++e) {
+    const long r0 = expert_offsets[e], r1 = expert_offsets[e + 1];
+    if (r1 <= r0) continue;
+    const uint16_t* W = w2_experts[e];
+#pragma omp parallel for schedule(dynamic)
+    for (long r = r0; r < r1; ++r) {
+      const double* hr = h + r * F;
+      for (int n = 0; n < H; ++n) {
+        const uint16_t* wn = W + static_cast<long>(n) * F;
+        double acc = 0.0;
+        for (int f = 0; f < F; ++f) acc += hr[f] * bf16_value(wn[f]);
+        y[r * H + n] = acc;
+      }
+    }
+  }
+  return 0;
+}
+
+// Step 6: weighted unpermute / combine.
+//   out[t][n] = sum over slots j = 0..k-1 with row_id_map[t][j] >= 0 of
+//               topk_w[t][j] * y[row_id_map[t][j]][n]
+int oracle_unpermute_combine(int T, int H, int k, const double* y, const int32_t* row_id_map,
+                             const double* topk_w, double* out) {
+#pragma omp parallel for
+  for (int t = 0; t < T; ++t) {
+    double* o = out + static_cast<long>(t) * H;
+    for (int n = 0; n < H; ++n) o[n] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const long row = row_id_map[static_cast<long>(t) * k + j];
+      if (row < 0) continue;
+      const double w = topk_w[static_cast<long>(t) * k + j];
+      for (int n = 0; n < H; ++n) o[n] += w * y[row * H + n];
+    }
+  }
+  return 0;
+}
+
+// The whole layer: route -> permute -> gather -> GEMM1+SwiGLU -> GEMM2 -> combine.
+// topk_idx_out / topk_w_out / tokens_per_expert_out may be NULL.
+int oracle_moe_forward(int T, int H, int F, int E, int k, int renormalize, int interleave,
+                       double clamp, const float* logits, const uint16_t* x,
+                       const uint16_t* const* w1_experts, const uint16_t* const* w2_experts,
+                       double* out, int32_t* topk_idx_out, double* topk_w_out,
+                       int32_t* tokens_per_expert_out) {
+  const long R = static_cast<long>(T) * k;
+  std::vector<int32_t> idx(R), row_id_map(R), permuted_token(R), counts(E), offsets(E + 1);
+  std::vector<double> w(R);
+  int rc = oracle_route_topk(T, E, k, renormalize, logits, idx.data(), w.data());
+  if (rc) return rc;
+  rc = oracle_permute(T, E, k, idx.data(), counts.data(), offsets.data(), row_id_map.data(),
+                      permuted_token.data());
+  if (rc) return rc;
+  std::vector<uint16_t> x_perm(static_cast<size_t>(R) * H);
+  oracle_gather_rows(R, H, x, permuted_token.data(), x_perm.data());
+  std::vector<double> h(static_cast<size_t>(R) * F), y(static_cast<size_t>(R) * H);
+  rc = oracle_gemm1_swiglu(R, H, F, E, interleave, clamp, offsets.data(), x_perm.data(),
+                           w1_experts, h.data());
+  if (rc) return rc;
+  rc = oracle_gemm2(R, H, F, E, offsets.data(), h.data(), w2_experts, y.data());
+  if (rc) return rc;
+  oracle_unpermute_combine(T, H, k, y.data(), row_id_map.data(), w.data(), out);
+  if (topk_idx_out) std::memcpy(topk_idx_out, idx.data(), sizeof(int32_t) * R);
+  if (topk_w_out) std::memcpy(topk_w_out, w.data(), sizeof(double) * R);
+  if (tokens_per_expert_out) std::memcpy(tokens_per_expert_out, counts.data(), sizeof(int32_t) * E);
+  return 0;
+}
+
+// Second, permutation-free evaluation of the same layer for given routes: for
+// every token and slot, run the selected expert's MLP on the token's own row
+// and accumulate the weighted result.  Used to cross-check the permuted form.
+int oracle_dense_bruteforce(int T, int H, int F, int E, int k, int interleave, double clamp,
+                            const int32_t* topk_idx, const double* topk_w, const uint16_t* x,
+                            const uint16_t* const* w1_experts,
+                            const uint16_t* const* w2_experts, double* out) {
+#pragma omp parallel for schedule(dynamic)
+  for (int t = 0; t < T; ++t) {
+    std::vector<double> xr(H), hv(F);
+    for (int c = 0; c < H; ++c) xr[c] = bf16_value(x[static_cast<long>(t) * H + c]);
+    double* o = out + static_cast<long>(t) * H;
+    for (int n = 0; n < H; ++n) o[n] = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const int e = topk_idx[static_cast<long>(t) * k + j];
+      if (e < 0) continue;
+      const uint16_t* W1 = w1_experts[e];
+      const uint16_t* W2 = w2_experts[e];
+      for (int f = 0; f < F; ++f) {
+        double g = 0.0, u = 0.0;
+        for (int c = 0; c < H; ++c) {
+          g += xr[c] * bf16_value(W1[gate_row(f, F, interleave) * static_cast<long>(H) + c]);
+          u += xr[c] * bf16_value(W1[up_row(f, F, interleave) * static_cast<long>(H) + c]);
+        }
+        hv[f] = swiglu(g, u, clamp);
+      }
+      const double w = topk_w[static_cast<long>(t) * k + j];
+      for (int n = 0; n < H; ++n) {
+        double acc = 0.0;
+        for (int f = 0; f < F; ++f) acc += hv[f] * bf16_value(W2[static_cast<long>(n) * F + f]);
+        o[n] += w * acc;
+      }
+    }
+  }
+  return 0;
+}
+
+}  // extern "C"
