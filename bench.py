@@ -1,0 +1,387 @@
+"""Benchmark of the MoE expert-FFN forward on GB300.
+
+One step = one moe_forward (route -> permute -> GEMM1+SwiGLU -> GEMM2 ->
+combine) over one batch of synthetic tokens already resident in HBM.  The
+default workload is the Mixtral-shaped layer (T=4096, H=4096, F=14336, E=8,
+top-2, bf16).  Its 2.8 GB of weights exceed the 129 MB L2, so no flush is
+needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload mixtral|skewed|decode|tiny] [--T T]
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
+own batch of T tokens with the same weights (weak scaling, no data-path
+collective); the step time is the maximum over ranks.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on this machine's host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE layer fwd TFLOP/s & tokens/s at 1 GB300; % of tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOADS = {
+    "mixtral": (mi.MIXTRAL, "Mixtral-shaped MoE FFN layer: T=4096 H=4096 F=14336 E=8 top-2 bf16"),
+    "skewed": (mi.SKEWED, "fine-grained skewed MoE FFN: T=8192 H=7168 F=2048 E=256 top-8 "
+                          "bf16, Zipf(1.1) expert bias"),
+    "decode": (mi.DECODE, "decode-sized MoE FFN: H=2048 F=768 E=128 top-8 bf16"),
+    "tiny": (mi.TINY, "tiny MoE FFN: T=64 H=256 F=512 E=8 top-2 bf16"),
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral")
+    ap.add_argument("--T", type=int, default=0, help="override the token count")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Maximum of a per-rank scalar over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(shape, inp_host, n_tokens: int):
+    """Run the oracle on the first n tokens; returns (seconds, flops)."""
+    import oracle
+    x = inp_host["x"][:n_tokens]
+    lg = inp_host["logits"][:n_tokens]
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, lg, inp_host["w1"], inp_host["w2"], shape.k,
+                       interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
+    dt = time.perf_counter() - t0
+    return dt, shape.with_T(n_tokens).flops()
+
+
+def cpu_baseline(shape, inp_host, target_s: float):
+    import oracle
+    oracle.build()
+    dt1, _ = oracle_sample(shape, inp_host, 1)
+    n = int(max(1, min(shape.T, math.floor(target_s / max(dt1, 1e-6)))))
+    dt, flops = oracle_sample(shape, inp_host, n)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {n} of {shape.T} tokens of the same workload (fp64 oracle, "
+                      f"{dt:.1f} s)"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def bench_ours(args, shape, desc):
+    import mixture_experts_ffn_permute_gb300 as moe
+    from mixture_experts_ffn_permute_gb300 import _build
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    _build.build()
+    moe.load()
+    peaks, peak_src = load_peaks()
+
+    # weights shared by all ranks (seed 0); each rank routes its own tokens
+    w1 = mi.make_w1(shape, 0, dev)
+    w2 = mi.make_w2(shape, 0, dev)
+    x = mi.make_x(shape, rank, dev)
+    logits = mi.make_logits(shape, rank, dev)
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True,
+                         shape.glu_interleave, shape.swiglu_clamp)
+    ws = moe.alloc_workspace(p, dev)
+    out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        moe.forward(p, x, logits, w1, w2, out, ws)
+
+    moe.clear_device_status(ws)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    launches_per_step = moe.last_launch_count()
+    K = args.steps
+
+    # ---- device-resident timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        moe.stage_timing_begin(K)
+        ev0.record(stream)
+        for _ in range(K):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        stages = moe.stage_timing_end()
+        barrier(world)
+    ms_local = ev0.elapsed_time(ev1) / K
+    status = moe.get_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status, status)}")
+    ms = reduce_max(ms_local, world, dev)
+    sec = ms / 1e3
+
+    # ---- end to end: pinned host inputs -> device -> forward -> host output
+    xh = x.cpu().pin_memory()
+    lh = logits.cpu().pin_memory()
+    oh = torch.empty_like(out, device="cpu").pin_memory()
+    xd, ld = torch.empty_like(x), torch.empty_like(logits)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        ld.copy_(lh, non_blocking=True)
+        moe.forward(p, xd, ld, w1, w2, out, ws)
+        oh.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    K2 = max(3, K // 2)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / K2, world, dev)
+
+    flops = shape.flops()
+    gemm1_ms = stages.get("gemm1_swiglu", float("nan"))
+    gemm1_flops = 4.0 * shape.R * shape.H * shape.F
+    peak_key = "bf16_tflops_sustained"
+    ach = gemm1_flops / (gemm1_ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": world * flops / sec / 1e12,
+        "unit": "TFLOP/s",
+        "tokens_per_s": world * shape.T / sec,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": desc, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
+                   "k": shape.k, "l2": "inputs larger than L2 (weights %.2f GB), no flush"
+                   % (2 * 3 * shape.E * shape.F * shape.H / 1e9)},
+        "roofline": {"kernel": "grouped_gemm_kernel<SwiGLU> (GEMM1)", "bound": "tensor",
+                     "achieved": ach, "peak": peaks[peak_key], "unit": "TFLOP/s",
+                     "frac": ach / peaks[peak_key], "traffic": None,
+                     "peak_source": f"{peak_key} ({peak_src})"},
+        "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 2},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+        "stages_ms": {k: round(v, 5) for k, v in stages.items() if not k.startswith("_")},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {"x": x.cpu(), "logits": logits.cpu(), "w1": w1.cpu(), "w2": w2.cpu()}
+        line["cpu_baseline"] = cpu_baseline(shape, host, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def bench_reference(args, shape, desc):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    # Inputs of the same workload on the host; only the experts the sample
+    # routes to are materialised (the oracle takes per-expert weights).
+    x = mi.make_x(shape, 0)[:64]
+    logits = mi.make_logits(shape, 0)
+    idx, _ = oracle.route_topk(logits[:64], shape.k)
+    used = sorted(set(idx.ravel().tolist()))
+    w1 = [None] * shape.E
+    w2 = [None] * shape.E
+    for e in used:  # same distributions as moe_inputs, drawn per used expert
+        g = torch.Generator().manual_seed(1000 + e)
+        w1[e] = torch.randn(2 * shape.F, shape.H, generator=g).mul_(
+            1 / math.sqrt(shape.H)).to(torch.bfloat16)
+        w2[e] = torch.randn(shape.H, shape.F, generator=g).mul_(
+            1 / math.sqrt(shape.F)).to(torch.bfloat16)
+    host = {"x": x, "logits": logits[:64], "w1": w1, "w2": w2}
+    steps, warm = args.steps, max(args.warmup, 1)
+    dt1, _ = oracle_sample(shape, host, 1)
+    budget = 150.0 / (steps + warm)
+    n = int(max(1, min(64, math.floor(budget / max(dt1, 1e-6)))))
+    for _ in range(warm - 1):
+        oracle_sample(shape, host, n)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_sample(shape, host, n)
+    dt = (time.perf_counter() - t0) / steps
+    flops = shape.with_T(n).flops()
+    val = flops / dt / 1e12
+    line = {
+        "metric": METRIC, "impl": "reference", "value": val, "unit": "TFLOP/s",
+        "tokens_per_s": n / dt, "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
+                   "k": shape.k},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"first {n} of {shape.T} tokens per step (fp64 oracle)"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    shape, desc = WORKLOADS[args.workload]
+    if args.T:
+        shape = shape.with_T(args.T)
+        desc = desc + f" (T={args.T})"
+    elif args.workload == "decode":
+        desc = desc + f" T={shape.T}"
+    if args.impl == "reference":
+        bench_reference(args, shape, desc)
+    else:
+        bench_ours(args, shape, desc)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts expert-FFN
+ * forward: top-k routing -> permute -> grouped GEMM1 + SwiGLU -> grouped
+ * GEMM2 -> weighted unpermute/combine, on one GPU.
+ *
+ * The layer is the one the "[SM90] Add W4A8 MegaMoE support" page (FlashInfer)
+ * describes in its description and Usage section: expert indices per token
+ * with -1 masking a route, fp32 routing weights, two expert GEMMs, clamped
+ * SwiGLU and a top-k reduction; hidden width a multiple of 256 and
+ * intermediate width a multiple of 128.  Permute/unpermute are the row
+ * reorderings of "add permute fusion into hybrid ep" (Megatron-LM, PR
+ * description); the gate/up pairing and its interleave option follow
+ * "Support GEMM + Swiglu fused MLP" (Megatron-LM, description and the review
+ * of moe_mlp_glu_interleave_size).
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, row-major
+ *     and dense, 16-byte aligned.  The library never allocates device memory
+ *     and never frees caller memory.  Inputs are never written; every output
+ *     element is overwritten.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *     enqueued asynchronously on it; no entry point synchronises the host or
+ *     reads device data on the host, except moe_get_device_status.
+ *   - `ws` is caller-provided scratch of at least moe_workspace_size() bytes,
+ *     256-byte aligned.  It may be reused by consecutive calls on the same
+ *     stream; calls that overlap in time must not share a workspace.
+ *   - Argument checks run on the host before any launch and return a status
+ *     without touching the GPU.  A failed launch returns MOE_ERR_CUDA.
+ *     Device-side faults the kernels detect themselves (a bounded wait that
+ *     ran out, an index out of range) are recorded in the workspace status
+ *     word and read back with moe_get_device_status.
+ *   - bf16 tensors are raw 16-bit bfloat16 values.
+ *
+ * Shapes: T tokens, H hidden, F expert intermediate, E experts, k routes per
+ * token, R = T*k permuted rows.
+ */
+#ifndef MOE_FFN_H_
+#define MOE_FFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,        /* null pointer, k > E, negative size ... */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* H % 256, F % 128, interleave rule, E/k limits */
+  MOE_ERR_MISALIGNED = 3,         /* a pointer not 16-byte (ws: 256-byte) aligned */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,
+  MOE_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait ran out (device status) */
+  MOE_ERR_DEVICE_INDEX = 7        /* a kernel saw an out-of-range index (device status) */
+} moe_status;
+
+typedef enum { MOE_PREC_BF16 = 0 } moe_precision;
+
+/* Problem description shared by all entry points. */
+typedef struct moe_problem {
+  int32_t T, H, F, E, k;
+  /* 1: routing weights = softmax over the k selected logits (default);
+     0: the full-softmax probability of each selected expert. */
+  int32_t renormalize;
+  /* Row order of W1 [E, 2F, H]:
+     0  -> rows [gate_0 .. gate_{F-1} | up_0 .. up_{F-1}];
+     I  -> alternating blocks of I gate rows then I up rows.
+     I must divide F and be 32, 64 or a multiple of 128. */
+  int32_t glu_interleave;
+  /* SwiGLU clamp c: h = silu(min(g, c)) * clamp(u, -c, c); <= 0 or non-finite
+     means no clamp. */
+  float swiglu_clamp;
+  int32_t precision; /* moe_precision */
+} moe_problem;
+
+/* Limits checked by every entry point. */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 32
+
+/* Human-readable name of a status code (static storage, never NULL). */
+MOE_API const char* moe_status_string(int status);
+
+/* Bytes of scratch every entry point needs for this problem (0 if the
+ * problem itself is invalid).  Sized for the worst case of the routing, so
+ * one workspace serves every call with the same sizes. */
+MOE_API size_t moe_workspace_size(const moe_problem* p);
+
+/* Step 1 -- top-k routing ("[SM90] Add W4A8 MegaMoE support", Usage: int
+ * expert indices and fp32 weights per route).
+ *   logits   [T, E] fp32
+ *   topk_idx [T, k] int32 out: experts by logit descending, ties to the lower
+ *            expert id (exact fp32 comparisons)
+ *   topk_w   [T, k] fp32  out: softmax over the selected logits
+ *            (renormalize=1) or full-softmax probabilities (renormalize=0). */
+MOE_API int moe_route_topk(const moe_problem* p, const float* logits, int32_t* topk_idx,
+                           float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 2 -- permute ("add permute fusion into hybrid ep", PR description):
+ * stable scatter of routes into expert-contiguous rows, experts ascending,
+ * tokens ascending within an expert.
+ *   topk_idx          [T, k] int32, -1 = masked route (not counted)
+ *   x                 [T, H] bf16, may be NULL when x_perm is NULL
+ *   x_perm            [R, H] bf16 out or NULL: x_perm[r] = x[permuted_token[r]],
+ *                     zero rows for the masked tail
+ *   row_id_map        [T, k] int32 out: permuted row of route (t, j), -1 masked
+ *   permuted_token    [R] int32 out: token of each row, -1 for the masked tail
+ *   tokens_per_expert [E] int32 out
+ *   expert_offsets    [E + 1] int32 out: exclusive prefix sum of the counts
+ * A route index outside [-1, E) or an expert listed twice by one token is
+ * recorded as MOE_ERR_DEVICE_INDEX in the device status. */
+MOE_API int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x,
+                        void* x_perm, int32_t* row_id_map, int32_t* permuted_token,
+                        int32_t* tokens_per_expert, int32_t* expert_offsets, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* Steps 3-5 -- grouped expert MLP on permuted rows ("Support GEMM + Swiglu
+ * fused MLP"; MegaMoE description: two expert GEMMs and clamped SwiGLU).
+ *   x_perm         [R, H] bf16, rows of expert e at
+ *                  [expert_offsets[e], expert_offsets[e+1])
+ *   expert_offsets [E + 1] int32 (device), non-decreasing, offsets[E] <= R
+ *   w1             [E, 2F, H] bf16 (gate/up rows per glu_interleave)
+ *   w2             [E, H, F] bf16
+ *   y_perm         [R, H] bf16 out: y = silu-glu(x W1^T) W2^T per row, NOT
+ *                  weighted; rows >= expert_offsets[E] are set to zero. */
+MOE_API int moe_grouped_swiglu_mlp(const moe_problem* p, const void* x_perm,
+                                   const int32_t* expert_offsets, const void* w1,
+                                   const void* w2, void* y_perm, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* Step 6 -- weighted unpermute/combine (MegaMoE description: top-k
+ * reduction):  out[t] = sum_{j=0..k-1, row_id_map[t][j] >= 0}
+ *                        topk_w[t][j] * y_perm[row_id_map[t][j]],
+ * summed in fp32 in slot order j = 0..k-1 and rounded once to bf16, so the
+ * result is bitwise reproducible.
+ *   y_perm [R, H] bf16, row_id_map [T, k] int32, topk_w [T, k] fp32,
+ *   out [T, H] bf16 out. */
+MOE_API int moe_unpermute_combine(const moe_problem* p, const void* y_perm,
+                                  const int32_t* row_id_map, const float* topk_w, void* out,
+                                  void* stream);
+
+/* The whole layer, steps 1-6, enqueued on `stream` with no host round trip.
+ *   x [T, H] bf16, logits [T, E] fp32, w1 [E, 2F, H] bf16, w2 [E, H, F] bf16
+ *   out [T, H] bf16 out
+ *   topk_idx_out [T, k] int32, topk_w_out [T, k] fp32,
+ *   tokens_per_expert_out [E] int32: optional copies of the routing (NULL to
+ *   skip). */
+MOE_API int moe_forward(const moe_problem* p, const void* x, const float* logits,
+                        const void* w1, const void* w2, void* out, int32_t* topk_idx_out,
+                        float* topk_w_out, int32_t* tokens_per_expert_out, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the status the kernels recorded in `ws`
+ * since the last moe_clear_device_status (MOE_OK if none). */
+MOE_API int moe_get_device_status(void* ws, void* stream);
+
+/* Resets the workspace status word (enqueued on `stream`). */
+MOE_API int moe_clear_device_status(void* ws, void* stream);
+
+/* Number of kernel launches the last successful call on this thread
+ * enqueued (for launch accounting in benchmarks). */
+MOE_API int moe_last_launch_count(void);
+
+/* Per-stage timing of moe_forward with CUDA events (for benchmarks).
+ * moe_stage_timing_begin(n) makes the next n moe_forward calls on this
+ * thread record an event on their stream before each stage and after the
+ * last (events created once, reused); moe_stage_timing_end synchronises the
+ * device, writes the average milliseconds of each stage over the recorded
+ * calls into ms[0 .. *n_stages) (at most max_stages entries) and stops
+ * recording.  Stage i is named by moe_stage_name(i).  Returns a status. */
+MOE_API int moe_stage_timing_begin(int n_calls);
+MOE_API int moe_stage_timing_end(float* ms, int max_stages, int* n_stages, int* n_calls);
+MOE_API const char* moe_stage_name(int i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H_ */

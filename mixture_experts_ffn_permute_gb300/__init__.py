@@ -1,0 +1,222 @@
+"""Python binding of libmoeffn.so, the GB300 (sm_103a) MoE expert-FFN library.
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  PyTorch provides device memory and the current stream.  The
+function names mirror the C entry points of ``include/moe_ffn.h``:
+
+    route_topk            -> moe_route_topk
+    permute               -> moe_permute
+    grouped_swiglu_mlp    -> moe_grouped_swiglu_mlp
+    unpermute_combine     -> moe_unpermute_combine
+    forward               -> moe_forward
+
+There is no CPU fallback: if the library is missing or a call returns an
+error status, a ``MoEError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Dict, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoeffn.so")
+
+MOE_OK = 0
+STATUS_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
+    3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",
+    6: "MOE_ERR_DEVICE_TIMEOUT", 7: "MOE_ERR_DEVICE_INDEX",
+}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class Problem(ctypes.Structure):
+    """Mirror of ``moe_problem``."""
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("F", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("renormalize", ctypes.c_int32), ("glu_interleave", ctypes.c_int32),
+                ("swiglu_clamp", ctypes.c_float), ("precision", ctypes.c_int32)]
+
+    @classmethod
+    def make(cls, T, H, F, E, k, renormalize=True, glu_interleave=0, swiglu_clamp=0.0):
+        return cls(int(T), int(H), int(F), int(E), int(k), int(bool(renormalize)),
+                   int(glu_interleave), float(swiglu_clamp), 0)
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libmoeffn.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    vp, sz, ci = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    pp = ctypes.POINTER(Problem)
+    sigs = {
+        "moe_status_string": ([ci], ctypes.c_char_p),
+        "moe_workspace_size": ([pp], sz),
+        "moe_route_topk": ([pp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_permute": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_grouped_swiglu_mlp": ([pp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_unpermute_combine": ([pp, vp, vp, vp, vp, vp], ci),
+        "moe_forward": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_get_device_status": ([vp, vp], ci),
+        "moe_clear_device_status": ([vp, vp], ci),
+        "moe_last_launch_count": ([], ci),
+        "moe_stage_timing_begin": ([ci], ci),
+        "moe_stage_timing_end": ([ctypes.POINTER(ctypes.c_float), ci,
+                                  ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)], ci),
+        "moe_stage_name": ([ci], ctypes.c_char_p),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the MoE library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _call(name: str, *args):
+    rc = getattr(load(), name)(*args)
+    if rc != MOE_OK:
+        raise MoEError(name, rc)
+
+
+def workspace_size(p: Problem) -> int:
+    return int(load().moe_workspace_size(ctypes.byref(p)))
+
+
+def alloc_workspace(p: Problem, device="cuda") -> torch.Tensor:
+    """A uint8 device tensor sized by moe_workspace_size (256-byte aligned)."""
+    n = workspace_size(p)
+    if n == 0:
+        raise MoEError("moe_workspace_size", 1)
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def last_launch_count() -> int:
+    return int(load().moe_last_launch_count())
+
+
+def stage_timing_begin(n_calls: int) -> None:
+    _call("moe_stage_timing_begin", int(n_calls))
+
+
+def stage_timing_end() -> Dict[str, float]:
+    """Average milliseconds per moe_forward stage over the recorded calls."""
+    ms = (ctypes.c_float * 16)()
+    ns, nc = ctypes.c_int(0), ctypes.c_int(0)
+    _call("moe_stage_timing_end", ms, 16, ctypes.byref(ns), ctypes.byref(nc))
+    lib = load()
+    res = {lib.moe_stage_name(i).decode(): float(ms[i]) for i in range(ns.value)}
+    res["_calls"] = nc.value
+    return res
+
+
+def get_device_status(ws: torch.Tensor, stream=None) -> int:
+    return int(load().moe_get_device_status(_ptr(ws), _stream(stream)))
+
+
+def clear_device_status(ws: torch.Tensor, stream=None) -> None:
+    _call("moe_clear_device_status", _ptr(ws), _stream(stream))
+
+
+def route_topk(p: Problem, logits, topk_idx, topk_w, ws=None, stream=None) -> None:
+    _call("moe_route_topk", ctypes.byref(p), _ptr(logits), _ptr(topk_idx), _ptr(topk_w),
+          _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream))
+
+
+def permute(p: Problem, topk_idx, x, x_perm, row_id_map, permuted_token, tokens_per_expert,
+            expert_offsets, ws, stream=None) -> None:
+    _call("moe_permute", ctypes.byref(p), _ptr(topk_idx), _ptr(x), _ptr(x_perm),
+          _ptr(row_id_map), _ptr(permuted_token), _ptr(tokens_per_expert),
+          _ptr(expert_offsets), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def grouped_swiglu_mlp(p: Problem, x_perm, expert_offsets, w1, w2, y_perm, ws,
+                       stream=None) -> None:
+    _call("moe_grouped_swiglu_mlp", ctypes.byref(p), _ptr(x_perm), _ptr(expert_offsets),
+          _ptr(w1), _ptr(w2), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def unpermute_combine(p: Problem, y_perm, row_id_map, topk_w, out, stream=None) -> None:
+    _call("moe_unpermute_combine", ctypes.byref(p), _ptr(y_perm), _ptr(row_id_map),
+          _ptr(topk_w), _ptr(out), _stream(stream))
+
+
+def forward(p: Problem, x, logits, w1, w2, out, ws, topk_idx=None, topk_w=None,
+            tokens_per_expert=None, stream=None) -> None:
+    _call("moe_forward", ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(w1), _ptr(w2),
+          _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(tokens_per_expert), _ptr(ws),
+          ws.numel(), _stream(stream))
+
+
+class MoEFFN:
+    """Convenience holder: weights + a reusable workspace for one problem size."""
+
+    def __init__(self, w1: torch.Tensor, w2: torch.Tensor, k: int, renormalize=True,
+                 glu_interleave=0, swiglu_clamp=0.0):
+        E, twoF, H = w1.shape
+        self.w1, self.w2 = w1, w2
+        self.H, self.F, self.E, self.k = H, twoF // 2, E, k
+        self.renormalize, self.glu_interleave, self.swiglu_clamp = (
+            renormalize, glu_interleave, swiglu_clamp)
+        self._ws = None
+        self._ws_T = -1
+
+    def problem(self, T: int) -> Problem:
+        return Problem.make(T, self.H, self.F, self.E, self.k, self.renormalize,
+                            self.glu_interleave, self.swiglu_clamp)
+
+    def __call__(self, x: torch.Tensor, logits: torch.Tensor,
+                 return_routing: bool = False) -> Dict[str, torch.Tensor]:
+        T = x.shape[0]
+        p = self.problem(T)
+        if self._ws is None or T > self._ws_T:
+            self._ws = alloc_workspace(p, device=x.device)
+            self._ws_T = T
+        out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
+        res = {"out": out}
+        if return_routing:
+            res["topk_idx"] = torch.empty(T, self.k, dtype=torch.int32, device=x.device)
+            res["topk_w"] = torch.empty(T, self.k, dtype=torch.float32, device=x.device)
+            res["tokens_per_expert"] = torch.empty(self.E, dtype=torch.int32, device=x.device)
+        forward(p, x, logits, self.w1, self.w2, out, self._ws, res.get("topk_idx"),
+                res.get("topk_w"), res.get("tokens_per_expert"))
+        return res
+
+
+__all__ = ["Problem", "MoEError", "MoEFFN", "load", "workspace_size", "alloc_workspace",
+           "route_topk", "permute", "grouped_swiglu_mlp", "unpermute_combine", "forward",
+           "get_device_status", "clear_device_status", "last_launch_count", "LIB_PATH",
+           "stage_timing_begin", "stage_timing_end"]

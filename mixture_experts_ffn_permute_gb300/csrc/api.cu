@@ -1,0 +1,453 @@
+// C ABI of the MoE expert-FFN library: argument checks, workspace layout and
+// the launch sequences of each entry point (declared in include/moe_ffn.h).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/moe_ffn.h"
+#include "internal.h"
+
+namespace moe {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+thread_local int g_launches = 0;
+
+// Stage names of moe_forward, in launch order.
+constexpr int kNumStages = 8;
+const char* const kStageNames[kNumStages] = {"route_topk", "chunk_histogram", "scan",
+                                             "scatter", "gather_rows", "gemm1_swiglu",
+                                             "gemm2", "combine"};
+
+// Event ring for moe_stage_timing_begin/end (one row of kNumStages+1 events
+// per recorded call).
+struct StageTimer {
+  bool on = false;
+  int capacity = 0;
+  int used = 0;
+  cudaEvent_t* ev = nullptr;
+  void mark(int call, int i, cudaStream_t s) {
+    if (on && call < capacity) cudaEventRecord(ev[call * (kNumStages + 1) + i], s);
+  }
+};
+thread_local StageTimer g_timer;
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+// Byte offsets of every scratch region inside the caller's workspace.
+struct Layout {
+  size_t status, chunk_counts, tokens_per_expert, expert_offsets, mtile_prefix, topk_idx, topk_w,
+      row_id_map, permuted_token, x_perm, h, y, total;
+};
+
+Layout layout_of(const moe_problem& p) {
+  const size_t T = p.T, E = p.E, R = static_cast<size_t>(p.T) * p.k;
+  const size_t nchunks = (T + kChunkTokens - 1) / kChunkTokens;
+  Layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.status = take(sizeof(uint32_t));
+  L.chunk_counts = take(sizeof(int32_t) * nchunks * E);
+  L.tokens_per_expert = take(sizeof(int32_t) * E);
+  L.expert_offsets = take(sizeof(int32_t) * (E + 1));
+  L.mtile_prefix = take(sizeof(int32_t) * (E + 1));
+  L.topk_idx = take(sizeof(int32_t) * R);
+  L.topk_w = take(sizeof(float) * R);
+  L.row_id_map = take(sizeof(int32_t) * R);
+  L.permuted_token = take(sizeof(int32_t) * R);
+  L.x_perm = take(2 * R * static_cast<size_t>(p.H));
+  L.h = take(2 * R * static_cast<size_t>(p.F));
+  L.y = take(2 * R * static_cast<size_t>(p.H));
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int check_routing(const moe_problem* p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->E < 1 || p->k < 1 || p->k > p->E) return MOE_ERR_INVALID_ARG;
+  if (p->E > MOE_MAX_EXPERTS || p->k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(p->T) * p->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int check_full(const moe_problem* p) {
+  int rc = check_routing(p);
+  if (rc != MOE_OK) return rc;
+  if (p->H <= 0 || p->F <= 0) return MOE_ERR_INVALID_ARG;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED_SHAPE;
+  // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
+  if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int I = p->glu_interleave;
+  if (I < 0) return MOE_ERR_INVALID_ARG;
+  if (I != 0 && (p->F % I != 0 || !(I == 32 || I == 64 || I % 128 == 0)))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const long long R = static_cast<long long>(p->T) * p->k;
+  if (R * p->H >= (1LL << 40) || static_cast<long long>(p->E) * 2 * p->F >= (1LL << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int check_ws(const moe_problem* p, void* ws, size_t ws_bytes) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < layout_of(*p).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+#define MOE_REQUIRE_PTR(ptr)                            \
+  do {                                                  \
+    if (!(ptr)) return MOE_ERR_INVALID_ARG;             \
+    if (!aligned16(ptr)) return MOE_ERR_MISALIGNED;     \
+  } while (0)
+
+#define MOE_LAUNCH(expr)                          \
+  do {                                            \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
+    ++launches;                                   \
+  } while (0)
+
+float clamp_of(const moe_problem* p) {
+  const float c = p->swiglu_clamp;
+  return (c > 0.f && std::isfinite(c)) ? c : 0.f;
+}
+
+// GEMM1 (x_perm -> h with SwiGLU) then GEMM2 (h -> y).
+int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
+            const int32_t* mtp, const void* w1, const void* w2, void* h, void* y,
+            uint32_t* status, cudaStream_t s, int& launches, StageTimer* tm = nullptr,
+            int call = 0, int mark = 0) {
+  const int R = p->T * p->k;
+  GroupedGemmArgs g1{};
+  g1.epi = Epi::kSwiGLU;
+  g1.a = x_perm;
+  g1.a_rows = R;
+  g1.b = w1;
+  g1.b_rows_per_expert = 2 * p->F;
+  g1.E = p->E;
+  g1.K = p->H;
+  g1.n_tiles = p->F / (kBN / 2);
+  g1.expert_offsets = offsets;
+  g1.mtile_prefix = mtp;
+  g1.out = h;
+  g1.ldo = p->F;
+  g1.out_rows = R;
+  g1.F = p->F;
+  g1.interleave = p->glu_interleave;
+  g1.clamp = clamp_of(p);
+  g1.status = status;
+  MOE_LAUNCH(launch_grouped_gemm(g1, s));
+  if (tm) tm->mark(call, mark, s);
+  GroupedGemmArgs g2{};
+  g2.epi = Epi::kPlain;
+  g2.a = h;
+  g2.a_rows = R;
+  g2.b = w2;
+  g2.b_rows_per_expert = p->H;
+  g2.E = p->E;
+  g2.K = p->F;
+  g2.n_tiles = p->H / kBN;
+  g2.expert_offsets = offsets;
+  g2.mtile_prefix = mtp;
+  g2.out = y;
+  g2.ldo = p->H;
+  g2.out_rows = R;
+  g2.F = p->F;
+  g2.status = status;
+  MOE_LAUNCH(launch_grouped_gemm(g2, s));
+  if (tm) tm->mark(call, mark + 1, s);
+  return MOE_OK;
+}
+
+// histogram -> scan -> scatter; fills row maps, counts and offsets.
+int run_permute(const moe_problem* p, const int32_t* topk_idx, int32_t* row_id_map,
+                int32_t* permuted_token, int32_t* tokens_per_expert, int32_t* expert_offsets,
+                int32_t* mtp, void* ws, const Layout& L, cudaStream_t s, int& launches,
+                StageTimer* tm = nullptr, int call = 0, int mark = 0) {
+  const int R = p->T * p->k;
+  const int nchunks = ceil_div(p->T, kChunkTokens);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  int32_t* cc = at<int32_t>(ws, L.chunk_counts);
+  if (nchunks > 0) MOE_LAUNCH(launch_chunk_histogram(topk_idx, p->T, p->E, p->k, cc, status, s));
+  if (tm) tm->mark(call, mark, s);
+  MOE_LAUNCH(launch_scan(cc, nchunks, p->E, R, tokens_per_expert, expert_offsets, mtp,
+                         permuted_token, s));
+  if (tm) tm->mark(call, mark + 1, s);
+  if (nchunks > 0)
+    MOE_LAUNCH(launch_scatter(topk_idx, p->T, p->E, p->k, cc, row_id_map, permuted_token, s));
+  if (tm) tm->mark(call, mark + 2, s);
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_DEVICE_INDEX: return "MOE_ERR_DEVICE_INDEX";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+size_t moe_workspace_size(const moe_problem* p) {
+  if (check_full(p) != MOE_OK && check_routing(p) != MOE_OK) return 0;
+  moe_problem q = *p;
+  if (q.H < 0) q.H = 0;
+  if (q.F < 0) q.F = 0;
+  return layout_of(q).total;
+}
+
+int moe_route_topk(const moe_problem* p, const float* logits, int32_t* topk_idx, float* topk_w,
+                   void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  int rc = check_routing(p);
+  if (rc != MOE_OK) return rc;
+  if (p->T == 0) { g_launches = 0; return MOE_OK; }
+  MOE_REQUIRE_PTR(logits);
+  MOE_REQUIRE_PTR(topk_idx);
+  MOE_REQUIRE_PTR(topk_w);
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, topk_idx,
+                               topk_w, s));
+  g_launches = launches;
+  return MOE_OK;
+}
+
+int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, void* x_perm,
+                int32_t* row_id_map, int32_t* permuted_token, int32_t* tokens_per_expert,
+                int32_t* expert_offsets, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_routing(p);
+  if (rc != MOE_OK) return rc;
+  if (x_perm) {
+    if (p->H <= 0 || p->H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    MOE_REQUIRE_PTR(x);
+    MOE_REQUIRE_PTR(x_perm);
+  }
+  MOE_REQUIRE_PTR(tokens_per_expert);
+  MOE_REQUIRE_PTR(expert_offsets);
+  if (p->T > 0) {
+    MOE_REQUIRE_PTR(topk_idx);
+    MOE_REQUIRE_PTR(row_id_map);
+    MOE_REQUIRE_PTR(permuted_token);
+  }
+  moe_problem q = *p;  // permute uses only the routing regions of the workspace
+  q.H = 0;
+  q.F = 0;
+  rc = check_ws(&q, ws, ws_bytes);
+  if (rc != MOE_OK) return rc;
+  const Layout L = layout_of(q);
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = run_permute(p, topk_idx, row_id_map, permuted_token, tokens_per_expert, expert_offsets,
+                   at<int32_t>(ws, L.mtile_prefix), ws, L, s, launches);
+  if (rc != MOE_OK) return rc;
+  if (x_perm && p->T > 0)
+    MOE_LAUNCH(launch_gather_rows(x, permuted_token, p->T * p->k, p->H, x_perm, s));
+  g_launches = launches;
+  return MOE_OK;
+}
+
+int moe_grouped_swiglu_mlp(const moe_problem* p, const void* x_perm,
+                           const int32_t* expert_offsets, const void* w1, const void* w2,
+                           void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  rc = check_ws(p, ws, ws_bytes);
+  if (rc != MOE_OK) return rc;
+  MOE_REQUIRE_PTR(expert_offsets);
+  MOE_REQUIRE_PTR(w1);
+  MOE_REQUIRE_PTR(w2);
+  if (p->T == 0) { g_launches = 0; return MOE_OK; }
+  MOE_REQUIRE_PTR(x_perm);
+  MOE_REQUIRE_PTR(y_perm);
+  const Layout L = layout_of(*p);
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
+  MOE_LAUNCH(launch_mtile_prefix_from_offsets(expert_offsets, p->E, p->T * p->k, mtp, status, s));
+  rc = run_mlp(p, x_perm, expert_offsets, mtp, w1, w2, at<void>(ws, L.h), y_perm, status, s,
+               launches);
+  if (rc != MOE_OK) return rc;
+  g_launches = launches;
+  return MOE_OK;
+}
+
+int moe_unpermute_combine(const moe_problem* p, const void* y_perm, const int32_t* row_id_map,
+                          const float* topk_w, void* out, void* stream) {
+  int rc = check_routing(p);
+  if (rc != MOE_OK) return rc;
+  if (p->H <= 0 || p->H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (p->T == 0) { g_launches = 0; return MOE_OK; }
+  MOE_REQUIRE_PTR(y_perm);
+  MOE_REQUIRE_PTR(row_id_map);
+  MOE_REQUIRE_PTR(topk_w);
+  MOE_REQUIRE_PTR(out);
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_LAUNCH(launch_combine(y_perm, row_id_map, topk_w, p->T, p->H, p->k, out, s));
+  g_launches = launches;
+  return MOE_OK;
+}
+
+int moe_forward(const moe_problem* p, const void* x, const float* logits, const void* w1,
+                const void* w2, void* out, int32_t* topk_idx_out, float* topk_w_out,
+                int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  rc = check_ws(p, ws, ws_bytes);
+  if (rc != MOE_OK) return rc;
+  MOE_REQUIRE_PTR(w1);
+  MOE_REQUIRE_PTR(w2);
+  if (topk_idx_out && !aligned16(topk_idx_out)) return MOE_ERR_MISALIGNED;
+  if (topk_w_out && !aligned16(topk_w_out)) return MOE_ERR_MISALIGNED;
+  if (tokens_per_expert_out && !aligned16(tokens_per_expert_out)) return MOE_ERR_MISALIGNED;
+  const Layout L = layout_of(*p);
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* tpe = tokens_per_expert_out ? tokens_per_expert_out
+                                       : at<int32_t>(ws, L.tokens_per_expert);
+  if (p->T == 0) {
+    if (tokens_per_expert_out)
+      MOE_LAUNCH(cudaMemsetAsync(tokens_per_expert_out, 0, sizeof(int32_t) * p->E, s));
+    g_launches = launches;
+    return MOE_OK;
+  }
+  MOE_REQUIRE_PTR(x);
+  MOE_REQUIRE_PTR(logits);
+  MOE_REQUIRE_PTR(out);
+  const int R = p->T * p->k;
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.topk_idx);
+  float* wts = topk_w_out ? topk_w_out : at<float>(ws, L.topk_w);
+  int32_t* off = at<int32_t>(ws, L.expert_offsets);
+  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
+  int32_t* rmap = at<int32_t>(ws, L.row_id_map);
+  int32_t* ptok = at<int32_t>(ws, L.permuted_token);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h = at<void>(ws, L.h);
+  void* y = at<void>(ws, L.y);
+
+  const int call = g_timer.on ? g_timer.used++ : 0;
+  StageTimer& tm = g_timer;
+  tm.mark(call, 0, s);
+  MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
+  tm.mark(call, 1, s);
+  rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2);
+  if (rc != MOE_OK) return rc;
+  MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
+  tm.mark(call, 5, s);
+  rc = run_mlp(p, x_perm, off, mtp, w1, w2, h, y, status, s, launches, &tm, call, 6);
+  if (rc != MOE_OK) return rc;
+  MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
+  tm.mark(call, 8, s);
+  g_launches = launches;
+  return MOE_OK;
+}
+
+int moe_get_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (word & (1u << MOE_ERR_DEVICE_TIMEOUT)) return MOE_ERR_DEVICE_TIMEOUT;
+  if (word & (1u << MOE_ERR_DEVICE_INDEX)) return MOE_ERR_DEVICE_INDEX;
+  return MOE_OK;
+}
+
+int moe_clear_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_last_launch_count(void) { return g_launches; }
+
+int moe_stage_timing_begin(int n_calls) {
+  if (n_calls <= 0) return MOE_ERR_INVALID_ARG;
+  StageTimer& t = g_timer;
+  if (n_calls > t.capacity) {
+    if (t.ev) {
+      for (int i = 0; i < t.capacity * (kNumStages + 1); ++i) cudaEventDestroy(t.ev[i]);
+      delete[] t.ev;
+    }
+    t.ev = new cudaEvent_t[n_calls * (kNumStages + 1)];
+    for (int i = 0; i < n_calls * (kNumStages + 1); ++i)
+      if (cudaEventCreate(&t.ev[i]) != cudaSuccess) return MOE_ERR_CUDA;
+    t.capacity = n_calls;
+  }
+  t.used = 0;
+  t.on = true;
+  return MOE_OK;
+}
+
+int moe_stage_timing_end(float* ms, int max_stages, int* n_stages, int* n_calls) {
+  StageTimer& t = g_timer;
+  t.on = false;
+  const int calls = t.used < t.capacity ? t.used : t.capacity;
+  if (n_calls) *n_calls = calls;
+  if (n_stages) *n_stages = kNumStages;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  for (int i = 0; i < kNumStages && i < max_stages; ++i) {
+    double acc = 0.0;
+    for (int c = 0; c < calls; ++c) {
+      float v = 0.f;
+      if (cudaEventElapsedTime(&v, t.ev[c * (kNumStages + 1) + i],
+                               t.ev[c * (kNumStages + 1) + i + 1]) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      acc += v;
+    }
+    if (ms) ms[i] = calls ? static_cast<float>(acc / calls) : 0.f;
+  }
+  return MOE_OK;
+}
+
+const char* moe_stage_name(int i) {
+  return (i >= 0 && i < kNumStages) ? kStageNames[i] : "";
+}
+
+}  // extern "C"

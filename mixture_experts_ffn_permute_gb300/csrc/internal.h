@@ -1,0 +1,82 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Tokens per routing chunk: the unit of the per-chunk expert histogram and
+// of the stable scatter (one warp scatters one chunk in token order).
+constexpr int kChunkTokens = 64;
+
+// Grouped-GEMM tiling (rows of permuted tokens x output columns x K step).
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+
+inline int ceil_div(long a, long b) { return static_cast<int>((a + b - 1) / b); }
+
+int num_sms();
+
+// Step 1: routing.
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize,
+                              int32_t* topk_idx, float* topk_w, cudaStream_t s);
+
+// Step 2a: per-chunk expert histogram of topk_idx (also validates indices).
+cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int T, int E, int k,
+                                   int32_t* chunk_counts, uint32_t* status, cudaStream_t s);
+
+// Step 2b: turn chunk histograms into per-(chunk, expert) row bases and
+// produce tokens_per_expert, expert_offsets, the m-tile prefix and the
+// masked-tail fill of permuted_token.
+cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int R,
+                        int32_t* tokens_per_expert, int32_t* expert_offsets,
+                        int32_t* mtile_prefix, int32_t* permuted_token, cudaStream_t s);
+
+// Step 2c: stable scatter -> row_id_map and permuted_token.
+cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
+                           const int32_t* chunk_base, int32_t* row_id_map,
+                           int32_t* permuted_token, cudaStream_t s);
+
+// x_perm[r] = x[permuted_token[r]] (zero row for -1).
+cudaError_t launch_gather_rows(const void* x, const int32_t* permuted_token, int R, int H,
+                               void* x_perm, cudaStream_t s);
+
+// m-tile prefix from caller-supplied expert offsets (validated on device).
+cudaError_t launch_mtile_prefix_from_offsets(const int32_t* expert_offsets, int E, int R,
+                                             int32_t* mtile_prefix, uint32_t* status,
+                                             cudaStream_t s);
+
+// Step 6: out[t] = sum_j w[t][j] * y[row_id_map[t][j]] in slot order.
+cudaError_t launch_combine(const void* y, const int32_t* row_id_map, const float* topk_w,
+                           int T, int H, int k, void* out, cudaStream_t s);
+
+// Steps 3-5: grouped GEMMs on tcgen05.
+enum class Epi : int { kSwiGLU = 0, kPlain = 1 };
+
+struct GroupedGemmArgs {
+  Epi epi;
+  const void* a;               // [a_rows, K] bf16 (permuted rows)
+  int a_rows;
+  const void* b;               // [E * b_rows_per_expert, K] bf16
+  int b_rows_per_expert;
+  int E;
+  int K;
+  int n_tiles;                 // output tiles per expert along N
+  const int32_t* expert_offsets;
+  const int32_t* mtile_prefix;
+  void* out;                   // bf16 rows of ldo elements
+  int ldo;
+  int out_rows;                // rows >= expert_offsets[E] .. out_rows are zeroed (kPlain)
+  int F;                       // SwiGLU: intermediate width
+  int interleave;              // SwiGLU: GLU interleave (0, 32, 64 or multiple of 128)
+  float clamp;                 // SwiGLU clamp (<= 0: none)
+  uint32_t* status;
+};
+
+cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s);
+
+}  // namespace moe

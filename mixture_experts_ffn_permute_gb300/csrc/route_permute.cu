@@ -1,0 +1,401 @@
+// Routing, permute bookkeeping, row gather and the weighted combine.
+//
+// Routing ("[SM90] Add W4A8 MegaMoE support", Usage: integer expert indices
+// and fp32 weights per route) runs one warp per token.  The permute ("add
+// permute fusion into hybrid ep", PR description: rows reordered into
+// expert-contiguous order) is a three-kernel histogram / scan / scatter
+// whose scatter is stable in token order, so row assignment is deterministic
+// and matches a sequential walk over (expert, token).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouteWarps = 8;
+
+struct Cand {
+  float v;
+  int id;  // INT_MAX = none
+};
+
+// (value descending, id ascending); "none" loses to everything.
+__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
+  if (b.id == INT_MAX) return a.id != INT_MAX;
+  if (a.id == INT_MAX) return false;
+  return a.v > b.v || (a.v == b.v && a.id < b.id);
+}
+
+__device__ __forceinline__ Cand warp_best(Cand c) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Cand o;
+    o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
+    o.id = __shfl_xor_sync(0xffffffffu, c.id, off);
+    if (better(o, c)) c = o;
+  }
+  return c;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// One warp per token; the token's logits are staged in shared memory and
+// each lane owns experts lane, lane+32, ... (at most 32 of them).
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  extern __shared__ float s_logits[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* row = s_logits + static_cast<size_t>(warp) * E;
+  const int per_lane = (E + 31) >> 5;
+  for (int t = blockIdx.x * kRouteWarps + warp; t < T; t += gridDim.x * kRouteWarps) {
+    const float* src = logits + static_cast<size_t>(t) * E;
+    for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
+    __syncwarp();
+    uint32_t taken = 0;
+    Cand mine{0.f, INT_MAX};
+    float top = 0.f;
+    for (int j = 0; j < k; ++j) {
+      Cand c{0.f, INT_MAX};
+      for (int i = 0; i < per_lane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !(taken & (1u << i))) {
+          Cand o{row[e], e};
+          if (better(o, c)) c = o;
+        }
+      }
+      c = warp_best(c);
+      if (c.id != INT_MAX && (c.id & 31) == lane) taken |= 1u << (c.id >> 5);
+      if (lane == j) mine = c;
+      if (j == 0) top = c.v;
+    }
+    // weights: exp(l - l_top) normalised over the selected (or all) experts
+    float ex = (lane < k) ? expf(mine.v - top) : 0.f;
+    float denom;
+    if (renormalize) {
+      denom = warp_sum(ex);
+    } else {
+      float part = 0.f;
+      for (int e = lane; e < E; e += 32) part += expf(row[e] - top);
+      denom = warp_sum(part);
+    }
+    if (lane < k) {
+      topk_idx[static_cast<size_t>(t) * k + lane] = mine.id;
+      topk_w[static_cast<size_t>(t) * k + lane] = ex / denom;
+    }
+    __syncwarp();
+  }
+}
+
+// Per-chunk expert histogram (shared-memory counters) plus index validation:
+// an index outside [-1, E) or an expert listed twice by one token is
+// recorded in the status word and the route is treated as masked.
+__global__ void __launch_bounds__(256)
+chunk_histogram_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
+                       int32_t* __restrict__ chunk_counts, uint32_t* status) {
+  extern __shared__ int32_t s_cnt[];
+  const int chunk = blockIdx.x;
+  const int t0 = chunk * kChunkTokens;
+  const int nt = min(kChunkTokens, T - t0);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int nr = nt * k;
+  const int32_t* idx = topk_idx + static_cast<size_t>(t0) * k;
+  for (int r = threadIdx.x; r < nr; r += blockDim.x) {
+    const int e = idx[r];
+    if (e == -1) continue;
+    if (e < -1 || e >= E) {
+      record_status(status, kStatusIndex);
+      continue;
+    }
+    const int t = r / k, j = r - t * k;
+    bool dup = false;
+    for (int jj = 0; jj < j; ++jj) dup |= (idx[t * k + jj] == e);
+    if (dup) {
+      record_status(status, kStatusIndex);
+      continue;
+    }
+    atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[static_cast<size_t>(chunk) * E + e] = s_cnt[e];
+}
+
+// Block-wide exclusive scan over up to 1024 values (one per thread).
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    s_warp[lane] = w;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int excl = x - v + (warp > 0 ? s_warp[warp - 1] : 0);
+  if (total) *total = s_warp[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return excl;
+}
+
+// One CTA of 1024 threads; thread e owns expert e.
+__global__ void __launch_bounds__(1024)
+scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E, int R,
+            int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ expert_offsets,
+            int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ permuted_token) {
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  int count = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      int32_t* p = chunk_counts + static_cast<size_t>(c) * E + e;
+      const int v = *p;
+      *p = count;  // exclusive within the expert
+      count += v;
+    }
+  }
+  int total = 0;
+  const int off = block_exclusive_scan(e < E ? count : 0, s_warp, &total);
+  const int mt = (count + kBM - 1) / kBM;
+  int mt_total = 0;
+  const int mt_off = block_exclusive_scan(e < E ? mt : 0, s_warp, &mt_total);
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) chunk_counts[static_cast<size_t>(c) * E + e] += off;
+    tokens_per_expert[e] = count;
+    expert_offsets[e] = off;
+    mtile_prefix[e] = mt_off;
+  }
+  if (e == 0) {
+    expert_offsets[E] = total;
+    mtile_prefix[E] = mt_total;
+  }
+  for (int r = total + e; r < R; r += blockDim.x) permuted_token[r] = -1;
+}
+
+// One warp per chunk.  Routes are visited in (token, slot) order, 32 at a
+// time; lanes holding the same expert are grouped with __match_any_sync and
+// ranked by lane, and the group's lowest lane advances the expert's running
+// row counter.  A token lists an expert at most once, so (token, slot) order
+// is token order within every expert: the scatter is stable.
+__global__ void __launch_bounds__(32)
+scatter_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
+               const int32_t* __restrict__ chunk_base, int32_t* __restrict__ row_id_map,
+               int32_t* __restrict__ permuted_token) {
+  extern __shared__ int32_t s_next[];
+  const int chunk = blockIdx.x, lane = threadIdx.x;
+  const int t0 = chunk * kChunkTokens;
+  const int nt = min(kChunkTokens, T - t0);
+  for (int e = lane; e < E; e += 32) s_next[e] = chunk_base[static_cast<size_t>(chunk) * E + e];
+  __syncwarp();
+  const int nr = nt * k;
+  const size_t base = static_cast<size_t>(t0) * k;
+  for (int r0 = 0; r0 < nr; r0 += 32) {
+    const int r = r0 + lane;
+    int e = -1;
+    if (r < nr) {
+      e = topk_idx[base + r];
+      const int t = r / k, j = r - t * k;
+      bool dup = false;
+      for (int jj = 0; jj < j; ++jj) dup |= (topk_idx[base + t * k + jj] == e);
+      if (e < 0 || e >= E || dup) e = -1;
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int leader = __ffs(peers) - 1;
+    int start = 0;
+    if (e >= 0) start = s_next[e];
+    __syncwarp();
+    if (e >= 0 && lane == leader) s_next[e] = start + __popc(peers);
+    __syncwarp();
+    if (r < nr) {
+      const int t = t0 + r / k;
+      if (e >= 0) {
+        const int row = start + rank;
+        row_id_map[base + r] = row;
+        permuted_token[row] = t;
+      } else {
+        row_id_map[base + r] = -1;
+      }
+    }
+  }
+}
+
+// x_perm[r] = x[permuted_token[r]] in 16-byte vectors; a grid-stride loop
+// over rows, one CTA per row at a time.
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ permuted_token,
+                   int R, int vecs_per_row, uint4* __restrict__ x_perm) {
+  for (int r = blockIdx.x; r < R; r += gridDim.x) {
+    const int t = permuted_token[r];
+    uint4* dst = x_perm + static_cast<size_t>(r) * vecs_per_row;
+    if (t < 0) {
+      for (int v = threadIdx.x; v < vecs_per_row; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+    } else {
+      const uint4* src = x + static_cast<size_t>(t) * vecs_per_row;
+      for (int v = threadIdx.x; v < vecs_per_row; v += blockDim.x) dst[v] = __ldg(src + v);
+    }
+  }
+}
+
+// Validates caller-supplied offsets (non-decreasing, offsets[0] == 0,
+// offsets[E] <= R) and builds the m-tile prefix.  Bad offsets are recorded
+// and replaced by an empty problem.
+__global__ void __launch_bounds__(1024)
+mtile_prefix_kernel(const int32_t* __restrict__ offsets, int E, int R,
+                    int32_t* __restrict__ mtile_prefix, uint32_t* status) {
+  __shared__ int s_warp[32];
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  const int e = threadIdx.x;
+  int mt = 0;
+  if (e < E) {
+    const int a = offsets[e], b = offsets[e + 1];
+    if (b < a || a < 0 || b > R || (e == 0 && a != 0)) s_bad = 1;
+    mt = (b > a) ? (b - a + kBM - 1) / kBM : 0;
+  }
+  __syncthreads();
+  const bool bad = s_bad != 0;
+  if (bad) mt = 0;
+  int total = 0;
+  const int off = block_exclusive_scan(e < E ? mt : 0, s_warp, &total);
+  if (e < E) mtile_prefix[e] = off;
+  if (e == 0) {
+    mtile_prefix[E] = total;
+    if (bad) record_status(status, kStatusIndex);
+  }
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 p = __bfloat1622float2(h[i]);
+    f[2 * i] = p.x;
+    f[2 * i + 1] = p.y;
+  }
+}
+
+// out[t][c..c+8) = sum_{j} w[t][j] * y[row][c..c+8), fp32 in slot order.
+__global__ void __launch_bounds__(256)
+combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_id_map,
+               const float* __restrict__ topk_w, int T, int vecs_per_row, int k,
+               uint4* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int v = blockIdx.y * blockDim.x + threadIdx.x;
+  if (t >= T || v >= vecs_per_row) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int row = __ldg(row_id_map + static_cast<size_t>(t) * k + j);
+    if (row < 0) continue;
+    const float w = __ldg(topk_w + static_cast<size_t>(t) * k + j);
+    float f[8];
+    bf16x8_to_f32(__ldg(y + static_cast<size_t>(row) * vecs_per_row + v), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+  }
+  uint4 o;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+  out[static_cast<size_t>(t) * vecs_per_row + v] = o;
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize,
+                              int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const size_t smem = sizeof(float) * kRouteWarps * E;
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(route_topk_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+  }
+  const int blocks = min(ceil_div(T, kRouteWarps), num_sms() * 8);
+  route_topk_kernel<<<blocks, kRouteWarps * 32, smem, s>>>(logits, T, E, k, renormalize,
+                                                           topk_idx, topk_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int T, int E, int k,
+                                   int32_t* chunk_counts, uint32_t* status, cudaStream_t s) {
+  const int nchunks = ceil_div(T, kChunkTokens);
+  if (nchunks == 0) return cudaSuccess;
+  chunk_histogram_kernel<<<nchunks, 256, sizeof(int32_t) * E, s>>>(topk_idx, T, E, k,
+                                                                   chunk_counts, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int R,
+                        int32_t* tokens_per_expert, int32_t* expert_offsets,
+                        int32_t* mtile_prefix, int32_t* permuted_token, cudaStream_t s) {
+  scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, R, tokens_per_expert,
+                                 expert_offsets, mtile_prefix, permuted_token);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
+                           const int32_t* chunk_base, int32_t* row_id_map,
+                           int32_t* permuted_token, cudaStream_t s) {
+  const int nchunks = ceil_div(T, kChunkTokens);
+  if (nchunks == 0) return cudaSuccess;
+  scatter_kernel<<<nchunks, 32, sizeof(int32_t) * E, s>>>(topk_idx, T, E, k, chunk_base,
+                                                          row_id_map, permuted_token);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* permuted_token, int R, int H,
+                               void* x_perm, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const int vecs = H / 8;
+  const int blocks = min(R, num_sms() * 8);
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), permuted_token, R,
+                                            vecs, static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mtile_prefix_from_offsets(const int32_t* expert_offsets, int E, int R,
+                                             int32_t* mtile_prefix, uint32_t* status,
+                                             cudaStream_t s) {
+  mtile_prefix_kernel<<<1, 1024, 0, s>>>(expert_offsets, E, R, mtile_prefix, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* row_id_map, const float* topk_w,
+                           int T, int H, int k, void* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int vecs = H / 8;
+  dim3 grid(T, ceil_div(vecs, 256));
+  combine_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(y), row_id_map, topk_w, T,
+                                      vecs, k, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,55 @@
+"""Comparison helpers shared by the GPU parity tests.
+
+Floating-point contract (bf16 path): per element
+    |gpu - oracle| <= 1e-2 + 1e-2 * |oracle|
+and over the whole tensor
+    RMS relative error sqrt(sum (gpu - oracle)^2 / sum oracle^2) <= 5e-3.
+Routing indices, row maps and counts are compared bit for bit.
+"""
+import numpy as np
+import torch
+
+ATOL = 1e-2
+RTOL = 1e-2
+RMS_BF16 = 5e-3
+
+
+def to_f64(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        return t.detach().to(torch.float64).cpu().numpy()
+    return np.asarray(t, np.float64)
+
+
+def rms_rel(gpu: np.ndarray, ref: np.ndarray) -> float:
+    den = float(np.sum(ref * ref))
+    num = float(np.sum((gpu - ref) ** 2))
+    if den == 0.0:
+        return 0.0 if num == 0.0 else float("inf")
+    return (num / den) ** 0.5
+
+
+def assert_bf16_close(gpu, ref, what: str = "", rms: float = RMS_BF16):
+    g = to_f64(gpu)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - r)
+    bound = ATOL + RTOL * np.abs(r)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; worst at {i}: "
+                             f"gpu={g[i]!r} oracle={r[i]!r}")
+    e = rms_rel(g, r)
+    assert e <= rms, f"{what}: RMS relative error {e:.3e} > {rms:.1e}"
+    return e
+
+
+def assert_equal(gpu, ref, what: str = ""):
+    g = gpu.detach().cpu().numpy() if isinstance(gpu, torch.Tensor) else np.asarray(gpu)
+    r = np.asarray(ref)
+    assert g.shape == r.shape, (what, g.shape, r.shape)
+    if not np.array_equal(g, r):
+        d = np.argwhere(g != r)
+        raise AssertionError(f"{what}: {len(d)} mismatches, first at {tuple(d[0])}: "
+                             f"gpu={g[tuple(d[0])]} oracle={r[tuple(d[0])]}")

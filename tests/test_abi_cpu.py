@@ -1,0 +1,104 @@
+"""CPU checks of the C ABI: the library loads without a GPU, exports every
+entry point include/moe_ffn.h declares, and rejects bad arguments on the
+host before any CUDA call (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_ffn_permute_gb300 as moe
+from mixture_experts_ffn_permute_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return moe.load()
+
+
+def declared_symbols():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert "moe_forward" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in moe.STATUS_NAMES.items():
+        assert lib.moe_status_string(code).decode() == name
+
+
+def P(**kw):
+    base = dict(T=64, H=256, F=512, E=8, k=2)
+    base.update(kw)
+    return moe.Problem.make(**base)
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    a = moe.workspace_size(P(T=64))
+    b = moe.workspace_size(P(T=128))
+    assert 0 < a < b
+    assert a % 256 == 0
+    # at least the three permuted activations: x_perm, h, y (bf16)
+    R = 64 * 2
+    assert a >= 2 * R * (256 + 512 + 256)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=9), 1), (dict(k=0), 1), (dict(E=0), 1), (dict(T=-1), 1),
+    (dict(H=200), 2), (dict(F=100), 2), (dict(E=2000, k=2), 2), (dict(k=33, E=64), 2),
+    (dict(glu_interleave=48), 2), (dict(glu_interleave=-1), 1), (dict(glu_interleave=1024), 2),
+])
+def test_forward_rejects_bad_problems(lib, kw, code):
+    p = P(**kw)
+    fake = ctypes.c_void_p(1 << 20)
+    rc = lib.moe_forward(ctypes.byref(p), fake, fake, fake, fake, fake, None, None, None, fake,
+                         1 << 40, None)
+    assert rc == code
+
+
+def test_forward_rejects_bad_pointers_and_workspace(lib):
+    p = P()
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    big = 1 << 40
+    ws_need = moe.workspace_size(p)
+    assert lib.moe_forward(ctypes.byref(p), None, a, a, a, a, None, None, None, a, big, None) == 1
+    assert lib.moe_forward(ctypes.byref(p), mis, a, a, a, a, None, None, None, a, big, None) == 3
+    # workspace must be 256-byte aligned and large enough
+    ws_mis = ctypes.c_void_p((1 << 20) + 16)
+    assert lib.moe_forward(ctypes.byref(p), a, a, a, a, a, None, None, None, ws_mis, big,
+                           None) == 3
+    assert lib.moe_forward(ctypes.byref(p), a, a, a, a, a, None, None, None, a, ws_need - 1,
+                           None) == 4
+    assert lib.moe_forward(None, a, a, a, a, a, None, None, None, a, big, None) == 1
+
+
+def test_other_entry_points_validate(lib):
+    p = P()
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    assert lib.moe_route_topk(ctypes.byref(P(k=9)), a, a, a, None, 0, None) == 1
+    assert lib.moe_route_topk(ctypes.byref(p), mis, a, a, None, 0, None) == 3
+    assert lib.moe_permute(ctypes.byref(p), a, None, None, a, a, None, a, a, 1 << 30, None) == 1
+    assert lib.moe_grouped_swiglu_mlp(ctypes.byref(P(F=96)), a, a, a, a, a, a, 1 << 40,
+                                      None) == 2
+    assert lib.moe_unpermute_combine(ctypes.byref(P(H=12)), a, a, a, a, None) == 2
+    assert lib.moe_get_device_status(None, None) == 1
+
+
+def test_binding_raises_without_library(tmp_path):
+    with pytest.raises(ImportError):
+        moe.load(str(tmp_path / "missing.so"))

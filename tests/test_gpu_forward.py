@@ -1,0 +1,145 @@
+"""GPU parity of the fused moe_forward against the fp64 oracle.
+
+Small shapes are compared element by element over the whole output.  The
+full-size workloads (Mixtral-shaped, fine-grained skewed, decode) run the
+GPU exactly as the benchmark does and are compared on sampled tokens, which
+the oracle evaluates one by one; routing and counts are compared in full.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+import mixture_experts_ffn_permute_gb300 as moe
+from mixture_experts_ffn_permute_gb300 import _build
+from parity import assert_bf16_close, assert_equal
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+    moe.load()
+
+
+def run_forward(shape, inp, ws=None, renorm=True):
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, renorm, shape.glu_interleave,
+                         shape.swiglu_clamp)
+    if ws is None:
+        ws = moe.alloc_workspace(p)
+    moe.clear_device_status(ws)
+    out = torch.full((shape.T, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty(shape.T, shape.k, dtype=torch.int32, device=DEV)
+    w = torch.empty(shape.T, shape.k, dtype=torch.float32, device=DEV)
+    tpe = torch.empty(shape.E, dtype=torch.int32, device=DEV)
+    moe.forward(p, inp["x"], inp["logits"], inp["w1"], inp["w2"], out, ws, idx, w, tpe)
+    status = moe.get_device_status(ws)
+    assert status == 0, moe.STATUS_NAMES[status]
+    return {"out": out, "topk_idx": idx, "topk_w": w, "tokens_per_expert": tpe, "ws": ws}
+
+
+def to_dev(inp):
+    return {k: v.to(DEV) for k, v in inp.items()}
+
+
+SMALL = [
+    mi.TINY,
+    mi.MoEShape("ragged", T=333, H=512, F=384, E=7, k=3),
+    mi.MoEShape("il32clamp", T=128, H=256, F=256, E=8, k=2, glu_interleave=32, swiglu_clamp=7.0),
+    mi.MoEShape("skew-small", T=512, H=256, F=256, E=64, k=8, zipf_s=1.1),
+    mi.MoEShape("t1", T=1, H=256, F=128, E=8, k=2),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+def test_forward_small(shape):
+    inp = mi.make_inputs(shape, seed=0)
+    ref = oracle.moe_forward(inp["x"], inp["logits"], inp["w1"], inp["w2"], shape.k,
+                             interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
+    res = run_forward(shape, to_dev(inp))
+    assert_equal(res["topk_idx"], ref["topk_idx"], "topk_idx")
+    assert_equal(res["tokens_per_expert"], ref["tokens_per_expert"], "tokens_per_expert")
+    np.testing.assert_allclose(res["topk_w"].cpu().numpy(), ref["topk_w"], rtol=3e-6, atol=1e-7)
+    assert_bf16_close(res["out"], ref["out"], f"out[{shape.name}]")
+
+
+def test_forward_unnormalised_weights():
+    shape = mi.TINY
+    inp = mi.make_inputs(shape, seed=2)
+    ref = oracle.moe_forward(inp["x"], inp["logits"], inp["w1"], inp["w2"], shape.k,
+                             renormalize=False)
+    res = run_forward(shape, to_dev(inp), renorm=False)
+    assert_bf16_close(res["out"], ref["out"], "out (full-softmax weights)")
+
+
+@pytest.mark.parametrize("T", [1, 8, 32])
+def test_forward_decode_full_dims(T):
+    shape = mi.DECODE.with_T(T)
+    inp = mi.make_inputs(shape, seed=0)
+    ref = oracle.moe_forward(inp["x"], inp["logits"], inp["w1"], inp["w2"], shape.k)
+    res = run_forward(shape, to_dev(inp))
+    assert_equal(res["topk_idx"], ref["topk_idx"], "topk_idx")
+    assert_bf16_close(res["out"], ref["out"], f"out[decode T={T}]")
+
+
+def test_forward_is_bitwise_deterministic_and_reuses_workspace():
+    shape = mi.MoEShape("det", T=300, H=512, F=256, E=16, k=4)
+    a = to_dev(mi.make_inputs(shape, seed=0))
+    b = dict(a)
+    b["logits"] = mi.make_logits(shape, seed=99).to(DEV)
+    r1 = run_forward(shape, a)
+    ws = r1["ws"]
+    r2 = run_forward(shape, b, ws=ws)      # different routing on the same workspace
+    r3 = run_forward(shape, a, ws=ws)
+    assert torch.equal(r1["out"].view(torch.int16), r3["out"].view(torch.int16))
+    fresh = run_forward(shape, b)
+    assert torch.equal(r2["out"].view(torch.int16), fresh["out"].view(torch.int16))
+    assert moe.last_launch_count() >= 5
+
+
+# ------------------------------------------------------------------ full size, sampled
+
+def sampled_check(shape, n_sample, seed=0):
+    torch.manual_seed(0)
+    inp = mi.make_inputs(shape, seed=seed, device=DEV)
+    res = run_forward(shape, inp)
+    logits_h = inp["logits"].cpu()
+    # routing of every token and the expert histogram: bit-exact
+    idx_ref, w_ref = oracle.route_topk(logits_h, shape.k)
+    assert_equal(res["topk_idx"], idx_ref, "topk_idx")
+    perm = oracle.permute(idx_ref, shape.E)
+    assert_equal(res["tokens_per_expert"], perm["tokens_per_expert"], "tokens_per_expert")
+    # outputs of sampled tokens, evaluated by the oracle one token set at a time
+    g = np.random.default_rng(1234)
+    toks = np.sort(g.choice(shape.T, size=min(n_sample, shape.T), replace=False))
+    used = sorted(set(idx_ref[toks].ravel().tolist()))
+    w1 = [None] * shape.E
+    w2 = [None] * shape.E
+    for e in used:
+        w1[e] = inp["w1"][e].cpu()
+        w2[e] = inp["w2"][e].cpu()
+    ti = torch.from_numpy(toks).to(DEV)
+    ref = oracle.moe_forward(inp["x"][ti].cpu(), logits_h[toks], w1, w2, shape.k)
+    assert_bf16_close(res["out"][ti], ref["out"], f"out[{shape.name}] sampled")
+    out = res["out"]
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.slow
+def test_forward_mixtral_full_size_sampled():
+    sampled_check(mi.MIXTRAL, 8)
+
+
+@pytest.mark.slow
+def test_forward_skewed_full_size_sampled():
+    sampled_check(mi.SKEWED, 4)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T", [128, 256])
+def test_forward_decode_full_size_sampled(T):
+    sampled_check(mi.DECODE.with_T(T), 16)
