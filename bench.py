@@ -49,11 +49,13 @@ WORKLOADS = {
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral")
     ap.add_argument("--T", type=int, default=0, help="override the token count")
+    ap.add_argument("--E", type=int, default=0, help="override the expert count (profiling)")
+    ap.add_argument("--k", type=int, default=0, help="override top-k (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
@@ -372,6 +374,10 @@ def bench_reference(args, shape, desc):
 def main(argv=None):
     args = parse_args(argv)
     shape, desc = WORKLOADS[args.workload]
+    if args.E or args.k:
+        import dataclasses
+        shape = dataclasses.replace(shape, E=args.E or shape.E, k=args.k or shape.k)
+        desc = desc + f" (E={shape.E}, k={shape.k})"
     if args.T:
         shape = shape.with_T(args.T)
         desc = desc + f" (T={args.T})"
