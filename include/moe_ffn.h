@@ -156,6 +156,39 @@ MOE_API int moe_forward(const moe_problem* p, const void* x, const float* logits
                         float* topk_w_out, int32_t* tokens_per_expert_out, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* Capacity, in int32 entries, of the fixed device scratch that
+ * moe_permute_noalloc uses: ceil(T / 64) * E + E + 1 must not exceed it. */
+#define MOE_NOALLOC_SCRATCH_INTS (1 << 18)
+
+/* moe_permute for callers that cannot allocate device memory or hand the
+ * library a workspace -- for example code that runs while a stream is being
+ * captured into a CUDA graph (cudaMalloc is not allowed there), or a host
+ * framework whose device memory all belongs to its own pool and which has
+ * no way to pass scratch through a plain C call.  It takes the same
+ * arguments as moe_permute minus the workspace and writes the same outputs.
+ * Its scratch (the per-chunk expert histograms and the m-tile prefix) lives
+ * in one fixed array of MOE_NOALLOC_SCRATCH_INTS int32 (1 MiB) that every GPU
+ * loading this library keeps until the process exits; nothing is allocated
+ * or freed, by this call or by anything it calls.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture on the device.
+ *   - Every call on a device shares the one array.  Calls whose work can
+ *     overlap on the GPU (different streams without ordering between them)
+ *     race on it and give wrong results; serialise them.  Each call
+ *     overwrites every scratch entry it reads, so stale contents from an
+ *     earlier call do no harm.
+ *   - Problems needing more scratch than the array holds are rejected with
+ *     MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - Index errors are handled as in moe_permute (bad routes are treated
+ *     as masked) but are not reported: there is no workspace status word.
+ * The source pages have no counterpart to this entry point; it exists only
+ * for callers without an allocator. */
+MOE_API int moe_permute_noalloc(const moe_problem* p, const int32_t* topk_idx, const void* x,
+                                void* x_perm, int32_t* row_id_map, int32_t* permuted_token,
+                                int32_t* tokens_per_expert, int32_t* expert_offsets,
+                                void* stream);
+
 /* Synchronises `stream`, returns the status the kernels recorded in `ws`
  * since the last moe_clear_device_status (MOE_OK if none). */
 MOE_API int moe_get_device_status(void* ws, void* stream);

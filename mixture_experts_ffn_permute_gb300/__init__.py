@@ -81,6 +81,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_stage_timing_end": ([ctypes.POINTER(ctypes.c_float), ci,
                                   ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)], ci),
         "moe_stage_name": ([ci], ctypes.c_char_p),
+        "moe_permute_noalloc": ([pp, vp, vp, vp, vp, vp, vp, vp, vp], ci),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -163,6 +164,16 @@ def permute(p: Problem, topk_idx, x, x_perm, row_id_map, permuted_token, tokens_
           _ptr(expert_offsets), _ptr(ws), ws.numel(), _stream(stream))
 
 
+def permute_noalloc(p: Problem, topk_idx, x, x_perm, row_id_map, permuted_token,
+                    tokens_per_expert, expert_offsets, stream=None) -> None:
+    """moe_permute without a workspace, for callers that cannot allocate device
+    memory (e.g. while a stream is being captured): the library uses its own
+    fixed 1 MiB device scratch.  Calls that may overlap on the GPU race."""
+    _call("moe_permute_noalloc", ctypes.byref(p), _ptr(topk_idx), _ptr(x), _ptr(x_perm),
+          _ptr(row_id_map), _ptr(permuted_token), _ptr(tokens_per_expert),
+          _ptr(expert_offsets), _stream(stream))
+
+
 def grouped_swiglu_mlp(p: Problem, x_perm, expert_offsets, w1, w2, y_perm, ws,
                        stream=None) -> None:
     _call("moe_grouped_swiglu_mlp", ctypes.byref(p), _ptr(x_perm), _ptr(expert_offsets),
@@ -219,4 +230,4 @@ class MoEFFN:
 __all__ = ["Problem", "MoEError", "MoEFFN", "load", "workspace_size", "alloc_workspace",
            "route_topk", "permute", "grouped_swiglu_mlp", "unpermute_combine", "forward",
            "get_device_status", "clear_device_status", "last_launch_count", "LIB_PATH",
-           "stage_timing_begin", "stage_timing_end"]
+           "stage_timing_begin", "stage_timing_end", "permute_noalloc"]
