@@ -57,6 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--E", type=int, default=0, help="override the expert count (profiling)")
     ap.add_argument("--k", type=int, default=0, help="override top-k (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fusion", type=int, default=0,
+                    help="moe_problem.fusion bits: 1 = TMA-gather A rows, 2 = combine in GEMM2")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args(argv)
@@ -184,11 +186,16 @@ def oracle_sample(shape, inp_host, n_tokens: int):
 
 
 def cpu_baseline(shape, inp_host, target_s: float):
+    """Time the oracle on the first n tokens, n grown until the run takes about
+    target_s seconds of wall time (capped at the whole batch)."""
     import oracle
     oracle.build()
-    dt1, _ = oracle_sample(shape, inp_host, 1)
-    n = int(max(1, min(shape.T, math.floor(target_s / max(dt1, 1e-6)))))
-    dt, flops = oracle_sample(shape, inp_host, n)
+    n = min(shape.T, 16)
+    while True:
+        dt, flops = oracle_sample(shape, inp_host, n)
+        if dt >= target_s / 3 or n >= shape.T:
+            break
+        n = int(min(shape.T, max(2 * n, n * 0.8 * target_s / max(dt, 1e-6))))
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"first {n} of {shape.T} tokens of the same workload (fp64 oracle, "
@@ -215,7 +222,7 @@ def bench_ours(args, shape, desc):
     x = mi.make_x(shape, rank, dev)
     logits = mi.make_logits(shape, rank, dev)
     p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True,
-                         shape.glu_interleave, shape.swiglu_clamp)
+                         shape.glu_interleave, shape.swiglu_clamp, args.fusion)
     ws = moe.alloc_workspace(p, dev)
     out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -296,7 +303,7 @@ def bench_ours(args, shape, desc):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": desc, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
-                   "k": shape.k, "l2": "inputs larger than L2 (weights %.2f GB), no flush"
+                   "k": shape.k, "fusion": args.fusion, "l2": "inputs larger than L2 (weights %.2f GB), no flush"
                    % (2 * 3 * shape.E * shape.F * shape.H / 1e9)},
         "roofline": {"kernel": "grouped_gemm_kernel<SwiGLU> (GEMM1)", "bound": "tensor",
                      "achieved": ach, "peak": peaks[peak_key], "unit": "TFLOP/s",

@@ -78,7 +78,19 @@ typedef struct moe_problem {
      means no clamp. */
   float swiglu_clamp;
   int32_t precision; /* moe_precision */
+  /* Fusion options of moe_forward (bit mask; 0 = the default, fastest
+     measured form: permuted copy of x and a separate combine kernel):
+       MOE_FUSE_GATHER_A  GEMM1 gathers its A rows straight from x with TMA
+                          tile::gather4, so no permuted copy of x is written;
+       MOE_FUSE_COMBINE   the weighted top-k reduction runs in GEMM2's
+                          epilogue (bf16 partials + per-token arrival counters,
+                          slot-ordered sum by the last arrival).
+     Both give results within the same tolerance of the exact layer. */
+  int32_t fusion;
 } moe_problem;
+
+#define MOE_FUSE_GATHER_A 1
+#define MOE_FUSE_COMBINE 2
 
 /* Limits checked by every entry point. */
 #define MOE_MAX_EXPERTS 1024

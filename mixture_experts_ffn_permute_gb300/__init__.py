@@ -26,6 +26,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoeffn.so")
 
 MOE_OK = 0
+FUSE_GATHER_A = 1   # GEMM1 gathers A rows from x with TMA gather4
+FUSE_COMBINE = 2    # weighted top-k reduction in GEMM2's epilogue
 STATUS_NAMES = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
     3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",
@@ -44,12 +46,14 @@ class Problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("F", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("glu_interleave", ctypes.c_int32),
-                ("swiglu_clamp", ctypes.c_float), ("precision", ctypes.c_int32)]
+                ("swiglu_clamp", ctypes.c_float), ("precision", ctypes.c_int32),
+                ("fusion", ctypes.c_int32)]
 
     @classmethod
-    def make(cls, T, H, F, E, k, renormalize=True, glu_interleave=0, swiglu_clamp=0.0):
+    def make(cls, T, H, F, E, k, renormalize=True, glu_interleave=0, swiglu_clamp=0.0,
+             fusion=0):
         return cls(int(T), int(H), int(F), int(E), int(k), int(bool(renormalize)),
-                   int(glu_interleave), float(swiglu_clamp), 0)
+                   int(glu_interleave), float(swiglu_clamp), 0, int(fusion))
 
 
 _lib = None

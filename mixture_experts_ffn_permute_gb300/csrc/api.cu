@@ -32,8 +32,8 @@ thread_local int g_launches = 0;
 // Stage names of moe_forward, in launch order.
 constexpr int kNumStages = 8;
 const char* const kStageNames[kNumStages] = {"route_topk", "chunk_histogram", "scan",
-                                             "scatter", "gather_rows", "gemm1_swiglu",
-                                             "gemm2", "combine"};
+                                             "scatter",    "gather_rows",     "gemm1_swiglu",
+                                             "gemm2",      "combine"};
 
 // Event ring for moe_stage_timing_begin/end (one row of kNumStages+1 events
 // per recorded call).
@@ -55,7 +55,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 // Byte offsets of every scratch region inside the caller's workspace.
 struct Layout {
   size_t status, chunk_counts, tokens_per_expert, expert_offsets, mtile_prefix, topk_idx, topk_w,
-      row_id_map, permuted_token, x_perm, h, y, total;
+      row_id_map, permuted_token, counters, x_perm, h, y, total;
 };
 
 Layout layout_of(const moe_problem& p) {
@@ -77,6 +77,7 @@ Layout layout_of(const moe_problem& p) {
   L.topk_w = take(sizeof(float) * R);
   L.row_id_map = take(sizeof(int32_t) * R);
   L.permuted_token = take(sizeof(int32_t) * R);
+  L.counters = take(sizeof(int32_t) * T * (p.H > 0 ? (static_cast<size_t>(p.H) + kBN - 1) / kBN : 0));
   L.x_perm = take(2 * R * static_cast<size_t>(p.H));
   L.h = take(2 * R * static_cast<size_t>(p.F));
   L.y = take(2 * R * static_cast<size_t>(p.H));
@@ -104,6 +105,7 @@ int check_full(const moe_problem* p) {
   if (rc != MOE_OK) return rc;
   if (p->H <= 0 || p->F <= 0) return MOE_ERR_INVALID_ARG;
   if (p->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
   if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int I = p->glu_interleave;
@@ -141,10 +143,21 @@ float clamp_of(const moe_problem* p) {
 }
 
 // GEMM1 (x_perm -> h with SwiGLU) then GEMM2 (h -> y).
+// Fused form (moe_forward): fused != nullptr gathers GEMM1's A rows from x by
+// permuted_token and runs the weighted combine in GEMM2's epilogue into out.
+struct FusedIO {
+  bool gather, combine;
+  const int32_t* permuted_token;
+  const int32_t* row_id_map;
+  const float* topk_w;
+  int32_t* counters;
+  void* out;
+};
+
 int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
             const int32_t* mtp, const void* w1, const void* w2, void* h, void* y,
             uint32_t* status, cudaStream_t s, int& launches, StageTimer* tm = nullptr,
-            int call = 0, int mark = 0) {
+            int call = 0, int mark = 0, const FusedIO* fused = nullptr) {
   const int R = p->T * p->k;
   GroupedGemmArgs g1{};
   g1.epi = Epi::kSwiGLU;
@@ -164,6 +177,10 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
   g1.interleave = p->glu_interleave;
   g1.clamp = clamp_of(p);
   g1.status = status;
+  if (fused && fused->gather) {
+    g1.permuted_token = fused->permuted_token;
+    g1.x_rows = p->T;
+  }
   MOE_LAUNCH(launch_grouped_gemm(g1, s));
   if (tm) tm->mark(call, mark, s);
   GroupedGemmArgs g2{};
@@ -182,6 +199,16 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
   g2.out_rows = R;
   g2.F = p->F;
   g2.status = status;
+  if (fused && fused->combine) {
+    g2.epi = Epi::kCombine;
+    g2.out = fused->out;
+    g2.partials = y;
+    g2.permuted_token = fused->permuted_token;
+    g2.row_id_map = fused->row_id_map;
+    g2.topk_w = fused->topk_w;
+    g2.counters = fused->counters;
+    g2.k = p->k;
+  }
   MOE_LAUNCH(launch_grouped_gemm(g2, s));
   if (tm) tm->mark(call, mark + 1, s);
   return MOE_OK;
@@ -191,12 +218,14 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
 int run_permute(const moe_problem* p, const int32_t* topk_idx, int32_t* row_id_map,
                 int32_t* permuted_token, int32_t* tokens_per_expert, int32_t* expert_offsets,
                 int32_t* mtp, void* ws, const Layout& L, cudaStream_t s, int& launches,
-                StageTimer* tm = nullptr, int call = 0, int mark = 0) {
+                StageTimer* tm = nullptr, int call = 0, int mark = 0,
+                int32_t* counters = nullptr, int ncnt = 0) {
   const int R = p->T * p->k;
   const int nchunks = ceil_div(p->T, kChunkTokens);
   uint32_t* status = at<uint32_t>(ws, L.status);
   int32_t* cc = at<int32_t>(ws, L.chunk_counts);
-  if (nchunks > 0) MOE_LAUNCH(launch_chunk_histogram(topk_idx, p->T, p->E, p->k, cc, status, s));
+  if (nchunks > 0)
+    MOE_LAUNCH(launch_chunk_histogram(topk_idx, p->T, p->E, p->k, cc, status, s, counters, ncnt));
   if (tm) tm->mark(call, mark, s);
   MOE_LAUNCH(launch_scan(cc, nchunks, p->E, R, tokens_per_expert, expert_offsets, mtp,
                          permuted_token, s));
@@ -368,19 +397,25 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   void* x_perm = at<void>(ws, L.x_perm);
   void* h = at<void>(ws, L.h);
   void* y = at<void>(ws, L.y);
+  int32_t* counters = at<int32_t>(ws, L.counters);
+  const bool fuse_gather = (p->fusion & MOE_FUSE_GATHER_A) != 0;
+  const bool fuse_combine = (p->fusion & MOE_FUSE_COMBINE) != 0;
 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
   tm.mark(call, 0, s);
   MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
   tm.mark(call, 1, s);
-  rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2);
+  rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2,
+                   fuse_combine ? counters : nullptr, p->H / kBN);
   if (rc != MOE_OK) return rc;
-  MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
+  if (!fuse_gather) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   tm.mark(call, 5, s);
-  rc = run_mlp(p, x_perm, off, mtp, w1, w2, h, y, status, s, launches, &tm, call, 6);
+  const FusedIO fused{fuse_gather, fuse_combine, ptok, rmap, wts, counters, out};
+  rc = run_mlp(p, fuse_gather ? x : x_perm, off, mtp, w1, w2, h, y, status, s, launches, &tm,
+               call, 6, &fused);
   if (rc != MOE_OK) return rc;
-  MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
+  if (!fuse_combine) MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
   tm.mark(call, 8, s);
   g_launches = launches;
   return MOE_OK;

@@ -4,13 +4,23 @@
 // enumerated from the device-side m-tile prefix, so ragged and empty experts
 // need no host round trip and no padding of the permuted rows.  Per tile
 //   D[128 x 256] = A[rows of expert e, K] * B[256 weight rows of e, K]^T
-// accumulates in fp32 in TMEM; the epilogue applies either SwiGLU (GEMM1:
-// gate and up halves of the tile -> 128 outputs, "Support GEMM + Swiglu fused
-// MLP") or a plain bf16 store (GEMM2; the weighted top-k reduction of the
-// "[SM90] Add W4A8 MegaMoE support" description runs in the combine step).
+// accumulates in fp32 in TMEM.  Epilogues:
+//   kSwiGLU   GEMM1: gate and up halves of the tile -> 128 SwiGLU outputs
+//             ("Support GEMM + Swiglu fused MLP")
+//   kPlain    GEMM2: unweighted bf16 rows y (the stand-alone MLP entry point)
+//   kCombine  GEMM2 fused with the weighted top-k reduction of the
+//             "[SM90] Add W4A8 MegaMoE support" description: each row's
+//             w * y goes to a bf16 partial buffer, a per-(token, n-tile)
+//             counter counts arrivals, and the last arriving route sums the
+//             token's partials in slot order j = 0..k-1 (fixed order, so the
+//             result does not depend on which route finished last).
+// With kGatherA the A rows are gathered straight from the token matrix x by
+// permuted_token with TMA tile::gather4 (4 rows per copy), so the permuted
+// copy of x never exists in HBM.
 //
 // Warp roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer: A tile 128x64 and two B boxes 128x64 per stage
+//   warp 0      TMA producer: A tile 128x64 (one 128-row box, or 32 four-row
+//               gathers issued by the 32 lanes) and two B boxes 128x64 per stage
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2..5  epilogue: tcgen05.ld -> math -> global stores
 // A 4-stage smem ring (full/empty mbarriers) feeds the MMA; two TMEM
@@ -51,6 +61,13 @@ struct KParams {
   int E, K, n_tiles, b_rows_per_expert, ldo_vec, out_rows, F, interleave, ieff;
   float clamp;
   uint32_t* status;
+  // gathered A rows / fused combine
+  const int32_t* permuted_token;  // [R] token of each permuted row
+  const int32_t* row_id_map;      // [T, k]
+  const float* topk_w;            // [T, k]
+  int32_t* counters;              // [T, n_tiles], zero at launch
+  uint4* partials;                // [R, ldo] bf16 weighted rows
+  int k;
 };
 
 struct Tile {
@@ -85,7 +102,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <Epi kEpi>
+static_assert(kBN / 8 == 32, "the combine reduction maps one 16-byte vector to each lane");
+
+__device__ __forceinline__ void add_bf16x8(const uint4& v, float (&acc)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    acc[2 * i] += f.x;
+    acc[2 * i + 1] += f.y;
+  }
+}
+
+template <Epi kEpi, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, const KParams p) {
@@ -137,48 +166,81 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      const uint64_t pol_a = policy_evict_last();
-      const uint64_t pol_b = policy_evict_normal();
-      int stage = 0;
-      uint32_t phase = 0;
-      long issued = 0;
-      for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, s_mtp, p.E, p.n_tiles);
-        const int a_row = s_off[t.e] + t.m * kBM;
-        int b_row0, b_row1;
-        const int b_base = t.e * p.b_rows_per_expert;
-        if (kEpi == Epi::kSwiGLU) {
-          const int f0 = t.n * (kBN / 2);
-          if (p.interleave == 0) {
-            b_row0 = f0;
-            b_row1 = p.F + f0;
-          } else if (p.ieff == 128) {  // interleave a multiple of 128
-            b_row0 = (f0 / p.interleave) * 2 * p.interleave + f0 % p.interleave;
-            b_row1 = b_row0 + p.interleave;
-          } else {  // interleave 32 or 64: the 256 rows from 2*f0 hold 128 gate/up pairs
-            b_row0 = 2 * f0;
-            b_row1 = 2 * f0 + static_cast<int>(kBBoxRows);
-          }
-        } else {
-          b_row0 = t.n * kBN;
-          b_row1 = b_row0 + static_cast<int>(kBBoxRows);
+    // Lane 0 drives the ring (waits, expect-tx, B boxes, plain A box); with a
+    // gathered A every lane also issues one 4-row gather per stage: rows
+    // 4*lane .. 4*lane+3 of the tile.
+    const uint64_t pol_a = policy_evict_last();
+    const uint64_t pol_b = policy_evict_normal();
+    int stage = 0;
+    uint32_t phase = 0;
+    long issued = 0;
+    bool go = true;
+    for (int tile = blockIdx.x; tile < total_tiles && go; tile += gridDim.x) {
+      go = __shfl_sync(0xffffffffu, lane == 0 ? (*abort_flag == 0) : 0, 0) != 0;
+      if (!go) break;
+      const Tile t = decode_tile(tile, s_mtp, p.E, p.n_tiles);
+      const int seg_start = s_off[t.e];
+      const int seg_rows = s_off[t.e + 1] - seg_start;
+      const int a_row = seg_start + t.m * kBM;
+      int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
+      if (kGatherA) {
+        // token rows of this lane's four tile rows; rows past the segment
+        // read token 0 (their results are never stored)
+        const int base = t.m * kBM + 4 * lane;
+        int tk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rr = base + i;
+          const int v = rr < seg_rows ? __ldg(p.permuted_token + seg_start + rr) : 0;
+          tk[i] = v < 0 ? 0 : v;
         }
-        b_row0 += b_base;
-        b_row1 += b_base;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { *abort_flag = 1; break; }
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          const int kx = kb * kBK;
-          tma_load_2d(sA + stage * kABytes, &map_a, kx, a_row, &full[stage], pol_a);
+        g0 = tk[0]; g1 = tk[1]; g2 = tk[2]; g3 = tk[3];
+      }
+      int b_row0, b_row1;
+      const int b_base = t.e * p.b_rows_per_expert;
+      if (kEpi == Epi::kSwiGLU) {
+        const int f0 = t.n * (kBN / 2);
+        if (p.interleave == 0) {
+          b_row0 = f0;
+          b_row1 = p.F + f0;
+        } else if (p.ieff == 128) {  // interleave a multiple of 128
+          b_row0 = (f0 / p.interleave) * 2 * p.interleave + f0 % p.interleave;
+          b_row1 = b_row0 + p.interleave;
+        } else {  // interleave 32 or 64: the 256 rows from 2*f0 hold 128 gate/up pairs
+          b_row0 = 2 * f0;
+          b_row1 = 2 * f0 + static_cast<int>(kBBoxRows);
+        }
+      } else {
+        b_row0 = t.n * kBN;
+        b_row1 = b_row0 + static_cast<int>(kBBoxRows);
+      }
+      b_row0 += b_base;
+      b_row1 += b_base;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(&empty[stage], phase ^ 1, p.status) ? 1 : 0;
+          if (ok) mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          else *abort_flag = 1;
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { go = false; break; }
+        const int kx = kb * kBK;
+        if (kGatherA)
+          tma_gather4(sA + stage * kABytes + lane * 512, &map_a, kx, g0, g1, g2, g3, &full[stage],
+                      pol_a);
+        if (lane == 0) {
+          if (!kGatherA) tma_load_2d(sA + stage * kABytes, &map_a, kx, a_row, &full[stage], pol_a);
           uint8_t* b_dst = sB + stage * kBBytes;
           tma_load_2d(b_dst, &map_b, kx, b_row0, &full[stage], pol_b);
           tma_load_2d(b_dst + kBBytes / 2, &map_b, kx, b_row1, &full[stage], pol_b);
-          ++issued;
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
+        ++issued;
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
-      // Leave no bulk copy in flight: wait for the last fill of every stage.
+    }
+    // Leave no bulk copy in flight: wait for the last fill of every stage.
+    if (lane == 0) {
       for (int i = 1; i <= kStages && i <= issued; ++i) {
         int s = stage - i;
         uint32_t ph = phase;
@@ -266,7 +328,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                                           packed[4 * v + 3]);
           }
         }
-      } else {
+      } else if (kEpi == Epi::kPlain) {
         uint4* dst = p.out + out_row * p.ldo_vec + (t.n * kBN) / 8;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
@@ -283,6 +345,69 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                   pack_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
           }
         }
+      } else {
+        // kCombine: partial = w * y (bf16) for this route; last arrival sums.
+        int tok = 0, nvalid = 0;
+        float w = 0.f;
+        if (row_ok) {
+          tok = __ldg(p.permuted_token + out_row);
+          const int32_t* rm = p.row_id_map + static_cast<long>(tok) * p.k;
+          int j = 0;
+          for (int jj = 0; jj < p.k; ++jj) {
+            const int v = __ldg(rm + jj);
+            nvalid += v >= 0;
+            if (v == out_row) j = jj;
+          }
+          w = __ldg(p.topk_w + static_cast<long>(tok) * p.k + j);
+        }
+        const int col_vec = (t.n * kBN) / 8;
+        uint4* dst = (nvalid == 1 ? p.out + static_cast<long>(tok) * p.ldo_vec
+                                  : p.partials + out_row * p.ldo_vec) + col_vec;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld_32x32b_x32(t_lane + c * 32, a);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[c * 4 + v] = make_uint4(
+                  pack_bf16(w * __uint_as_float(a[8 * v + 0]), w * __uint_as_float(a[8 * v + 1])),
+                  pack_bf16(w * __uint_as_float(a[8 * v + 2]), w * __uint_as_float(a[8 * v + 3])),
+                  pack_bf16(w * __uint_as_float(a[8 * v + 4]), w * __uint_as_float(a[8 * v + 5])),
+                  pack_bf16(w * __uint_as_float(a[8 * v + 6]), w * __uint_as_float(a[8 * v + 7])));
+          }
+        }
+        // The accumulator is no longer needed: release it before the reduction.
+        tc_fence_before();
+        mbar_arrive(&tempty[buf]);
+        // Arrival count per (token, n-tile); the last arriving route's warp
+        // reduces that token's partials, one 16-byte column vector per lane.
+        bool last = false;
+        if (row_ok && nvalid > 1) {
+          __threadfence();
+          const int prev = atomicAdd(p.counters + static_cast<long>(tok) * p.n_tiles + t.n, 1);
+          last = prev == nvalid - 1;
+        }
+        __threadfence();
+        uint32_t todo = __ballot_sync(0xffffffffu, last);
+        __syncwarp();
+        while (todo) {
+          const int src = __ffs(todo) - 1;
+          todo &= todo - 1;
+          const int tk = __shfl_sync(0xffffffffu, tok, src);
+          const int32_t* rm = p.row_id_map + static_cast<long>(tk) * p.k;
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int jj = 0; jj < p.k; ++jj) {  // slot order: deterministic
+            const int r = __ldg(rm + jj);
+            if (r < 0) continue;
+            add_bf16x8(__ldcg(p.partials + static_cast<long>(r) * p.ldo_vec + col_vec + lane), acc);
+          }
+          p.out[static_cast<long>(tk) * p.ldo_vec + col_vec + lane] =
+              make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
+                         pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
+        }
+        continue;  // tempty already released
       }
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
@@ -343,15 +468,14 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <Epi kEpi>
-cudaError_t launch_impl(const GroupedGemmArgs& g, const CUtensorMap& ma, const CUtensorMap& mb,
-                        const KParams& kp, int grid, cudaStream_t s) {
-  (void)g;
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kEpi>,
+template <Epi kEpi, bool kGatherA>
+cudaError_t launch_impl(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
+                        int grid, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kEpi, kGatherA>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
   if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<kEpi><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, kp);
+  grouped_gemm_kernel<kEpi, kGatherA><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, kp);
   return cudaGetLastError();
 }
 
@@ -360,7 +484,10 @@ cudaError_t launch_impl(const GroupedGemmArgs& g, const CUtensorMap& ma, const C
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s) {
   if (g.a_rows == 0) return cudaSuccess;
   CUtensorMap ma, mb;
-  if (!make_map_2d(&ma, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K), kBM))
+  const bool gather = g.permuted_token != nullptr && g.epi == Epi::kSwiGLU;
+  // gathered A: a map over the token matrix x [x_rows, K] with one-row boxes
+  if (!make_map_2d(&ma, g.a, static_cast<uint64_t>(gather ? g.x_rows : g.a_rows),
+                   static_cast<uint64_t>(g.K), gather ? 1u : static_cast<uint32_t>(kBM)))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&mb, g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
                    static_cast<uint64_t>(g.K), kBBoxRows))
@@ -380,12 +507,26 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s) {
   kp.ieff = (g.interleave == 0 || g.interleave % 128 == 0) ? 128 : g.interleave;
   kp.clamp = g.clamp;
   kp.status = g.status;
+  kp.permuted_token = g.permuted_token;
+  kp.row_id_map = g.row_id_map;
+  kp.topk_w = g.topk_w;
+  kp.counters = g.counters;
+  kp.partials = static_cast<uint4*>(g.partials);
+  kp.k = g.k;
   // Upper bound on tiles: every expert may add one ragged m-tile.
   const long max_mtiles = ceil_div(g.a_rows, kBM) + std::min(g.E, g.a_rows);
   const long max_tiles = max_mtiles * g.n_tiles;
   const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
-  if (g.epi == Epi::kSwiGLU) return launch_impl<Epi::kSwiGLU>(g, ma, mb, kp, grid, s);
-  return launch_impl<Epi::kPlain>(g, ma, mb, kp, grid, s);
+  switch (g.epi) {
+    case Epi::kSwiGLU:
+      return gather ? launch_impl<Epi::kSwiGLU, true>(ma, mb, kp, grid, s)
+                    : launch_impl<Epi::kSwiGLU, false>(ma, mb, kp, grid, s);
+    case Epi::kPlain:
+      return launch_impl<Epi::kPlain, false>(ma, mb, kp, grid, s);
+    case Epi::kCombine:
+      return launch_impl<Epi::kCombine, false>(ma, mb, kp, grid, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

@@ -1,0 +1,334 @@
+// Decode-sized grouped GEMMs: the weight rows are the MMA's M side and the
+// few tokens of each expert its N side ("swap-AB").
+//
+// At decode sizes an expert sees a handful of tokens, so a 128-token-row tile
+// would be almost empty and every CTA would pull a 128-row activation tile
+// from L2 for each 64-deep K step while reading far fewer weight bytes from
+// HBM.  Here a tile is 128 weight rows x kN (= 32) token rows:
+//   D[128 x kN] = W[128 weight rows of e, K] * X[kN token rows of e, K]^T
+// so each K step moves 16 KB of weights and 4 KB of activations, and the
+// layer streams its weights once at HBM speed.  The tile count is
+// (expert, weight-row tile, token tile), token tiles fastest so that CTAs
+// sharing a weight tile run together and the second read hits L2.
+//
+// Epilogues:
+//   GEMM1 (kSwiGLU): the 128 weight rows are 64 gate rows and the matching
+//     64 up rows; the accumulator goes through shared memory so one thread
+//     sees both halves, and h[token row][f] is stored as bf16.
+//   GEMM2 (kPlain):  y[token row][feature] bf16, 32 consecutive features per
+//     warp store.
+// Pipeline, TMEM double buffering and bounded waits are as in
+// grouped_gemm.cu; the per-expert tile prefix is computed by every CTA from
+// expert_offsets at start-up.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);  // grouped_gemm.cu
+
+namespace {
+
+constexpr int kN = 32;                                 // token rows per tile
+constexpr int kM = 128;                                // weight rows per tile
+constexpr int kStagesS = 8;
+constexpr int kThreadsS = 192;
+constexpr uint32_t kWBytes = kM * kBK * 2;             // 16 KB
+constexpr uint32_t kXBytes = kN * kBK * 2;             // 4 KB
+constexpr uint32_t kStageBytesS = kWBytes + kXBytes;   // 20 KB
+constexpr uint32_t kTmemColsS = 64;                    // two kN-column accumulators
+constexpr uint32_t kIdescS = idesc_bf16_f32(kM, kN);
+constexpr int kMaxES = 1024;
+constexpr int kDPitch = kN + 1;                        // padded fp32 row of the exchange tile
+constexpr size_t kSmemBytesS = 1024 + kStagesS * kStageBytesS + 256 +
+                               3 * (kMaxES + 1) * sizeof(int32_t) +
+                               kM * kDPitch * sizeof(float);
+
+struct SParams {
+  const int32_t* expert_offsets;
+  uint16_t* out;               // bf16 [rows, ldo]
+  int E, K, w_tiles, w_rows_per_expert, ldo, F, interleave;
+  float clamp;
+  uint32_t* status;
+};
+
+struct STile {
+  int e, m, n;  // expert, weight-row tile, token tile
+};
+
+__device__ __forceinline__ STile decode_stile(int tile, const int32_t* tp, const int32_t* ntk,
+                                              int E, int w_tiles) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tp[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  STile t;
+  t.e = lo;
+  const int local = tile - tp[lo];
+  const int nt = ntk[lo];
+  t.m = local / nt;
+  t.n = local - t.m * nt;
+  return t;
+}
+
+__device__ __forceinline__ float silu_s(float z) { return z / (1.0f + expf(-z)); }
+
+template <Epi kEpi>
+__global__ void __launch_bounds__(kThreadsS, 1)
+grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
+                         const __grid_constant__ CUtensorMap map_x, const SParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sW = smem;
+  uint8_t* sX = smem + kStagesS * kWBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sX + kStagesS * kXBytes);
+  uint64_t* empty = full + kStagesS;
+  uint64_t* tfull = empty + kStagesS;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStagesS * kStageBytesS + 256);
+  int32_t* s_tp = s_off + (kMaxES + 1);   // tile prefix per expert
+  int32_t* s_ntk = s_tp + (kMaxES + 1);   // token tiles per expert
+  float* sD = reinterpret_cast<float*>(s_ntk + (kMaxES + 1));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= p.E; i += kThreadsS) s_off[i] = p.expert_offsets[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&map_w);
+    prefetch_tensormap(&map_x);
+  }
+  if (warp == 1) tmem_alloc<kTmemColsS>(tmem_slot);
+  __syncthreads();
+  // tile prefix: expert e owns w_tiles * ceil(rows_e / kN) tiles
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < p.E; ++e) {
+      const int rows = s_off[e + 1] - s_off[e];
+      const int nt = rows > 0 ? (rows + kN - 1) / kN : 0;
+      s_ntk[e] = nt;
+      s_tp[e] = acc;
+      acc += nt * p.w_tiles;
+    }
+    s_tp[p.E] = acc;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = s_tp[p.E];
+  const int num_kb = p.K / kBK;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_normal();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+        const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
+        const int x_row = s_off[t.e] + t.n * kN;
+        int w_row0, w_row1;
+        if (kEpi == Epi::kSwiGLU) {
+          const int f0 = t.m * (kM / 2);
+          if (p.interleave == 32) {
+            w_row0 = 2 * f0;
+            w_row1 = 2 * f0 + kM / 2;
+          } else if (p.interleave == 0) {
+            w_row0 = f0;
+            w_row1 = p.F + f0;
+          } else {  // 64 or a multiple of 128: 64 whole gate rows, then 64 up rows
+            w_row0 = (f0 / p.interleave) * 2 * p.interleave + f0 % p.interleave;
+            w_row1 = w_row0 + p.interleave;
+          }
+        } else {
+          w_row0 = t.m * kM;
+          w_row1 = w_row0 + kM / 2;
+        }
+        w_row0 += t.e * p.w_rows_per_expert;
+        w_row1 += t.e * p.w_rows_per_expert;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { *abort_flag = 1; break; }
+          mbar_arrive_expect_tx(&full[stage], kStageBytesS);
+          const int kx = kb * kBK;
+          uint8_t* w_dst = sW + stage * kWBytes;
+          tma_load_2d(w_dst, &map_w, kx, w_row0, &full[stage], pol_w);
+          tma_load_2d(w_dst + kWBytes / 2, &map_w, kx, w_row1, &full[stage], pol_w);
+          tma_load_2d(sX + stage * kXBytes, &map_x, kx, x_row, &full[stage], pol_x);
+          ++issued;
+          if (++stage == kStagesS) { stage = 0; phase ^= 1; }
+        }
+      }
+      for (int i = 1; i <= kStagesS && i <= issued; ++i) {
+        int s = stage - i;
+        uint32_t ph = phase;
+        if (s < 0) { s += kStagesS; ph ^= 1; }
+        mbar_wait(&full[s], ph, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t tph = (local >> 1) & 1;
+        if (!mbar_wait(&tempty[buf], tph ^ 1, p.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kN;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t w_desc = sw128_kmajor_desc(smem_u32(sW + stage * kWBytes));
+          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + stage * kXBytes));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, kIdescS, (kb | kk) != 0);
+          mma_commit(&empty[stage]);
+          if (++stage == kStagesS) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) { *abort_flag = 1; break; }
+        mma_commit(&tfull[buf]);
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, p.status);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int et = threadIdx.x - 64;  // 0..127
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t tph = (local >> 1) & 1;
+      if (!mbar_wait(&tfull[buf], tph, p.status)) { *abort_flag = 1; break; }
+      tc_fence_after();
+      const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
+      const int seg_rows = s_off[t.e + 1] - s_off[t.e];
+      const int tok0 = t.n * kN;  // first token row of the tile inside the expert
+      const long row0 = static_cast<long>(s_off[t.e]) + tok0;
+      uint32_t a[32];
+      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kN, a);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+      const int wrow = quad * 32 + lane;  // weight row inside the tile
+      if (kEpi == Epi::kPlain) {
+        const int feat = t.m * kM + wrow;
+#pragma unroll
+        for (int n = 0; n < kN; ++n) {
+          if (tok0 + n < seg_rows) {
+            const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(a[n]));
+            p.out[(row0 + n) * p.ldo + feat] = *reinterpret_cast<const uint16_t*>(&v);
+          }
+        }
+      } else {
+        // exchange: gate and up rows of one output column live in different warps
+#pragma unroll
+        for (int n = 0; n < kN; ++n) sD[wrow * kDPitch + n] = __uint_as_float(a[n]);
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const int ie = (p.interleave == 32) ? 32 : 64;
+        const int fl = et & 63;                    // output column inside the tile
+        const int grow = (fl / ie) * 2 * ie + fl % ie;
+        const int urow = grow + ie;
+        const bool clamp = p.clamp > 0.f && isfinite(p.clamp);
+        const int f = t.m * (kM / 2) + fl;
+#pragma unroll 4
+        for (int n = et >> 6; n < kN; n += 2) {
+          if (tok0 + n < seg_rows) {
+            float g = sD[grow * kDPitch + n], u = sD[urow * kDPitch + n];
+            if (clamp) {
+              g = fminf(g, p.clamp);
+              u = fminf(fmaxf(u, -p.clamp), p.clamp);
+            }
+            const __nv_bfloat16 v = __float2bfloat16_rn(silu_s(g) * u);
+            p.out[(row0 + n) * p.ldo + f] = *reinterpret_cast<const uint16_t*>(&v);
+          }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<kTmemColsS>(tmem_base);
+  }
+}
+
+template <Epi kEpi>
+cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx, const SParams& sp,
+                             int grid, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_swap_kernel<kEpi>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytesS));
+  if (err != cudaSuccess) return err;
+  grouped_gemm_swap_kernel<kEpi><<<grid, kThreadsS, kSmemBytesS, s>>>(mw, mx, sp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s) {
+  if (g.a_rows == 0) return cudaSuccess;
+  if (g.E > kMaxES) return cudaErrorInvalidValue;
+  CUtensorMap mw, mx;
+  // weights: 64-row boxes; tokens: kN-row boxes
+  if (!make_map_2d(&mw, g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
+                   static_cast<uint64_t>(g.K), kM / 2))
+    return cudaErrorInvalidValue;
+  if (!make_map_2d(&mx, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K), kN))
+    return cudaErrorInvalidValue;
+  SParams sp;
+  sp.expert_offsets = g.expert_offsets;
+  sp.out = static_cast<uint16_t*>(g.out);
+  sp.E = g.E;
+  sp.K = g.K;
+  sp.w_rows_per_expert = g.b_rows_per_expert;
+  sp.ldo = g.ldo;
+  sp.F = g.F;
+  sp.interleave = g.interleave;
+  sp.clamp = g.clamp;
+  sp.status = g.status;
+  sp.w_tiles = (g.epi == Epi::kSwiGLU) ? g.F / (kM / 2) : g.ldo / kM;
+  // every expert may add one ragged token tile
+  const long max_tiles = (static_cast<long>(ceil_div(g.a_rows, kN)) + std::min(g.E, g.a_rows)) *
+                         sp.w_tiles;
+  const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
+  if (g.epi == Epi::kSwiGLU) return launch_swap_impl<Epi::kSwiGLU>(mw, mx, sp, grid, s);
+  if (g.epi == Epi::kPlain) return launch_swap_impl<Epi::kPlain>(mw, mx, sp, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -26,8 +26,12 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
                               int32_t* topk_idx, float* topk_w, cudaStream_t s);
 
 // Step 2a: per-chunk expert histogram of topk_idx (also validates indices).
+// When `counters` is not NULL the kernel also zeroes counters[t * ncnt ..
+// (t+1) * ncnt) for the tokens of its chunk (the fused combine's arrival
+// counters).
 cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int T, int E, int k,
-                                   int32_t* chunk_counts, uint32_t* status, cudaStream_t s);
+                                   int32_t* chunk_counts, uint32_t* status, cudaStream_t s,
+                                   int32_t* counters = nullptr, int ncnt = 0);
 
 // Step 2b: turn chunk histograms into per-(chunk, expert) row bases and
 // produce tokens_per_expert, expert_offsets, the m-tile prefix and the
@@ -55,7 +59,7 @@ cudaError_t launch_combine(const void* y, const int32_t* row_id_map, const float
                            int T, int H, int k, void* out, cudaStream_t s);
 
 // Steps 3-5: grouped GEMMs on tcgen05.
-enum class Epi : int { kSwiGLU = 0, kPlain = 1 };
+enum class Epi : int { kSwiGLU = 0, kPlain = 1, kCombine = 2 };
 
 struct GroupedGemmArgs {
   Epi epi;
@@ -75,6 +79,15 @@ struct GroupedGemmArgs {
   int interleave;              // SwiGLU: GLU interleave (0, 32, 64 or multiple of 128)
   float clamp;                 // SwiGLU clamp (<= 0: none)
   uint32_t* status;
+  // kSwiGLU with permuted_token != NULL: A rows are gathered from a = x [x_rows, K]
+  // kCombine: the fused weighted top-k reduction into out = [T, ldo]
+  const int32_t* permuted_token = nullptr;
+  int x_rows = 0;
+  const int32_t* row_id_map = nullptr;
+  const float* topk_w = nullptr;
+  int32_t* counters = nullptr;  // [T, n_tiles], zero before the launch
+  void* partials = nullptr;     // [R, ldo] bf16
+  int k = 0;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s);

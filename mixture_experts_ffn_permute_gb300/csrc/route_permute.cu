@@ -103,11 +103,16 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int ren
 // recorded in the status word and the route is treated as masked.
 __global__ void __launch_bounds__(256)
 chunk_histogram_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
-                       int32_t* __restrict__ chunk_counts, uint32_t* status) {
+                       int32_t* __restrict__ chunk_counts, uint32_t* status,
+                       int32_t* __restrict__ counters, int ncnt) {
   extern __shared__ int32_t s_cnt[];
   const int chunk = blockIdx.x;
   const int t0 = chunk * kChunkTokens;
   const int nt = min(kChunkTokens, T - t0);
+  if (counters) {
+    int32_t* c = counters + static_cast<size_t>(t0) * ncnt;
+    for (int i = threadIdx.x; i < nt * ncnt; i += blockDim.x) c[i] = 0;
+  }
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
   const int nr = nt * k;
@@ -345,11 +350,12 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
 }
 
 cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int T, int E, int k,
-                                   int32_t* chunk_counts, uint32_t* status, cudaStream_t s) {
+                                   int32_t* chunk_counts, uint32_t* status, cudaStream_t s,
+                                   int32_t* counters, int ncnt) {
   const int nchunks = ceil_div(T, kChunkTokens);
   if (nchunks == 0) return cudaSuccess;
-  chunk_histogram_kernel<<<nchunks, 256, sizeof(int32_t) * E, s>>>(topk_idx, T, E, k,
-                                                                   chunk_counts, status);
+  chunk_histogram_kernel<<<nchunks, 256, sizeof(int32_t) * E, s>>>(
+      topk_idx, T, E, k, chunk_counts, status, counters, ncnt);
   return cudaGetLastError();
 }
 

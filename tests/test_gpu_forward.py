@@ -26,9 +26,9 @@ def built():
     moe.load()
 
 
-def run_forward(shape, inp, ws=None, renorm=True):
+def run_forward(shape, inp, ws=None, renorm=True, fusion=0):
     p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, renorm, shape.glu_interleave,
-                         shape.swiglu_clamp)
+                         shape.swiglu_clamp, fusion)
     if ws is None:
         ws = moe.alloc_workspace(p)
     moe.clear_device_status(ws)
@@ -65,6 +65,27 @@ def test_forward_small(shape):
     assert_equal(res["tokens_per_expert"], ref["tokens_per_expert"], "tokens_per_expert")
     np.testing.assert_allclose(res["topk_w"].cpu().numpy(), ref["topk_w"], rtol=3e-6, atol=1e-7)
     assert_bf16_close(res["out"], ref["out"], f"out[{shape.name}]")
+
+
+FUSION_SHAPES = [mi.TINY, mi.MoEShape("ragged", T=333, H=512, F=384, E=7, k=3),
+                 mi.MoEShape("skew-small", T=512, H=256, F=256, E=64, k=8, zipf_s=1.1)]
+
+
+@pytest.mark.parametrize("fusion", [moe.FUSE_GATHER_A, moe.FUSE_COMBINE,
+                                    moe.FUSE_GATHER_A | moe.FUSE_COMBINE])
+@pytest.mark.parametrize("shape", FUSION_SHAPES, ids=lambda s: s.name)
+def test_forward_fusion_variants(shape, fusion):
+    inp = mi.make_inputs(shape, seed=3)
+    ref = oracle.moe_forward(inp["x"], inp["logits"], inp["w1"], inp["w2"], shape.k)
+    d = to_dev(inp)
+    res = run_forward(shape, d, fusion=fusion)
+    assert_bf16_close(res["out"], ref["out"], f"out[{shape.name}, fusion={fusion}]")
+    if not fusion & moe.FUSE_COMBINE:
+        # gathering A from x instead of a permuted copy changes no arithmetic
+        base = run_forward(shape, d, fusion=0)
+        assert torch.equal(res["out"].view(torch.int16), base["out"].view(torch.int16))
+    again = run_forward(shape, d, ws=res["ws"], fusion=fusion)
+    assert torch.equal(res["out"].view(torch.int16), again["out"].view(torch.int16))
 
 
 def test_forward_unnormalised_weights():
