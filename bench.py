@@ -57,6 +57,10 @@ def parse_args(argv=None):
     ap.add_argument("--E", type=int, default=0, help="override the expert count (profiling)")
     ap.add_argument("--k", type=int, default=0, help="override top-k (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time CUDA-graph replays of one forward (stage times from an eager pass)")
+    ap.add_argument("--kernel", type=int, default=0,
+                    help="moe_problem.kernel: 0 auto, 1 token-row tiles, 2 weight-row tiles")
     ap.add_argument("--fusion", type=int, default=0,
                     help="moe_problem.fusion bits: 1 = TMA-gather A rows, 2 = combine in GEMM2")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -222,7 +226,7 @@ def bench_ours(args, shape, desc):
     x = mi.make_x(shape, rank, dev)
     logits = mi.make_logits(shape, rank, dev)
     p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True,
-                         shape.glu_interleave, shape.swiglu_clamp, args.fusion)
+                         shape.glu_interleave, shape.swiglu_clamp, args.fusion, args.kernel)
     ws = moe.alloc_workspace(p, dev)
     out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -238,18 +242,41 @@ def bench_ours(args, shape, desc):
     K = args.steps
 
     # ---- device-resident timed region
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
-        moe.stage_timing_begin(K)
+        if graph is None:
+            moe.stage_timing_begin(K)
         ev0.record(stream)
         for _ in range(K):
-            step()
+            if graph is None:
+                step()
+            else:
+                graph.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-        stages = moe.stage_timing_end()
+        if graph is None:
+            stages = moe.stage_timing_end()
         barrier(world)
+    if graph is not None:  # per-stage times from an eager pass of the same call
+        moe.stage_timing_begin(min(K, 200))
+        for _ in range(min(K, 200)):
+            step()
+        stages = moe.stage_timing_end()
     ms_local = ev0.elapsed_time(ev1) / K
     status = moe.get_device_status(ws)
     if status != 0:
@@ -303,7 +330,8 @@ def bench_ours(args, shape, desc):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": desc, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
-                   "k": shape.k, "fusion": args.fusion, "l2": "inputs larger than L2 (weights %.2f GB), no flush"
+                   "k": shape.k, "fusion": args.fusion, "kernel": args.kernel,
+                   "timing": "cuda-graph replay" if args.graph else "eager launches", "l2": "inputs larger than L2 (weights %.2f GB), no flush"
                    % (2 * 3 * shape.E * shape.F * shape.H / 1e9)},
         "roofline": {"kernel": "grouped_gemm_kernel<SwiGLU> (GEMM1)", "bound": "tensor",
                      "achieved": ach, "peak": peaks[peak_key], "unit": "TFLOP/s",

@@ -87,10 +87,20 @@ typedef struct moe_problem {
                           slot-ordered sum by the last arrival).
      Both give results within the same tolerance of the exact layer. */
   int32_t fusion;
+  /* GEMM tiling (moe_problem.kernel):
+       MOE_KERNEL_AUTO          weight-row tiles when T*k <= 32*E, else token-row tiles
+       MOE_KERNEL_TOKEN_TILES   128 permuted token rows x 256 weight rows per tile
+       MOE_KERNEL_WEIGHT_TILES  128 weight rows x 32 token rows per tile (decode
+                                sizes: weights stream once at HBM speed); the
+                                fusion options do not apply to it. */
+  int32_t kernel;
 } moe_problem;
 
 #define MOE_FUSE_GATHER_A 1
 #define MOE_FUSE_COMBINE 2
+#define MOE_KERNEL_AUTO 0
+#define MOE_KERNEL_TOKEN_TILES 1
+#define MOE_KERNEL_WEIGHT_TILES 2
 
 /* Limits checked by every entry point. */
 #define MOE_MAX_EXPERTS 1024

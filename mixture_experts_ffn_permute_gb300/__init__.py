@@ -28,6 +28,9 @@ LIB_PATH = os.path.join(_HERE, "libmoeffn.so")
 MOE_OK = 0
 FUSE_GATHER_A = 1   # GEMM1 gathers A rows from x with TMA gather4
 FUSE_COMBINE = 2    # weighted top-k reduction in GEMM2's epilogue
+KERNEL_AUTO = 0
+KERNEL_TOKEN_TILES = 1   # 128 token rows x 256 weight rows per tile
+KERNEL_WEIGHT_TILES = 2  # 128 weight rows x 32 token rows per tile (decode sizes)
 STATUS_NAMES = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
     3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",
@@ -47,13 +50,13 @@ class Problem(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("glu_interleave", ctypes.c_int32),
                 ("swiglu_clamp", ctypes.c_float), ("precision", ctypes.c_int32),
-                ("fusion", ctypes.c_int32)]
+                ("fusion", ctypes.c_int32), ("kernel", ctypes.c_int32)]
 
     @classmethod
     def make(cls, T, H, F, E, k, renormalize=True, glu_interleave=0, swiglu_clamp=0.0,
-             fusion=0):
+             fusion=0, kernel=0):
         return cls(int(T), int(H), int(F), int(E), int(k), int(bool(renormalize)),
-                   int(glu_interleave), float(swiglu_clamp), 0, int(fusion))
+                   int(glu_interleave), float(swiglu_clamp), 0, int(fusion), int(kernel))
 
 
 _lib = None

@@ -106,6 +106,7 @@ int check_full(const moe_problem* p) {
   if (p->H <= 0 || p->F <= 0) return MOE_ERR_INVALID_ARG;
   if (p->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
+  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_WEIGHT_TILES) return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
   if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int I = p->glu_interleave;
@@ -136,6 +137,13 @@ int check_ws(const moe_problem* p, void* ws, size_t ws_bytes) {
     if ((expr) != cudaSuccess) return MOE_ERR_CUDA; \
     ++launches;                                   \
   } while (0)
+
+// Weight-row tiles (swap-AB) when experts see few tokens on average.
+bool use_weight_tiles(const moe_problem* p) {
+  if (p->kernel == MOE_KERNEL_WEIGHT_TILES) return true;
+  if (p->kernel == MOE_KERNEL_TOKEN_TILES) return false;
+  return static_cast<long long>(p->T) * p->k <= 32LL * p->E;
+}
 
 float clamp_of(const moe_problem* p) {
   const float c = p->swiglu_clamp;
@@ -177,11 +185,12 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
   g1.interleave = p->glu_interleave;
   g1.clamp = clamp_of(p);
   g1.status = status;
-  if (fused && fused->gather) {
+  const bool swap = use_weight_tiles(p);
+  if (fused && fused->gather && !swap) {
     g1.permuted_token = fused->permuted_token;
     g1.x_rows = p->T;
   }
-  MOE_LAUNCH(launch_grouped_gemm(g1, s));
+  MOE_LAUNCH(swap ? launch_grouped_gemm_swap(g1, s) : launch_grouped_gemm(g1, s));
   if (tm) tm->mark(call, mark, s);
   GroupedGemmArgs g2{};
   g2.epi = Epi::kPlain;
@@ -199,7 +208,7 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
   g2.out_rows = R;
   g2.F = p->F;
   g2.status = status;
-  if (fused && fused->combine) {
+  if (fused && fused->combine && !swap) {
     g2.epi = Epi::kCombine;
     g2.out = fused->out;
     g2.partials = y;
@@ -209,7 +218,7 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
     g2.counters = fused->counters;
     g2.k = p->k;
   }
-  MOE_LAUNCH(launch_grouped_gemm(g2, s));
+  MOE_LAUNCH(swap ? launch_grouped_gemm_swap(g2, s) : launch_grouped_gemm(g2, s));
   if (tm) tm->mark(call, mark + 1, s);
   return MOE_OK;
 }
@@ -398,17 +407,24 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   void* h = at<void>(ws, L.h);
   void* y = at<void>(ws, L.y);
   int32_t* counters = at<int32_t>(ws, L.counters);
-  const bool fuse_gather = (p->fusion & MOE_FUSE_GATHER_A) != 0;
-  const bool fuse_combine = (p->fusion & MOE_FUSE_COMBINE) != 0;
+  const bool swap = use_weight_tiles(p);
+  const bool fuse_gather = !swap && (p->fusion & MOE_FUSE_GATHER_A) != 0;
+  const bool fuse_combine = !swap && (p->fusion & MOE_FUSE_COMBINE) != 0;
 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
   tm.mark(call, 0, s);
   MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
   tm.mark(call, 1, s);
-  rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2,
-                   fuse_combine ? counters : nullptr, p->H / kBN);
-  if (rc != MOE_OK) return rc;
+  if (!fuse_combine && permute_small_fits(p->T, p->E, p->k)) {
+    // decode sizes: histogram + scan + scatter in one block
+    MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
+    for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
+  } else {
+    rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2,
+                     fuse_combine ? counters : nullptr, p->H / kBN);
+    if (rc != MOE_OK) return rc;
+  }
   if (!fuse_gather) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   tm.mark(call, 5, s);
   const FusedIO fused{fuse_gather, fuse_combine, ptok, rmap, wts, counters, out};

@@ -431,6 +431,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   }
 }
 
+template <Epi kEpi, bool kGatherA>
+cudaError_t launch_impl(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
+                        int grid, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kEpi, kGatherA>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+  if (err != cudaSuccess) return err;
+  grouped_gemm_kernel<kEpi, kGatherA><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 // ------------------------------------------------------------------ host side
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -438,7 +451,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn get_encode_fn() {
+static EncodeTiledFn get_encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -468,18 +481,6 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <Epi kEpi, bool kGatherA>
-cudaError_t launch_impl(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
-                        int grid, cudaStream_t s) {
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<kEpi, kGatherA>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-  if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<kEpi, kGatherA><<<grid, kThreads, kSmemBytes, s>>>(ma, mb, kp);
-  return cudaGetLastError();
-}
-
-}  // namespace
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s) {
   if (g.a_rows == 0) return cudaSuccess;

@@ -55,7 +55,7 @@ constexpr size_t kSmemBytesS = 1024 + kStagesS * kStageBytesS + 256 +
 struct SParams {
   const int32_t* expert_offsets;
   uint16_t* out;               // bf16 [rows, ldo]
-  int E, K, w_tiles, w_rows_per_expert, ldo, F, interleave;
+  int E, K, w_tiles, w_rows_per_expert, ldo, F, interleave, out_rows;
   float clamp;
   uint32_t* status;
 };
@@ -124,17 +124,40 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   }
   if (warp == 1) tmem_alloc<kTmemColsS>(tmem_slot);
   __syncthreads();
-  // tile prefix: expert e owns w_tiles * ceil(rows_e / kN) tiles
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int e = 0; e < p.E; ++e) {
+  // tile prefix: expert e owns w_tiles * ceil(rows_e / kN) tiles.  Thread i
+  // scans a run of at most ceil(E / 192) experts; runs are then offset by a
+  // scan over the threads.
+  {
+    __shared__ int s_part[kThreadsS / 32];
+    const int per = (p.E + kThreadsS - 1) / kThreadsS;
+    const int e0 = min(p.E, threadIdx.x * per), e1 = min(p.E, e0 + per);
+    int run = 0;
+    for (int e = e0; e < e1; ++e) {
       const int rows = s_off[e + 1] - s_off[e];
       const int nt = rows > 0 ? (rows + kN - 1) / kN : 0;
       s_ntk[e] = nt;
-      s_tp[e] = acc;
-      acc += nt * p.w_tiles;
+      run += nt * p.w_tiles;
     }
-    s_tp[p.E] = acc;
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) s_part[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += s_part[w];
+    int acc = base + incl - run;
+    for (int e = e0; e < e1; ++e) {
+      s_tp[e] = acc;
+      acc += s_ntk[e] * p.w_tiles;
+    }
+    if (threadIdx.x == kThreadsS - 1) {
+      int total = 0;
+      for (int w = 0; w < kThreadsS / 32; ++w) total += s_part[w];
+      s_tp[p.E] = total;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -227,10 +250,16 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
     const int quad = warp & 3;
     const int et = threadIdx.x - 64;  // 0..127
     int local = 0;
-    for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++local) {
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
       const int buf = local & 1;
       const uint32_t tph = (local >> 1) & 1;
-      if (!mbar_wait(&tfull[buf], tph, p.status)) { *abort_flag = 1; break; }
+      const bool ok = mbar_wait(&tfull[buf], tph, p.status);
+      // All four epilogue warps leave together (they share named barrier 1);
+      // the vote is also the barrier that frees sD of the previous tile.
+      if (bar_red_or(1, 128, !ok || *abort_flag != 0)) {
+        *abort_flag = 1;
+        break;
+      }
       tc_fence_after();
       const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
       const int seg_rows = s_off[t.e + 1] - s_off[t.e];
@@ -255,7 +284,7 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
         // exchange: gate and up rows of one output column live in different warps
 #pragma unroll
         for (int n = 0; n < kN; ++n) sD[wrow * kDPitch + n] = __uint_as_float(a[n]);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        bar_sync_named(1, 128);
         const int ie = (p.interleave == 32) ? 32 : 64;
         const int fl = et & 63;                    // output column inside the tile
         const int grow = (fl / ie) * 2 * ie + fl % ie;
@@ -274,8 +303,15 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
             p.out[(row0 + n) * p.ldo + f] = *reinterpret_cast<const uint16_t*>(&v);
           }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
       }
+    }
+    // Rows past the last expert's segment (masked routes) are zero outputs.
+    if (kEpi == Epi::kPlain) {
+      const long first = s_off[p.E];
+      const long n = (static_cast<long>(p.out_rows) - first) * p.ldo;
+      for (long i = static_cast<long>(blockIdx.x) * 128 + et; i < n;
+           i += static_cast<long>(gridDim.x) * 128)
+        p.out[first * p.ldo + i] = 0;
     }
   }
 
@@ -317,6 +353,7 @@ cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s) {
   sp.K = g.K;
   sp.w_rows_per_expert = g.b_rows_per_expert;
   sp.ldo = g.ldo;
+  sp.out_rows = g.out_rows;
   sp.F = g.F;
   sp.interleave = g.interleave;
   sp.clamp = g.clamp;

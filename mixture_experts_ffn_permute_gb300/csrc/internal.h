@@ -40,6 +40,16 @@ cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int R,
                         int32_t* tokens_per_expert, int32_t* expert_offsets,
                         int32_t* mtile_prefix, int32_t* permuted_token, cudaStream_t s);
 
+// Step 2 in one block for decode sizes when every route is valid: same
+// outputs as histogram + scan + scatter.
+constexpr int kSmallRoutes = 4096;
+constexpr int kSmallExperts = 1024;
+bool permute_small_fits(int T, int E, int k);
+cudaError_t launch_permute_small(const int32_t* topk_idx, int T, int E, int k,
+                                 int32_t* tokens_per_expert, int32_t* expert_offsets,
+                                 int32_t* mtile_prefix, int32_t* row_id_map,
+                                 int32_t* permuted_token, cudaStream_t s);
+
 // Step 2c: stable scatter -> row_id_map and permuted_token.
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
                            const int32_t* chunk_base, int32_t* row_id_map,
@@ -91,5 +101,9 @@ struct GroupedGemmArgs {
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s);
+
+// The same GEMMs with weight rows on the MMA's M side and tokens on N, for
+// decode sizes (kSwiGLU and kPlain epilogues; no gather / combine fusion).
+cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s);
 
 }  // namespace moe

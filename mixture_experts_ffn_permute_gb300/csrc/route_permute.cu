@@ -331,6 +331,69 @@ combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_id_m
   out[static_cast<size_t>(t) * vecs_per_row + v] = o;
 }
 
+// Decode sizes (T*k <= kSmallRoutes, E <= kSmallExperts): expert histogram,
+// scan and the stable scatter in ONE block of 1024 threads after the routing
+// kernel, so a decode step pays one permute launch instead of three.  Same
+// results as chunk_histogram / scan / scatter, bit for bit, for routes that
+// are all valid (moe_forward's own routing).
+__global__ void __launch_bounds__(1024)
+permute_small_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
+                     int32_t* __restrict__ tokens_per_expert,
+                     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ mtile_prefix,
+                     int32_t* __restrict__ row_id_map, int32_t* __restrict__ permuted_token) {
+  extern __shared__ int32_t s_small[];
+  __shared__ int s_warp[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = T * k;
+  int32_t* s_idx = s_small;
+  int32_t* s_cnt = s_small + R;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) s_idx[r] = __ldg(topk_idx + r);
+  __syncthreads();
+  // histogram
+  for (int r = threadIdx.x; r < R; r += blockDim.x) atomicAdd(&s_cnt[s_idx[r]], 1);
+  __syncthreads();
+  // scan (thread e owns expert e)
+  const int e = threadIdx.x;
+  const int count = e < E ? s_cnt[e] : 0;
+  int total = 0;
+  const int off = block_exclusive_scan(count, s_warp, &total);
+  const int mt = (count + kBM - 1) / kBM;
+  int mt_total = 0;
+  const int mt_off = block_exclusive_scan(e < E ? mt : 0, s_warp, &mt_total);
+  if (e < E) {
+    tokens_per_expert[e] = count;
+    expert_offsets[e] = off;
+    mtile_prefix[e] = mt_off;
+    s_cnt[e] = off;  // next free row of expert e
+  }
+  if (e == 0) {
+    expert_offsets[E] = total;
+    mtile_prefix[E] = mt_total;
+  }
+  __syncthreads();
+  // stable scatter by warp 0, 32 routes at a time in (token, slot) order
+  if (warp == 0) {
+    for (int r0 = 0; r0 < R; r0 += 32) {
+      const int r = r0 + lane;
+      const int ex_id = r < R ? s_idx[r] : -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, ex_id);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int leader = __ffs(peers) - 1;
+      int start = 0;
+      if (ex_id >= 0) start = s_cnt[ex_id];
+      __syncwarp();
+      if (ex_id >= 0 && lane == leader) s_cnt[ex_id] = start + __popc(peers);
+      __syncwarp();
+      if (ex_id >= 0) {
+        const int row_id = start + rank;
+        row_id_map[r] = row_id;
+        permuted_token[row_id] = r / k;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize,
@@ -391,6 +454,21 @@ cudaError_t launch_mtile_prefix_from_offsets(const int32_t* expert_offsets, int 
                                              int32_t* mtile_prefix, uint32_t* status,
                                              cudaStream_t s) {
   mtile_prefix_kernel<<<1, 1024, 0, s>>>(expert_offsets, E, R, mtile_prefix, status);
+  return cudaGetLastError();
+}
+
+bool permute_small_fits(int T, int E, int k) {
+  return static_cast<long>(T) * k <= kSmallRoutes && E <= kSmallExperts && T > 0;
+}
+
+cudaError_t launch_permute_small(const int32_t* topk_idx, int T, int E, int k,
+                                 int32_t* tokens_per_expert, int32_t* expert_offsets,
+                                 int32_t* mtile_prefix, int32_t* row_id_map,
+                                 int32_t* permuted_token, cudaStream_t s) {
+  const size_t smem = sizeof(int32_t) * (static_cast<size_t>(T) * k + E);
+  permute_small_kernel<<<1, 1024, smem, s>>>(topk_idx, T, E, k, tokens_per_expert,
+                                             expert_offsets, mtile_prefix, row_id_map,
+                                             permuted_token);
   return cudaGetLastError();
 }
 

@@ -26,9 +26,9 @@ def built():
     moe.load()
 
 
-def run_forward(shape, inp, ws=None, renorm=True, fusion=0):
+def run_forward(shape, inp, ws=None, renorm=True, fusion=0, kernel=0):
     p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, renorm, shape.glu_interleave,
-                         shape.swiglu_clamp, fusion)
+                         shape.swiglu_clamp, fusion, kernel)
     if ws is None:
         ws = moe.alloc_workspace(p)
     moe.clear_device_status(ws)
@@ -55,12 +55,17 @@ SMALL = [
 ]
 
 
+KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES]
+KERNEL_IDS = ["token_tiles", "weight_tiles"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
-def test_forward_small(shape):
+def test_forward_small(shape, kernel):
     inp = mi.make_inputs(shape, seed=0)
     ref = oracle.moe_forward(inp["x"], inp["logits"], inp["w1"], inp["w2"], shape.k,
                              interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
-    res = run_forward(shape, to_dev(inp))
+    res = run_forward(shape, to_dev(inp), kernel=kernel)
     assert_equal(res["topk_idx"], ref["topk_idx"], "topk_idx")
     assert_equal(res["tokens_per_expert"], ref["tokens_per_expert"], "tokens_per_expert")
     np.testing.assert_allclose(res["topk_w"].cpu().numpy(), ref["topk_w"], rtol=3e-6, atol=1e-7)
@@ -97,12 +102,13 @@ def test_forward_unnormalised_weights():
     assert_bf16_close(res["out"], ref["out"], "out (full-softmax weights)")
 
 
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("T", [1, 8, 32])
-def test_forward_decode_full_dims(T):
+def test_forward_decode_full_dims(T, kernel):
     shape = mi.DECODE.with_T(T)
     inp = mi.make_inputs(shape, seed=0)
     ref = oracle.moe_forward(inp["x"], inp["logits"], inp["w1"], inp["w2"], shape.k)
-    res = run_forward(shape, to_dev(inp))
+    res = run_forward(shape, to_dev(inp), kernel=kernel)
     assert_equal(res["topk_idx"], ref["topk_idx"], "topk_idx")
     assert_bf16_close(res["out"], ref["out"], f"out[decode T={T}]")
 

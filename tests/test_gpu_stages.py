@@ -150,14 +150,18 @@ def _routed_inputs(shape, seed=0, mask=0.0):
     return inp, idx, w, perm, xp
 
 
+KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES]
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles"])
 @pytest.mark.parametrize("shape", MLP_CASES, ids=lambda s: s.name)
-def test_grouped_swiglu_mlp(shape):
+def test_grouped_swiglu_mlp(shape, kernel):
     inp, idx, w, perm, xp = _routed_inputs(shape, seed=1)
     h = oracle.gemm1_swiglu(xp, perm["expert_offsets"], inp["w1"], shape.F, shape.glu_interleave,
                             shape.swiglu_clamp)
     y_ref = oracle.gemm2(h, perm["expert_offsets"], inp["w2"], shape.H)
     p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True, shape.glu_interleave,
-                         shape.swiglu_clamp)
+                         shape.swiglu_clamp, kernel=kernel)
     ws = moe.alloc_workspace(p)
     moe.clear_device_status(ws)
     R = shape.R
@@ -169,14 +173,15 @@ def test_grouped_swiglu_mlp(shape):
     assert_bf16_close(y, y_ref, f"y_perm[{shape.name}]")
 
 
-def test_grouped_mlp_masked_tail_rows_are_zero():
+@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles"])
+def test_grouped_mlp_masked_tail_rows_are_zero(kernel):
     shape = mi.MoEShape("masked", T=100, H=256, F=256, E=6, k=2)
     inp, idx, w, perm, xp = _routed_inputs(shape, seed=4, mask=0.25)
     n = int(perm["expert_offsets"][-1])
     assert n < shape.R
     h = oracle.gemm1_swiglu(xp, perm["expert_offsets"], inp["w1"], shape.F)
     y_ref = oracle.gemm2(h, perm["expert_offsets"], inp["w2"], shape.H)
-    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k)
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, kernel=kernel)
     ws = moe.alloc_workspace(p)
     y = torch.full((shape.R, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
     moe.grouped_swiglu_mlp(p, torch.from_numpy(xp.view(np.int16)).view(torch.bfloat16).to(DEV),
