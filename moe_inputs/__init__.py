@@ -158,3 +158,77 @@ def random_weights(T: int, k: int, seed: int = 0) -> torch.Tensor:
     """Seeded positive routing weights (fp32 [T, k]) for combine-only tests."""
     g = _gen(seed + 13, "cpu")
     return torch.rand(T, k, generator=g, dtype=torch.float32).add_(0.05).contiguous()
+
+
+# ------------------------------------------------------------------ low precision inputs
+#
+# The low-precision workload's tensors are quantised from the same seeded
+# normal draws (this is how its inputs are made, not part of the layer):
+#   activations: per 1x128 block, s = amax / 448, code = E4M3(x / s) (torch's
+#     round-to-nearest-even cast after clamping to +-448)
+#   weights (per expert tensor): g = amax / 448; per 16 values along K,
+#     s_b = E4M3(amax_b / (6 g)); q = E2M1(w / (s_b g)) round-to-nearest-even,
+#     saturating at 6; two codes per byte, the even index in the low nibble.
+#     (6 * s_b <= 448, the decoder-range rule for NVFP4 scales.)
+
+def quantize_fp8_rows(x: torch.Tensor, block: int = 128):
+    """x [T, H] float -> (codes uint8 [T, H], scales fp32 [T, H/block])."""
+    T, H = x.shape
+    xb = x.float().reshape(T, H // block, block)
+    amax = xb.abs().amax(-1)
+    s = amax / 448.0
+    s = torch.where(amax > 0, s, torch.ones_like(s))
+    q = (xb / s[..., None]).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).reshape(T, H).contiguous(), s.contiguous()
+
+
+def _e2m1_code(a: torch.Tensor) -> torch.Tensor:
+    """Round-to-nearest-even E2M1 code (0..7) of magnitudes a >= 0, saturating."""
+    code = torch.zeros_like(a, dtype=torch.uint8)
+    # boundaries between codes; equality goes to the even code
+    for c, lo, incl in ((1, 0.25, False), (2, 0.75, True), (3, 1.25, False), (4, 1.75, True),
+                        (5, 2.5, False), (6, 3.5, True), (7, 5.0, False)):
+        above = a >= lo if incl else a > lo
+        code = torch.where(above, torch.full_like(code, c), code)
+    return code
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """w [N, K] float -> (packed uint8 [N, K/2], scales uint8 [N, K/16], g fp32 scalar)."""
+    N, K = w.shape
+    wf = w.float()
+    amax = wf.abs().max()
+    g = (amax / 448.0) if amax > 0 else torch.ones((), device=w.device)
+    blocks = wf.reshape(N, K // 16, 16)
+    bmax = blocks.abs().amax(-1)
+    s8 = (bmax / (6.0 * g)).clamp_(max=448.0).to(torch.float8_e4m3fn)
+    sv = s8.float()
+    denom = (sv * g)[..., None]
+    ratio = torch.where(denom > 0, blocks / torch.where(denom > 0, denom, torch.ones_like(denom)),
+                        torch.zeros_like(blocks))
+    code = _e2m1_code(ratio.abs()) | (ratio < 0).to(torch.uint8) << 3
+    code = code.reshape(N, K)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).contiguous()
+    return packed, s8.view(torch.uint8).contiguous(), g.float().reshape(())
+
+
+def make_lowprec_inputs(shape: MoEShape, seed: int = 0, device="cpu",
+                        weights: bool = True) -> Dict[str, Optional[torch.Tensor]]:
+    """FP8 activations (+ fp32 scales), fp32 logits and NVFP4 weights."""
+    g = _gen(seed + 1, device)
+    x = torch.randn(shape.T, shape.H, generator=g, device=device, dtype=torch.float32)
+    xq, xs = quantize_fp8_rows(x)
+    out = {"logits": make_logits(shape, seed, device), "xq": xq, "xs": xs}
+    if weights:
+        for name, rows, cols, sd in (("w1", 2 * shape.F, shape.H, seed + 2),
+                                     ("w2", shape.H, shape.F, seed + 3)):
+            gw = _gen(sd, device)
+            q = torch.empty(shape.E, rows, cols // 2, dtype=torch.uint8, device=device)
+            sc = torch.empty(shape.E, rows, cols // 16, dtype=torch.uint8, device=device)
+            gs = torch.empty(shape.E, dtype=torch.float32, device=device)
+            for e in range(shape.E):
+                wf = torch.randn(rows, cols, generator=gw, device=device,
+                                 dtype=torch.float32).mul_(1.0 / math.sqrt(cols))
+                q[e], sc[e], gs[e] = quantize_nvfp4(wf)
+            out[name + "q"], out[name + "s"], out[name + "g"] = q, sc, gs
+    return out

@@ -64,6 +64,15 @@ def _load():
                                         vp, vp, vp, vp], ci),
                 "oracle_dense_bruteforce": ([ci, ci, ci, ci, ci, ci, cd, vp, vp, vp, vp,
                                              vp, vp], ci),
+                "oracle_e4m3_value": ([ctypes.c_uint8], cd),
+                "oracle_e2m1_value": ([ctypes.c_uint8], cd),
+                "oracle_e4m3_encode": ([ctypes.c_float], ctypes.c_uint8),
+                "oracle_requant_fp8_block": ([vp, ci, vp], None),
+                "oracle_gemm1_swiglu_lowprec": ([cl, ci, ci, ci, ci, cd, vp, vp, vp, vp, vp, vp,
+                                                 ci, vp], ci),
+                "oracle_gemm2_lowprec": ([cl, ci, ci, ci, vp, vp, vp, vp, vp, vp], ci),
+                "oracle_moe_forward_lowprec": ([ci, ci, ci, ci, ci, ci, ci, cd, vp, vp, vp, vp,
+                                                vp, vp, vp, vp, vp, vp, vp, vp], ci),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -240,3 +249,90 @@ def dense_bruteforce(x, topk_idx, topk_w, w1, w2, interleave: int = 0,
                                            _expert_ptrs(w2s), _p(out)),
            "oracle_dense_bruteforce")
     return out
+
+
+# ---------------------------------------------------------------- low precision
+
+def e4m3_value(code: int) -> float:
+    return _load().oracle_e4m3_value(int(code))
+
+
+def e2m1_value(code: int) -> float:
+    return _load().oracle_e2m1_value(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def requant_fp8_block(h) -> np.ndarray:
+    hh = _np(h, np.float64)
+    out = np.empty_like(hh)
+    _load().oracle_requant_fp8_block(_p(hh), hh.shape[0], _p(out))
+    return out
+
+
+def _bytes_experts(w, E: int):
+    if isinstance(w, (list, tuple)):
+        return [None if m is None else _np(m, np.uint8) for m in w]
+    a = _np(w, np.uint8)
+    return [a[e] for e in range(E)]
+
+
+def _byte_ptrs(ws):
+    arr = (ctypes.c_void_p * len(ws))()
+    for i, w in enumerate(ws):
+        arr[i] = None if w is None else w.ctypes.data
+    return arr
+
+
+def gemm1_swiglu_lowprec(xq_perm, xs_perm, expert_offsets, w1q, w1s, g1, F: int,
+                         interleave: int = 0, clamp: float = 0.0, requant: bool = True):
+    xq = _np(xq_perm, np.uint8)
+    xs = _np(xs_perm, np.float32)
+    off = _np(expert_offsets, np.int32)
+    E = off.shape[0] - 1
+    R, H = xq.shape
+    q, sc = _bytes_experts(w1q, E), _bytes_experts(w1s, E)
+    g = _np(g1, np.float32)
+    h = np.empty((R, F), np.float64)
+    _check(_load().oracle_gemm1_swiglu_lowprec(R, H, F, E, interleave, float(clamp), _p(off),
+                                               _p(xq), _p(xs), _byte_ptrs(q), _byte_ptrs(sc),
+                                               _p(g), int(requant), _p(h)),
+           "oracle_gemm1_swiglu_lowprec")
+    return h
+
+
+def gemm2_lowprec(h, expert_offsets, w2q, w2s, g2, H: int):
+    hh = _np(h, np.float64)
+    off = _np(expert_offsets, np.int32)
+    E = off.shape[0] - 1
+    R, F = hh.shape
+    q, sc = _bytes_experts(w2q, E), _bytes_experts(w2s, E)
+    g = _np(g2, np.float32)
+    y = np.empty((R, H), np.float64)
+    _check(_load().oracle_gemm2_lowprec(R, H, F, E, _p(off), _p(hh), _byte_ptrs(q),
+                                        _byte_ptrs(sc), _p(g), _p(y)), "oracle_gemm2_lowprec")
+    return y
+
+
+def moe_forward_lowprec(xq, xs, logits, w1q, w1s, g1, w2q, w2s, g2, k: int,
+                        renormalize: bool = True, interleave: int = 0, clamp: float = 0.0):
+    """The FP8-activation / NVFP4-weight layer on the given tokens.  Weight
+    arguments are [E, ...] byte tensors or per-expert lists (None = unused)."""
+    xqa = _np(xq, np.uint8)
+    xsa = _np(xs, np.float32)
+    lg = _np(logits, np.float32)
+    T, H = xqa.shape
+    E = lg.shape[1]
+    q1, s1 = _bytes_experts(w1q, E), _bytes_experts(w1s, E)
+    q2, s2 = _bytes_experts(w2q, E), _bytes_experts(w2s, E)
+    F = 2 * next(m for m in q2 if m is not None).shape[1]
+    out = np.empty((T, H), np.float64)
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    _check(_load().oracle_moe_forward_lowprec(
+        T, H, F, E, k, int(renormalize), interleave, float(clamp), _p(lg), _p(xqa), _p(xsa),
+        _byte_ptrs(q1), _byte_ptrs(s1), _p(_np(g1, np.float32)), _byte_ptrs(q2), _byte_ptrs(s2),
+        _p(_np(g2, np.float32)), _p(out), _p(idx), _p(w)), "oracle_moe_forward_lowprec")
+    return {"out": out, "topk_idx": idx, "topk_w": w}

@@ -60,6 +60,51 @@ inline long up_row(long f, long F, long I) {
 
 inline double silu(double z) { return z / (1.0 + std::exp(-z)); }
 
+// ---- low-precision formats (OCP 8-bit and 4-bit floating point) ----------
+// E4M3 ("fn" variant, no infinities): sign, 4 exponent bits (bias 7), 3
+// mantissa bits; exponent field 0 is subnormal; S.1111.111 is NaN.
+inline double e4m3_value(uint8_t c) {
+  const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return std::nan("");
+  const double v = (e == 0) ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return sgn ? -v : v;
+}
+
+// E2M1: sign, 2 exponent bits (bias 1), 1 mantissa bit; exponent 0 subnormal.
+inline double e2m1_value(uint8_t n) {
+  const int sgn = (n >> 3) & 1, e = (n >> 1) & 3, m = n & 1;
+  const double v = (e == 0) ? 0.5 * m : std::ldexp(1.0 + m / 2.0, e - 1);
+  return sgn ? -v : v;
+}
+
+// Nearest E4M3 code to x, ties to the even code, magnitudes above the
+// largest finite value (448) saturate to it.  Found by trying every finite
+// code: slow and plain.
+inline uint8_t e4m3_encode(float x) {
+  if (std::isnan(x)) return 0x7F;
+  const double a = std::fabs(static_cast<double>(x));
+  int best = 0;
+  double best_d = a;  // distance to code 0 (value 0)
+  for (int c = 1; c < 127; ++c) {  // 127 = NaN
+    const double d = std::fabs(e4m3_value(static_cast<uint8_t>(c)) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  if (a >= 448.0) best = 0x7E;
+  return static_cast<uint8_t>(best | (std::signbit(x) && best != 0 ? 0x80 : 0));
+}
+
+// NVFP4 weight element k of a packed row: two E2M1 values per byte, the even
+// index in the low nibble; one E4M3 scale per 16 values; times the tensor's
+// fp32 scale g.
+inline double nvfp4_value(const uint8_t* q_row, const uint8_t* s_row, long k, double g) {
+  const uint8_t byte = q_row[k >> 1];
+  const uint8_t nib = (k & 1) ? (byte >> 4) : (byte & 15);
+  return e2m1_value(nib) * e4m3_value(s_row[k >> 4]) * g;
+}
+
 // clamp <= 0 or non-finite means "no clamp".
 inline double swiglu(double g, double u, double c) {
   if (c > 0 && std::isfinite(c)) {
@@ -336,6 +381,141 @@ int oracle_dense_bruteforce(int T, int H, int F, int E, int k, int interleave, d
       }
     }
   }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Low-precision variant (the MegaMoE page's formats: FP8 E4M3 activations
+// with fp32 scales per 128 channels, NVFP4 weights = E2M1 values with E4M3
+// scales per 16 values and an fp32 scale per expert weight tensor).
+
+double oracle_e4m3_value(uint8_t c) { return e4m3_value(c); }
+double oracle_e2m1_value(uint8_t n) { return e2m1_value(n); }
+uint8_t oracle_e4m3_encode(float x) { return e4m3_encode(x); }
+
+// Re-quantisation of one row block of h to FP8 (the split GEMM1 epilogue of
+// the MegaMoE page stores its output with per-128 scales): s = amax / 448 in
+// fp32 (s = 1 when the block is all zero), code = E4M3(h / s) computed in
+// fp32, returned value = E4M3 value * s.  n <= 128 values.
+void oracle_requant_fp8_block(const double* h, int n, double* out) {
+  float amax = 0.f;
+  for (int i = 0; i < n; ++i) amax = std::fmax(amax, std::fabs(static_cast<float>(h[i])));
+  const float s = amax > 0.f ? amax / 448.0f : 1.0f;
+  for (int i = 0; i < n; ++i) {
+    const float v = static_cast<float>(h[i]) / s;
+    out[i] = e4m3_value(e4m3_encode(v)) * static_cast<double>(s);
+  }
+}
+
+// GEMM1 + SwiGLU on dequantised operands, rows of each expert:
+//   x_hat[r][c]  = E4M3(xq[r][c]) * xs[r][c / 128]
+//   w_hat[n][c]  = E2M1(q) * E4M3(s[n][c / 16]) * g1[e]
+//   h = silu(min(g, clamp)) * clamp(u, -clamp, clamp), then (requant != 0)
+//   every 128-wide block of a row re-quantised to FP8 as above.
+// w1q[e]: [2F, H/2] bytes, w1s[e]: [2F, H/16] bytes.
+int oracle_gemm1_swiglu_lowprec(long R, int H, int F, int E, int interleave, double clamp,
+                                const int32_t* expert_offsets, const uint8_t* xq_perm,
+                                const float* xs_perm, const uint8_t* const* w1q,
+                                const uint8_t* const* w1s, const float* g1, int requant,
+                                double* h) {
+  if (interleave > 0 && F % interleave != 0) return -1;
+  if (H % 128 != 0 || F % 128 != 0) return -1;
+  for (int e = 0; e < E; ++e)
+    if (expert_offsets[e + 1] > expert_offsets[e] && (!w1q[e] || !w1s[e])) return -2;
+  for (long r = expert_offsets[E]; r < R; ++r)
+    for (int f = 0; f < F; ++f) h[r * F + f] = 0.0;
+  for (int e = 0; e < E; ++e) {
+    const long r0 = expert_offsets[e], r1 = expert_offsets[e + 1];
+    if (r1 <= r0) continue;
+#pragma omp parallel for schedule(dynamic)
+    for (long r = r0; r < r1; ++r) {
+      std::vector<double> xr(H), hr(F);
+      for (int c = 0; c < H; ++c)
+        xr[c] = e4m3_value(xq_perm[r * H + c]) * static_cast<double>(xs_perm[r * (H / 128) + c / 128]);
+      for (int f = 0; f < F; ++f) {
+        const long rg = gate_row(f, F, interleave), ru = up_row(f, F, interleave);
+        const uint8_t* qg = w1q[e] + rg * (H / 2);
+        const uint8_t* sg = w1s[e] + rg * (H / 16);
+        const uint8_t* qu = w1q[e] + ru * (H / 2);
+        const uint8_t* su = w1s[e] + ru * (H / 16);
+        double g = 0.0, u = 0.0;
+        for (int c = 0; c < H; ++c) {
+          g += xr[c] * nvfp4_value(qg, sg, c, g1[e]);
+          u += xr[c] * nvfp4_value(qu, su, c, g1[e]);
+        }
+        hr[f] = swiglu(g, u, clamp);
+      }
+      if (requant) {
+        for (int b = 0; b < F; b += 128) oracle_requant_fp8_block(&hr[b], 128, &h[r * F + b]);
+      } else {
+        for (int f = 0; f < F; ++f) h[r * F + f] = hr[f];
+      }
+    }
+  }
+  return 0;
+}
+
+// GEMM2 on dequantised NVFP4 weights: y[r][n] = sum_f h[r][f] * w2_hat[n][f].
+// w2q[e]: [H, F/2] bytes, w2s[e]: [H, F/16] bytes.
+int oracle_gemm2_lowprec(long R, int H, int F, int E, const int32_t* expert_offsets,
+                         const double* h, const uint8_t* const* w2q, const uint8_t* const* w2s,
+                         const float* g2, double* y) {
+  for (int e = 0; e < E; ++e)
+    if (expert_offsets[e + 1] > expert_offsets[e] && (!w2q[e] || !w2s[e])) return -2;
+  for (long r = expert_offsets[E]; r < R; ++r)
+    for (int n = 0; n < H; ++n) y[r * H + n] = 0.0;
+  for (int e = 0; e < E; ++e) {
+    const long r0 = expert_offsets[e], r1 = expert_offsets[e + 1];
+    if (r1 <= r0) continue;
+#pragma omp parallel for schedule(dynamic)
+    for (long r = r0; r < r1; ++r) {
+      for (int n = 0; n < H; ++n) {
+        const uint8_t* q = w2q[e] + static_cast<long>(n) * (F / 2);
+        const uint8_t* sc = w2s[e] + static_cast<long>(n) * (F / 16);
+        double acc = 0.0;
+        for (int f = 0; f < F; ++f) acc += h[r * F + f] * nvfp4_value(q, sc, f, g2[e]);
+        y[r * H + n] = acc;
+      }
+    }
+  }
+  return 0;
+}
+
+// The whole low-precision layer: route -> permute -> gather (codes and
+// scales) -> GEMM1 + SwiGLU + FP8 re-quantisation -> GEMM2 -> combine.
+int oracle_moe_forward_lowprec(int T, int H, int F, int E, int k, int renormalize,
+                               int interleave, double clamp, const float* logits,
+                               const uint8_t* xq, const float* xs, const uint8_t* const* w1q,
+                               const uint8_t* const* w1s, const float* g1,
+                               const uint8_t* const* w2q, const uint8_t* const* w2s,
+                               const float* g2, double* out, int32_t* topk_idx_out,
+                               double* topk_w_out) {
+  const long R = static_cast<long>(T) * k;
+  std::vector<int32_t> idx(R), row_id_map(R), permuted_token(R), counts(E), offsets(E + 1);
+  std::vector<double> w(R);
+  int rc = oracle_route_topk(T, E, k, renormalize, logits, idx.data(), w.data());
+  if (rc) return rc;
+  rc = oracle_permute(T, E, k, idx.data(), counts.data(), offsets.data(), row_id_map.data(),
+                      permuted_token.data());
+  if (rc) return rc;
+  std::vector<uint8_t> xq_perm(static_cast<size_t>(R) * H, 0);
+  std::vector<float> xs_perm(static_cast<size_t>(R) * (H / 128), 1.0f);
+  for (long r = 0; r < R; ++r) {
+    const int t = permuted_token[r];
+    if (t < 0) continue;
+    std::memcpy(&xq_perm[r * H], xq + static_cast<long>(t) * H, H);
+    std::memcpy(&xs_perm[r * (H / 128)], xs + static_cast<long>(t) * (H / 128),
+                sizeof(float) * (H / 128));
+  }
+  std::vector<double> h(static_cast<size_t>(R) * F), y(static_cast<size_t>(R) * H);
+  rc = oracle_gemm1_swiglu_lowprec(R, H, F, E, interleave, clamp, offsets.data(), xq_perm.data(),
+                                   xs_perm.data(), w1q, w1s, g1, 1, h.data());
+  if (rc) return rc;
+  rc = oracle_gemm2_lowprec(R, H, F, E, offsets.data(), h.data(), w2q, w2s, g2, y.data());
+  if (rc) return rc;
+  oracle_unpermute_combine(T, H, k, y.data(), row_id_map.data(), w.data(), out);
+  if (topk_idx_out) std::memcpy(topk_idx_out, idx.data(), sizeof(int32_t) * R);
+  if (topk_w_out) std::memcpy(topk_w_out, w.data(), sizeof(double) * R);
   return 0;
 }
 
