@@ -43,6 +43,9 @@ WORKLOADS = {
                           "bf16, Zipf(1.1) expert bias"),
     "decode": (mi.DECODE, "decode-sized MoE FFN: H=2048 F=768 E=128 top-8 bf16"),
     "tiny": (mi.TINY, "tiny MoE FFN: T=64 H=256 F=512 E=8 top-2 bf16"),
+    "lowprec": (mi.LOWPREC, "low-precision MoE FFN: T=4096 H=7168 F=2048 E=256 top-8, FP8 "
+                            "activations (fp32 scale / 128), NVFP4 weights, GLU interleave 32, "
+                            "clamp 7, bf16 out"),
 }
 
 
@@ -180,11 +183,16 @@ class ClockSampler:
 def oracle_sample(shape, inp_host, n_tokens: int):
     """Run the oracle on the first n tokens; returns (seconds, flops)."""
     import oracle
-    x = inp_host["x"][:n_tokens]
     lg = inp_host["logits"][:n_tokens]
     t0 = time.perf_counter()
-    oracle.moe_forward(x, lg, inp_host["w1"], inp_host["w2"], shape.k,
-                       interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
+    if shape.lowprec:
+        h = inp_host
+        oracle.moe_forward_lowprec(h["xq"][:n_tokens], h["xs"][:n_tokens], lg, h["w1q"], h["w1s"],
+                                   h["w1g"], h["w2q"], h["w2s"], h["w2g"], shape.k,
+                                   interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
+    else:
+        oracle.moe_forward(inp_host["x"][:n_tokens], lg, inp_host["w1"], inp_host["w2"], shape.k,
+                           interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
     dt = time.perf_counter() - t0
     return dt, shape.with_T(n_tokens).flops()
 
@@ -221,18 +229,37 @@ def bench_ours(args, shape, desc):
     peaks, peak_src = load_peaks()
 
     # weights shared by all ranks (seed 0); each rank routes its own tokens
-    w1 = mi.make_w1(shape, 0, dev)
-    w2 = mi.make_w2(shape, 0, dev)
-    x = mi.make_x(shape, rank, dev)
-    logits = mi.make_logits(shape, rank, dev)
     p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True,
-                         shape.glu_interleave, shape.swiglu_clamp, args.fusion, args.kernel)
+                         shape.glu_interleave, shape.swiglu_clamp, args.fusion, args.kernel,
+                         moe.PREC_FP8_NVFP4 if shape.lowprec else moe.PREC_BF16)
     ws = moe.alloc_workspace(p, dev)
     out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if shape.lowprec:
+        lp = mi.make_lowprec_inputs(shape, 0, dev)
+        if rank:
+            lp.update({k: v for k, v in mi.make_lowprec_inputs(shape, rank, dev, weights=False).items()})
+        prepared = torch.empty(moe.prepared_scales_size(p), dtype=torch.uint8, device=dev)
+        moe.prepare_weights(p, lp["w1s"], lp["w2s"], prepared)
+        x, logits = lp["xq"], lp["logits"]
+        xs = lp["xs"]
+        weight_bytes = sum(lp[n].numel() for n in ("w1q", "w1s", "w2q", "w2s"))
+
+        def fwd(xx, ll):
+            moe.forward_fp8_nvfp4(p, xx, xs, ll, lp["w1q"], lp["w1g"], lp["w2q"], lp["w2g"],
+                                  prepared, out, ws)
+    else:
+        w1 = mi.make_w1(shape, 0, dev)
+        w2 = mi.make_w2(shape, 0, dev)
+        x = mi.make_x(shape, rank, dev)
+        logits = mi.make_logits(shape, rank, dev)
+        weight_bytes = 2 * (w1.numel() + w2.numel())
+
+        def fwd(xx, ll):
+            moe.forward(p, xx, ll, w1, w2, out, ws)
 
     def step():
-        moe.forward(p, x, logits, w1, w2, out, ws)
+        fwd(x, logits)
 
     moe.clear_device_status(ws)
     for _ in range(max(args.warmup, 3)):
@@ -285,15 +312,21 @@ def bench_ours(args, shape, desc):
     sec = ms / 1e3
 
     # ---- end to end: pinned host inputs -> device -> forward -> host output
-    xh = x.cpu().pin_memory()
-    lh = logits.cpu().pin_memory()
+    # every per-step input (tokens, their scales when FP8, router logits) goes
+    # host -> device each step; the weights are parameters and stay resident
+    step_inputs = [x, logits] + ([xs] if shape.lowprec else [])
+    hosts = [t.cpu().pin_memory() for t in step_inputs]
+    devs = [torch.empty_like(t) for t in step_inputs]
     oh = torch.empty_like(out, device="cpu").pin_memory()
-    xd, ld = torch.empty_like(x), torch.empty_like(logits)
 
     def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        ld.copy_(lh, non_blocking=True)
-        moe.forward(p, xd, ld, w1, w2, out, ws)
+        for hsrc, ddst in zip(hosts, devs):
+            ddst.copy_(hsrc, non_blocking=True)
+        if shape.lowprec:
+            moe.forward_fp8_nvfp4(p, devs[0], devs[2], devs[1], lp["w1q"], lp["w1g"], lp["w2q"],
+                                  lp["w2g"], prepared, out, ws)
+        else:
+            fwd(devs[0], devs[1])
         oh.copy_(out, non_blocking=True)
 
     for _ in range(2):
@@ -327,26 +360,30 @@ def bench_ours(args, shape, desc):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "fp8xnvfp4->f16 mma" if shape.lowprec else "bf16",
         "data": "synthetic",
         "config": {"workload": desc, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
                    "k": shape.k, "fusion": args.fusion, "kernel": args.kernel,
+                   "precision": "fp8-act/nvfp4-weight" if shape.lowprec else "bf16",
                    "timing": "cuda-graph replay" if args.graph else "eager launches", "l2": "inputs larger than L2 (weights %.2f GB), no flush"
-                   % (2 * 3 * shape.E * shape.F * shape.H / 1e9)},
+                   % (weight_bytes / 1e9)},
         "roofline": {"kernel": "grouped_gemm_kernel<SwiGLU> (GEMM1)", "bound": "tensor",
                      "achieved": ach, "peak": peaks[peak_key], "unit": "TFLOP/s",
                      "frac": ach / peaks[peak_key], "traffic": None,
                      "peak_source": f"{peak_key} ({peak_src})"},
         "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": x.numel() * 2 + logits.numel() * 4,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in step_inputs),
                 "d2h_bytes_per_step": out.numel() * 2},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
         "stages_ms": {k: round(v, 5) for k, v in stages.items() if not k.startswith("_")},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = {"x": x.cpu(), "logits": logits.cpu(), "w1": w1.cpu(), "w2": w2.cpu()}
+        if shape.lowprec:
+            host = {k: v.cpu() for k, v in lp.items()}
+        else:
+            host = {"x": x.cpu(), "logits": logits.cpu(), "w1": w1.cpu(), "w2": w2.cpu()}
         line["cpu_baseline"] = cpu_baseline(shape, host, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -365,19 +402,30 @@ def bench_reference(args, shape, desc):
     oracle.build()
     # Inputs of the same workload on the host; only the experts the sample
     # routes to are materialised (the oracle takes per-expert weights).
-    x = mi.make_x(shape, 0)[:64]
-    logits = mi.make_logits(shape, 0)
-    idx, _ = oracle.route_topk(logits[:64], shape.k)
+    logits = mi.make_logits(shape, 0)[:64]
+    idx, _ = oracle.route_topk(logits, shape.k)
     used = sorted(set(idx.ravel().tolist()))
-    w1 = [None] * shape.E
-    w2 = [None] * shape.E
-    for e in used:  # same distributions as moe_inputs, drawn per used expert
-        g = torch.Generator().manual_seed(1000 + e)
-        w1[e] = torch.randn(2 * shape.F, shape.H, generator=g).mul_(
-            1 / math.sqrt(shape.H)).to(torch.bfloat16)
-        w2[e] = torch.randn(shape.H, shape.F, generator=g).mul_(
-            1 / math.sqrt(shape.F)).to(torch.bfloat16)
-    host = {"x": x, "logits": logits[:64], "w1": w1, "w2": w2}
+    if shape.lowprec:
+        xq, xs = mi.quantize_fp8_rows(mi.make_x(shape.with_T(64), 0).float())
+        host = {"logits": logits, "xq": xq, "xs": xs}
+        for name, rows, cols in (("w1", 2 * shape.F, shape.H), ("w2", shape.H, shape.F)):
+            qs, ss = [None] * shape.E, [None] * shape.E
+            gs = torch.ones(shape.E)
+            for e in used:  # same distributions as moe_inputs, drawn per used expert
+                g = torch.Generator().manual_seed(1000 + e + (0 if name == "w1" else 5000))
+                wf = torch.randn(rows, cols, generator=g).mul_(1 / math.sqrt(cols))
+                qs[e], ss[e], gs[e] = mi.quantize_nvfp4(wf)
+            host[name + "q"], host[name + "s"], host[name + "g"] = qs, ss, gs
+    else:
+        w1 = [None] * shape.E
+        w2 = [None] * shape.E
+        for e in used:  # same distributions as moe_inputs, drawn per used expert
+            g = torch.Generator().manual_seed(1000 + e)
+            w1[e] = torch.randn(2 * shape.F, shape.H, generator=g).mul_(
+                1 / math.sqrt(shape.H)).to(torch.bfloat16)
+            w2[e] = torch.randn(shape.H, shape.F, generator=g).mul_(
+                1 / math.sqrt(shape.F)).to(torch.bfloat16)
+        host = {"x": mi.make_x(shape.with_T(64), 0), "logits": logits, "w1": w1, "w2": w2}
     steps, warm = args.steps, max(args.warmup, 1)
     dt1, _ = oracle_sample(shape, host, 1)
     budget = 150.0 / (steps + warm)

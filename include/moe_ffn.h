@@ -61,7 +61,7 @@ typedef enum {
   MOE_ERR_DEVICE_INDEX = 7        /* a kernel saw an out-of-range index (device status) */
 } moe_status;
 
-typedef enum { MOE_PREC_BF16 = 0 } moe_precision;
+typedef enum { MOE_PREC_BF16 = 0, MOE_PREC_FP8_NVFP4 = 1 } moe_precision;
 
 /* Problem description shared by all entry points. */
 typedef struct moe_problem {
@@ -210,6 +210,43 @@ MOE_API int moe_permute_noalloc(const moe_problem* p, const int32_t* topk_idx, c
                                 void* x_perm, int32_t* row_id_map, int32_t* permuted_token,
                                 int32_t* tokens_per_expert, int32_t* expert_offsets,
                                 void* stream);
+
+/* ---- Low-precision layer (precision = MOE_PREC_FP8_NVFP4) ----------------
+ * The formats of the "[SM90] Add W4A8 MegaMoE support" page's Usage section:
+ * FP8 E4M3 activations with one fp32 scale per 128 channels, NVFP4 weights =
+ * E2M1 codes (two per byte, the even index in the low nibble) with one E4M3
+ * scale per 16 values along K and one fp32 scale per expert weight tensor.
+ * The weights stay 4-bit in HBM.  GEMM1's SwiGLU output is re-quantised to
+ * E4M3 with one fp32 scale (amax / 448) per 128 values of a row before
+ * GEMM2, as that page's split GEMM1 does.  Output bf16.  Token-row tiles
+ * only (moe_problem.kernel and .fusion are ignored). */
+
+/* Bytes of the prepared scale buffer for W1 and W2 together. */
+MOE_API size_t moe_prepared_scales_size(const moe_problem* p);
+
+/* Re-lays the E4M3 block scales of both weight tensors into the order the
+ * kernels stream them (per expert, per 128 weight rows, per 64-deep K step:
+ * 128 rows x 4 scales), the analogue of the page's weight transform before
+ * the call.  Run once per set of weights.
+ *   w1_scale [E, 2F, H/16] bytes, w2_scale [E, H, F/16] bytes (device)
+ *   prepared  device buffer of moe_prepared_scales_size() bytes, 16-aligned */
+MOE_API int moe_prepare_weights(const moe_problem* p, const uint8_t* w1_scale,
+                                const uint8_t* w2_scale, void* prepared, size_t prepared_bytes,
+                                void* stream);
+
+/* The whole low-precision layer.
+ *   xq [T, H] E4M3 codes, xs [T, H/128] fp32, logits [T, E] fp32
+ *   w1q [E, 2F, H/2], w2q [E, H, F/2] packed E2M1 codes (GLU interleave as
+ *   in moe_problem), w1_gscale / w2_gscale [E] fp32, prepared scales from
+ *   moe_prepare_weights; out [T, H] bf16; optional routing copies as in
+ *   moe_forward; ws of moe_workspace_size(p) bytes. */
+MOE_API int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* xs,
+                                  const float* logits, const uint8_t* w1q,
+                                  const float* w1_gscale, const uint8_t* w2q,
+                                  const float* w2_gscale, const void* prepared_scales, void* out,
+                                  int32_t* topk_idx_out, float* topk_w_out,
+                                  int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes,
+                                  void* stream);
 
 /* Synchronises `stream`, returns the status the kernels recorded in `ws`
  * since the last moe_clear_device_status (MOE_OK if none). */

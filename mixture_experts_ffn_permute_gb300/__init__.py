@@ -54,9 +54,10 @@ class Problem(ctypes.Structure):
 
     @classmethod
     def make(cls, T, H, F, E, k, renormalize=True, glu_interleave=0, swiglu_clamp=0.0,
-             fusion=0, kernel=0):
+             fusion=0, kernel=0, precision=0):
         return cls(int(T), int(H), int(F), int(E), int(k), int(bool(renormalize)),
-                   int(glu_interleave), float(swiglu_clamp), 0, int(fusion), int(kernel))
+                   int(glu_interleave), float(swiglu_clamp), int(precision), int(fusion),
+                   int(kernel))
 
 
 _lib = None
@@ -89,6 +90,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                   ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)], ci),
         "moe_stage_name": ([ci], ctypes.c_char_p),
         "moe_permute_noalloc": ([pp, vp, vp, vp, vp, vp, vp, vp, vp], ci),
+        "moe_prepared_scales_size": ([pp], sz),
+        "moe_prepare_weights": ([pp, vp, vp, vp, sz, vp], ci),
+        "moe_forward_fp8_nvfp4": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                   vp], ci),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -199,6 +204,28 @@ def forward(p: Problem, x, logits, w1, w2, out, ws, topk_idx=None, topk_w=None,
           ws.numel(), _stream(stream))
 
 
+PREC_BF16 = 0
+PREC_FP8_NVFP4 = 1
+
+
+def prepared_scales_size(p: Problem) -> int:
+    return int(load().moe_prepared_scales_size(ctypes.byref(p)))
+
+
+def prepare_weights(p: Problem, w1_scale, w2_scale, prepared, stream=None) -> None:
+    """Re-lay NVFP4 block scales into the order the low-precision kernels stream them."""
+    _call("moe_prepare_weights", ctypes.byref(p), _ptr(w1_scale), _ptr(w2_scale), _ptr(prepared),
+          prepared.numel() * prepared.element_size(), _stream(stream))
+
+
+def forward_fp8_nvfp4(p: Problem, xq, xs, logits, w1q, w1_gscale, w2q, w2_gscale, prepared,
+                      out, ws, topk_idx=None, topk_w=None, tokens_per_expert=None,
+                      stream=None) -> None:
+    _call("moe_forward_fp8_nvfp4", ctypes.byref(p), _ptr(xq), _ptr(xs), _ptr(logits), _ptr(w1q),
+          _ptr(w1_gscale), _ptr(w2q), _ptr(w2_gscale), _ptr(prepared), _ptr(out), _ptr(topk_idx),
+          _ptr(topk_w), _ptr(tokens_per_expert), _ptr(ws), ws.numel(), _stream(stream))
+
+
 class MoEFFN:
     """Convenience holder: weights + a reusable workspace for one problem size."""
 
@@ -237,4 +264,5 @@ class MoEFFN:
 __all__ = ["Problem", "MoEError", "MoEFFN", "load", "workspace_size", "alloc_workspace",
            "route_topk", "permute", "grouped_swiglu_mlp", "unpermute_combine", "forward",
            "get_device_status", "clear_device_status", "last_launch_count", "LIB_PATH",
-           "stage_timing_begin", "stage_timing_end", "permute_noalloc"]
+           "stage_timing_begin", "stage_timing_end", "permute_noalloc",
+           "prepared_scales_size", "prepare_weights", "forward_fp8_nvfp4"]

@@ -104,7 +104,8 @@ int check_full(const moe_problem* p) {
   int rc = check_routing(p);
   if (rc != MOE_OK) return rc;
   if (p->H <= 0 || p->F <= 0) return MOE_ERR_INVALID_ARG;
-  if (p->precision != MOE_PREC_BF16) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (p->precision != MOE_PREC_BF16 && p->precision != MOE_PREC_FP8_NVFP4)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
   if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
   if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_WEIGHT_TILES) return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
@@ -331,6 +332,7 @@ int moe_grouped_swiglu_mlp(const moe_problem* p, const void* x_perm,
                            void* y_perm, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_full(p);
   if (rc != MOE_OK) return rc;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
   rc = check_ws(p, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
   MOE_REQUIRE_PTR(expert_offsets);
@@ -374,6 +376,7 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
                 int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_full(p);
   if (rc != MOE_OK) return rc;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
   rc = check_ws(p, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
   MOE_REQUIRE_PTR(w1);
@@ -432,6 +435,137 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
                call, 6, &fused);
   if (rc != MOE_OK) return rc;
   if (!fuse_combine) MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
+  tm.mark(call, 8, s);
+  g_launches = launches;
+  return MOE_OK;
+}
+
+size_t moe_prepared_scales_size(const moe_problem* p) {
+  if (check_full(p) != MOE_OK) return 0;
+  return static_cast<size_t>(p->E) * (2 * static_cast<size_t>(p->F) * p->H / 16 +
+                                      static_cast<size_t>(p->H) * p->F / 16);
+}
+
+int moe_prepare_weights(const moe_problem* p, const uint8_t* w1_scale, const uint8_t* w2_scale,
+                        void* prepared, size_t prepared_bytes, void* stream) {
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  if (p->precision != MOE_PREC_FP8_NVFP4) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE_PTR(w1_scale);
+  MOE_REQUIRE_PTR(w2_scale);
+  MOE_REQUIRE_PTR(prepared);
+  if (prepared_bytes < moe_prepared_scales_size(p)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* dst = static_cast<uint8_t*>(prepared);
+  MOE_LAUNCH(launch_prepare_scales(w1_scale, dst, p->E, 2 * p->F, p->H, s));
+  MOE_LAUNCH(launch_prepare_scales(w2_scale, dst + static_cast<size_t>(p->E) * 2 * p->F * p->H / 16,
+                                   p->E, p->H, p->F, s));
+  g_launches = launches;
+  return MOE_OK;
+}
+
+int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* xs,
+                          const float* logits, const uint8_t* w1q, const float* w1_gscale,
+                          const uint8_t* w2q, const float* w2_gscale, const void* prepared_scales,
+                          void* out, int32_t* topk_idx_out, float* topk_w_out,
+                          int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes,
+                          void* stream) {
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  if (p->precision != MOE_PREC_FP8_NVFP4) return MOE_ERR_INVALID_ARG;
+  rc = check_ws(p, ws, ws_bytes);
+  if (rc != MOE_OK) return rc;
+  MOE_REQUIRE_PTR(w1q);
+  MOE_REQUIRE_PTR(w2q);
+  MOE_REQUIRE_PTR(w1_gscale);
+  MOE_REQUIRE_PTR(w2_gscale);
+  MOE_REQUIRE_PTR(prepared_scales);
+  if (topk_idx_out && !aligned16(topk_idx_out)) return MOE_ERR_MISALIGNED;
+  if (topk_w_out && !aligned16(topk_w_out)) return MOE_ERR_MISALIGNED;
+  if (tokens_per_expert_out && !aligned16(tokens_per_expert_out)) return MOE_ERR_MISALIGNED;
+  const Layout L = layout_of(*p);
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* tpe = tokens_per_expert_out ? tokens_per_expert_out
+                                       : at<int32_t>(ws, L.tokens_per_expert);
+  if (p->T == 0) {
+    if (tokens_per_expert_out)
+      MOE_LAUNCH(cudaMemsetAsync(tokens_per_expert_out, 0, sizeof(int32_t) * p->E, s));
+    g_launches = launches;
+    return MOE_OK;
+  }
+  MOE_REQUIRE_PTR(xq);
+  MOE_REQUIRE_PTR(xs);
+  MOE_REQUIRE_PTR(logits);
+  MOE_REQUIRE_PTR(out);
+  const int R = p->T * p->k;
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.topk_idx);
+  float* wts = topk_w_out ? topk_w_out : at<float>(ws, L.topk_w);
+  int32_t* off = at<int32_t>(ws, L.expert_offsets);
+  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
+  int32_t* rmap = at<int32_t>(ws, L.row_id_map);
+  int32_t* ptok = at<int32_t>(ws, L.permuted_token);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h = at<void>(ws, L.h);
+  void* y = at<void>(ws, L.y);
+  const uint8_t* sc1 = static_cast<const uint8_t*>(prepared_scales);
+  const uint8_t* sc2 = sc1 + static_cast<size_t>(p->E) * 2 * p->F * p->H / 16;
+
+  const int call = g_timer.on ? g_timer.used++ : 0;
+  StageTimer& tm = g_timer;
+  tm.mark(call, 0, s);
+  MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
+  tm.mark(call, 1, s);
+  if (permute_small_fits(p->T, p->E, p->k)) {
+    MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
+    for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
+  } else {
+    rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2);
+    if (rc != MOE_OK) return rc;
+  }
+  MOE_LAUNCH(launch_gather_dequant_fp8(xq, xs, ptok, R, p->H, x_perm, s));
+  tm.mark(call, 5, s);
+  GroupedGemmArgs g1{};
+  g1.epi = Epi::kSwiGLU;
+  g1.a = x_perm;
+  g1.a_rows = R;
+  g1.b = w1q;
+  g1.b_rows_per_expert = 2 * p->F;
+  g1.E = p->E;
+  g1.K = p->H;
+  g1.n_tiles = p->F / (kBN / 2);
+  g1.expert_offsets = off;
+  g1.mtile_prefix = mtp;
+  g1.out = h;
+  g1.ldo = p->F;
+  g1.out_rows = R;
+  g1.F = p->F;
+  g1.interleave = p->glu_interleave;
+  g1.clamp = clamp_of(p);
+  g1.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_fp4(g1, sc1, w1_gscale, s));
+  tm.mark(call, 6, s);
+  GroupedGemmArgs g2{};
+  g2.epi = Epi::kPlain;
+  g2.a = h;
+  g2.a_rows = R;
+  g2.b = w2q;
+  g2.b_rows_per_expert = p->H;
+  g2.E = p->E;
+  g2.K = p->F;
+  g2.n_tiles = p->H / kBN;
+  g2.expert_offsets = off;
+  g2.mtile_prefix = mtp;
+  g2.out = y;
+  g2.ldo = p->H;
+  g2.out_rows = R;
+  g2.F = p->F;
+  g2.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_fp4(g2, sc2, w2_gscale, s));
+  tm.mark(call, 7, s);
+  MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
   tm.mark(call, 8, s);
   g_launches = launches;
   return MOE_OK;

@@ -106,4 +106,17 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s);
 // decode sizes (kSwiGLU and kPlain epilogues; no gather / combine fusion).
 cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s);
 
+// NVFP4-weight GEMMs (a = f16 rows, b = packed E2M1 codes [E * rows, K / 2],
+// scales in the prepared layout, gscale = per-expert fp32 tensor scales).
+// kSwiGLU stores FP8-requantised h as f16; kPlain stores bf16 y.
+cudaError_t launch_grouped_gemm_fp4(const GroupedGemmArgs& g, const uint8_t* scales,
+                                    const float* gscale, cudaStream_t s);
+// [E][N][K/16] E4M3 scales -> [E][N/128][K/64][128][4]
+cudaError_t launch_prepare_scales(const uint8_t* src, uint8_t* dst, int E, int N, int K,
+                                  cudaStream_t s);
+// FP8 rows (E4M3 codes + fp32 scales per 128) gathered by permuted_token into f16.
+cudaError_t launch_gather_dequant_fp8(const uint8_t* xq, const float* xs,
+                                      const int32_t* permuted_token, int R, int H, void* x_perm,
+                                      cudaStream_t s);
+
 }  // namespace moe
