@@ -40,20 +40,27 @@ bool make_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 
 namespace {
 
-constexpr int kStagesF = 3;
+// Three rings: activations (TMA), packed weight codes + scales (TMA + bulk
+// copy; deep, so HBM latency is covered), and the expanded f16 weight tiles
+// the MMA reads (written by the transform warps).
+constexpr int kStagesA = 4;
+constexpr int kStagesR = 6;
+constexpr int kStagesB = 3;
 constexpr int kThreadsF = 448;
 constexpr int kTransformThreads = 256;
 constexpr uint32_t kABytesF = kBM * kBK * 2;       // 16 KB f16
 constexpr uint32_t kB16Bytes = kBN * kBK * 2;      // 32 KB f16
 constexpr uint32_t kRawBytes = kBN * kBK / 2;      // 8 KB packed E2M1
 constexpr uint32_t kScBytes = kBN * kBK / 16;      // 1 KB E4M3 scales
-constexpr uint32_t kTxBytesF = kABytesF + kRawBytes + kScBytes;
+constexpr uint32_t kTxRaw = kRawBytes + kScBytes;
 constexpr uint32_t kTmemColsF = 2 * kBN;
 // kind::f16 with f16 A and B (format 0), fp32 accumulator
 constexpr uint32_t kIdescF16 = (1u << 4) | ((kBN >> 3) << 17) | ((kBM >> 4) << 24);
 constexpr int kMaxEF = 1024;
-constexpr size_t kSmemBytesF = 1024 + kStagesF * (kABytesF + kB16Bytes + kRawBytes + kScBytes) +
-                               256 + 2 * (kMaxEF + 1) * sizeof(int32_t);
+constexpr size_t kRingBytes = kStagesA * kABytesF + kStagesB * kB16Bytes +
+                              kStagesR * (kRawBytes + kScBytes);
+constexpr size_t kSmemBytesF = 1024 + kRingBytes + 256 + 2 * (kMaxEF + 1) * sizeof(int32_t);
+static_assert(kSmemBytesF <= 232448, "shared memory budget");
 
 struct FParams {
   const int32_t* expert_offsets;
@@ -137,23 +144,26 @@ template <Epi kEpi>
 __global__ void __launch_bounds__(kThreadsF, 1)
 grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_q, const FParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base, kept as a shared-array pointer so that accesses
+  // compile to shared-memory instructions
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;
-  uint8_t* sB = sA + kStagesF * kABytesF;
-  uint8_t* sRaw = sB + kStagesF * kB16Bytes;
-  uint8_t* sSc = sRaw + kStagesF * kRawBytes;
-  uint64_t* tfull = reinterpret_cast<uint64_t*>(sSc + kStagesF * kScBytes);
-  uint64_t* bfull = tfull + kStagesF;
-  uint64_t* empty = bfull + kStagesF;
-  uint64_t* afull = empty + kStagesF;   // accumulator ready
-  uint64_t* aempty = afull + 2;         // accumulator drained
+  uint8_t* sB = sA + kStagesA * kABytesF;
+  uint8_t* sRaw = sB + kStagesB * kB16Bytes;
+  uint8_t* sSc = sRaw + kStagesR * kRawBytes;
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + kRingBytes);
+  uint64_t* a_empty = a_full + kStagesA;
+  uint64_t* r_full = a_empty + kStagesA;
+  uint64_t* r_empty = r_full + kStagesR;
+  uint64_t* b_full = r_empty + kStagesR;
+  uint64_t* b_empty = b_full + kStagesB;
+  uint64_t* afull = b_empty + kStagesB;  // accumulator ready
+  uint64_t* aempty = afull + 2;          // accumulator drained
   uint64_t* drain = aempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* s_off = reinterpret_cast<int32_t*>(
-      sSc + kStagesF * kScBytes + 256);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kRingBytes + 256);
   int32_t* s_mtp = s_off + (p.E + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,10 +172,17 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
     s_mtp[i] = p.mtile_prefix[i];
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesF; ++s) {
-      mbar_init(&tfull[s], 1);
-      mbar_init(&bfull[s], kTransformThreads);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kStagesA; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < kStagesR; ++s) {
+      mbar_init(&r_full[s], 1);
+      mbar_init(&r_empty[s], kTransformThreads);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
+      mbar_init(&b_full[s], kTransformThreads);
+      mbar_init(&b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&afull[b], 1);
@@ -193,8 +210,8 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
     if (lane == 0) {
       const uint64_t pol_a = policy_evict_last();
       const uint64_t pol_b = policy_evict_normal();
-      int stage = 0;
-      uint32_t phase = 0;
+      int sa = 0, sr = 0;
+      uint32_t pa = 0, pr = 0;
       long issued = 0;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
         const FTile t = decode_ftile(tile, s_mtp, p.E, p.n_tiles);
@@ -221,31 +238,41 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
         const uint8_t* sc0 = p.scales + ((rb_base + r0 / 128) * kblocks) * 512;
         const uint8_t* sc1 = p.scales + ((rb_base + r1 / 128) * kblocks) * 512;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { *abort_flag = 1; break; }
-          mbar_arrive_expect_tx(&tfull[stage], kTxBytesF);
-          tma_load_2d(sA + stage * kABytesF, &map_a, kb * kBK, a_row, &tfull[stage], pol_a);
-          uint8_t* raw = sRaw + stage * kRawBytes;
-          tma_load_2d(raw, &map_q, kb * (kBK / 2), qrow0, &tfull[stage], pol_b);
-          tma_load_2d(raw + kRawBytes / 2, &map_q, kb * (kBK / 2), qrow1, &tfull[stage], pol_b);
-          uint8_t* sc = sSc + stage * kScBytes;
-          bulk_load(sc, sc0 + static_cast<long>(kb) * 512, 512, &tfull[stage]);
-          bulk_load(sc + 512, sc1 + static_cast<long>(kb) * 512, 512, &tfull[stage]);
+          if (!mbar_wait(&a_empty[sa], pa ^ 1, p.status)) { *abort_flag = 1; break; }
+          mbar_arrive_expect_tx(&a_full[sa], kABytesF);
+          tma_load_2d(sA + sa * kABytesF, &map_a, kb * kBK, a_row, &a_full[sa], pol_a);
+          if (!mbar_wait(&r_empty[sr], pr ^ 1, p.status)) { *abort_flag = 1; break; }
+          mbar_arrive_expect_tx(&r_full[sr], kTxRaw);
+          uint8_t* raw = sRaw + sr * kRawBytes;
+          tma_load_2d(raw, &map_q, kb * (kBK / 2), qrow0, &r_full[sr], pol_b);
+          tma_load_2d(raw + kRawBytes / 2, &map_q, kb * (kBK / 2), qrow1, &r_full[sr], pol_b);
+          uint8_t* sc = sSc + sr * kScBytes;
+          bulk_load(sc, sc0 + static_cast<long>(kb) * 512, 512, &r_full[sr]);
+          bulk_load(sc + 512, sc1 + static_cast<long>(kb) * 512, 512, &r_full[sr]);
           ++issued;
-          if (++stage == kStagesF) { stage = 0; phase ^= 1; }
+          if (++sa == kStagesA) { sa = 0; pa ^= 1; }
+          if (++sr == kStagesR) { sr = 0; pr ^= 1; }
         }
       }
-      for (int i = 1; i <= kStagesF && i <= issued; ++i) {
-        int s = stage - i;
-        uint32_t ph = phase;
-        if (s < 0) { s += kStagesF; ph ^= 1; }
-        mbar_wait(&tfull[s], ph, p.status);
+      // Leave no bulk copy in flight.
+      for (int i = 1; i <= kStagesA && i <= issued; ++i) {
+        int s = sa - i;
+        uint32_t ph = pa;
+        if (s < 0) { s += kStagesA; ph ^= 1; }
+        mbar_wait(&a_full[s], ph, p.status);
+      }
+      for (int i = 1; i <= kStagesR && i <= issued; ++i) {
+        int s = sr - i;
+        uint32_t ph = pr;
+        if (s < 0) { s += kStagesR; ph ^= 1; }
+        mbar_wait(&r_full[s], ph, p.status);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int sa = 0, sb = 0;
+      uint32_t pa = 0, pb = 0;
       int local = 0;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++local) {
         const int buf = local & 1;
@@ -255,16 +282,20 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
         const uint32_t d_tmem = tmem_base + buf * kBN;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&tfull[stage], phase, p.status) ||
-              !mbar_wait(&bfull[stage], phase, p.status)) { ok = false; break; }
+          if (!mbar_wait(&a_full[sa], pa, p.status) || !mbar_wait(&b_full[sb], pb, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint64_t a_desc = sw128_kmajor_desc(smem_u32(sA + stage * kABytesF));
-          const uint64_t b_desc = sw128_kmajor_desc(smem_u32(sB + stage * kB16Bytes));
+          const uint64_t a_desc = sw128_kmajor_desc(smem_u32(sA + sa * kABytesF));
+          const uint64_t b_desc = sw128_kmajor_desc(smem_u32(sB + sb * kB16Bytes));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             mma_bf16_ss(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, kIdescF16, (kb | kk) != 0);
-          mma_commit(&empty[stage]);
-          if (++stage == kStagesF) { stage = 0; phase ^= 1; }
+          mma_commit(&a_empty[sa]);
+          mma_commit(&b_empty[sb]);
+          if (++sa == kStagesA) { sa = 0; pa ^= 1; }
+          if (++sb == kStagesB) { sb = 0; pb ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
         mma_commit(&afull[buf]);
@@ -275,22 +306,26 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
   } else if (warp >= 6) {
     // ---------------------------------------------------------------- transform
     const int row = threadIdx.x - 6 * 32;  // weight row of the B tile, 0..255
-    int stage = 0;
-    uint32_t phase = 0;
+    int sr = 0, sb = 0;
+    uint32_t pr = 0, pb = 0;
     for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
       bool ok = true;
       for (int kb = 0; kb < num_kb; ++kb) {
-        if (!mbar_wait(&tfull[stage], phase, p.status)) { ok = false; break; }
-        const uint8_t* raw = sRaw + stage * kRawBytes + row * 32;
+        if (!mbar_wait(&r_full[sr], pr, p.status) || !mbar_wait(&b_empty[sb], pb ^ 1, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* raw = sRaw + sr * kRawBytes + row * 32;
         const uint4 q0 = *reinterpret_cast<const uint4*>(raw);
         const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 16);
-        const uint32_t sw = *reinterpret_cast<const uint32_t*>(sSc + stage * kScBytes + row * 4);
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(sSc + sr * kScBytes + row * 4);
+        mbar_arrive(&r_empty[sr]);  // codes and scales are in registers now
         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        uint8_t* dst = sB + stage * kB16Bytes + row * 128;
+        uint8_t* dst = sB + sb * kB16Bytes + row * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // 16 values per E4M3 scale
-          const uint32_t sb = (sw >> (8 * j)) & 0xFFu;
-          const uint32_t s2 = e4m3x2_to_f16x2(sb | (sb << 8));
+          const uint32_t sbyte = (sw >> (8 * j)) & 0xFFu;
+          const uint32_t s2 = e4m3x2_to_f16x2(sbyte | (sbyte << 8));
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {  // two 16-byte chunks of 8 values
             const uint32_t w = qw[2 * j + h2];
@@ -304,8 +339,9 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bfull[stage]);
-        if (++stage == kStagesF) { stage = 0; phase ^= 1; }
+        mbar_arrive(&b_full[sb]);
+        if (++sr == kStagesR) { sr = 0; pr ^= 1; }
+        if (++sb == kStagesB) { sb = 0; pb ^= 1; }
       }
       if (!ok) { *abort_flag = 1; break; }
     }
