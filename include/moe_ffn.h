@@ -88,11 +88,15 @@ typedef struct moe_problem {
      Both give results within the same tolerance of the exact layer. */
   int32_t fusion;
   /* GEMM tiling (moe_problem.kernel):
-       MOE_KERNEL_AUTO          weight-row tiles when T*k <= 32*E, else token-row tiles
+       MOE_KERNEL_AUTO          T*k <= 32*E: weight-row tiles; <= 512*E: wide
+                                weight-row tiles; else token-row tiles
        MOE_KERNEL_TOKEN_TILES   128 permuted token rows x 256 weight rows per tile
-       MOE_KERNEL_WEIGHT_TILES  128 weight rows x 32 token rows per tile (decode
-                                sizes: weights stream once at HBM speed); the
-                                fusion options do not apply to it. */
+       MOE_KERNEL_WEIGHT_TILES  128 weight rows x up to 32 token rows per tile
+                                (decode sizes: weights stream once at HBM speed)
+       MOE_KERNEL_WEIGHT_TILES_WIDE  128 weight rows x up to 256 token rows per
+                                tile, N fitted to the expert's rows (ragged
+                                experts pad at most 15 rows)
+     The fusion options do not apply to the weight-row tilings. */
   int32_t kernel;
 } moe_problem;
 
@@ -101,6 +105,7 @@ typedef struct moe_problem {
 #define MOE_KERNEL_AUTO 0
 #define MOE_KERNEL_TOKEN_TILES 1
 #define MOE_KERNEL_WEIGHT_TILES 2
+#define MOE_KERNEL_WEIGHT_TILES_WIDE 3
 
 /* Limits checked by every entry point. */
 #define MOE_MAX_EXPERTS 1024

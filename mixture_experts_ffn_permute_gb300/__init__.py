@@ -30,7 +30,8 @@ FUSE_GATHER_A = 1   # GEMM1 gathers A rows from x with TMA gather4
 FUSE_COMBINE = 2    # weighted top-k reduction in GEMM2's epilogue
 KERNEL_AUTO = 0
 KERNEL_TOKEN_TILES = 1   # 128 token rows x 256 weight rows per tile
-KERNEL_WEIGHT_TILES = 2  # 128 weight rows x 32 token rows per tile (decode sizes)
+KERNEL_WEIGHT_TILES = 2  # 128 weight rows x up to 32 token rows per tile (decode sizes)
+KERNEL_WEIGHT_TILES_WIDE = 3  # 128 weight rows x up to 256 token rows, N fitted per tile
 STATUS_NAMES = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
     3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",

@@ -107,7 +107,8 @@ int check_full(const moe_problem* p) {
   if (p->precision != MOE_PREC_BF16 && p->precision != MOE_PREC_FP8_NVFP4)
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
-  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_WEIGHT_TILES) return MOE_ERR_INVALID_ARG;
+  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_WEIGHT_TILES_WIDE)
+    return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
   if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int I = p->glu_interleave;
@@ -139,12 +140,18 @@ int check_ws(const moe_problem* p, void* ws, size_t ws_bytes) {
     ++launches;                                   \
   } while (0)
 
-// Weight-row tiles (swap-AB) when experts see few tokens on average.
-bool use_weight_tiles(const moe_problem* p) {
-  if (p->kernel == MOE_KERNEL_WEIGHT_TILES) return true;
-  if (p->kernel == MOE_KERNEL_TOKEN_TILES) return false;
-  return static_cast<long long>(p->T) * p->k <= 32LL * p->E;
+// GEMM tiling for this problem: weight-row tiles (swap-AB) when experts see
+// few tokens on average.
+int gemm_tiling(const moe_problem* p) {
+  if (p->kernel != MOE_KERNEL_AUTO) return p->kernel;
+  const long long routes = static_cast<long long>(p->T) * p->k;
+  if (routes <= 32LL * p->E) return MOE_KERNEL_WEIGHT_TILES;
+  // ragged experts of up to a few hundred rows: N fitted per expert
+  if (routes <= 512LL * p->E) return MOE_KERNEL_WEIGHT_TILES_WIDE;
+  return MOE_KERNEL_TOKEN_TILES;
 }
+
+bool use_weight_tiles(const moe_problem* p) { return gemm_tiling(p) != MOE_KERNEL_TOKEN_TILES; }
 
 float clamp_of(const moe_problem* p) {
   const float c = p->swiglu_clamp;
@@ -191,7 +198,8 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
     g1.permuted_token = fused->permuted_token;
     g1.x_rows = p->T;
   }
-  MOE_LAUNCH(swap ? launch_grouped_gemm_swap(g1, s) : launch_grouped_gemm(g1, s));
+  const bool wide = gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES_WIDE;
+  MOE_LAUNCH(swap ? launch_grouped_gemm_swap(g1, wide, s) : launch_grouped_gemm(g1, s));
   if (tm) tm->mark(call, mark, s);
   GroupedGemmArgs g2{};
   g2.epi = Epi::kPlain;
@@ -219,7 +227,7 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
     g2.counters = fused->counters;
     g2.k = p->k;
   }
-  MOE_LAUNCH(swap ? launch_grouped_gemm_swap(g2, s) : launch_grouped_gemm(g2, s));
+  MOE_LAUNCH(swap ? launch_grouped_gemm_swap(g2, wide, s) : launch_grouped_gemm(g2, s));
   if (tm) tm->mark(call, mark + 1, s);
   return MOE_OK;
 }

@@ -1,15 +1,19 @@
 // Decode-sized grouped GEMMs: the weight rows are the MMA's M side and the
 // few tokens of each expert its N side ("swap-AB").
 //
-// At decode sizes an expert sees a handful of tokens, so a 128-token-row tile
-// would be almost empty and every CTA would pull a 128-row activation tile
-// from L2 for each 64-deep K step while reading far fewer weight bytes from
-// HBM.  Here a tile is 128 weight rows x kN (= 32) token rows:
-//   D[128 x kN] = W[128 weight rows of e, K] * X[kN token rows of e, K]^T
-// so each K step moves 16 KB of weights and 4 KB of activations, and the
-// layer streams its weights once at HBM speed.  The tile count is
-// (expert, weight-row tile, token tile), token tiles fastest so that CTAs
-// sharing a weight tile run together and the second read hits L2.
+// A tile is 128 weight rows x up to kNmax token rows of one expert:
+//   D[128 x N] = W[128 weight rows of e, K] * X[N token rows of e, K]^T
+// with N = the expert's remaining rows rounded up to 16 (at most kNmax), set
+// per tile in the instruction descriptor.  Two instances:
+//   kNmax = 32,  8 stages: decode sizes, where an expert sees a handful of
+//     tokens: a K step moves 16 KB of weights and 4 KB of activations, so
+//     the weights stream once at HBM speed;
+//   kNmax = 256, 4 stages: ragged experts of tens to hundreds of rows: a
+//     token tile pads at most 15 rows, where a 128-row token tile pads up to
+//     127 (the full MMA shape 128 x 256 when the expert has the rows).
+// Tokens are loaded in 32-row boxes, only as many as the tile needs.  The
+// tile count is (expert, weight-row tile, token tile), token tiles fastest so
+// that CTAs sharing a weight tile run together and the second read hits L2.
 //
 // Epilogues:
 //   GEMM1 (kSwiGLU): the 128 weight rows are 64 gate rows and the matching
@@ -37,20 +41,28 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 
 namespace {
 
-constexpr int kN = 32;                                 // token rows per tile
 constexpr int kM = 128;                                // weight rows per tile
-constexpr int kStagesS = 8;
+constexpr int kXBox = 32;                              // token rows per small TMA box
+constexpr int kXBoxWide = 128;                         // token rows per large TMA box
 constexpr int kThreadsS = 192;
 constexpr uint32_t kWBytes = kM * kBK * 2;             // 16 KB
-constexpr uint32_t kXBytes = kN * kBK * 2;             // 4 KB
-constexpr uint32_t kStageBytesS = kWBytes + kXBytes;   // 20 KB
-constexpr uint32_t kTmemColsS = 64;                    // two kN-column accumulators
-constexpr uint32_t kIdescS = idesc_bf16_f32(kM, kN);
 constexpr int kMaxES = 1024;
-constexpr int kDPitch = kN + 1;                        // padded fp32 row of the exchange tile
-constexpr size_t kSmemBytesS = 1024 + kStagesS * kStageBytesS + 256 +
-                               3 * (kMaxES + 1) * sizeof(int32_t) +
-                               kM * kDPitch * sizeof(float);
+constexpr int kDPitch = 33;                            // padded fp32 row of the exchange chunk
+// wide instance: token tiles of up to kWideN rows, kWideStages-deep ring
+constexpr int kWideN = 256;
+constexpr int kWideStages = 4;
+
+template <int kNmax, int kStages>
+struct SwapCfg {
+  static constexpr uint32_t kXBytes = kNmax * kBK * 2;
+  static constexpr uint32_t kStageBytes = kWBytes + kXBytes;
+  static constexpr uint32_t kTmemCols = 2 * kNmax;     // two accumulators
+  static constexpr size_t kSmem = 1024 + kStages * kStageBytes + 256 +
+                                  3 * (kMaxES + 1) * sizeof(int32_t) +
+                                  kM * kDPitch * sizeof(float);
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kTmemCols >= 32 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM allocation");
+};
 
 struct SParams {
   const int32_t* expert_offsets;
@@ -82,24 +94,26 @@ __device__ __forceinline__ STile decode_stile(int tile, const int32_t* tp, const
 
 __device__ __forceinline__ float silu_s(float z) { return z / (1.0f + expf(-z)); }
 
-template <Epi kEpi>
+template <Epi kEpi, int kNmax, int kStages>
 __global__ void __launch_bounds__(kThreadsS, 1)
 grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
-                         const __grid_constant__ CUtensorMap map_x, const SParams p) {
+                         const __grid_constant__ CUtensorMap map_x,
+                         const __grid_constant__ CUtensorMap map_xw, const SParams p) {
+  using Cfg = SwapCfg<kNmax, kStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, kept as a shared-array pointer so that accesses
   // compile to shared-memory instructions
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sW = smem;
-  uint8_t* sX = smem + kStagesS * kWBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sX + kStagesS * kXBytes);
-  uint64_t* empty = full + kStagesS;
-  uint64_t* tfull = empty + kStagesS;
+  uint8_t* sX = smem + kStages * kWBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sX + kStages * Cfg::kXBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStagesS * kStageBytesS + 256);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * Cfg::kStageBytes + 256);
   int32_t* s_tp = s_off + (kMaxES + 1);   // tile prefix per expert
   int32_t* s_ntk = s_tp + (kMaxES + 1);   // token tiles per expert
   float* sD = reinterpret_cast<float*>(s_ntk + (kMaxES + 1));
@@ -107,7 +121,7 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i <= p.E; i += kThreadsS) s_off[i] = p.expert_offsets[i];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesS; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -122,11 +136,12 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&map_w);
     prefetch_tensormap(&map_x);
+    if (kNmax > kXBox) prefetch_tensormap(&map_xw);
   }
-  if (warp == 1) tmem_alloc<kTmemColsS>(tmem_slot);
+  if (warp == 1) tmem_alloc<Cfg::kTmemCols>(tmem_slot);
   __syncthreads();
-  // tile prefix: expert e owns w_tiles * ceil(rows_e / kN) tiles.  Thread i
-  // scans a run of at most ceil(E / 192) experts; runs are then offset by a
+  // tile prefix: expert e owns w_tiles * ceil(rows_e / kNmax) tiles.  Thread
+  // i scans a run of at most ceil(E / 192) experts; runs are then offset by a
   // scan over the threads.
   {
     __shared__ int s_part[kThreadsS / 32];
@@ -135,7 +150,7 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
     int run = 0;
     for (int e = e0; e < e1; ++e) {
       const int rows = s_off[e + 1] - s_off[e];
-      const int nt = rows > 0 ? (rows + kN - 1) / kN : 0;
+      const int nt = rows > 0 ? (rows + kNmax - 1) / kNmax : 0;
       s_ntk[e] = nt;
       run += nt * p.w_tiles;
     }
@@ -177,7 +192,14 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
       long issued = 0;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
         const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
-        const int x_row = s_off[t.e] + t.n * kN;
+        const int tok0 = t.n * kNmax;
+        const int nval = min(kNmax, s_off[t.e + 1] - s_off[t.e] - tok0);
+        // few TMA ops per stage: one 32-row box, or 128-row boxes
+        const bool wide_box = kNmax > kXBox && nval > kXBox;
+        const int box_rows = wide_box ? kXBoxWide : kXBox;
+        const int nbox = (nval + box_rows - 1) / box_rows;
+        const uint32_t x_bytes = static_cast<uint32_t>(nbox * box_rows * kBK * 2);
+        const int x_row = s_off[t.e] + tok0;
         int w_row0, w_row1;
         if (kEpi == Epi::kSwiGLU) {
           const int f0 = t.m * (kM / 2);
@@ -199,20 +221,23 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
         w_row1 += t.e * p.w_rows_per_expert;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { *abort_flag = 1; break; }
-          mbar_arrive_expect_tx(&full[stage], kStageBytesS);
+          mbar_arrive_expect_tx(&full[stage], kWBytes + x_bytes);
           const int kx = kb * kBK;
           uint8_t* w_dst = sW + stage * kWBytes;
           tma_load_2d(w_dst, &map_w, kx, w_row0, &full[stage], pol_w);
           tma_load_2d(w_dst + kWBytes / 2, &map_w, kx, w_row1, &full[stage], pol_w);
-          tma_load_2d(sX + stage * kXBytes, &map_x, kx, x_row, &full[stage], pol_x);
+          uint8_t* x_dst = sX + stage * Cfg::kXBytes;
+          for (int b = 0; b < nbox; ++b)
+            tma_load_2d(x_dst + b * box_rows * kBK * 2, wide_box ? &map_xw : &map_x, kx,
+                        x_row + b * box_rows, &full[stage], pol_x);
           ++issued;
-          if (++stage == kStagesS) { stage = 0; phase ^= 1; }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      for (int i = 1; i <= kStagesS && i <= issued; ++i) {
+      for (int i = 1; i <= kStages && i <= issued; ++i) {
         int s = stage - i;
         uint32_t ph = phase;
-        if (s < 0) { s += kStagesS; ph ^= 1; }
+        if (s < 0) { s += kStages; ph ^= 1; }
         mbar_wait(&full[s], ph, p.status);
       }
     }
@@ -225,20 +250,24 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++local) {
         const int buf = local & 1;
         const uint32_t tph = (local >> 1) & 1;
+        const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
+        const int nval = min(kNmax, s_off[t.e + 1] - s_off[t.e] - t.n * kNmax);
+        const uint32_t nmma = static_cast<uint32_t>((nval + 15) & ~15);  // MMA N: multiple of 16
+        const uint32_t idesc = idesc_bf16_f32(kM, nmma);
         if (!mbar_wait(&tempty[buf], tph ^ 1, p.status)) { *abort_flag = 1; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * kN;
+        const uint32_t d_tmem = tmem_base + buf * kNmax;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint64_t w_desc = sw128_kmajor_desc(smem_u32(sW + stage * kWBytes));
-          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + stage * kXBytes));
+          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + stage * Cfg::kXBytes));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, kIdescS, (kb | kk) != 0);
+            mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
           mma_commit(&empty[stage]);
-          if (++stage == kStagesS) { stage = 0; phase ^= 1; }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
         mma_commit(&tfull[buf]);
@@ -250,6 +279,12 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
     // ---------------------------------------------------------------- epilogue
     const int quad = warp & 3;
     const int et = threadIdx.x - 64;  // 0..127
+    const int wrow = quad * 32 + lane;  // weight row inside the tile
+    const int ie = (p.interleave == 32) ? 32 : 64;
+    const int fl = et & 63;  // SwiGLU output column inside the tile
+    const int grow = (fl / ie) * 2 * ie + fl % ie;
+    const int urow = grow + ie;
+    const bool clamp = p.clamp > 0.f && isfinite(p.clamp);
     int local = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
       const int buf = local & 1;
@@ -263,45 +298,47 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
       }
       tc_fence_after();
       const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
-      const int seg_rows = s_off[t.e + 1] - s_off[t.e];
-      const int tok0 = t.n * kN;  // first token row of the tile inside the expert
+      const int tok0 = t.n * kNmax;  // first token row of the tile inside the expert
+      const int nval = min(kNmax, s_off[t.e + 1] - s_off[t.e] - tok0);
+      const int nchunk = (nval + 31) / 32;
       const long row0 = static_cast<long>(s_off[t.e]) + tok0;
-      uint32_t a[32];
-      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kN, a);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&tempty[buf]);
-      const int wrow = quad * 32 + lane;  // weight row inside the tile
-      if (kEpi == Epi::kPlain) {
-        const int feat = t.m * kM + wrow;
-#pragma unroll
-        for (int n = 0; n < kN; ++n) {
-          if (tok0 + n < seg_rows) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(a[n]));
-            p.out[(row0 + n) * p.ldo + feat] = *reinterpret_cast<const uint16_t*>(&v);
-          }
+      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kNmax;
+      for (int c = 0; c < nchunk; ++c) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(t_lane + c * 32, a);
+        tmem_ld_wait();
+        if (c == nchunk - 1) {  // the accumulator is no longer needed
+          tc_fence_before();
+          mbar_arrive(&tempty[buf]);
         }
-      } else {
-        // exchange: gate and up rows of one output column live in different warps
+        const int n0 = c * 32;
+        if (kEpi == Epi::kPlain) {
+          const int feat = t.m * kM + wrow;
 #pragma unroll
-        for (int n = 0; n < kN; ++n) sD[wrow * kDPitch + n] = __uint_as_float(a[n]);
-        bar_sync_named(1, 128);
-        const int ie = (p.interleave == 32) ? 32 : 64;
-        const int fl = et & 63;                    // output column inside the tile
-        const int grow = (fl / ie) * 2 * ie + fl % ie;
-        const int urow = grow + ie;
-        const bool clamp = p.clamp > 0.f && isfinite(p.clamp);
-        const int f = t.m * (kM / 2) + fl;
-#pragma unroll 4
-        for (int n = et >> 6; n < kN; n += 2) {
-          if (tok0 + n < seg_rows) {
-            float g = sD[grow * kDPitch + n], u = sD[urow * kDPitch + n];
-            if (clamp) {
-              g = fminf(g, p.clamp);
-              u = fminf(fmaxf(u, -p.clamp), p.clamp);
+          for (int n = 0; n < 32; ++n) {
+            if (n0 + n < nval) {
+              const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(a[n]));
+              p.out[(row0 + n0 + n) * p.ldo + feat] = *reinterpret_cast<const uint16_t*>(&v);
             }
-            const __nv_bfloat16 v = __float2bfloat16_rn(silu_s(g) * u);
-            p.out[(row0 + n) * p.ldo + f] = *reinterpret_cast<const uint16_t*>(&v);
+          }
+        } else {
+          // exchange: gate and up rows of one output column live in different warps
+          if (c > 0) bar_sync_named(1, 128);  // previous chunk's readers are done
+#pragma unroll
+          for (int n = 0; n < 32; ++n) sD[wrow * kDPitch + n] = __uint_as_float(a[n]);
+          bar_sync_named(1, 128);
+          const int f = t.m * (kM / 2) + fl;
+#pragma unroll 4
+          for (int n = et >> 6; n < 32; n += 2) {
+            if (n0 + n < nval) {
+              float g = sD[grow * kDPitch + n], u = sD[urow * kDPitch + n];
+              if (clamp) {
+                g = fminf(g, p.clamp);
+                u = fminf(fmaxf(u, -p.clamp), p.clamp);
+              }
+              const __nv_bfloat16 v = __float2bfloat16_rn(silu_s(g) * u);
+              p.out[(row0 + n0 + n) * p.ldo + f] = *reinterpret_cast<const uint16_t*>(&v);
+            }
           }
         }
       }
@@ -320,32 +357,37 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc<kTmemColsS>(tmem_base);
+    tmem_dealloc<Cfg::kTmemCols>(tmem_base);
   }
 }
 
-template <Epi kEpi>
-cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx, const SParams& sp,
-                             int grid, cudaStream_t s) {
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_swap_kernel<kEpi>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytesS));
+template <Epi kEpi, int kNmax, int kStages>
+cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx,
+                             const CUtensorMap& mxw, const SParams& sp, int grid,
+                             cudaStream_t s) {
+  using Cfg = SwapCfg<kNmax, kStages>;
+  auto kern = grouped_gemm_swap_kernel<kEpi, kNmax, kStages>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kSmem));
   if (err != cudaSuccess) return err;
-  grouped_gemm_swap_kernel<kEpi><<<grid, kThreadsS, kSmemBytesS, s>>>(mw, mx, sp);
+  kern<<<grid, kThreadsS, Cfg::kSmem, s>>>(mw, mx, mxw, sp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s) {
+cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaStream_t s) {
   if (g.a_rows == 0) return cudaSuccess;
   if (g.E > kMaxES) return cudaErrorInvalidValue;
-  CUtensorMap mw, mx;
-  // weights: 64-row boxes; tokens: kN-row boxes
+  CUtensorMap mw, mx, mxw;
+  // weights: 64-row boxes; tokens: 32-row and 128-row boxes
   if (!make_map_2d(&mw, g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
                    static_cast<uint64_t>(g.K), kM / 2))
     return cudaErrorInvalidValue;
-  if (!make_map_2d(&mx, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K), kN))
+  if (!make_map_2d(&mx, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K), kXBox))
+    return cudaErrorInvalidValue;
+  if (!make_map_2d(&mxw, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K),
+                   kXBoxWide))
     return cudaErrorInvalidValue;
   SParams sp;
   sp.expert_offsets = g.expert_offsets;
@@ -360,12 +402,17 @@ cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s) {
   sp.clamp = g.clamp;
   sp.status = g.status;
   sp.w_tiles = (g.epi == Epi::kSwiGLU) ? g.F / (kM / 2) : g.ldo / kM;
+  const int nmax = wide ? kWideN : 32;
   // every expert may add one ragged token tile
-  const long max_tiles = (static_cast<long>(ceil_div(g.a_rows, kN)) + std::min(g.E, g.a_rows)) *
-                         sp.w_tiles;
+  const long max_tiles =
+      (static_cast<long>(ceil_div(g.a_rows, nmax)) + std::min(g.E, g.a_rows)) * sp.w_tiles;
   const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
-  if (g.epi == Epi::kSwiGLU) return launch_swap_impl<Epi::kSwiGLU>(mw, mx, sp, grid, s);
-  if (g.epi == Epi::kPlain) return launch_swap_impl<Epi::kPlain>(mw, mx, sp, grid, s);
+  if (g.epi == Epi::kSwiGLU)
+    return wide ? launch_swap_impl<Epi::kSwiGLU, kWideN, kWideStages>(mw, mx, mxw, sp, grid, s)
+                : launch_swap_impl<Epi::kSwiGLU, 32, 8>(mw, mx, mxw, sp, grid, s);
+  if (g.epi == Epi::kPlain)
+    return wide ? launch_swap_impl<Epi::kPlain, kWideN, kWideStages>(mw, mx, mxw, sp, grid, s)
+                : launch_swap_impl<Epi::kPlain, 32, 8>(mw, mx, mxw, sp, grid, s);
   return cudaErrorInvalidValue;
 }
 

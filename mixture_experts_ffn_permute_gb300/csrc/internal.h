@@ -102,9 +102,9 @@ struct GroupedGemmArgs {
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s);
 
-// The same GEMMs with weight rows on the MMA's M side and tokens on N, for
-// decode sizes (kSwiGLU and kPlain epilogues; no gather / combine fusion).
-cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s);
+// The same GEMMs with weight rows on the MMA's M side and up to 32 (wide:
+// 256) tokens on N (kSwiGLU and kPlain epilogues; no gather / combine fusion).
+cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaStream_t s);
 
 // NVFP4-weight GEMMs (a = f16 rows, b = packed E2M1 codes [E * rows, K / 2],
 // scales in the prepared layout, gscale = per-expert fp32 tensor scales).

@@ -55,8 +55,8 @@ SMALL = [
 ]
 
 
-KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES]
-KERNEL_IDS = ["token_tiles", "weight_tiles"]
+KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE]
+KERNEL_IDS = ["token_tiles", "weight_tiles", "weight_tiles_wide"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
@@ -130,10 +130,10 @@ def test_forward_is_bitwise_deterministic_and_reuses_workspace():
 
 # ------------------------------------------------------------------ full size, sampled
 
-def sampled_check(shape, n_sample, seed=0):
+def sampled_check(shape, n_sample, seed=0, kernel=0):
     torch.manual_seed(0)
     inp = mi.make_inputs(shape, seed=seed, device=DEV)
-    res = run_forward(shape, inp)
+    res = run_forward(shape, inp, kernel=kernel)
     logits_h = inp["logits"].cpu()
     # routing of every token and the expert histogram: bit-exact
     idx_ref, w_ref = oracle.route_topk(logits_h, shape.k)
@@ -162,8 +162,10 @@ def test_forward_mixtral_full_size_sampled():
 
 
 @pytest.mark.slow
-def test_forward_skewed_full_size_sampled():
-    sampled_check(mi.SKEWED, 4)
+@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_WIDE],
+                         ids=["auto", "weight_tiles_wide"])
+def test_forward_skewed_full_size_sampled(kernel):
+    sampled_check(mi.SKEWED, 4, kernel=kernel)
 
 
 @pytest.mark.slow
