@@ -50,6 +50,9 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr uint32_t kTmemCols = 2 * kBN;              // two accumulators
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 constexpr int kMaxE = 1024;
+// mbarriers: full/empty per stage, 2 + 2 accumulator, drain; then the TMEM
+// address word and the abort flag
+static_assert((2 * kStages + 5) * 8 + 8 <= 256, "barrier area");
 constexpr size_t kSmemBytes =
     1024 /*alignment slack*/ + kStages * kStageBytes + 256 /*barriers*/ +
     2 * (kMaxE + 1) * sizeof(int32_t) /*offsets + m-tile prefix*/;

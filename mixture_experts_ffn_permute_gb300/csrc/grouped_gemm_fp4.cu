@@ -59,6 +59,9 @@ constexpr uint32_t kIdescF16 = (1u << 4) | ((kBN >> 3) << 17) | ((kBM >> 4) << 2
 constexpr int kMaxEF = 1024;
 constexpr size_t kRingBytes = kStagesA * kABytesF + kStagesB * kB16Bytes +
                               kStagesR * (kRawBytes + kScBytes);
+// mbarriers of the three rings, 2 + 2 accumulator, drain; then the TMEM
+// address word and the abort flag
+static_assert((2 * (kStagesA + kStagesR + kStagesB) + 5) * 8 + 8 <= 256, "barrier area");
 constexpr size_t kSmemBytesF = 1024 + kRingBytes + 256 + 2 * (kMaxEF + 1) * sizeof(int32_t);
 static_assert(kSmemBytesF <= 232448, "shared memory budget");
 

@@ -50,14 +50,27 @@ constexpr int kMaxES = 1024;
 constexpr int kDPitch = 33;                            // padded fp32 row of the exchange chunk
 // wide instance: token tiles of up to kWideN rows, kWideStages-deep ring
 constexpr int kWideN = 256;
-constexpr int kWideStages = 4;
+#ifndef MOE_WIDE_W
+#define MOE_WIDE_W 4
+#endif
+#ifndef MOE_WIDE_X
+#define MOE_WIDE_X 4
+#endif
+constexpr int kWideW = MOE_WIDE_W;   // weight-ring depth (HBM)
+constexpr int kWideX = MOE_WIDE_X;   // token-ring depth (L2)
 
-template <int kNmax, int kStages>
+// Separate rings for the weight tiles (from HBM: deep) and the token tiles
+// (from L2).
+template <int kNmax, int kWStages, int kXStages>
 struct SwapCfg {
   static constexpr uint32_t kXBytes = kNmax * kBK * 2;
-  static constexpr uint32_t kStageBytes = kWBytes + kXBytes;
+  static constexpr uint32_t kRingBytes = kWStages * kWBytes + kXStages * kXBytes;
   static constexpr uint32_t kTmemCols = 2 * kNmax;     // two accumulators
-  static constexpr size_t kSmem = 1024 + kStages * kStageBytes + 256 +
+  // mbarriers (full/empty per stage of both rings, 2 + 2 accumulator, drain)
+  // plus the TMEM address word and the abort flag
+  static constexpr uint32_t kBarBytes = 512;
+  static_assert((2 * (kWStages + kXStages) + 5) * 8 + 8 <= kBarBytes, "barrier area");
+  static constexpr size_t kSmem = 1024 + kRingBytes + kBarBytes +
                                   3 * (kMaxES + 1) * sizeof(int32_t) +
                                   kM * kDPitch * sizeof(float);
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -94,26 +107,28 @@ __device__ __forceinline__ STile decode_stile(int tile, const int32_t* tp, const
 
 __device__ __forceinline__ float silu_s(float z) { return z / (1.0f + expf(-z)); }
 
-template <Epi kEpi, int kNmax, int kStages>
+template <Epi kEpi, int kNmax, int kWStages, int kXStages>
 __global__ void __launch_bounds__(kThreadsS, 1)
 grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
                          const __grid_constant__ CUtensorMap map_x,
                          const __grid_constant__ CUtensorMap map_xw, const SParams p) {
-  using Cfg = SwapCfg<kNmax, kStages>;
+  using Cfg = SwapCfg<kNmax, kWStages, kXStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, kept as a shared-array pointer so that accesses
   // compile to shared-memory instructions
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sW = smem;
-  uint8_t* sX = smem + kStages * kWBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sX + kStages * Cfg::kXBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint8_t* sX = smem + kWStages * kWBytes;
+  uint64_t* w_full = reinterpret_cast<uint64_t*>(smem + Cfg::kRingBytes);
+  uint64_t* w_empty = w_full + kWStages;
+  uint64_t* x_full = w_empty + kWStages;
+  uint64_t* x_empty = x_full + kXStages;
+  uint64_t* tfull = x_empty + kXStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * Cfg::kStageBytes + 256);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + Cfg::kRingBytes + Cfg::kBarBytes);
   int32_t* s_tp = s_off + (kMaxES + 1);   // tile prefix per expert
   int32_t* s_ntk = s_tp + (kMaxES + 1);   // token tiles per expert
   float* sD = reinterpret_cast<float*>(s_ntk + (kMaxES + 1));
@@ -121,9 +136,13 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i <= p.E; i += kThreadsS) s_off[i] = p.expert_offsets[i];
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kWStages; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], 1);
+    }
+    for (int s = 0; s < kXStages; ++s) {
+      mbar_init(&x_full[s], 1);
+      mbar_init(&x_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -187,8 +206,8 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_normal();
       const uint64_t pol_x = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
+      int sw = 0, sx = 0;
+      uint32_t pw = 0, px = 0;
       long issued = 0;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
         const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
@@ -220,32 +239,41 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
         w_row0 += t.e * p.w_rows_per_expert;
         w_row1 += t.e * p.w_rows_per_expert;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { *abort_flag = 1; break; }
-          mbar_arrive_expect_tx(&full[stage], kWBytes + x_bytes);
           const int kx = kb * kBK;
-          uint8_t* w_dst = sW + stage * kWBytes;
-          tma_load_2d(w_dst, &map_w, kx, w_row0, &full[stage], pol_w);
-          tma_load_2d(w_dst + kWBytes / 2, &map_w, kx, w_row1, &full[stage], pol_w);
-          uint8_t* x_dst = sX + stage * Cfg::kXBytes;
+          if (!mbar_wait(&w_empty[sw], pw ^ 1, p.status)) { *abort_flag = 1; break; }
+          mbar_arrive_expect_tx(&w_full[sw], kWBytes);
+          uint8_t* w_dst = sW + sw * kWBytes;
+          tma_load_2d(w_dst, &map_w, kx, w_row0, &w_full[sw], pol_w);
+          tma_load_2d(w_dst + kWBytes / 2, &map_w, kx, w_row1, &w_full[sw], pol_w);
+          if (!mbar_wait(&x_empty[sx], px ^ 1, p.status)) { *abort_flag = 1; break; }
+          mbar_arrive_expect_tx(&x_full[sx], x_bytes);
+          uint8_t* x_dst = sX + sx * Cfg::kXBytes;
           for (int b = 0; b < nbox; ++b)
             tma_load_2d(x_dst + b * box_rows * kBK * 2, wide_box ? &map_xw : &map_x, kx,
-                        x_row + b * box_rows, &full[stage], pol_x);
+                        x_row + b * box_rows, &x_full[sx], pol_x);
           ++issued;
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          if (++sw == kWStages) { sw = 0; pw ^= 1; }
+          if (++sx == kXStages) { sx = 0; px ^= 1; }
         }
       }
-      for (int i = 1; i <= kStages && i <= issued; ++i) {
-        int s = stage - i;
-        uint32_t ph = phase;
-        if (s < 0) { s += kStages; ph ^= 1; }
-        mbar_wait(&full[s], ph, p.status);
+      for (int i = 1; i <= kWStages && i <= issued; ++i) {
+        int s = sw - i;
+        uint32_t ph = pw;
+        if (s < 0) { s += kWStages; ph ^= 1; }
+        mbar_wait(&w_full[s], ph, p.status);
+      }
+      for (int i = 1; i <= kXStages && i <= issued; ++i) {
+        int s = sx - i;
+        uint32_t ph = px;
+        if (s < 0) { s += kXStages; ph ^= 1; }
+        mbar_wait(&x_full[s], ph, p.status);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int sw = 0, sx = 0;
+      uint32_t pw = 0, px = 0;
       int local = 0;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++local) {
         const int buf = local & 1;
@@ -259,15 +287,20 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
         const uint32_t d_tmem = tmem_base + buf * kNmax;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, p.status)) { ok = false; break; }
+          if (!mbar_wait(&w_full[sw], pw, p.status) || !mbar_wait(&x_full[sx], px, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint64_t w_desc = sw128_kmajor_desc(smem_u32(sW + stage * kWBytes));
-          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + stage * Cfg::kXBytes));
+          const uint64_t w_desc = sw128_kmajor_desc(smem_u32(sW + sw * kWBytes));
+          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + sx * Cfg::kXBytes));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
-          mma_commit(&empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          mma_commit(&w_empty[sw]);
+          mma_commit(&x_empty[sx]);
+          if (++sw == kWStages) { sw = 0; pw ^= 1; }
+          if (++sx == kXStages) { sx = 0; px ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
         mma_commit(&tfull[buf]);
@@ -361,12 +394,12 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   }
 }
 
-template <Epi kEpi, int kNmax, int kStages>
+template <Epi kEpi, int kNmax, int kWStages, int kXStages>
 cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx,
                              const CUtensorMap& mxw, const SParams& sp, int grid,
                              cudaStream_t s) {
-  using Cfg = SwapCfg<kNmax, kStages>;
-  auto kern = grouped_gemm_swap_kernel<kEpi, kNmax, kStages>;
+  using Cfg = SwapCfg<kNmax, kWStages, kXStages>;
+  auto kern = grouped_gemm_swap_kernel<kEpi, kNmax, kWStages, kXStages>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::kSmem));
   if (err != cudaSuccess) return err;
@@ -408,11 +441,11 @@ cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaSt
       (static_cast<long>(ceil_div(g.a_rows, nmax)) + std::min(g.E, g.a_rows)) * sp.w_tiles;
   const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
   if (g.epi == Epi::kSwiGLU)
-    return wide ? launch_swap_impl<Epi::kSwiGLU, kWideN, kWideStages>(mw, mx, mxw, sp, grid, s)
-                : launch_swap_impl<Epi::kSwiGLU, 32, 8>(mw, mx, mxw, sp, grid, s);
+    return wide ? launch_swap_impl<Epi::kSwiGLU, kWideN, kWideW, kWideX>(mw, mx, mxw, sp, grid, s)
+                : launch_swap_impl<Epi::kSwiGLU, 32, 10, 6>(mw, mx, mxw, sp, grid, s);
   if (g.epi == Epi::kPlain)
-    return wide ? launch_swap_impl<Epi::kPlain, kWideN, kWideStages>(mw, mx, mxw, sp, grid, s)
-                : launch_swap_impl<Epi::kPlain, 32, 8>(mw, mx, mxw, sp, grid, s);
+    return wide ? launch_swap_impl<Epi::kPlain, kWideN, kWideW, kWideX>(mw, mx, mxw, sp, grid, s)
+                : launch_swap_impl<Epi::kPlain, 32, 10, 6>(mw, mx, mxw, sp, grid, s);
   return cudaErrorInvalidValue;
 }
 
