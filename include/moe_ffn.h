@@ -96,6 +96,10 @@ typedef struct moe_problem {
        MOE_KERNEL_WEIGHT_TILES_WIDE  128 weight rows x up to 256 token rows per
                                 tile, N fitted to the expert's rows (ragged
                                 experts pad at most 15 rows)
+       MOE_KERNEL_TOKEN_TILES_PAIR  token-row tiles run by 2-CTA clusters that
+                                take two m-tiles of one weight tile and
+                                multicast the weight tile's halves to each
+                                other (each weight byte read once per pair)
      The fusion options do not apply to the weight-row tilings. */
   int32_t kernel;
 } moe_problem;
@@ -106,6 +110,7 @@ typedef struct moe_problem {
 #define MOE_KERNEL_TOKEN_TILES 1
 #define MOE_KERNEL_WEIGHT_TILES 2
 #define MOE_KERNEL_WEIGHT_TILES_WIDE 3
+#define MOE_KERNEL_TOKEN_TILES_PAIR 4
 
 /* Limits checked by every entry point. */
 #define MOE_MAX_EXPERTS 1024

@@ -107,7 +107,7 @@ int check_full(const moe_problem* p) {
   if (p->precision != MOE_PREC_BF16 && p->precision != MOE_PREC_FP8_NVFP4)
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
-  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_WEIGHT_TILES_WIDE)
+  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_TOKEN_TILES_PAIR)
     return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
   if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -151,7 +151,10 @@ int gemm_tiling(const moe_problem* p) {
   return MOE_KERNEL_TOKEN_TILES;
 }
 
-bool use_weight_tiles(const moe_problem* p) { return gemm_tiling(p) != MOE_KERNEL_TOKEN_TILES; }
+bool use_weight_tiles(const moe_problem* p) {
+  const int t = gemm_tiling(p);
+  return t == MOE_KERNEL_WEIGHT_TILES || t == MOE_KERNEL_WEIGHT_TILES_WIDE;
+}
 
 float clamp_of(const moe_problem* p) {
   const float c = p->swiglu_clamp;
@@ -198,6 +201,7 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
     g1.permuted_token = fused->permuted_token;
     g1.x_rows = p->T;
   }
+  g1.pair = gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_PAIR;
   const bool wide = gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES_WIDE;
   MOE_LAUNCH(swap ? launch_grouped_gemm_swap(g1, wide, s) : launch_grouped_gemm(g1, s));
   if (tm) tm->mark(call, mark, s);
@@ -217,6 +221,7 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
   g2.out_rows = R;
   g2.F = p->F;
   g2.status = status;
+  g2.pair = gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_PAIR;
   if (fused && fused->combine && !swap) {
     g2.epi = Epi::kCombine;
     g2.out = fused->out;

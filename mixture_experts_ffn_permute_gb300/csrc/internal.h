@@ -98,6 +98,8 @@ struct GroupedGemmArgs {
   int32_t* counters = nullptr;  // [T, n_tiles], zero before the launch
   void* partials = nullptr;     // [R, ldo] bf16
   int k = 0;
+  // token-row tiles as 2-CTA clusters sharing (multicasting) the weight tile
+  bool pair = false;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s);

@@ -55,8 +55,9 @@ SMALL = [
 ]
 
 
-KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE]
-KERNEL_IDS = ["token_tiles", "weight_tiles", "weight_tiles_wide"]
+KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE,
+           moe.KERNEL_TOKEN_TILES_PAIR]
+KERNEL_IDS = ["token_tiles", "weight_tiles", "weight_tiles_wide", "token_tiles_pair"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
@@ -157,8 +158,10 @@ def sampled_check(shape, n_sample, seed=0, kernel=0):
 
 
 @pytest.mark.slow
-def test_forward_mixtral_full_size_sampled():
-    sampled_check(mi.MIXTRAL, 8)
+@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_TOKEN_TILES_PAIR],
+                         ids=["auto", "token_tiles_pair"])
+def test_forward_mixtral_full_size_sampled(kernel):
+    sampled_check(mi.MIXTRAL, 8, kernel=kernel)
 
 
 @pytest.mark.slow

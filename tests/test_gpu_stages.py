@@ -150,10 +150,12 @@ def _routed_inputs(shape, seed=0, mask=0.0):
     return inp, idx, w, perm, xp
 
 
-KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE]
+KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE,
+           moe.KERNEL_TOKEN_TILES_PAIR]
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_wide"])
+@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_wide",
+                                                "token_tiles_pair"])
 @pytest.mark.parametrize("shape", MLP_CASES, ids=lambda s: s.name)
 def test_grouped_swiglu_mlp(shape, kernel):
     inp, idx, w, perm, xp = _routed_inputs(shape, seed=1)
@@ -173,7 +175,8 @@ def test_grouped_swiglu_mlp(shape, kernel):
     assert_bf16_close(y, y_ref, f"y_perm[{shape.name}]")
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_wide"])
+@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_wide",
+                                                "token_tiles_pair"])
 def test_grouped_mlp_masked_tail_rows_are_zero(kernel):
     shape = mi.MoEShape("masked", T=100, H=256, F=256, E=6, k=2)
     inp, idx, w, perm, xp = _routed_inputs(shape, seed=4, mask=0.25)
