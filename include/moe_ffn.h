@@ -85,11 +85,12 @@ typedef struct moe_problem {
        MOE_FUSE_COMBINE   the weighted top-k reduction runs in GEMM2's
                           epilogue (bf16 partials + per-token arrival counters,
                           slot-ordered sum by the last arrival).
-     Both give results within the same tolerance of the exact layer. */
+     Both give results within the same tolerance of the exact layer.  They
+     apply to the 1-CTA token-row tilings only. */
   int32_t fusion;
   /* GEMM tiling (moe_problem.kernel):
        MOE_KERNEL_AUTO          T*k <= 32*E: weight-row tiles; <= 512*E: wide
-                                weight-row tiles; else token-row tiles
+                                weight-row tiles; else 2-CTA token-row tiles
        MOE_KERNEL_TOKEN_TILES   128 permuted token rows x 256 weight rows per tile
        MOE_KERNEL_WEIGHT_TILES  128 weight rows x up to 32 token rows per tile
                                 (decode sizes: weights stream once at HBM speed)
@@ -100,6 +101,9 @@ typedef struct moe_problem {
                                 take two m-tiles of one weight tile and
                                 multicast the weight tile's halves to each
                                 other (each weight byte read once per pair)
+       MOE_KERNEL_TOKEN_TILES_2CTA  256 token rows x 256 weight rows per CTA
+                                pair with tcgen05.mma.cta_group::2 (each CTA
+                                loads half of both operands)
      The fusion options do not apply to the weight-row tilings. */
   int32_t kernel;
 } moe_problem;
@@ -111,6 +115,7 @@ typedef struct moe_problem {
 #define MOE_KERNEL_WEIGHT_TILES 2
 #define MOE_KERNEL_WEIGHT_TILES_WIDE 3
 #define MOE_KERNEL_TOKEN_TILES_PAIR 4
+#define MOE_KERNEL_TOKEN_TILES_2CTA 5
 
 /* Limits checked by every entry point. */
 #define MOE_MAX_EXPERTS 1024

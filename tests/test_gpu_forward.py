@@ -56,8 +56,9 @@ SMALL = [
 
 
 KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE,
-           moe.KERNEL_TOKEN_TILES_PAIR]
-KERNEL_IDS = ["token_tiles", "weight_tiles", "weight_tiles_wide", "token_tiles_pair"]
+           moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA]
+KERNEL_IDS = ["token_tiles", "weight_tiles", "weight_tiles_wide", "token_tiles_pair",
+              "token_tiles_2cta"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
@@ -84,13 +85,14 @@ def test_forward_fusion_variants(shape, fusion):
     inp = mi.make_inputs(shape, seed=3)
     ref = oracle.moe_forward(inp["x"], inp["logits"], inp["w1"], inp["w2"], shape.k)
     d = to_dev(inp)
-    res = run_forward(shape, d, fusion=fusion)
+    tok = moe.KERNEL_TOKEN_TILES  # the fusions belong to the 1-CTA token-row tiling
+    res = run_forward(shape, d, fusion=fusion, kernel=tok)
     assert_bf16_close(res["out"], ref["out"], f"out[{shape.name}, fusion={fusion}]")
     if not fusion & moe.FUSE_COMBINE:
         # gathering A from x instead of a permuted copy changes no arithmetic
-        base = run_forward(shape, d, fusion=0)
+        base = run_forward(shape, d, fusion=0, kernel=tok)
         assert torch.equal(res["out"].view(torch.int16), base["out"].view(torch.int16))
-    again = run_forward(shape, d, ws=res["ws"], fusion=fusion)
+    again = run_forward(shape, d, ws=res["ws"], fusion=fusion, kernel=tok)
     assert torch.equal(res["out"].view(torch.int16), again["out"].view(torch.int16))
 
 
@@ -158,8 +160,9 @@ def sampled_check(shape, n_sample, seed=0, kernel=0):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_TOKEN_TILES_PAIR],
-                         ids=["auto", "token_tiles_pair"])
+@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_TOKEN_TILES_PAIR,
+                                    moe.KERNEL_TOKEN_TILES_2CTA],
+                         ids=["auto", "token_tiles_pair", "token_tiles_2cta"])
 def test_forward_mixtral_full_size_sampled(kernel):
     sampled_check(mi.MIXTRAL, 8, kernel=kernel)
 
