@@ -36,6 +36,12 @@ import torch  # noqa: E402
 import moe_inputs as mi  # noqa: E402
 
 METRIC = "MoE layer fwd TFLOP/s & tokens/s at 1 GB300; % of tensor/HBM roofline"
+# GEMM kernel (file and instance) behind each moe_problem.kernel value
+KERNEL_NAMES = {1: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU> (GEMM1, 1-CTA 128x256 tiles)"),
+                2: ("grouped_gemm_swap.cu", "grouped_gemm_swap_kernel<SwiGLU,32> (GEMM1)"),
+                3: ("grouped_gemm_swap.cu", "grouped_gemm_swap_kernel<SwiGLU,256> (GEMM1)"),
+                4: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU,pair> (GEMM1, multicast pair)"),
+                5: ("grouped_gemm_2cta.cu", "grouped_gemm_2cta_kernel<SwiGLU> (GEMM1, cta_group::2)")}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOADS = {
     "mixtral": (mi.MIXTRAL, "Mixtral-shaped MoE FFN layer: T=4096 H=4096 F=14336 E=8 top-2 bf16"),
@@ -69,6 +75,23 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args(argv)
+
+
+def ncu_traffic(kernel_file: str, workload: str):
+    """DRAM bytes (read + write) per GEMM1 launch from the committed ncu
+    summary, if it was taken on the current source of the kernel's file."""
+    import hashlib
+    src = os.path.join(ROOT, "mixture_experts_ffn_permute_gb300", "csrc", kernel_file)
+    table = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(table):
+            f = line.split()
+            if len(f) >= 5 and not line.startswith("#") and f[0] == sha and f[1] == workload:
+                return float(f[3]) + float(f[4])
+    except OSError:
+        pass
+    return None
 
 
 def load_peaks():
@@ -344,6 +367,10 @@ def bench_ours(args, shape, desc):
     e2e_ms = reduce_max(e0.elapsed_time(e1) / K2, world, dev)
 
     flops = shape.flops()
+    kid = moe.selected_kernel(p)
+    kfile, kname = KERNEL_NAMES.get(kid, ("grouped_gemm_fp4.cu", "grouped_gemm_fp4_kernel<SwiGLU>"))
+    if shape.lowprec:
+        kfile, kname = "grouped_gemm_fp4.cu", "grouped_gemm_fp4_kernel<SwiGLU> (GEMM1, NVFP4 weights)"
     gemm1_ms = stages.get("gemm1_swiglu", float("nan"))
     gemm1_flops = 4.0 * shape.R * shape.H * shape.F
     peak_key = "bf16_tflops_sustained"
@@ -367,9 +394,11 @@ def bench_ours(args, shape, desc):
                    "precision": "fp8-act/nvfp4-weight" if shape.lowprec else "bf16",
                    "timing": "cuda-graph replay" if args.graph else "eager launches", "l2": "inputs larger than L2 (weights %.2f GB), no flush"
                    % (weight_bytes / 1e9)},
-        "roofline": {"kernel": "grouped_gemm_kernel<SwiGLU> (GEMM1)", "bound": "tensor",
+        "roofline": {"kernel": kname, "bound": "tensor",
                      "achieved": ach, "peak": peaks[peak_key], "unit": "TFLOP/s",
-                     "frac": ach / peaks[peak_key], "traffic": None,
+                     "frac": ach / peaks[peak_key],
+                     "traffic": ncu_traffic(kfile, args.workload if not args.T and not args.E
+                                            and not args.k else "custom"),
                      "peak_source": f"{peak_key} ({peak_src})"},
         "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms,

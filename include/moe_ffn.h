@@ -270,6 +270,10 @@ MOE_API int moe_get_device_status(void* ws, void* stream);
 /* Resets the workspace status word (enqueued on `stream`). */
 MOE_API int moe_clear_device_status(void* ws, void* stream);
 
+/* The GEMM tiling moe_forward uses for this problem (a MOE_KERNEL_* value
+ * other than MOE_KERNEL_AUTO), or -1 for an invalid problem. */
+MOE_API int moe_selected_kernel(const moe_problem* p);
+
 /* Number of kernel launches the last successful call on this thread
  * enqueued (for launch accounting in benchmarks). */
 MOE_API int moe_last_launch_count(void);

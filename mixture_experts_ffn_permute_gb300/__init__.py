@@ -88,6 +88,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_get_device_status": ([vp, vp], ci),
         "moe_clear_device_status": ([vp, vp], ci),
         "moe_last_launch_count": ([], ci),
+        "moe_selected_kernel": ([pp], ci),
         "moe_stage_timing_begin": ([ci], ci),
         "moe_stage_timing_end": ([ctypes.POINTER(ctypes.c_float), ci,
                                   ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)], ci),
@@ -138,6 +139,11 @@ def alloc_workspace(p: Problem, device="cuda") -> torch.Tensor:
     ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
     off = (-ws.data_ptr()) % 256
     return ws[off:off + n]
+
+
+def selected_kernel(p: Problem) -> int:
+    """The GEMM tiling (KERNEL_*) moe_forward picks for this problem."""
+    return int(load().moe_selected_kernel(ctypes.byref(p)))
 
 
 def last_launch_count() -> int:
@@ -268,4 +274,4 @@ __all__ = ["Problem", "MoEError", "MoEFFN", "load", "workspace_size", "alloc_wor
            "route_topk", "permute", "grouped_swiglu_mlp", "unpermute_combine", "forward",
            "get_device_status", "clear_device_status", "last_launch_count", "LIB_PATH",
            "stage_timing_begin", "stage_timing_end", "permute_noalloc",
-           "prepared_scales_size", "prepare_weights", "forward_fp8_nvfp4"]
+           "prepared_scales_size", "prepare_weights", "forward_fp8_nvfp4", "selected_kernel"]

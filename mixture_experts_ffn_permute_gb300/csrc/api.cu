@@ -612,6 +612,12 @@ int moe_clear_device_status(void* ws, void* stream) {
 
 int moe_last_launch_count(void) { return g_launches; }
 
+int moe_selected_kernel(const moe_problem* p) {
+  if (check_full(p) != MOE_OK) return -1;
+  if (p->precision == MOE_PREC_FP8_NVFP4) return MOE_KERNEL_TOKEN_TILES;
+  return gemm_tiling(p);
+}
+
 int moe_stage_timing_begin(int n_calls) {
   if (n_calls <= 0) return MOE_ERR_INVALID_ARG;
   StageTimer& t = g_timer;
