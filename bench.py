@@ -41,7 +41,9 @@ KERNEL_NAMES = {1: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU> (GEMM1, 1-CT
                 2: ("grouped_gemm_swap.cu", "grouped_gemm_swap_kernel<SwiGLU,32> (GEMM1)"),
                 3: ("grouped_gemm_swap.cu", "grouped_gemm_swap_kernel<SwiGLU,256> (GEMM1)"),
                 4: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU,pair> (GEMM1, multicast pair)"),
-                5: ("grouped_gemm_2cta.cu", "grouped_gemm_2cta_kernel<SwiGLU> (GEMM1, cta_group::2)")}
+                5: ("grouped_gemm_2cta.cu", "grouped_gemm_2cta_kernel<SwiGLU> (GEMM1, cta_group::2)"),
+                6: ("grouped_gemm_swap2.cu",
+                    "grouped_gemm_swap2_kernel<SwiGLU> (GEMM1, weight rows on M, cta_group::2)")}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOADS = {
     "mixtral": (mi.MIXTRAL, "Mixtral-shaped MoE FFN layer: T=4096 H=4096 F=14336 E=8 top-2 bf16"),
@@ -92,6 +94,18 @@ def ncu_traffic(kernel_file: str, workload: str):
     except OSError:
         pass
     return None
+
+
+def gemm1_algorithmic_bytes(shape, used_experts: int) -> float:
+    """HBM bytes GEMM1 cannot avoid: the gate/up weights of every expert that
+    received tokens, the permuted activation rows read once and h written once.
+
+    bf16: 2F*H*2 per expert, R*H*2 in, R*F*2 out.  FP8/NVFP4: 2F*H/2 packed
+    E2M1 + 2F*H/16 E4M3 block scales per expert; the rows come in as f16 (the
+    gather dequantises the E4M3 tokens), R*H*2, and h goes out as f16, R*F*2."""
+    R, H, F = shape.R, shape.H, shape.F
+    w = (2 * F * H / 2 + 2 * F * H / 16) if shape.lowprec else 2 * F * H * 2
+    return used_experts * w + R * H * 2 + R * F * 2
 
 
 def load_peaks():
@@ -366,6 +380,16 @@ def bench_ours(args, shape, desc):
     barrier(world)
     e2e_ms = reduce_max(e0.elapsed_time(e1) / K2, world, dev)
 
+    # experts that received tokens (untimed extra call): their weights are the
+    # bytes GEMM1 must stream
+    tpe = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    if shape.lowprec:
+        moe.forward_fp8_nvfp4(p, x, xs, logits, lp["w1q"], lp["w1g"], lp["w2q"], lp["w2g"],
+                              prepared, out, ws, tokens_per_expert=tpe)
+    else:
+        moe.forward(p, x, logits, w1, w2, out, ws, tokens_per_expert=tpe)
+    used_experts = int((tpe > 0).sum().item())
+
     flops = shape.flops()
     kid = moe.selected_kernel(p)
     kfile, kname = KERNEL_NAMES.get(kid, ("grouped_gemm_fp4.cu", "grouped_gemm_fp4_kernel<SwiGLU>"))
@@ -373,8 +397,19 @@ def bench_ours(args, shape, desc):
         kfile, kname = "grouped_gemm_fp4.cu", "grouped_gemm_fp4_kernel<SwiGLU> (GEMM1, NVFP4 weights)"
     gemm1_ms = stages.get("gemm1_swiglu", float("nan"))
     gemm1_flops = 4.0 * shape.R * shape.H * shape.F
+    gemm1_bytes = gemm1_algorithmic_bytes(shape, used_experts)
     peak_key = "bf16_tflops_sustained"
-    ach = gemm1_flops / (gemm1_ms / 1e3) / 1e12
+    gemm1_s = gemm1_ms / 1e3
+    t_tensor = gemm1_flops / (peaks[peak_key] * 1e12)
+    t_hbm = gemm1_bytes / (peaks["hbm_gbs"] * 1e9)
+    tensor_roof = {"bound": "tensor", "achieved": gemm1_flops / gemm1_s / 1e12,
+                   "peak": peaks[peak_key], "unit": "TFLOP/s",
+                   "peak_source": f"{peak_key} ({peak_src})"}
+    hbm_roof = {"bound": "hbm", "achieved": gemm1_bytes / gemm1_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "peak_source": f"hbm_gbs ({peak_src})"}
+    for r in (tensor_roof, hbm_roof):
+        r["frac"] = r["achieved"] / r["peak"]
+    main, other = (hbm_roof, tensor_roof) if t_hbm > t_tensor else (tensor_roof, hbm_roof)
     line = {
         "metric": METRIC,
         "value": world * flops / sec / 1e12,
@@ -394,12 +429,16 @@ def bench_ours(args, shape, desc):
                    "precision": "fp8-act/nvfp4-weight" if shape.lowprec else "bf16",
                    "timing": "cuda-graph replay" if args.graph else "eager launches", "l2": "inputs larger than L2 (weights %.2f GB), no flush"
                    % (weight_bytes / 1e9)},
-        "roofline": {"kernel": kname, "bound": "tensor",
-                     "achieved": ach, "peak": peaks[peak_key], "unit": "TFLOP/s",
-                     "frac": ach / peaks[peak_key],
+        "roofline": {"kernel": kname, "bound": main["bound"],
+                     "achieved": main["achieved"], "peak": main["peak"], "unit": main["unit"],
+                     "frac": main["frac"],
                      "traffic": ncu_traffic(kfile, args.workload if not args.T and not args.E
                                             and not args.k else "custom"),
-                     "peak_source": f"{peak_key} ({peak_src})"},
+                     "peak_source": main["peak_source"],
+                     "algorithmic": {"flops": gemm1_flops, "bytes": gemm1_bytes,
+                                     "experts_with_tokens": used_experts},
+                     "other_roof": {k: other[k] for k in ("bound", "achieved", "peak", "unit",
+                                                         "frac")}},
         "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in step_inputs),

@@ -89,8 +89,9 @@ typedef struct moe_problem {
      apply to the 1-CTA token-row tilings only. */
   int32_t fusion;
   /* GEMM tiling (moe_problem.kernel):
-       MOE_KERNEL_AUTO          T*k <= 32*E: weight-row tiles; <= 512*E: wide
-                                weight-row tiles; else 2-CTA token-row tiles
+       MOE_KERNEL_AUTO          T*k <= 2*E (at most two routes per expert on
+                                average): weight-row tiles; else 2-CTA
+                                weight-row tiles
        MOE_KERNEL_TOKEN_TILES   128 permuted token rows x 256 weight rows per tile
        MOE_KERNEL_WEIGHT_TILES  128 weight rows x up to 32 token rows per tile
                                 (decode sizes: weights stream once at HBM speed)
@@ -104,6 +105,12 @@ typedef struct moe_problem {
        MOE_KERNEL_TOKEN_TILES_2CTA  256 token rows x 256 weight rows per CTA
                                 pair with tcgen05.mma.cta_group::2 (each CTA
                                 loads half of both operands)
+       MOE_KERNEL_WEIGHT_TILES_2CTA  256 weight rows x up to 256 token rows per
+                                CTA pair (cta_group::2), N fitted to the
+                                expert's rows (pads at most 31 rows); tiles of
+                                experts with one token tile (weight-streaming)
+                                interleaved with those of experts with more
+                                (MMA-bound)
      The fusion options do not apply to the weight-row tilings. */
   int32_t kernel;
 } moe_problem;
@@ -116,6 +123,7 @@ typedef struct moe_problem {
 #define MOE_KERNEL_WEIGHT_TILES_WIDE 3
 #define MOE_KERNEL_TOKEN_TILES_PAIR 4
 #define MOE_KERNEL_TOKEN_TILES_2CTA 5
+#define MOE_KERNEL_WEIGHT_TILES_2CTA 6
 
 /* Limits checked by every entry point. */
 #define MOE_MAX_EXPERTS 1024

@@ -107,7 +107,7 @@ int check_full(const moe_problem* p) {
   if (p->precision != MOE_PREC_BF16 && p->precision != MOE_PREC_FP8_NVFP4)
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
-  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_TOKEN_TILES_2CTA)
+  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_WEIGHT_TILES_2CTA)
     return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
   if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -140,16 +140,16 @@ int check_ws(const moe_problem* p, void* ws, size_t ws_bytes) {
     ++launches;                                   \
   } while (0)
 
-// GEMM tiling for this problem: weight-row tiles (swap-AB) when experts see
-// few tokens on average.
+// GEMM tiling for this problem.  With at most two routes per expert on
+// average the 32-token weight-row tiles give the most CTAs streaming the
+// weights; otherwise 2-CTA weight-row tiles, whose N fits each expert's rows
+// (a ragged expert pads at most 31 rows) -- on GB300 they match or beat the
+// token-row tilings even for experts with thousands of rows.
 int gemm_tiling(const moe_problem* p) {
   if (p->kernel != MOE_KERNEL_AUTO) return p->kernel;
   const long long routes = static_cast<long long>(p->T) * p->k;
-  if (routes <= 32LL * p->E) return MOE_KERNEL_WEIGHT_TILES;
-  // ragged experts of up to a few hundred rows: N fitted per expert
-  if (routes <= 512LL * p->E) return MOE_KERNEL_WEIGHT_TILES_WIDE;
-  // experts with many rows: 256 x 256 tiles on CTA pairs
-  return MOE_KERNEL_TOKEN_TILES_2CTA;
+  if (routes <= 2LL * p->E) return MOE_KERNEL_WEIGHT_TILES;
+  return MOE_KERNEL_WEIGHT_TILES_2CTA;
 }
 
 bool use_weight_tiles(const moe_problem* p) {
@@ -205,10 +205,12 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
   g1.pair = gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_PAIR;
   const bool wide = gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES_WIDE;
   const bool cta2 = gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_2CTA;
-  if (cta2) g1.permuted_token = nullptr;  // no gathered-A form
-  MOE_LAUNCH(swap   ? launch_grouped_gemm_swap(g1, wide, s)
-             : cta2 ? launch_grouped_gemm_2cta(g1, s)
-                    : launch_grouped_gemm(g1, s));
+  const bool swap2 = gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES_2CTA;
+  if (cta2 || swap2) g1.permuted_token = nullptr;  // no gathered-A form
+  MOE_LAUNCH(swap    ? launch_grouped_gemm_swap(g1, wide, s)
+             : cta2  ? launch_grouped_gemm_2cta(g1, s)
+             : swap2 ? launch_grouped_gemm_swap2(g1, s)
+                     : launch_grouped_gemm(g1, s));
   if (tm) tm->mark(call, mark, s);
   GroupedGemmArgs g2{};
   g2.epi = Epi::kPlain;
@@ -227,7 +229,7 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
   g2.F = p->F;
   g2.status = status;
   g2.pair = gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_PAIR;
-  if (fused && fused->combine && !swap && !cta2) {
+  if (fused && fused->combine && !swap && !cta2 && !swap2) {
     g2.epi = Epi::kCombine;
     g2.out = fused->out;
     g2.partials = y;
@@ -237,9 +239,10 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
     g2.counters = fused->counters;
     g2.k = p->k;
   }
-  MOE_LAUNCH(swap   ? launch_grouped_gemm_swap(g2, wide, s)
-             : cta2 ? launch_grouped_gemm_2cta(g2, s)
-                    : launch_grouped_gemm(g2, s));
+  MOE_LAUNCH(swap    ? launch_grouped_gemm_swap(g2, wide, s)
+             : cta2  ? launch_grouped_gemm_2cta(g2, s)
+             : swap2 ? launch_grouped_gemm_swap2(g2, s)
+                     : launch_grouped_gemm(g2, s));
   if (tm) tm->mark(call, mark + 1, s);
   return MOE_OK;
 }
@@ -430,7 +433,8 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   void* h = at<void>(ws, L.h);
   void* y = at<void>(ws, L.y);
   int32_t* counters = at<int32_t>(ws, L.counters);
-  const bool plain_tiles = use_weight_tiles(p) || gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_2CTA;
+  const bool plain_tiles = use_weight_tiles(p) || gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_2CTA ||
+                           gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES_2CTA;
   const bool fuse_gather = !plain_tiles && (p->fusion & MOE_FUSE_GATHER_A) != 0;
   const bool fuse_combine = !plain_tiles && (p->fusion & MOE_FUSE_COMBINE) != 0;
 

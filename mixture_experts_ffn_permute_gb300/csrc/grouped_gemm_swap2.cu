@@ -1,0 +1,507 @@
+// Weight-row tiles on CTA pairs: tcgen05.mma.cta_group::2 with the weight
+// rows on M (256 per pair) and the expert's tokens on N (fitted per tile).
+//
+// Ragged experts of a few hundred rows waste up to a whole 256-row tile when
+// tokens are on M; with tokens on N a tile pads at most 31 rows.  A pair tile
+// is 256 weight rows x N token rows (N <= 256, a multiple of 32):
+//   CTA r loads 128 weight rows (GEMM1: 64 gate + the matching 64 up rows of
+//   output columns f0 + 64 r .. f0 + 64 r + 63; GEMM2: output features
+//   128 r .. 128 r + 127 of the 256) and token rows r*N/2 .. (r+1)*N/2 - 1;
+//   the leader issues M=256 MMAs that read both CTAs' halves; each CTA's TMEM
+//   receives its 128 weight rows x N tokens.
+// So each CTA's epilogue is the 1-CTA weight-row epilogue (GEMM1 exchanges
+// gate and up rows through shared memory, 32 tokens at a time).
+// Synchronisation as in grouped_gemm_2cta.cu; every wait bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);  // grouped_gemm.cu
+
+namespace {
+
+constexpr int kThreadsP = 192;
+constexpr int kMP = 128;                       // weight rows per CTA
+constexpr int kNmaxP = 256;                    // token rows per pair tile
+constexpr int kStagesP = 6;
+constexpr uint32_t kWBytesP = kMP * kBK * 2;   // 16 KB
+constexpr uint32_t kXBytesP = (kNmaxP / 2) * kBK * 2;  // 16 KB: this CTA's token half
+constexpr uint32_t kStageP = kWBytesP + kXBytesP;
+constexpr uint32_t kTmemColsP = 2 * kNmaxP;
+constexpr int kMaxEP = 1024;
+constexpr int kDPitchP = 33;
+constexpr uint32_t kBarBytesP = 256;
+static_assert((2 * kStagesP + 5) * 8 + 8 <= kBarBytesP, "barrier area");
+constexpr size_t kSmemP = 1024 + kStagesP * kStageP + kBarBytesP +
+                          4 * (kMaxEP + 1) * sizeof(int32_t) + kMP * kDPitchP * sizeof(float);
+static_assert(kSmemP + 1024 <= 232448, "shared memory budget (dynamic + the 1024-aligned static part)");
+
+struct PParams {
+  const int32_t* expert_offsets;
+  uint16_t* out;  // bf16 [rows, ldo]
+  int E, K, w_tiles, w_rows_per_expert, ldo, F, interleave, out_rows;
+  float clamp;
+  uint32_t* status;
+};
+
+struct PTile {
+  int e, m, n;  // expert, weight pair tile, token tile
+  bool hot;
+};
+
+// Token tiles of a hot expert are visited in groups of kGroupP: all weight
+// tiles for one group, the token tile innermost.  A weight tile is then read
+// by the group's tiles at about the same time (one HBM read), and a token
+// tile comes back after one sweep of the group (it stays in L2) instead of
+// after a sweep over all of the expert's rows.
+#ifndef MOE_SWAP2_GROUP
+#define MOE_SWAP2_GROUP 8
+#endif
+constexpr int kGroupP = MOE_SWAP2_GROUP;
+
+
+// Tile order.  Experts with more than one token tile ("hot": their weight
+// tiles are reused from L2 and the MMAs bound them) and experts with one
+// ("cold": every tile streams fresh weights from HBM) form two lists, each
+// expert-major with the token tile innermost.  The lists are merged in
+// proportion -- position t is hot iff floor((t+1) nh / N) > floor(t nh / N) --
+// so that every wave of CTA pairs mixes compute-bound and HBM-bound tiles and
+// the weight stream overlaps the tensor-core work instead of alternating
+// with it.
+struct Sched {
+  const int32_t* hot_prefix;   // [E+1] tiles of hot experts before e
+  const int32_t* cold_prefix;  // [E+1] tiles of cold experts before e
+  const int32_t* ntk;          // [E] token tiles of e
+  int E, w_tiles, nh, nc;
+};
+
+__device__ __forceinline__ PTile decode_ptile(int tile, const Sched& s) {
+  const long long n = static_cast<long long>(s.nh) + s.nc;
+  const int hb = static_cast<int>(static_cast<long long>(tile) * s.nh / n);
+  const int ha = static_cast<int>(static_cast<long long>(tile + 1) * s.nh / n);
+  const bool hot = ha > hb;
+  const int idx = hot ? hb : tile - hb;
+  const int32_t* pf = hot ? s.hot_prefix : s.cold_prefix;
+  int lo = 0, hi = s.E - 1;  // the last expert whose first tile is <= idx
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pf[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  PTile t;
+  t.e = lo;
+  t.hot = hot;
+  const int local = idx - pf[lo];
+  const int nt = s.ntk[lo];
+  const int per_group = kGroupP * s.w_tiles;
+  const int g = local / per_group;
+  const int within = local - g * per_group;
+  const int gsz = min(kGroupP, nt - g * kGroupP);
+  t.m = within / gsz;
+  t.n = g * kGroupP + (within - t.m * gsz);
+  return t;
+}
+
+// Token rows this CTA loads for a tile of nval tokens: half = ceil(nval / 2)
+// rounded up to 16, and the smallest box of 16/32/64/128 rows that holds it.
+__device__ __forceinline__ int half_rows(int nval) { return ((nval + 1) / 2 + 15) & ~15; }
+__device__ __forceinline__ int box_index(int half) {
+  return half <= 16 ? 0 : half <= 32 ? 1 : half <= 64 ? 2 : 3;
+}
+
+__device__ __forceinline__ uint32_t mapa_p(uint32_t smem_addr, uint32_t cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(cta));
+  return r;
+}
+
+__device__ __forceinline__ void tma_load_pair(void* smem_dst, const CUtensorMap* map, int32_t c0,
+                                              int32_t c1, uint32_t bar_cluster, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void commit_pair_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(static_cast<uint16_t>(0x3))
+      : "memory");
+}
+
+__device__ __forceinline__ float silu_p(float z) { return z / (1.0f + expf(-z)); }
+
+template <Epi kEpi>
+__global__ void __launch_bounds__(kThreadsP, 1)
+grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
+                          const __grid_constant__ CUtensorMap map_x16,
+                          const __grid_constant__ CUtensorMap map_x32,
+                          const __grid_constant__ CUtensorMap map_x64,
+                          const __grid_constant__ CUtensorMap map_x128, const PParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sW = smem;
+  uint8_t* sX = smem + kStagesP * kWBytesP;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStagesP * kStageP);
+  uint64_t* empty = full + kStagesP;
+  uint64_t* tfull = empty + kStagesP;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStagesP * kStageP + kBarBytesP);
+  int32_t* s_hp = s_off + (kMaxEP + 1);
+  int32_t* s_cp = s_hp + (kMaxEP + 1);
+  int32_t* s_ntk = s_cp + (kMaxEP + 1);
+  float* sD = reinterpret_cast<float*>(s_ntk + (kMaxEP + 1));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  for (int i = threadIdx.x; i <= p.E; i += kThreadsP) s_off[i] = p.expert_offsets[i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesP; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&map_w);
+    prefetch_tensormap(&map_x16);
+    prefetch_tensormap(&map_x32);
+    prefetch_tensormap(&map_x64);
+    prefetch_tensormap(&map_x128);
+  }
+  if (warp == 1) {  // one warp of each CTA allocates the pair's columns together
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "n"(kTmemColsP)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  {  // tile prefixes: expert e owns w_tiles * ceil(rows_e / 256) pair tiles
+    __shared__ int s_part[2][kThreadsP / 32];
+    const int per = (p.E + kThreadsP - 1) / kThreadsP;
+    const int e0 = min(p.E, static_cast<int>(threadIdx.x) * per), e1 = min(p.E, e0 + per);
+    int run_h = 0, run_c = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int rows = s_off[e + 1] - s_off[e];
+      const int nt = rows > 0 ? (rows + kNmaxP - 1) / kNmaxP : 0;
+      s_ntk[e] = nt;
+      if (nt > 1) run_h += nt * p.w_tiles; else run_c += nt * p.w_tiles;
+    }
+    int inc_h = run_h, inc_c = run_c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int yh = __shfl_up_sync(0xffffffffu, inc_h, off);
+      const int yc = __shfl_up_sync(0xffffffffu, inc_c, off);
+      if (lane >= off) { inc_h += yh; inc_c += yc; }
+    }
+    if (lane == 31) { s_part[0][warp] = inc_h; s_part[1][warp] = inc_c; }
+    __syncthreads();
+    int acc_h = inc_h - run_h, acc_c = inc_c - run_c;
+    for (int w = 0; w < warp; ++w) { acc_h += s_part[0][w]; acc_c += s_part[1][w]; }
+    for (int e = e0; e < e1; ++e) {
+      s_hp[e] = acc_h;
+      s_cp[e] = acc_c;
+      const int nt = s_ntk[e];
+      if (nt > 1) acc_h += nt * p.w_tiles; else acc_c += nt * p.w_tiles;
+    }
+    if (threadIdx.x == kThreadsP - 1) {
+      int th = 0, tc = 0;
+      for (int w = 0; w < kThreadsP / 32; ++w) { th += s_part[0][w]; tc += s_part[1][w]; }
+      s_hp[p.E] = th;
+      s_cp[p.E] = tc;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before anything signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const Sched sched{s_hp, s_cp, s_ntk, p.E, p.w_tiles, s_hp[p.E], s_cp[p.E]};
+  const int total_tiles = sched.nh + sched.nc;
+  const int tile0 = static_cast<int>(blockIdx.x >> 1);
+  const int tstride = static_cast<int>(gridDim.x >> 1);
+  const int num_kb = p.K / kBK;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_normal();
+      const uint64_t pol_w_once = policy_evict_first();  // a cold expert's tile: read once
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      for (int tile = tile0; tile < total_tiles && !*abort_flag; tile += tstride) {
+        const PTile t = decode_ptile(tile, sched);
+        const int tok0 = t.n * kNmaxP;
+        const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - tok0);
+        const int half = half_rows(nval);
+        const int bi = box_index(half);
+        const int box = 16 << bi;
+        const CUtensorMap* mx = bi == 0 ? &map_x16 : bi == 1 ? &map_x32 : bi == 2 ? &map_x64
+                                                                                  : &map_x128;
+        const int x_row = s_off[t.e] + tok0 + static_cast<int>(rank) * half;
+        int w_row0, w_row1;
+        if (kEpi == Epi::kSwiGLU) {
+          const int f0 = t.m * kMP + static_cast<int>(rank) * 64;  // this CTA's 64 outputs
+          if (p.interleave == 32) {
+            w_row0 = 2 * f0;
+            w_row1 = 2 * f0 + 64;
+          } else if (p.interleave == 0) {
+            w_row0 = f0;
+            w_row1 = p.F + f0;
+          } else {  // 64 or a multiple of 128
+            w_row0 = (f0 / p.interleave) * 2 * p.interleave + f0 % p.interleave;
+            w_row1 = w_row0 + p.interleave;
+          }
+        } else {
+          w_row0 = t.m * (2 * kMP) + static_cast<int>(rank) * kMP;
+          w_row1 = w_row0 + 64;
+        }
+        w_row0 += t.e * p.w_rows_per_expert;
+        w_row1 += t.e * p.w_rows_per_expert;
+        const uint32_t bytes = kWBytesP + static_cast<uint32_t>(box) * kBK * 2;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { *abort_flag = 1; break; }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+          const uint32_t bar = mapa_p(smem_u32(&full[stage]), 0);
+          const int kx = kb * kBK;
+          uint8_t* w_dst = sW + stage * kWBytesP;
+          const uint64_t pw = t.hot ? pol_w : pol_w_once;
+          tma_load_pair(w_dst, &map_w, kx, w_row0, bar, pw);
+          tma_load_pair(w_dst + kWBytesP / 2, &map_w, kx, w_row1, bar, pw);
+          tma_load_pair(sX + stage * kXBytesP, mx, kx, x_row, bar, pol_x);
+          ++issued;
+          if (++stage == kStagesP) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (leader) {
+        for (int i = 1; i <= kStagesP && i <= issued; ++i) {
+          int s = stage - i;
+          uint32_t ph = phase;
+          if (s < 0) { s += kStagesP; ph ^= 1; }
+          mbar_wait(&full[s], ph, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA (leader only)
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = tile0; tile < total_tiles && !*abort_flag; tile += tstride, ++local) {
+        const int buf = local & 1;
+        const uint32_t tph = (local >> 1) & 1;
+        const PTile t = decode_ptile(tile, sched);
+        const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - t.n * kNmaxP);
+        const uint32_t nmma = static_cast<uint32_t>(2 * half_rows(nval));
+        const uint32_t idesc = idesc_bf16_f32(2 * kMP, nmma);
+        if (!mbar_wait(&tempty[buf], tph ^ 1, p.status)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kNmaxP;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t w_desc = sw128_kmajor_desc(smem_u32(sW + stage * kWBytesP));
+          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + stage * kXBytesP));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_pair(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
+          commit_pair_both(&empty[stage]);
+          if (++stage == kStagesP) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) { *abort_flag = 1; break; }
+        commit_pair_both(&tfull[buf]);
+      }
+      asm volatile(
+          "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+              smem_u32(drain))
+          : "memory");
+      mbar_wait(drain, 0, p.status);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int quad = warp & 3;
+    const int et = threadIdx.x - 64;
+    const int wrow = quad * 32 + lane;  // weight row inside this CTA's 128
+    const int ie = (p.interleave == 32) ? 32 : 64;
+    const int fl = et & 63;
+    const int grow = (fl / ie) * 2 * ie + fl % ie;
+    const int urow = grow + ie;
+    const bool clamp = p.clamp > 0.f && isfinite(p.clamp);
+    const uint32_t tempty_leader0 = mapa_p(smem_u32(&tempty[0]), 0);
+    const uint32_t tempty_leader1 = mapa_p(smem_u32(&tempty[1]), 0);
+    int local = 0;
+    for (int tile = tile0; tile < total_tiles; tile += tstride, ++local) {
+      const int buf = local & 1;
+      const uint32_t tph = (local >> 1) & 1;
+      const bool ok = mbar_wait(&tfull[buf], tph, p.status);
+      if (bar_red_or(1, 128, !ok || *abort_flag != 0)) {  // leave together
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const PTile t = decode_ptile(tile, sched);
+      const int tok0 = t.n * kNmaxP;
+      const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - tok0);
+      const int nchunk = (nval + 31) / 32;
+      const long row0 = static_cast<long>(s_off[t.e]) + tok0;
+      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kNmaxP;
+      for (int c = 0; c < nchunk; ++c) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(t_lane + c * 32, a);
+        tmem_ld_wait();
+        if (c == nchunk - 1) {  // the accumulator is no longer needed
+          tc_fence_before();
+          arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+        }
+        const int n0 = c * 32;
+        if (kEpi == Epi::kPlain) {
+          const int feat = t.m * (2 * kMP) + static_cast<int>(rank) * kMP + wrow;
+#pragma unroll
+          for (int n = 0; n < 32; ++n) {
+            if (n0 + n < nval) {
+              const __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(a[n]));
+              p.out[(row0 + n0 + n) * p.ldo + feat] = *reinterpret_cast<const uint16_t*>(&v);
+            }
+          }
+        } else {
+          if (c > 0) bar_sync_named(1, 128);
+#pragma unroll
+          for (int n = 0; n < 32; ++n) sD[wrow * kDPitchP + n] = __uint_as_float(a[n]);
+          bar_sync_named(1, 128);
+          const int f = t.m * kMP + static_cast<int>(rank) * 64 + fl;
+#pragma unroll 4
+          for (int n = et >> 6; n < 32; n += 2) {
+            if (n0 + n < nval) {
+              float g = sD[grow * kDPitchP + n], u = sD[urow * kDPitchP + n];
+              if (clamp) {
+                g = fminf(g, p.clamp);
+                u = fminf(fmaxf(u, -p.clamp), p.clamp);
+              }
+              const __nv_bfloat16 v = __float2bfloat16_rn(silu_p(g) * u);
+              p.out[(row0 + n0 + n) * p.ldo + f] = *reinterpret_cast<const uint16_t*>(&v);
+            }
+          }
+        }
+      }
+    }
+    if (kEpi == Epi::kPlain) {  // rows past the last expert's segment are zero
+      const long first = s_off[p.E];
+      const long n = (static_cast<long>(p.out_rows) - first) * p.ldo;
+      for (long i = static_cast<long>(blockIdx.x) * 128 + et; i < n;
+           i += static_cast<long>(gridDim.x) * 128)
+        p.out[first * p.ldo + i] = 0;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "n"(kTmemColsP)
+                 : "memory");
+  }
+}
+
+template <Epi kEpi>
+cudaError_t launch_swap2_impl(const CUtensorMap* maps, const PParams& pp, int grid,
+                              cudaStream_t s) {
+  auto kern = grouped_gemm_swap2_kernel<kEpi>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemP));
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreadsP, 1, 1);
+  cfg.dynamicSmemBytes = kSmemP;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], pp);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_swap2(const GroupedGemmArgs& g, cudaStream_t s) {
+  if (g.a_rows == 0) return cudaSuccess;
+  if (g.E > kMaxEP) return cudaErrorInvalidValue;
+  CUtensorMap maps[5];
+  if (!make_map_2d(&maps[0], g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
+                   static_cast<uint64_t>(g.K), 64))
+    return cudaErrorInvalidValue;
+  const uint32_t boxes[4] = {16, 32, 64, 128};
+  for (int i = 0; i < 4; ++i)
+    if (!make_map_2d(&maps[1 + i], g.a, static_cast<uint64_t>(g.a_rows),
+                     static_cast<uint64_t>(g.K), boxes[i]))
+      return cudaErrorInvalidValue;
+  PParams pp;
+  pp.expert_offsets = g.expert_offsets;
+  pp.out = static_cast<uint16_t*>(g.out);
+  pp.E = g.E;
+  pp.K = g.K;
+  pp.w_rows_per_expert = g.b_rows_per_expert;
+  pp.ldo = g.ldo;
+  pp.out_rows = g.out_rows;
+  pp.F = g.F;
+  pp.interleave = g.interleave;
+  pp.clamp = g.clamp;
+  pp.status = g.status;
+  // pair tiles along the weights: GEMM1 covers 128 output columns, GEMM2 256 features
+  pp.w_tiles = (g.epi == Epi::kSwiGLU) ? g.F / kMP : g.ldo / (2 * kMP);
+  const long max_tiles =
+      (static_cast<long>(ceil_div(g.a_rows, kNmaxP)) + std::min(g.E, g.a_rows)) * pp.w_tiles;
+  const long want = std::min<long>(num_sms() & ~1, 2 * max_tiles);
+  const int grid = static_cast<int>(std::max(2L, want & ~1L));
+  if (g.epi == Epi::kSwiGLU) return launch_swap2_impl<Epi::kSwiGLU>(maps, pp, grid, s);
+  if (g.epi == Epi::kPlain) return launch_swap2_impl<Epi::kPlain>(maps, pp, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -111,6 +111,9 @@ cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaSt
 // Token-row tiles on CTA pairs with tcgen05.mma.cta_group::2 (kSwiGLU, kPlain).
 cudaError_t launch_grouped_gemm_2cta(const GroupedGemmArgs& g, cudaStream_t s);
 
+// Weight-row tiles on CTA pairs (cta_group::2), tokens on N fitted per tile.
+cudaError_t launch_grouped_gemm_swap2(const GroupedGemmArgs& g, cudaStream_t s);
+
 // NVFP4-weight GEMMs (a = f16 rows, b = packed E2M1 codes [E * rows, K / 2],
 // scales in the prepared layout, gscale = per-expert fp32 tensor scales).
 // kSwiGLU stores FP8-requantised h as f16; kPlain stores bf16 y.

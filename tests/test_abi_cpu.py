@@ -102,3 +102,16 @@ def test_other_entry_points_validate(lib):
 def test_binding_raises_without_library(tmp_path):
     with pytest.raises(ImportError):
         moe.load(str(tmp_path / "missing.so"))
+
+
+def test_auto_tiling_selection():
+    """Auto picks 32-token weight-row tiles at <= 2 routes per expert, else 2-CTA weight-row tiles."""
+    lib = moe.load()
+    assert moe.selected_kernel(moe.Problem.make(T=1, H=2048, F=768, E=128, k=8)) == moe.KERNEL_WEIGHT_TILES
+    assert moe.selected_kernel(moe.Problem.make(T=64, H=2048, F=768, E=128, k=8)) == \
+        moe.KERNEL_WEIGHT_TILES_2CTA
+    assert moe.selected_kernel(moe.Problem.make(T=4096, H=4096, F=14336, E=8, k=2)) == \
+        moe.KERNEL_WEIGHT_TILES_2CTA
+    p = moe.Problem.make(T=4096, H=4096, F=14336, E=8, k=2, kernel=moe.KERNEL_TOKEN_TILES_2CTA)
+    assert moe.selected_kernel(p) == moe.KERNEL_TOKEN_TILES_2CTA
+    assert lib is not None

@@ -56,9 +56,9 @@ SMALL = [
 
 
 KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE,
-           moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA]
+           moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA, moe.KERNEL_WEIGHT_TILES_2CTA]
 KERNEL_IDS = ["token_tiles", "weight_tiles", "weight_tiles_wide", "token_tiles_pair",
-              "token_tiles_2cta"]
+              "token_tiles_2cta", "weight_tiles_2cta"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
@@ -168,8 +168,9 @@ def test_forward_mixtral_full_size_sampled(kernel):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_WIDE],
-                         ids=["auto", "weight_tiles_wide"])
+@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_WIDE,
+                                    moe.KERNEL_TOKEN_TILES_2CTA],
+                         ids=["auto", "weight_tiles_wide", "token_tiles_2cta"])
 def test_forward_skewed_full_size_sampled(kernel):
     sampled_check(mi.SKEWED, 4, kernel=kernel)
 

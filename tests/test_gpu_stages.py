@@ -151,11 +151,11 @@ def _routed_inputs(shape, seed=0, mask=0.0):
 
 
 KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE,
-           moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA]
+           moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA, moe.KERNEL_WEIGHT_TILES_2CTA]
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_wide",
-                                                "token_tiles_pair", "token_tiles_2cta"])
+                                                "token_tiles_pair", "token_tiles_2cta", "weight_tiles_2cta"])
 @pytest.mark.parametrize("shape", MLP_CASES, ids=lambda s: s.name)
 def test_grouped_swiglu_mlp(shape, kernel):
     inp, idx, w, perm, xp = _routed_inputs(shape, seed=1)
@@ -176,7 +176,7 @@ def test_grouped_swiglu_mlp(shape, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_wide",
-                                                "token_tiles_pair", "token_tiles_2cta"])
+                                                "token_tiles_pair", "token_tiles_2cta", "weight_tiles_2cta"])
 def test_grouped_mlp_masked_tail_rows_are_zero(kernel):
     shape = mi.MoEShape("masked", T=100, H=256, F=256, E=6, k=2)
     inp, idx, w, perm, xp = _routed_inputs(shape, seed=4, mask=0.25)
