@@ -241,8 +241,13 @@ MOE_API int moe_permute_noalloc(const moe_problem* p, const int32_t* topk_idx, c
  * scale per 16 values along K and one fp32 scale per expert weight tensor.
  * The weights stay 4-bit in HBM.  GEMM1's SwiGLU output is re-quantised to
  * E4M3 with one fp32 scale (amax / 448) per 128 values of a row before
- * GEMM2, as that page's split GEMM1 does.  Output bf16.  Token-row tiles
- * only (moe_problem.kernel and .fusion are ignored). */
+ * GEMM2, as that page's split GEMM1 does.  Output bf16.  Tilings
+ * (moe_problem.kernel): MOE_KERNEL_AUTO or MOE_KERNEL_TOKEN_TILES run 1-CTA
+ * 128-token x 256-weight-row tiles; MOE_KERNEL_WEIGHT_TILES_2CTA runs 2-CTA
+ * weight-row tiles (each CTA expands its 128 weight rows; the 1x128
+ * re-quantisation block of h spans both CTAs of a pair, whose per-token
+ * maxima are exchanged through distributed shared memory); any other value
+ * is MOE_ERR_INVALID_ARG.  moe_problem.fusion is ignored. */
 
 /* Bytes of the prepared scale buffer for W1 and W2 together. */
 MOE_API size_t moe_prepared_scales_size(const moe_problem* p);

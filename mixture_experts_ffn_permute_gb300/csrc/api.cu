@@ -109,6 +109,10 @@ int check_full(const moe_problem* p) {
   if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
   if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_WEIGHT_TILES_2CTA)
     return MOE_ERR_INVALID_ARG;
+  // the FP8/NVFP4 GEMMs come in two tilings
+  if (p->precision == MOE_PREC_FP8_NVFP4 && p->kernel != MOE_KERNEL_AUTO &&
+      p->kernel != MOE_KERNEL_TOKEN_TILES && p->kernel != MOE_KERNEL_WEIGHT_TILES_2CTA)
+    return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
   if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   const int I = p->glu_interleave;
@@ -150,6 +154,15 @@ int gemm_tiling(const moe_problem* p) {
   const long long routes = static_cast<long long>(p->T) * p->k;
   if (routes <= 2LL * p->E) return MOE_KERNEL_WEIGHT_TILES;
   return MOE_KERNEL_WEIGHT_TILES_2CTA;
+}
+
+// FP8/NVFP4 tiling: 1-CTA token-row tiles unless the 2-CTA weight-row tiles
+// are asked for (a cta_group::2 MMA costs the same for every N <= 256, so
+// fitting N to ragged experts saves no tensor time; the token-row tiles are
+// faster on GB300).
+int lowprec_tiling(const moe_problem* p) {
+  return p->kernel == MOE_KERNEL_WEIGHT_TILES_2CTA ? MOE_KERNEL_WEIGHT_TILES_2CTA
+                                                   : MOE_KERNEL_TOKEN_TILES;
 }
 
 bool use_weight_tiles(const moe_problem* p) {
@@ -569,7 +582,9 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
   g1.interleave = p->glu_interleave;
   g1.clamp = clamp_of(p);
   g1.status = status;
-  MOE_LAUNCH(launch_grouped_gemm_fp4(g1, sc1, w1_gscale, s));
+  const bool pair_tiles = lowprec_tiling(p) == MOE_KERNEL_WEIGHT_TILES_2CTA;
+  MOE_LAUNCH(pair_tiles ? launch_grouped_gemm_fp4_pair(g1, sc1, w1_gscale, s)
+                        : launch_grouped_gemm_fp4(g1, sc1, w1_gscale, s));
   tm.mark(call, 6, s);
   GroupedGemmArgs g2{};
   g2.epi = Epi::kPlain;
@@ -587,7 +602,8 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
   g2.out_rows = R;
   g2.F = p->F;
   g2.status = status;
-  MOE_LAUNCH(launch_grouped_gemm_fp4(g2, sc2, w2_gscale, s));
+  MOE_LAUNCH(pair_tiles ? launch_grouped_gemm_fp4_pair(g2, sc2, w2_gscale, s)
+                        : launch_grouped_gemm_fp4(g2, sc2, w2_gscale, s));
   tm.mark(call, 7, s);
   MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
   tm.mark(call, 8, s);
@@ -618,7 +634,7 @@ int moe_last_launch_count(void) { return g_launches; }
 
 int moe_selected_kernel(const moe_problem* p) {
   if (check_full(p) != MOE_OK) return -1;
-  if (p->precision == MOE_PREC_FP8_NVFP4) return MOE_KERNEL_TOKEN_TILES;
+  if (p->precision == MOE_PREC_FP8_NVFP4) return lowprec_tiling(p);
   return gemm_tiling(p);
 }
 

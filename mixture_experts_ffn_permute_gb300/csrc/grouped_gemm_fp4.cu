@@ -30,13 +30,15 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "lowprec.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 
 bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);  // grouped_gemm.cu (2-byte elements, 128-byte swizzle)
-bool make_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);  // 32 x 128 boxes
+bool make_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);  // grouped_gemm.cu (32-byte wide boxes, no swizzle)
 
 namespace {
 
@@ -94,51 +96,6 @@ __device__ __forceinline__ FTile decode_ftile(int tile, const int32_t* mtp, int 
   t.n = local / mt;
   t.m = local - t.n * mt;
   return t;
-}
-
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_u32(smem_dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Two E2M1 codes (low nibble = lower element) -> f16x2.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "r"(byte));
-  return r;
-}
-
-// Two E4M3 codes (low byte = lower element) -> f16x2.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "r"(two));
-  return r;
-}
-
-// (lo, hi) fp32 -> two E4M3 codes, round-to-nearest-even, saturating.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  __half2 x = *reinterpret_cast<__half2*>(&a);
-  __half2 y = *reinterpret_cast<__half2*>(&b);
-  __half2 z = __hmul2(x, y);
-  return *reinterpret_cast<uint32_t*>(&z);
 }
 
 __device__ __forceinline__ float silu_f4(float z) { return z / (1.0f + expf(-z)); }
@@ -528,7 +485,7 @@ cudaError_t launch_grouped_gemm_fp4(const GroupedGemmArgs& g, const uint8_t* sca
   if (!make_map_2d(&ma, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K), kBM))
     return cudaErrorInvalidValue;
   if (!make_map_u8(&mq, g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
-                   static_cast<uint64_t>(g.K) / 2))
+                   static_cast<uint64_t>(g.K) / 2, 128))
     return cudaErrorInvalidValue;
   FParams fp;
   fp.expert_offsets = g.expert_offsets;

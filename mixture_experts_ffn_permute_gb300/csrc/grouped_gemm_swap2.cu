@@ -10,7 +10,8 @@
 //   the leader issues M=256 MMAs that read both CTAs' halves; each CTA's TMEM
 //   receives its 128 weight rows x N tokens.
 // So each CTA's epilogue is the 1-CTA weight-row epilogue (GEMM1 exchanges
-// gate and up rows through shared memory, 32 tokens at a time).
+// gate and up rows through shared memory, 32 tokens at a time).  Tile order
+// and the cluster-scope helpers are in pair_tiles.cuh.
 // Synchronisation as in grouped_gemm_2cta.cu; every wait bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -20,6 +21,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "pair_tiles.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -30,8 +32,8 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 namespace {
 
 constexpr int kThreadsP = 192;
-constexpr int kMP = 128;                       // weight rows per CTA
-constexpr int kNmaxP = 256;                    // token rows per pair tile
+constexpr int kMP = pair::kM;                  // weight rows per CTA
+constexpr int kNmaxP = pair::kNmax;            // token rows per pair tile
 constexpr int kStagesP = 6;
 constexpr uint32_t kWBytesP = kMP * kBK * 2;   // 16 KB
 constexpr uint32_t kXBytesP = (kNmaxP / 2) * kBK * 2;  // 16 KB: this CTA's token half
@@ -52,108 +54,6 @@ struct PParams {
   float clamp;
   uint32_t* status;
 };
-
-struct PTile {
-  int e, m, n;  // expert, weight pair tile, token tile
-  bool hot;
-};
-
-// Token tiles of a hot expert are visited in groups of kGroupP: all weight
-// tiles for one group, the token tile innermost.  A weight tile is then read
-// by the group's tiles at about the same time (one HBM read), and a token
-// tile comes back after one sweep of the group (it stays in L2) instead of
-// after a sweep over all of the expert's rows.
-#ifndef MOE_SWAP2_GROUP
-#define MOE_SWAP2_GROUP 8
-#endif
-constexpr int kGroupP = MOE_SWAP2_GROUP;
-
-
-// Tile order.  Experts with more than one token tile ("hot": their weight
-// tiles are reused from L2 and the MMAs bound them) and experts with one
-// ("cold": every tile streams fresh weights from HBM) form two lists, each
-// expert-major with the token tile innermost.  The lists are merged in
-// proportion -- position t is hot iff floor((t+1) nh / N) > floor(t nh / N) --
-// so that every wave of CTA pairs mixes compute-bound and HBM-bound tiles and
-// the weight stream overlaps the tensor-core work instead of alternating
-// with it.
-struct Sched {
-  const int32_t* hot_prefix;   // [E+1] tiles of hot experts before e
-  const int32_t* cold_prefix;  // [E+1] tiles of cold experts before e
-  const int32_t* ntk;          // [E] token tiles of e
-  int E, w_tiles, nh, nc;
-};
-
-__device__ __forceinline__ PTile decode_ptile(int tile, const Sched& s) {
-  const long long n = static_cast<long long>(s.nh) + s.nc;
-  const int hb = static_cast<int>(static_cast<long long>(tile) * s.nh / n);
-  const int ha = static_cast<int>(static_cast<long long>(tile + 1) * s.nh / n);
-  const bool hot = ha > hb;
-  const int idx = hot ? hb : tile - hb;
-  const int32_t* pf = hot ? s.hot_prefix : s.cold_prefix;
-  int lo = 0, hi = s.E - 1;  // the last expert whose first tile is <= idx
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pf[mid] <= idx) lo = mid; else hi = mid - 1;
-  }
-  PTile t;
-  t.e = lo;
-  t.hot = hot;
-  const int local = idx - pf[lo];
-  const int nt = s.ntk[lo];
-  const int per_group = kGroupP * s.w_tiles;
-  const int g = local / per_group;
-  const int within = local - g * per_group;
-  const int gsz = min(kGroupP, nt - g * kGroupP);
-  t.m = within / gsz;
-  t.n = g * kGroupP + (within - t.m * gsz);
-  return t;
-}
-
-// Token rows this CTA loads for a tile of nval tokens: half = ceil(nval / 2)
-// rounded up to 16, and the smallest box of 16/32/64/128 rows that holds it.
-__device__ __forceinline__ int half_rows(int nval) { return ((nval + 1) / 2 + 15) & ~15; }
-__device__ __forceinline__ int box_index(int half) {
-  return half <= 16 ? 0 : half <= 32 ? 1 : half <= 64 ? 2 : 3;
-}
-
-__device__ __forceinline__ uint32_t mapa_p(uint32_t smem_addr, uint32_t cta) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(cta));
-  return r;
-}
-
-__device__ __forceinline__ void tma_load_pair(void* smem_dst, const CUtensorMap* map, int32_t c0,
-                                              int32_t c1, uint32_t bar_cluster, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
-      "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
-}
-
-__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void commit_pair_both(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(static_cast<uint16_t>(0x3))
-      : "memory");
-}
 
 __device__ __forceinline__ float silu_p(float z) { return z / (1.0f + expf(-z)); }
 
@@ -206,55 +106,17 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
     prefetch_tensormap(&map_x128);
   }
   if (warp == 1) {  // one warp of each CTA allocates the pair's columns together
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "n"(kTmemColsP)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    pair::tmem_alloc2<kTmemColsP>(tmem_slot);
   }
   __syncthreads();
-  {  // tile prefixes: expert e owns w_tiles * ceil(rows_e / 256) pair tiles
-    __shared__ int s_part[2][kThreadsP / 32];
-    const int per = (p.E + kThreadsP - 1) / kThreadsP;
-    const int e0 = min(p.E, static_cast<int>(threadIdx.x) * per), e1 = min(p.E, e0 + per);
-    int run_h = 0, run_c = 0;
-    for (int e = e0; e < e1; ++e) {
-      const int rows = s_off[e + 1] - s_off[e];
-      const int nt = rows > 0 ? (rows + kNmaxP - 1) / kNmaxP : 0;
-      s_ntk[e] = nt;
-      if (nt > 1) run_h += nt * p.w_tiles; else run_c += nt * p.w_tiles;
-    }
-    int inc_h = run_h, inc_c = run_c;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int yh = __shfl_up_sync(0xffffffffu, inc_h, off);
-      const int yc = __shfl_up_sync(0xffffffffu, inc_c, off);
-      if (lane >= off) { inc_h += yh; inc_c += yc; }
-    }
-    if (lane == 31) { s_part[0][warp] = inc_h; s_part[1][warp] = inc_c; }
-    __syncthreads();
-    int acc_h = inc_h - run_h, acc_c = inc_c - run_c;
-    for (int w = 0; w < warp; ++w) { acc_h += s_part[0][w]; acc_c += s_part[1][w]; }
-    for (int e = e0; e < e1; ++e) {
-      s_hp[e] = acc_h;
-      s_cp[e] = acc_c;
-      const int nt = s_ntk[e];
-      if (nt > 1) acc_h += nt * p.w_tiles; else acc_c += nt * p.w_tiles;
-    }
-    if (threadIdx.x == kThreadsP - 1) {
-      int th = 0, tc = 0;
-      for (int w = 0; w < kThreadsP / 32; ++w) { th += s_part[0][w]; tc += s_part[1][w]; }
-      s_hp[p.E] = th;
-      s_cp[p.E] = tc;
-    }
-  }
+  const pair::Sched sched =
+      pair::build_sched<kThreadsP>(s_off, p.E, p.w_tiles, s_ntk, s_hp, s_cp);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // both CTAs' barriers exist before anything signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const Sched sched{s_hp, s_cp, s_ntk, p.E, p.w_tiles, s_hp[p.E], s_cp[p.E]};
-  const int total_tiles = sched.nh + sched.nc;
+  const int total_tiles = sched.total();
   const int tile0 = static_cast<int>(blockIdx.x >> 1);
   const int tstride = static_cast<int>(gridDim.x >> 1);
   const int num_kb = p.K / kBK;
@@ -269,45 +131,30 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
       uint32_t phase = 0;
       long issued = 0;
       for (int tile = tile0; tile < total_tiles && !*abort_flag; tile += tstride) {
-        const PTile t = decode_ptile(tile, sched);
+        const pair::Tile t = pair::decode(tile, sched);
         const int tok0 = t.n * kNmaxP;
         const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - tok0);
-        const int half = half_rows(nval);
-        const int bi = box_index(half);
+        const int half = pair::half_rows(nval);
+        const int bi = pair::box_index(half);
         const int box = 16 << bi;
         const CUtensorMap* mx = bi == 0 ? &map_x16 : bi == 1 ? &map_x32 : bi == 2 ? &map_x64
                                                                                   : &map_x128;
         const int x_row = s_off[t.e] + tok0 + static_cast<int>(rank) * half;
         int w_row0, w_row1;
-        if (kEpi == Epi::kSwiGLU) {
-          const int f0 = t.m * kMP + static_cast<int>(rank) * 64;  // this CTA's 64 outputs
-          if (p.interleave == 32) {
-            w_row0 = 2 * f0;
-            w_row1 = 2 * f0 + 64;
-          } else if (p.interleave == 0) {
-            w_row0 = f0;
-            w_row1 = p.F + f0;
-          } else {  // 64 or a multiple of 128
-            w_row0 = (f0 / p.interleave) * 2 * p.interleave + f0 % p.interleave;
-            w_row1 = w_row0 + p.interleave;
-          }
-        } else {
-          w_row0 = t.m * (2 * kMP) + static_cast<int>(rank) * kMP;
-          w_row1 = w_row0 + 64;
-        }
+        pair::weight_rows(kEpi == Epi::kSwiGLU, t.m, rank, p.F, p.interleave, w_row0, w_row1);
         w_row0 += t.e * p.w_rows_per_expert;
         w_row1 += t.e * p.w_rows_per_expert;
         const uint32_t bytes = kWBytesP + static_cast<uint32_t>(box) * kBK * 2;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { *abort_flag = 1; break; }
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
-          const uint32_t bar = mapa_p(smem_u32(&full[stage]), 0);
+          const uint32_t bar = pair::mapa(smem_u32(&full[stage]), 0);
           const int kx = kb * kBK;
           uint8_t* w_dst = sW + stage * kWBytesP;
           const uint64_t pw = t.hot ? pol_w : pol_w_once;
-          tma_load_pair(w_dst, &map_w, kx, w_row0, bar, pw);
-          tma_load_pair(w_dst + kWBytesP / 2, &map_w, kx, w_row1, bar, pw);
-          tma_load_pair(sX + stage * kXBytesP, mx, kx, x_row, bar, pol_x);
+          pair::tma_load(w_dst, &map_w, kx, w_row0, bar, pw);
+          pair::tma_load(w_dst + kWBytesP / 2, &map_w, kx, w_row1, bar, pw);
+          pair::tma_load(sX + stage * kXBytesP, mx, kx, x_row, bar, pol_x);
           ++issued;
           if (++stage == kStagesP) { stage = 0; phase ^= 1; }
         }
@@ -330,9 +177,9 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
       for (int tile = tile0; tile < total_tiles && !*abort_flag; tile += tstride, ++local) {
         const int buf = local & 1;
         const uint32_t tph = (local >> 1) & 1;
-        const PTile t = decode_ptile(tile, sched);
+        const pair::Tile t = pair::decode(tile, sched);
         const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - t.n * kNmaxP);
-        const uint32_t nmma = static_cast<uint32_t>(2 * half_rows(nval));
+        const uint32_t nmma = static_cast<uint32_t>(2 * pair::half_rows(nval));
         const uint32_t idesc = idesc_bf16_f32(2 * kMP, nmma);
         if (!mbar_wait(&tempty[buf], tph ^ 1, p.status)) { *abort_flag = 1; break; }
         tc_fence_after();
@@ -345,17 +192,14 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
           const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + stage * kXBytesP));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_pair(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
-          commit_pair_both(&empty[stage]);
+            pair::mma(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
+          pair::commit_both(&empty[stage]);
           if (++stage == kStagesP) { stage = 0; phase ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
-        commit_pair_both(&tfull[buf]);
+        pair::commit_both(&tfull[buf]);
       }
-      asm volatile(
-          "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-              smem_u32(drain))
-          : "memory");
+      pair::commit_local(drain);
       mbar_wait(drain, 0, p.status);
     }
   } else {
@@ -368,8 +212,8 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
     const int grow = (fl / ie) * 2 * ie + fl % ie;
     const int urow = grow + ie;
     const bool clamp = p.clamp > 0.f && isfinite(p.clamp);
-    const uint32_t tempty_leader0 = mapa_p(smem_u32(&tempty[0]), 0);
-    const uint32_t tempty_leader1 = mapa_p(smem_u32(&tempty[1]), 0);
+    const uint32_t tempty_leader0 = pair::mapa(smem_u32(&tempty[0]), 0);
+    const uint32_t tempty_leader1 = pair::mapa(smem_u32(&tempty[1]), 0);
     int local = 0;
     for (int tile = tile0; tile < total_tiles; tile += tstride, ++local) {
       const int buf = local & 1;
@@ -380,7 +224,7 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
         break;
       }
       tc_fence_after();
-      const PTile t = decode_ptile(tile, sched);
+      const pair::Tile t = pair::decode(tile, sched);
       const int tok0 = t.n * kNmaxP;
       const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - tok0);
       const int nchunk = (nval + 31) / 32;
@@ -392,7 +236,7 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
         tmem_ld_wait();
         if (c == nchunk - 1) {  // the accumulator is no longer needed
           tc_fence_before();
-          arrive_cluster(buf ? tempty_leader1 : tempty_leader0);
+          pair::arrive_remote(buf ? tempty_leader1 : tempty_leader0);
         }
         const int n0 = c * 32;
         if (kEpi == Epi::kPlain) {
@@ -439,9 +283,7 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "n"(kTmemColsP)
-                 : "memory");
+    pair::tmem_dealloc2<kTmemColsP>(tmem_base);
   }
 }
 

@@ -119,6 +119,10 @@ cudaError_t launch_grouped_gemm_swap2(const GroupedGemmArgs& g, cudaStream_t s);
 // kSwiGLU stores FP8-requantised h as f16; kPlain stores bf16 y.
 cudaError_t launch_grouped_gemm_fp4(const GroupedGemmArgs& g, const uint8_t* scales,
                                     const float* gscale, cudaStream_t s);
+// The same GEMMs with weight-row tiles on CTA pairs (cta_group::2, N fitted per
+// expert); needs rows per expert a multiple of 128.
+cudaError_t launch_grouped_gemm_fp4_pair(const GroupedGemmArgs& g, const uint8_t* scales,
+                                         const float* gscale, cudaStream_t s);
 // [E][N][K/16] E4M3 scales -> [E][N/128][K/64][128][4]
 cudaError_t launch_prepare_scales(const uint8_t* src, uint8_t* dst, int E, int N, int K,
                                   cudaStream_t s);

@@ -24,9 +24,14 @@ def built():
     moe.load()
 
 
-def run_lowprec(shape, inp):
+# 1-CTA token-row tiles (the default) and the 2-CTA weight-row tiles
+KERNELS = [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_2CTA]
+KERNEL_IDS = ["token_tiles", "weight_tiles_2cta"]
+
+
+def run_lowprec(shape, inp, kernel=moe.KERNEL_AUTO):
     p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True, shape.glu_interleave,
-                         shape.swiglu_clamp, precision=moe.PREC_FP8_NVFP4)
+                         shape.swiglu_clamp, precision=moe.PREC_FP8_NVFP4, kernel=kernel)
     prepared = torch.empty(moe.prepared_scales_size(p), dtype=torch.uint8, device=DEV)
     moe.prepare_weights(p, inp["w1s"], inp["w2s"], prepared)
     ws = moe.alloc_workspace(p)
@@ -62,13 +67,14 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
-def test_lowprec_forward_small(shape):
+def test_lowprec_forward_small(shape, kernel):
     inp = mi.make_lowprec_inputs(shape, seed=0)
     ref = oracle.moe_forward_lowprec(inp["xq"], inp["xs"], inp["logits"], inp["w1q"], inp["w1s"],
                                      inp["w1g"], inp["w2q"], inp["w2s"], inp["w2g"], shape.k,
                                      interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
-    res = run_lowprec(shape, {k: v.to(DEV) for k, v in inp.items()})
+    res = run_lowprec(shape, {k: v.to(DEV) for k, v in inp.items()}, kernel)
     assert_equal(res["topk_idx"], ref["topk_idx"], "topk_idx")
     check(res["out"], ref["out"], shape.name)
 
@@ -90,10 +96,11 @@ def test_prepare_weights_layout():
 
 
 @pytest.mark.slow
-def test_lowprec_full_size_sampled():
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
+def test_lowprec_full_size_sampled(kernel):
     shape = mi.LOWPREC
     inp = mi.make_lowprec_inputs(shape, seed=0, device=DEV)
-    res = run_lowprec(shape, inp)
+    res = run_lowprec(shape, inp, kernel)
     logits_h = inp["logits"].cpu()
     idx_ref, _ = oracle.route_topk(logits_h, shape.k)
     assert_equal(res["topk_idx"], idx_ref, "topk_idx")
