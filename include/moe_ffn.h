@@ -243,7 +243,10 @@ MOE_API int moe_permute_noalloc(const moe_problem* p, const int32_t* topk_idx, c
  * E4M3 with one fp32 scale (amax / 448) per 128 values of a row before
  * GEMM2, as that page's split GEMM1 does.  Output bf16.  Tilings
  * (moe_problem.kernel): MOE_KERNEL_AUTO or MOE_KERNEL_TOKEN_TILES run 1-CTA
- * 128-token x 256-weight-row tiles; MOE_KERNEL_WEIGHT_TILES_2CTA runs 2-CTA
+ * 128-token x 256-weight-row tiles; MOE_KERNEL_WEIGHT_TILES_WIDE runs 1-CTA
+ * 128-weight-row x up to 192-token tiles fitted per expert, the weights
+ * expanded straight into tensor memory (the MMA's A operand) and the token
+ * rows shared by CTA pairs; MOE_KERNEL_WEIGHT_TILES_2CTA runs 2-CTA
  * weight-row tiles (each CTA expands its 128 weight rows; the 1x128
  * re-quantisation block of h spans both CTAs of a pair, whose per-token
  * maxima are exchanged through distributed shared memory); any other value

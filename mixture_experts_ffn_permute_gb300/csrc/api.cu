@@ -111,7 +111,8 @@ int check_full(const moe_problem* p) {
     return MOE_ERR_INVALID_ARG;
   // the FP8/NVFP4 GEMMs come in two tilings
   if (p->precision == MOE_PREC_FP8_NVFP4 && p->kernel != MOE_KERNEL_AUTO &&
-      p->kernel != MOE_KERNEL_TOKEN_TILES && p->kernel != MOE_KERNEL_WEIGHT_TILES_2CTA)
+      p->kernel != MOE_KERNEL_TOKEN_TILES && p->kernel != MOE_KERNEL_WEIGHT_TILES_WIDE &&
+      p->kernel != MOE_KERNEL_WEIGHT_TILES_2CTA)
     return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
   if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -161,8 +162,9 @@ int gemm_tiling(const moe_problem* p) {
 // fitting N to ragged experts saves no tensor time; the token-row tiles are
 // faster on GB300).
 int lowprec_tiling(const moe_problem* p) {
-  return p->kernel == MOE_KERNEL_WEIGHT_TILES_2CTA ? MOE_KERNEL_WEIGHT_TILES_2CTA
-                                                   : MOE_KERNEL_TOKEN_TILES;
+  if (p->kernel == MOE_KERNEL_WEIGHT_TILES_2CTA || p->kernel == MOE_KERNEL_WEIGHT_TILES_WIDE)
+    return p->kernel;
+  return MOE_KERNEL_TOKEN_TILES;
 }
 
 bool use_weight_tiles(const moe_problem* p) {
@@ -582,9 +584,11 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
   g1.interleave = p->glu_interleave;
   g1.clamp = clamp_of(p);
   g1.status = status;
-  const bool pair_tiles = lowprec_tiling(p) == MOE_KERNEL_WEIGHT_TILES_2CTA;
-  MOE_LAUNCH(pair_tiles ? launch_grouped_gemm_fp4_pair(g1, sc1, w1_gscale, s)
-                        : launch_grouped_gemm_fp4(g1, sc1, w1_gscale, s));
+  const int lt = lowprec_tiling(p);
+  MOE_LAUNCH(lt == MOE_KERNEL_WEIGHT_TILES_2CTA ? launch_grouped_gemm_fp4_pair(g1, sc1, w1_gscale, s)
+             : lt == MOE_KERNEL_WEIGHT_TILES_WIDE
+                 ? launch_grouped_gemm_fp4_tmem(g1, sc1, w1_gscale, s)
+                 : launch_grouped_gemm_fp4(g1, sc1, w1_gscale, s));
   tm.mark(call, 6, s);
   GroupedGemmArgs g2{};
   g2.epi = Epi::kPlain;
@@ -602,8 +606,10 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
   g2.out_rows = R;
   g2.F = p->F;
   g2.status = status;
-  MOE_LAUNCH(pair_tiles ? launch_grouped_gemm_fp4_pair(g2, sc2, w2_gscale, s)
-                        : launch_grouped_gemm_fp4(g2, sc2, w2_gscale, s));
+  MOE_LAUNCH(lt == MOE_KERNEL_WEIGHT_TILES_2CTA ? launch_grouped_gemm_fp4_pair(g2, sc2, w2_gscale, s)
+             : lt == MOE_KERNEL_WEIGHT_TILES_WIDE
+                 ? launch_grouped_gemm_fp4_tmem(g2, sc2, w2_gscale, s)
+                 : launch_grouped_gemm_fp4(g2, sc2, w2_gscale, s));
   tm.mark(call, 7, s);
   MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
   tm.mark(call, 8, s);

@@ -123,6 +123,11 @@ cudaError_t launch_grouped_gemm_fp4(const GroupedGemmArgs& g, const uint8_t* sca
 // expert); needs rows per expert a multiple of 128.
 cudaError_t launch_grouped_gemm_fp4_pair(const GroupedGemmArgs& g, const uint8_t* scales,
                                          const float* gscale, cudaStream_t s);
+// The same GEMMs with 1-CTA weight-row tiles (128 weight rows x N <= 192
+// tokens fitted per expert), the weights expanded into tensor memory; CTA
+// pairs share token rows by multicast.
+cudaError_t launch_grouped_gemm_fp4_tmem(const GroupedGemmArgs& g, const uint8_t* scales,
+                                         const float* gscale, cudaStream_t s);
 // [E][N][K/16] E4M3 scales -> [E][N/128][K/64][128][4]
 cudaError_t launch_prepare_scales(const uint8_t* src, uint8_t* dst, int E, int N, int K,
                                   cudaStream_t s);

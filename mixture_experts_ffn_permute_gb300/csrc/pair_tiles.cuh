@@ -80,8 +80,8 @@ __device__ __forceinline__ Tile decode(int tile, const Sched& s) {
 
 // Fills ntk[E], hot_prefix[E+1], cold_prefix[E+1] (shared memory) from the
 // expert offsets off[E+1] (shared memory); every thread of the block calls it.
-// Expert e owns w_tiles * ceil(rows_e / 256) pair tiles.
-template <int kThreads>
+// Expert e owns w_tiles * ceil(rows_e / kTok) tiles (kTok token rows per tile).
+template <int kThreads, int kTok = kNmax>
 __device__ __forceinline__ Sched build_sched(const int32_t* off, int E, int w_tiles, int32_t* ntk,
                                              int32_t* hp, int32_t* cp) {
   __shared__ int s_part[2][kThreads / 32];
@@ -91,7 +91,7 @@ __device__ __forceinline__ Sched build_sched(const int32_t* off, int E, int w_ti
   int run_h = 0, run_c = 0;
   for (int e = e0; e < e1; ++e) {
     const int rows = off[e + 1] - off[e];
-    const int nt = rows > 0 ? (rows + kNmax - 1) / kNmax : 0;
+    const int nt = rows > 0 ? (rows + kTok - 1) / kTok : 0;
     ntk[e] = nt;
     if (nt > 1) run_h += nt * w_tiles; else run_c += nt * w_tiles;
   }

@@ -24,9 +24,10 @@ def built():
     moe.load()
 
 
-# 1-CTA token-row tiles (the default) and the 2-CTA weight-row tiles
-KERNELS = [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_2CTA]
-KERNEL_IDS = ["token_tiles", "weight_tiles_2cta"]
+# token-row tiles (the default), weight-row tiles with the weights in tensor
+# memory, and 2-CTA weight-row tiles
+KERNELS = [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_WIDE, moe.KERNEL_WEIGHT_TILES_2CTA]
+KERNEL_IDS = ["token_tiles", "weight_tiles_tmem", "weight_tiles_2cta"]
 
 
 def run_lowprec(shape, inp, kernel=moe.KERNEL_AUTO):
