@@ -4,12 +4,18 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "../../include/moe_ffn.h"
 #include "internal.h"
 
 namespace moe {
+
+bool pdl_enabled() {
+  static const bool on = std::getenv("MOE_DISABLE_PDL") == nullptr;
+  return on;
+}
 
 int num_sms() {
   static int cache[64] = {0};

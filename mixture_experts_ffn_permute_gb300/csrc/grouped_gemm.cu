@@ -128,6 +128,7 @@ template <Epi kEpi, bool kGatherA, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, const KParams p) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, kept as a shared-array pointer so that accesses
   // compile to shared-memory instructions
@@ -500,23 +501,11 @@ cudaError_t launch_impl(const CUtensorMap& ma, const CUtensorMap& mb, const KPar
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
   if (err != cudaSuccess) return err;
-  if (!kPair) {
-    kern<<<grid, kThreads, kSmemBytes, s>>>(ma, mb, kp);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, kp);
+  if (!kPair)
+    return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s,
+                         1, ma, mb, kp);
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, 2,
+                       ma, mb, kp);
 }
 
 }  // namespace

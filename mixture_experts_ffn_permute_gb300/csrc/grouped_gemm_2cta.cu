@@ -132,6 +132,7 @@ template <Epi kEpi>
 __global__ void __launch_bounds__(kThreads2, 1)
 grouped_gemm_2cta_kernel(const __grid_constant__ CUtensorMap map_a,
                          const __grid_constant__ CUtensorMap map_b, const P2 p) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;
@@ -395,19 +396,8 @@ cudaError_t launch_2cta_impl(const CUtensorMap& ma, const CUtensorMap& mb, const
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmem2));
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads2, 1, 1);
-  cfg.dynamicSmemBytes = kSmem2;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, pp);
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads2), kSmem2, s, 2,
+                       ma, mb, pp);
 }
 
 }  // namespace

@@ -104,6 +104,7 @@ template <Epi kEpi>
 __global__ void __launch_bounds__(kThreadsF, 1)
 grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_q, const FParams p) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, kept as a shared-array pointer so that accesses
   // compile to shared-memory instructions
@@ -422,14 +423,15 @@ cudaError_t launch_fp4_impl(const CUtensorMap& ma, const CUtensorMap& mq, const 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytesF));
   if (err != cudaSuccess) return err;
-  grouped_gemm_fp4_kernel<kEpi><<<grid, kThreadsF, kSmemBytesF, s>>>(ma, mq, fp);
-  return cudaGetLastError();
+  return launch_kernel(grouped_gemm_fp4_kernel<kEpi>, dim3(static_cast<unsigned>(grid)),
+                       dim3(kThreadsF), kSmemBytesF, s, 1, ma, mq, fp);
 }
 
 // scales [E][N][K/16] -> [E][N/128][K/64][128][4]
 __global__ void __launch_bounds__(256)
 prepare_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int E, int N,
                       int K) {
+  pdl_enter();
   const long groups = static_cast<long>(E) * N * (K / 64);
   const int kblocks = K / 64;
   for (long g = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
@@ -450,6 +452,7 @@ __global__ void __launch_bounds__(256)
 gather_dequant_fp8_kernel(const uint8_t* __restrict__ xq, const float* __restrict__ xs,
                           const int32_t* __restrict__ permuted_token, int R, int H,
                           uint4* __restrict__ x_perm) {
+  pdl_enter();
   const int vecs = H / 8;
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
     const int t = permuted_token[r];
@@ -516,8 +519,7 @@ cudaError_t launch_prepare_scales(const uint8_t* src, uint8_t* dst, int E, int N
   const long groups = static_cast<long>(E) * N * (K / 64);
   if (groups == 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<long>((groups + 255) / 256, num_sms() * 16L));
-  prepare_scales_kernel<<<blocks, 256, 0, s>>>(src, dst, E, N, K);
-  return cudaGetLastError();
+  return launch_kernel(prepare_scales_kernel, dim3(blocks), dim3(256), 0, s, 1, src, dst, E, N, K);
 }
 
 cudaError_t launch_gather_dequant_fp8(const uint8_t* xq, const float* xs,
@@ -525,9 +527,8 @@ cudaError_t launch_gather_dequant_fp8(const uint8_t* xq, const float* xs,
                                       cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   const int blocks = std::min(R, num_sms() * 8);
-  gather_dequant_fp8_kernel<<<blocks, 256, 0, s>>>(xq, xs, permuted_token, R, H,
-                                                   static_cast<uint4*>(x_perm));
-  return cudaGetLastError();
+  return launch_kernel(gather_dequant_fp8_kernel, dim3(blocks), dim3(256), 0, s, 1, xq, xs,
+                       permuted_token, R, H, static_cast<uint4*>(x_perm));
 }
 
 }  // namespace moe

@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreadsQ, 1)
 grouped_gemm_fp4_pair_kernel(const __grid_constant__ CUtensorMap map_q,
                              const __grid_constant__ CUtensorMap map_q128,
                              const __grid_constant__ pair::TokenMaps map_x, const QParams p) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sX = smem;
@@ -520,19 +521,8 @@ cudaError_t launch_fp4_pair_impl(const CUtensorMap& map_q, const CUtensorMap& ma
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemQ));
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreadsQ, 1, 1);
-  cfg.dynamicSmemBytes = kSmemQ;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, map_q, map_q128, map_x, qp);
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsQ), kSmemQ, s, 2,
+                       map_q, map_q128, map_x, qp);
 }
 
 }  // namespace

@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
                          const __grid_constant__ CUtensorMap map_x,
                          const __grid_constant__ CUtensorMap map_xw, const SParams p) {
+  pdl_enter();
   using Cfg = SwapCfg<kNmax, kWStages, kXStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, kept as a shared-array pointer so that accesses
@@ -403,8 +404,8 @@ cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx,
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::kSmem));
   if (err != cudaSuccess) return err;
-  kern<<<grid, kThreadsS, Cfg::kSmem, s>>>(mw, mx, mxw, sp);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsS), Cfg::kSmem, s, 1,
+                       mw, mx, mxw, sp);
 }
 
 }  // namespace

@@ -64,6 +64,7 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
                           const __grid_constant__ CUtensorMap map_x32,
                           const __grid_constant__ CUtensorMap map_x64,
                           const __grid_constant__ CUtensorMap map_x128, const PParams p) {
+  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sW = smem;
@@ -294,19 +295,8 @@ cudaError_t launch_swap2_impl(const CUtensorMap* maps, const PParams& pp, int gr
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemP));
   if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreadsP, 1, 1);
-  cfg.dynamicSmemBytes = kSmemP;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], pp);
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsP), kSmemP, s, 2,
+                       maps[0], maps[1], maps[2], maps[3], maps[4], pp);
 }
 
 }  // namespace

@@ -21,6 +21,39 @@ inline int ceil_div(long a, long b) { return static_cast<int>((a + b - 1) / b); 
 
 int num_sms();
 
+// False when MOE_DISABLE_PDL is set in the environment (for A/B timing).
+bool pdl_enabled();
+
+// cudaLaunchKernelEx with programmatic stream serialization allowed (the
+// kernels wait with griddepcontrol.wait before touching global memory) and an
+// optional cluster of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Step 1: routing.
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize,
                               int32_t* topk_idx, float* topk_w, cudaStream_t s);

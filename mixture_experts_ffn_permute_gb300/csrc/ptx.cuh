@@ -94,6 +94,16 @@ __device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t nthreads, bool 
   return r != 0;
 }
 
+// Programmatic dependent launch.  Every kernel of the layer is launched with
+// programmatic stream serialization allowed, so it may be scheduled while the
+// previous kernel in the stream is still running; it therefore waits for that
+// kernel's completion (and memory) before its first global access, and lets
+// its own dependent launch right away.  Both are no-ops without the attribute.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

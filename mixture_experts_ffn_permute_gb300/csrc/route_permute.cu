@@ -55,6 +55,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  pdl_enter();
   extern __shared__ float s_logits[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* row = s_logits + static_cast<size_t>(warp) * E;
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(256)
 chunk_histogram_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
                        int32_t* __restrict__ chunk_counts, uint32_t* status,
                        int32_t* __restrict__ counters, int ncnt) {
+  pdl_enter();
   extern __shared__ int32_t s_cnt[];
   const int chunk = blockIdx.x;
   const int t0 = chunk * kChunkTokens;
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(1024)
 scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E, int R,
             int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ expert_offsets,
             int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ permuted_token) {
+  pdl_enter();
   __shared__ int s_warp[32];
   const int e = threadIdx.x;
   int count = 0;
@@ -209,6 +212,7 @@ __global__ void __launch_bounds__(32)
 scatter_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
                const int32_t* __restrict__ chunk_base, int32_t* __restrict__ row_id_map,
                int32_t* __restrict__ permuted_token) {
+  pdl_enter();
   extern __shared__ int32_t s_next[];
   const int chunk = blockIdx.x, lane = threadIdx.x;
   const int t0 = chunk * kChunkTokens;
@@ -253,6 +257,7 @@ scatter_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ permuted_token,
                    int R, int vecs_per_row, uint4* __restrict__ x_perm) {
+  pdl_enter();
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
     const int t = permuted_token[r];
     uint4* dst = x_perm + static_cast<size_t>(r) * vecs_per_row;
@@ -271,6 +276,7 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
 __global__ void __launch_bounds__(1024)
 mtile_prefix_kernel(const int32_t* __restrict__ offsets, int E, int R,
                     int32_t* __restrict__ mtile_prefix, uint32_t* status) {
+  pdl_enter();
   __shared__ int s_warp[32];
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
@@ -309,6 +315,7 @@ __global__ void __launch_bounds__(256)
 combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_id_map,
                const float* __restrict__ topk_w, int T, int vecs_per_row, int k,
                uint4* __restrict__ out) {
+  pdl_enter();
   const int t = blockIdx.x;
   const int v = blockIdx.y * blockDim.x + threadIdx.x;
   if (t >= T || v >= vecs_per_row) return;
@@ -341,6 +348,7 @@ permute_small_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
                      int32_t* __restrict__ tokens_per_expert,
                      int32_t* __restrict__ expert_offsets, int32_t* __restrict__ mtile_prefix,
                      int32_t* __restrict__ row_id_map, int32_t* __restrict__ permuted_token) {
+  pdl_enter();
   extern __shared__ int32_t s_small[];
   __shared__ int s_warp[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -407,9 +415,8 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
     if (err != cudaSuccess) return err;
   }
   const int blocks = min(ceil_div(T, kRouteWarps), num_sms() * 8);
-  route_topk_kernel<<<blocks, kRouteWarps * 32, smem, s>>>(logits, T, E, k, renormalize,
-                                                           topk_idx, topk_w);
-  return cudaGetLastError();
+  return launch_kernel(route_topk_kernel, dim3(blocks), dim3(kRouteWarps * 32), smem, s, 1,
+                       logits, T, E, k, renormalize, topk_idx, topk_w);
 }
 
 cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int T, int E, int k,
@@ -417,17 +424,15 @@ cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int T, int E, int k,
                                    int32_t* counters, int ncnt) {
   const int nchunks = ceil_div(T, kChunkTokens);
   if (nchunks == 0) return cudaSuccess;
-  chunk_histogram_kernel<<<nchunks, 256, sizeof(int32_t) * E, s>>>(
-      topk_idx, T, E, k, chunk_counts, status, counters, ncnt);
-  return cudaGetLastError();
+  return launch_kernel(chunk_histogram_kernel, dim3(nchunks), dim3(256), sizeof(int32_t) * E, s,
+                       1, topk_idx, T, E, k, chunk_counts, status, counters, ncnt);
 }
 
 cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int R,
                         int32_t* tokens_per_expert, int32_t* expert_offsets,
                         int32_t* mtile_prefix, int32_t* permuted_token, cudaStream_t s) {
-  scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, R, tokens_per_expert,
-                                 expert_offsets, mtile_prefix, permuted_token);
-  return cudaGetLastError();
+  return launch_kernel(scan_kernel, dim3(1), dim3(1024), 0, s, 1, chunk_counts, nchunks, E, R,
+                       tokens_per_expert, expert_offsets, mtile_prefix, permuted_token);
 }
 
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
@@ -435,9 +440,8 @@ cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
                            int32_t* permuted_token, cudaStream_t s) {
   const int nchunks = ceil_div(T, kChunkTokens);
   if (nchunks == 0) return cudaSuccess;
-  scatter_kernel<<<nchunks, 32, sizeof(int32_t) * E, s>>>(topk_idx, T, E, k, chunk_base,
-                                                          row_id_map, permuted_token);
-  return cudaGetLastError();
+  return launch_kernel(scatter_kernel, dim3(nchunks), dim3(32), sizeof(int32_t) * E, s, 1,
+                       topk_idx, T, E, k, chunk_base, row_id_map, permuted_token);
 }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* permuted_token, int R, int H,
@@ -445,16 +449,16 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* permuted_token, int
   if (R == 0) return cudaSuccess;
   const int vecs = H / 8;
   const int blocks = min(R, num_sms() * 8);
-  gather_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), permuted_token, R,
-                                            vecs, static_cast<uint4*>(x_perm));
-  return cudaGetLastError();
+  return launch_kernel(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, 1,
+                       static_cast<const uint4*>(x), permuted_token, R, vecs,
+                       static_cast<uint4*>(x_perm));
 }
 
 cudaError_t launch_mtile_prefix_from_offsets(const int32_t* expert_offsets, int E, int R,
                                              int32_t* mtile_prefix, uint32_t* status,
                                              cudaStream_t s) {
-  mtile_prefix_kernel<<<1, 1024, 0, s>>>(expert_offsets, E, R, mtile_prefix, status);
-  return cudaGetLastError();
+  return launch_kernel(mtile_prefix_kernel, dim3(1), dim3(1024), 0, s, 1, expert_offsets, E, R,
+                       mtile_prefix, status);
 }
 
 bool permute_small_fits(int T, int E, int k) {
@@ -466,10 +470,9 @@ cudaError_t launch_permute_small(const int32_t* topk_idx, int T, int E, int k,
                                  int32_t* mtile_prefix, int32_t* row_id_map,
                                  int32_t* permuted_token, cudaStream_t s) {
   const size_t smem = sizeof(int32_t) * (static_cast<size_t>(T) * k + E);
-  permute_small_kernel<<<1, 1024, smem, s>>>(topk_idx, T, E, k, tokens_per_expert,
-                                             expert_offsets, mtile_prefix, row_id_map,
-                                             permuted_token);
-  return cudaGetLastError();
+  return launch_kernel(permute_small_kernel, dim3(1), dim3(1024), smem, s, 1, topk_idx, T, E, k,
+                       tokens_per_expert, expert_offsets, mtile_prefix, row_id_map,
+                       permuted_token);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* row_id_map, const float* topk_w,
@@ -477,9 +480,8 @@ cudaError_t launch_combine(const void* y, const int32_t* row_id_map, const float
   if (T == 0) return cudaSuccess;
   const int vecs = H / 8;
   dim3 grid(T, ceil_div(vecs, 256));
-  combine_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(y), row_id_map, topk_w, T,
-                                      vecs, k, static_cast<uint4*>(out));
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, grid, dim3(256), 0, s, 1, static_cast<const uint4*>(y),
+                       row_id_map, topk_w, T, vecs, k, static_cast<uint4*>(out));
 }
 
 }  // namespace moe
