@@ -462,18 +462,29 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
   tm.mark(call, 0, s);
-  MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
-  tm.mark(call, 1, s);
-  if (!fuse_combine && permute_small_fits(p->T, p->E, p->k)) {
-    // decode sizes: histogram + scan + scatter in one block
-    MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
-    for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
+  if (!fuse_combine && route_permute_tiny_fits(p->T, p->E, p->k)) {
+    // the smallest decode steps: routing, permutation and (few rows) the
+    // gather in one block
+    const bool gather_here = !fuse_gather && R <= kTinyGatherRoutes;
+    MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx,
+                                         wts, tpe, off, mtp, rmap, ptok,
+                                         gather_here ? x : nullptr, p->H, x_perm, s));
+    for (int i = 1; i <= 4; ++i) tm.mark(call, i, s);
+    if (!fuse_gather && !gather_here) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   } else {
-    rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2,
-                     fuse_combine ? counters : nullptr, p->H / kBN);
-    if (rc != MOE_OK) return rc;
+    MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
+    tm.mark(call, 1, s);
+    if (!fuse_combine && permute_small_fits(p->T, p->E, p->k)) {
+      // decode sizes: histogram + scan + scatter in one block
+      MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
+      for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
+    } else {
+      rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2,
+                       fuse_combine ? counters : nullptr, p->H / kBN);
+      if (rc != MOE_OK) return rc;
+    }
+    if (!fuse_gather) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   }
-  if (!fuse_gather) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   tm.mark(call, 5, s);
   const FusedIO fused{fuse_gather, fuse_combine, ptok, rmap, wts, counters, out};
   rc = run_mlp(p, fuse_gather ? x : x_perm, off, mtp, w1, w2, h, y, status, s, launches, &tm,
@@ -561,14 +572,21 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
   tm.mark(call, 0, s);
-  MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
-  tm.mark(call, 1, s);
-  if (permute_small_fits(p->T, p->E, p->k)) {
-    MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
-    for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
+  if (route_permute_tiny_fits(p->T, p->E, p->k)) {
+    MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx,
+                                         wts, tpe, off, mtp, rmap, ptok, nullptr, p->H, nullptr,
+                                         s));
+    for (int i = 1; i <= 4; ++i) tm.mark(call, i, s);
   } else {
-    rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2);
-    if (rc != MOE_OK) return rc;
+    MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
+    tm.mark(call, 1, s);
+    if (permute_small_fits(p->T, p->E, p->k)) {
+      MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
+      for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
+    } else {
+      rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2);
+      if (rc != MOE_OK) return rc;
+    }
   }
   MOE_LAUNCH(launch_gather_dequant_fp8(xq, xs, ptok, R, p->H, x_perm, s));
   tm.mark(call, 5, s);

@@ -112,7 +112,6 @@ __global__ void __launch_bounds__(kThreadsS, 1)
 grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
                          const __grid_constant__ CUtensorMap map_x,
                          const __grid_constant__ CUtensorMap map_xw, const SParams p) {
-  pdl_enter();
   using Cfg = SwapCfg<kNmax, kWStages, kXStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, kept as a shared-array pointer so that accesses
@@ -135,7 +134,6 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   float* sD = reinterpret_cast<float*>(s_ntk + (kMaxES + 1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i <= p.E; i += kThreadsS) s_off[i] = p.expert_offsets[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(&w_full[s], 1);
@@ -159,6 +157,10 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
     if (kNmax > kXBox) prefetch_tensormap(&map_xw);
   }
   if (warp == 1) tmem_alloc<Cfg::kTmemCols>(tmem_slot);
+  // Everything above touches only this CTA's shared memory and tensor memory
+  // and the kernel parameters: it overlaps the previous kernel's tail.
+  pdl_enter();
+  for (int i = threadIdx.x; i <= p.E; i += kThreadsS) s_off[i] = p.expert_offsets[i];
   __syncthreads();
   // tile prefix: expert e owns w_tiles * ceil(rows_e / kNmax) tiles.  Thread
   // i scans a run of at most ceil(E / 192) experts; runs are then offset by a

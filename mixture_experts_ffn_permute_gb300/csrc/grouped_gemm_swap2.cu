@@ -64,7 +64,6 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
                           const __grid_constant__ CUtensorMap map_x32,
                           const __grid_constant__ CUtensorMap map_x64,
                           const __grid_constant__ CUtensorMap map_x128, const PParams p) {
-  pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sW = smem;
@@ -85,7 +84,6 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
-  for (int i = threadIdx.x; i <= p.E; i += kThreadsP) s_off[i] = p.expert_offsets[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesP; ++s) {
       mbar_init(&full[s], 1);
@@ -109,6 +107,10 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
   if (warp == 1) {  // one warp of each CTA allocates the pair's columns together
     pair::tmem_alloc2<kTmemColsP>(tmem_slot);
   }
+  // Everything above touches only this CTA's shared memory and tensor memory
+  // and the kernel parameters: it overlaps the previous kernel's tail.
+  pdl_enter();
+  for (int i = threadIdx.x; i <= p.E; i += kThreadsP) s_off[i] = p.expert_offsets[i];
   __syncthreads();
   const pair::Sched sched =
       pair::build_sched<kThreadsP>(s_off, p.E, p.w_tiles, s_ntk, s_hp, s_cp);

@@ -77,6 +77,19 @@ cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int R,
 // outputs as histogram + scan + scatter.
 constexpr int kSmallRoutes = 4096;
 constexpr int kSmallExperts = 1024;
+// The smallest decode steps: routing + permutation (+ the row gather when x is
+// not null) in one single-block launch.
+constexpr int kTinyTokens = 32;     // one routing warp per token
+constexpr int kTinyExperts = 256;   // staged logits: T * E floats of shared memory
+constexpr int kTinyRoutes = 256;
+constexpr int kTinyGatherRoutes = 64;  // rows one block gathers faster than a launch
+bool route_permute_tiny_fits(int T, int E, int k);
+cudaError_t launch_route_permute_tiny(const float* logits, int T, int E, int k, int renormalize,
+                                      int32_t* topk_idx, float* topk_w,
+                                      int32_t* tokens_per_expert, int32_t* expert_offsets,
+                                      int32_t* mtile_prefix, int32_t* row_id_map,
+                                      int32_t* permuted_token, const void* x, int H,
+                                      void* x_perm, cudaStream_t s);
 bool permute_small_fits(int T, int E, int k);
 cudaError_t launch_permute_small(const int32_t* topk_idx, int T, int E, int k,
                                  int32_t* tokens_per_expert, int32_t* expert_offsets,

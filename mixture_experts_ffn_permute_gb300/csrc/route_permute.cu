@@ -50,8 +50,53 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// One warp per token; the token's logits are staged in shared memory and
-// each lane owns experts lane, lane+32, ... (at most 32 of them).
+// Routes one token with one warp: its logits are staged in `row` (shared
+// memory) and each lane owns experts lane, lane+32, ... (at most 32 of them).
+// Writes the k expert ids (ties to the lowest id) and their weights, and the
+// ids to s_idx too when it is given.
+__device__ __forceinline__ void route_token(const float* __restrict__ src, float* row, int E,
+                                            int k, int renormalize, int lane,
+                                            int32_t* __restrict__ idx_out,
+                                            float* __restrict__ w_out, int32_t* s_idx) {
+  const int per_lane = (E + 31) >> 5;
+  for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
+  __syncwarp();
+  uint32_t taken = 0;
+  Cand mine{0.f, INT_MAX};
+  float top = 0.f;
+  for (int j = 0; j < k; ++j) {
+    Cand c{0.f, INT_MAX};
+    for (int i = 0; i < per_lane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken & (1u << i))) {
+        Cand o{row[e], e};
+        if (better(o, c)) c = o;
+      }
+    }
+    c = warp_best(c);
+    if (c.id != INT_MAX && (c.id & 31) == lane) taken |= 1u << (c.id >> 5);
+    if (lane == j) mine = c;
+    if (j == 0) top = c.v;
+  }
+  // weights: exp(l - l_top) normalised over the selected (or all) experts
+  float ex = (lane < k) ? expf(mine.v - top) : 0.f;
+  float denom;
+  if (renormalize) {
+    denom = warp_sum(ex);
+  } else {
+    float part = 0.f;
+    for (int e = lane; e < E; e += 32) part += expf(row[e] - top);
+    denom = warp_sum(part);
+  }
+  if (lane < k) {
+    idx_out[lane] = mine.id;
+    w_out[lane] = ex / denom;
+    if (s_idx) s_idx[lane] = mine.id;
+  }
+  __syncwarp();
+}
+
+// One warp per token.
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
@@ -59,44 +104,10 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int ren
   extern __shared__ float s_logits[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* row = s_logits + static_cast<size_t>(warp) * E;
-  const int per_lane = (E + 31) >> 5;
-  for (int t = blockIdx.x * kRouteWarps + warp; t < T; t += gridDim.x * kRouteWarps) {
-    const float* src = logits + static_cast<size_t>(t) * E;
-    for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
-    __syncwarp();
-    uint32_t taken = 0;
-    Cand mine{0.f, INT_MAX};
-    float top = 0.f;
-    for (int j = 0; j < k; ++j) {
-      Cand c{0.f, INT_MAX};
-      for (int i = 0; i < per_lane; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !(taken & (1u << i))) {
-          Cand o{row[e], e};
-          if (better(o, c)) c = o;
-        }
-      }
-      c = warp_best(c);
-      if (c.id != INT_MAX && (c.id & 31) == lane) taken |= 1u << (c.id >> 5);
-      if (lane == j) mine = c;
-      if (j == 0) top = c.v;
-    }
-    // weights: exp(l - l_top) normalised over the selected (or all) experts
-    float ex = (lane < k) ? expf(mine.v - top) : 0.f;
-    float denom;
-    if (renormalize) {
-      denom = warp_sum(ex);
-    } else {
-      float part = 0.f;
-      for (int e = lane; e < E; e += 32) part += expf(row[e] - top);
-      denom = warp_sum(part);
-    }
-    if (lane < k) {
-      topk_idx[static_cast<size_t>(t) * k + lane] = mine.id;
-      topk_w[static_cast<size_t>(t) * k + lane] = ex / denom;
-    }
-    __syncwarp();
-  }
+  for (int t = blockIdx.x * kRouteWarps + warp; t < T; t += gridDim.x * kRouteWarps)
+    route_token(logits + static_cast<size_t>(t) * E, row, E, k, renormalize, lane,
+                topk_idx + static_cast<size_t>(t) * k, topk_w + static_cast<size_t>(t) * k,
+                nullptr);
 }
 
 // Per-chunk expert histogram (shared-memory counters) plus index validation:
@@ -338,26 +349,21 @@ combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_id_m
   out[static_cast<size_t>(t) * vecs_per_row + v] = o;
 }
 
-// Decode sizes (T*k <= kSmallRoutes, E <= kSmallExperts): expert histogram,
-// scan and the stable scatter in ONE block of 1024 threads after the routing
-// kernel, so a decode step pays one permute launch instead of three.  Same
-// results as chunk_histogram / scan / scatter, bit for bit, for routes that
-// are all valid (moe_forward's own routing).
-__global__ void __launch_bounds__(1024)
-permute_small_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
-                     int32_t* __restrict__ tokens_per_expert,
-                     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ mtile_prefix,
-                     int32_t* __restrict__ row_id_map, int32_t* __restrict__ permuted_token) {
-  pdl_enter();
-  extern __shared__ int32_t s_small[];
-  __shared__ int s_warp[32];
+// Expert histogram, scan and the stable scatter of R = T*k routes in ONE
+// block of 1024 threads: s_idx (shared) holds the routes, s_cnt (shared) E
+// zeroed counters.  Same results as chunk_histogram / scan / scatter, bit for
+// bit, for routes that are all valid (moe_forward's own routing).  s_ptok,
+// when given, receives permuted_token in shared memory too.
+__device__ __forceinline__ void permute_block(const int32_t* s_idx, int32_t* s_cnt, int* s_warp,
+                                              int T, int E, int k,
+                                              int32_t* __restrict__ tokens_per_expert,
+                                              int32_t* __restrict__ expert_offsets,
+                                              int32_t* __restrict__ mtile_prefix,
+                                              int32_t* __restrict__ row_id_map,
+                                              int32_t* __restrict__ permuted_token,
+                                              int32_t* s_ptok) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int R = T * k;
-  int32_t* s_idx = s_small;
-  int32_t* s_cnt = s_small + R;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
-  for (int r = threadIdx.x; r < R; r += blockDim.x) s_idx[r] = __ldg(topk_idx + r);
-  __syncthreads();
   // histogram
   for (int r = threadIdx.x; r < R; r += blockDim.x) atomicAdd(&s_cnt[s_idx[r]], 1);
   __syncthreads();
@@ -397,8 +403,66 @@ permute_small_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
         const int row_id = start + rank;
         row_id_map[r] = row_id;
         permuted_token[row_id] = r / k;
+        if (s_ptok) s_ptok[row_id] = r / k;
       }
     }
+  }
+}
+
+// Decode sizes (T*k <= kSmallRoutes, E <= kSmallExperts): the permutation
+// after the routing kernel in one launch instead of three.
+__global__ void __launch_bounds__(1024)
+permute_small_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
+                     int32_t* __restrict__ tokens_per_expert,
+                     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ mtile_prefix,
+                     int32_t* __restrict__ row_id_map, int32_t* __restrict__ permuted_token) {
+  pdl_enter();
+  extern __shared__ int32_t s_small[];
+  __shared__ int s_warp[32];
+  const int R = T * k;
+  int32_t* s_idx = s_small;
+  int32_t* s_cnt = s_small + R;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) s_idx[r] = __ldg(topk_idx + r);
+  __syncthreads();
+  permute_block(s_idx, s_cnt, s_warp, T, E, k, tokens_per_expert, expert_offsets, mtile_prefix,
+                row_id_map, permuted_token, nullptr);
+}
+
+// The smallest decode steps (T <= kTinyTokens): routing, the permutation and
+// (when x is given) the row gather in ONE block, one warp per token for the
+// routing -- two kernel boundaries fewer than route + permute + gather.  Same
+// arithmetic as route_topk_kernel and permute_small_kernel (shared code).
+__global__ void __launch_bounds__(1024)
+route_permute_tiny_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
+                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                          int32_t* __restrict__ tokens_per_expert,
+                          int32_t* __restrict__ expert_offsets,
+                          int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ row_id_map,
+                          int32_t* __restrict__ permuted_token, const uint4* __restrict__ x,
+                          int vecs_per_row, uint4* __restrict__ x_perm) {
+  pdl_enter();
+  extern __shared__ int32_t s_tiny[];
+  __shared__ int s_warp[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = T * k;
+  int32_t* s_idx = s_tiny;
+  int32_t* s_cnt = s_idx + R;
+  int32_t* s_ptok = s_cnt + E;
+  float* s_rows = reinterpret_cast<float*>(s_ptok + R);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  if (warp < T)
+    route_token(logits + static_cast<size_t>(warp) * E, s_rows + static_cast<size_t>(warp) * E, E,
+                k, renormalize, lane, topk_idx + static_cast<size_t>(warp) * k,
+                topk_w + static_cast<size_t>(warp) * k, s_idx + warp * k);
+  __syncthreads();
+  permute_block(s_idx, s_cnt, s_warp, T, E, k, tokens_per_expert, expert_offsets, mtile_prefix,
+                row_id_map, permuted_token, s_ptok);
+  if (x == nullptr) return;
+  __syncthreads();
+  for (int i = threadIdx.x; i < R * vecs_per_row; i += blockDim.x) {
+    const int r = i / vecs_per_row, v = i - r * vecs_per_row;
+    x_perm[i] = __ldg(x + static_cast<size_t>(s_ptok[r]) * vecs_per_row + v);
   }
 }
 
@@ -473,6 +537,25 @@ cudaError_t launch_permute_small(const int32_t* topk_idx, int T, int E, int k,
   return launch_kernel(permute_small_kernel, dim3(1), dim3(1024), smem, s, 1, topk_idx, T, E, k,
                        tokens_per_expert, expert_offsets, mtile_prefix, row_id_map,
                        permuted_token);
+}
+
+bool route_permute_tiny_fits(int T, int E, int k) {
+  return T > 0 && T <= kTinyTokens && E <= kTinyExperts && T * k <= kTinyRoutes;
+}
+
+cudaError_t launch_route_permute_tiny(const float* logits, int T, int E, int k, int renormalize,
+                                      int32_t* topk_idx, float* topk_w,
+                                      int32_t* tokens_per_expert, int32_t* expert_offsets,
+                                      int32_t* mtile_prefix, int32_t* row_id_map,
+                                      int32_t* permuted_token, const void* x, int H,
+                                      void* x_perm, cudaStream_t s) {
+  const int R = T * k;
+  const size_t smem = sizeof(int32_t) * (2 * static_cast<size_t>(R) + E) +
+                      sizeof(float) * static_cast<size_t>(T) * E;
+  return launch_kernel(route_permute_tiny_kernel, dim3(1), dim3(1024), smem, s, 1, logits, T, E,
+                       k, renormalize, topk_idx, topk_w, tokens_per_expert, expert_offsets,
+                       mtile_prefix, row_id_map, permuted_token, static_cast<const uint4*>(x),
+                       H / 8, static_cast<uint4*>(x_perm));
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* row_id_map, const float* topk_w,

@@ -96,6 +96,30 @@ def test_forward_fusion_variants(shape, fusion):
     assert torch.equal(res["out"].view(torch.int16), again["out"].view(torch.int16))
 
 
+# Around the limits of the single-block routing + permutation (+ gather) used
+# by the smallest decode steps: T <= 32, E <= 256, T*k <= 256, gather in the
+# same block for T*k <= 64.
+TINY_EDGE = [mi.MoEShape("tiny-t1-k1", T=1, H=256, F=256, E=16, k=1),
+             mi.MoEShape("tiny-gather-edge", T=16, H=256, F=256, E=24, k=4),   # 64 routes
+             mi.MoEShape("tiny-t17", T=17, H=256, F=256, E=24, k=4),           # 68 routes
+             mi.MoEShape("tiny-t31", T=31, H=256, F=256, E=32, k=8),
+             mi.MoEShape("tiny-t32", T=32, H=256, F=256, E=40, k=8),           # 256 routes
+             mi.MoEShape("tiny-t33", T=33, H=256, F=256, E=40, k=8),           # other path
+             mi.MoEShape("tiny-e256", T=8, H=256, F=256, E=256, k=8),
+             mi.MoEShape("tiny-e257", T=8, H=256, F=256, E=257, k=8)]          # other path
+
+
+@pytest.mark.parametrize("shape", TINY_EDGE, ids=lambda s: s.name)
+def test_forward_tiny_decode_edges(shape):
+    inp = mi.make_inputs(shape, seed=5)
+    ref = oracle.moe_forward(inp["x"], inp["logits"], inp["w1"], inp["w2"], shape.k)
+    res = run_forward(shape, to_dev(inp))
+    assert_equal(res["topk_idx"], ref["topk_idx"], "topk_idx")
+    assert_equal(res["tokens_per_expert"], ref["tokens_per_expert"], "tokens_per_expert")
+    np.testing.assert_allclose(res["topk_w"].cpu().numpy(), ref["topk_w"], rtol=3e-6, atol=1e-7)
+    assert_bf16_close(res["out"], ref["out"], f"out[{shape.name}]")
+
+
 def test_forward_unnormalised_weights():
     shape = mi.TINY
     inp = mi.make_inputs(shape, seed=2)
