@@ -201,6 +201,25 @@ MOE_API int moe_forward(const moe_problem* p, const void* x, const float* logits
                         float* topk_w_out, int32_t* tokens_per_expert_out, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* The layer with the routing supplied by the caller (steps 2-6): the staged
+ * top-k indices and weights of the MegaMoE page's interface (description,
+ * item 5 of the changes; Usage: INT64 indices with -1 for a masked route and
+ * FP32 routing weights -- int32 indices here).
+ *   x [T, H] bf16, topk_idx [T, k] int32, topk_w [T, k] fp32,
+ *   w1 [E, 2F, H] bf16, w2 [E, H, F] bf16, out [T, H] bf16 out,
+ *   tokens_per_expert_out [E] int32 (optional).
+ * A slot with index -1 is skipped; a token whose slots are all masked gets a
+ * zero row.  An index outside [-1, E), or an expert repeated in a later slot
+ * of the same token, is treated as masked and recorded as
+ * MOE_ERR_DEVICE_INDEX in the workspace status word (moe_get_device_status).
+ * The weights are used as given (no normalisation).  bf16 precision only;
+ * moe_problem.fusion is ignored; moe_problem.kernel picks the GEMM tiling as
+ * for moe_forward. */
+MOE_API int moe_forward_routed(const moe_problem* p, const void* x, const int32_t* topk_idx,
+                               const float* topk_w, const void* w1, const void* w2, void* out,
+                               int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes,
+                               void* stream);
+
 /* Capacity, in int32 entries, of the fixed device scratch that
  * moe_permute_noalloc uses: ceil(T / 64) * E + E + 1 must not exceed it. */
 #define MOE_NOALLOC_SCRATCH_INTS (1 << 18)

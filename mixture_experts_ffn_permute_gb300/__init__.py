@@ -9,6 +9,7 @@ function names mirror the C entry points of ``include/moe_ffn.h``:
     grouped_swiglu_mlp    -> moe_grouped_swiglu_mlp
     unpermute_combine     -> moe_unpermute_combine
     forward               -> moe_forward
+    forward_routed        -> moe_forward_routed
 
 There is no CPU fallback: if the library is missing or a call returns an
 error status, a ``MoEError`` is raised.
@@ -86,6 +87,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_grouped_swiglu_mlp": ([pp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_unpermute_combine": ([pp, vp, vp, vp, vp, vp], ci),
         "moe_forward": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_forward_routed": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_get_device_status": ([vp, vp], ci),
         "moe_clear_device_status": ([vp, vp], ci),
         "moe_last_launch_count": ([], ci),
@@ -212,6 +214,13 @@ def forward(p: Problem, x, logits, w1, w2, out, ws, topk_idx=None, topk_w=None,
     _call("moe_forward", ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(w1), _ptr(w2),
           _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(tokens_per_expert), _ptr(ws),
           ws.numel(), _stream(stream))
+
+
+def forward_routed(p: Problem, x, topk_idx, topk_w, w1, w2, out, ws, tokens_per_expert=None,
+                   stream=None) -> None:
+    """The layer with caller-supplied routing (int32 [T, k], -1 = masked; fp32 [T, k])."""
+    _call("moe_forward_routed", ctypes.byref(p), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w1),
+          _ptr(w2), _ptr(out), _ptr(tokens_per_expert), _ptr(ws), ws.numel(), _stream(stream))
 
 
 PREC_BF16 = 0

@@ -496,6 +496,52 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   return MOE_OK;
 }
 
+int moe_forward_routed(const moe_problem* p, const void* x, const int32_t* topk_idx,
+                       const float* topk_w, const void* w1, const void* w2, void* out,
+                       int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
+  rc = check_ws(p, ws, ws_bytes);
+  if (rc != MOE_OK) return rc;
+  MOE_REQUIRE_PTR(w1);
+  MOE_REQUIRE_PTR(w2);
+  if (tokens_per_expert_out && !aligned16(tokens_per_expert_out)) return MOE_ERR_MISALIGNED;
+  const Layout L = layout_of(*p);
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* tpe = tokens_per_expert_out ? tokens_per_expert_out
+                                       : at<int32_t>(ws, L.tokens_per_expert);
+  if (p->T == 0) {
+    if (tokens_per_expert_out)
+      MOE_LAUNCH(cudaMemsetAsync(tokens_per_expert_out, 0, sizeof(int32_t) * p->E, s));
+    g_launches = launches;
+    return MOE_OK;
+  }
+  MOE_REQUIRE_PTR(x);
+  MOE_REQUIRE_PTR(topk_idx);
+  MOE_REQUIRE_PTR(topk_w);
+  MOE_REQUIRE_PTR(out);
+  const int R = p->T * p->k;
+  int32_t* off = at<int32_t>(ws, L.expert_offsets);
+  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
+  int32_t* rmap = at<int32_t>(ws, L.row_id_map);
+  int32_t* ptok = at<int32_t>(ws, L.permuted_token);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h = at<void>(ws, L.h);
+  void* y = at<void>(ws, L.y);
+  // the validating permutation: masked, out-of-range and repeated routes
+  rc = run_permute(p, topk_idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches);
+  if (rc != MOE_OK) return rc;
+  MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
+  rc = run_mlp(p, x_perm, off, mtp, w1, w2, h, y, status, s, launches);
+  if (rc != MOE_OK) return rc;
+  MOE_LAUNCH(launch_combine(y, rmap, topk_w, p->T, p->H, p->k, out, s));
+  g_launches = launches;
+  return MOE_OK;
+}
+
 size_t moe_prepared_scales_size(const moe_problem* p) {
   if (check_full(p) != MOE_OK) return 0;
   return static_cast<size_t>(p->E) * (2 * static_cast<size_t>(p->F) * p->H / 16 +

@@ -233,6 +233,26 @@ def moe_forward(x, logits, w1, w2, k: int, renormalize: bool = True, interleave:
     return {"out": out, "topk_idx": idx, "topk_w": w, "tokens_per_expert": counts}
 
 
+def moe_forward_routed(x, topk_idx, topk_w, w1, w2, interleave: int = 0, clamp: float = 0.0):
+    """The layer with the routing given (steps 2-6 of the MegaMoE page's
+    Usage: staged top-k indices with -1 for a masked route and FP32 weights),
+    composed from the stage functions above in their order.  Returns out
+    (fp64) and the permutation."""
+    idx = _np(topk_idx, np.int32)
+    if isinstance(w1, (list, tuple)):  # per-expert arrays, None for experts never routed to
+        E = len(w1)
+        F = next(w for w in w1 if w is not None).shape[0] // 2
+    else:
+        E, F = int(w1.shape[0]), int(w1.shape[1]) // 2
+    perm = permute(idx, E)
+    xp = gather_rows(x, perm["permuted_token"])
+    h = gemm1_swiglu(xp, perm["expert_offsets"], w1, F, interleave=interleave, clamp=clamp)
+    H = xp.shape[1]
+    y = gemm2(h, perm["expert_offsets"], w2, H)
+    out = unpermute_combine(y, perm["row_id_map"], topk_w)
+    return {"out": out, **perm}
+
+
 def dense_bruteforce(x, topk_idx, topk_w, w1, w2, interleave: int = 0,
                      clamp: float = 0.0) -> np.ndarray:
     xb = _np(x, np.uint16)

@@ -129,3 +129,17 @@ def test_lowprec_tiling_selection():
     assert moe.selected_kernel(mk(moe.KERNEL_WEIGHT_TILES_WIDE)) == moe.KERNEL_WEIGHT_TILES_WIDE
     for k in (moe.KERNEL_WEIGHT_TILES, moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA):
         assert moe.selected_kernel(mk(k)) == -1
+
+
+def test_forward_routed_validates(lib):
+    p = P()
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    big = 1 << 40
+    f = lib.moe_forward_routed
+    assert f(ctypes.byref(p), a, None, a, a, a, a, None, a, big, None) == 1   # topk_idx
+    assert f(ctypes.byref(p), a, a, None, a, a, a, None, a, big, None) == 1   # topk_w
+    assert f(ctypes.byref(p), a, mis, a, a, a, a, None, a, big, None) == 3
+    assert f(ctypes.byref(p), a, a, a, a, a, a, None, a, moe.workspace_size(p) - 1, None) == 4
+    lp = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, precision=moe.PREC_FP8_NVFP4)
+    assert f(ctypes.byref(lp), a, a, a, a, a, a, None, a, big, None) == 1    # bf16 only

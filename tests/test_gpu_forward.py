@@ -203,3 +203,64 @@ def test_forward_skewed_full_size_sampled(kernel):
 @pytest.mark.parametrize("T", [128, 256])
 def test_forward_decode_full_size_sampled(T):
     sampled_check(mi.DECODE.with_T(T), 16)
+
+
+# ---------------------------------------------------------------- caller-supplied routing
+
+ROUTED_SHAPES = [mi.MoEShape("routed-ragged", T=333, H=512, F=384, E=7, k=3),
+                 mi.MoEShape("routed-many", T=200, H=256, F=256, E=64, k=8, glu_interleave=64)]
+ROUTED_KERNELS = [moe.KERNEL_AUTO, moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES,
+                  moe.KERNEL_WEIGHT_TILES_WIDE, moe.KERNEL_TOKEN_TILES_2CTA,
+                  moe.KERNEL_WEIGHT_TILES_2CTA]
+ROUTED_IDS = ["auto", "token_tiles", "weight_tiles", "weight_tiles_wide", "token_tiles_2cta",
+              "weight_tiles_2cta"]
+
+
+def run_routed(shape, d, idx, w, kernel=0):
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True, shape.glu_interleave,
+                         shape.swiglu_clamp, kernel=kernel)
+    ws = moe.alloc_workspace(p)
+    moe.clear_device_status(ws)
+    out = torch.full((shape.T, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    tpe = torch.empty(shape.E, dtype=torch.int32, device=DEV)
+    moe.forward_routed(p, d["x"], idx.to(DEV), w.to(DEV), d["w1"], d["w2"], out, ws, tpe)
+    return out, tpe, moe.get_device_status(ws)
+
+
+@pytest.mark.parametrize("kernel", ROUTED_KERNELS, ids=ROUTED_IDS)
+@pytest.mark.parametrize("shape", ROUTED_SHAPES, ids=lambda s: s.name)
+def test_forward_routed_matches_oracle(shape, kernel):
+    """Masked slots are skipped, a token with every slot masked gets a zero row,
+    and the weights are used as given."""
+    inp = mi.make_inputs(shape, seed=6)
+    idx = mi.random_topk_idx(shape.T, shape.E, shape.k, seed=6, mask_frac=0.25)
+    idx[3] = -1
+    w = mi.random_weights(shape.T, shape.k, seed=6)
+    ref = oracle.moe_forward_routed(inp["x"], idx, w, inp["w1"], inp["w2"],
+                                    interleave=shape.glu_interleave)
+    out, tpe, st = run_routed(shape, to_dev(inp), idx, w, kernel)
+    assert st == 0, moe.STATUS_NAMES[st]
+    assert_equal(tpe, ref["tokens_per_expert"], "tokens_per_expert")
+    assert_bf16_close(out, ref["out"], f"out[{shape.name}]")
+    assert not out[3].float().abs().sum().item()
+
+
+def test_forward_routed_invalid_indices_are_masked():
+    """An index outside [-1, E) or an expert repeated in a later slot is
+    treated as masked and reported as MOE_ERR_DEVICE_INDEX."""
+    shape = ROUTED_SHAPES[0]
+    inp = mi.make_inputs(shape, seed=7)
+    idx = mi.random_topk_idx(shape.T, shape.E, shape.k, seed=7)
+    w = mi.random_weights(shape.T, shape.k, seed=7)
+    idx[10, 1] = shape.E          # out of range
+    idx[11, 0] = -5               # out of range
+    idx[12, 2] = idx[12, 0]       # repeated: the later slot is dropped
+    clean = idx.clone()
+    clean[10, 1] = -1
+    clean[11, 0] = -1
+    clean[12, 2] = -1
+    ref = oracle.moe_forward_routed(inp["x"], clean, w, inp["w1"], inp["w2"])
+    out, tpe, st = run_routed(shape, to_dev(inp), idx, w)
+    assert moe.STATUS_NAMES[st] == "MOE_ERR_DEVICE_INDEX"
+    assert_equal(tpe, ref["tokens_per_expert"], "tokens_per_expert")
+    assert_bf16_close(out, ref["out"], "out (invalid routes masked)")

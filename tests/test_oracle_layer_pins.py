@@ -137,3 +137,19 @@ def test_unused_experts_may_be_absent():
     w2l = [inp["w2"][e] if e in used else None for e in range(s.E)]
     part = oracle.moe_forward(inp["x"], inp["logits"], w1l, w2l, k=s.k)
     np.testing.assert_array_equal(full["out"], part["out"])
+
+
+def test_routed_composition_matches_bruteforce_with_masks():
+    """The staged oracle (permute -> gather -> GEMM1 -> GEMM2 -> combine) with
+    caller routing that masks slots equals the per-token brute force, and a
+    token with every slot masked gives a zero row."""
+    shape = mi.MoEShape("routed", T=40, H=64, F=96, E=6, k=3)
+    inp = mi.make_inputs(shape, seed=4)
+    idx = mi.random_topk_idx(shape.T, shape.E, shape.k, seed=4, mask_frac=0.3)
+    idx[5] = -1
+    w = mi.random_weights(shape.T, shape.k, seed=4)
+    got = oracle.moe_forward_routed(inp["x"], idx, w, inp["w1"], inp["w2"], interleave=32)
+    ref = oracle.dense_bruteforce(inp["x"], idx, w, inp["w1"], inp["w2"], interleave=32)
+    np.testing.assert_allclose(got["out"], ref, rtol=1e-12, atol=1e-12)
+    assert not got["out"][5].any()
+    assert int(got["tokens_per_expert"].sum()) == int((idx.numpy() >= 0).sum())
