@@ -113,6 +113,13 @@ typedef struct moe_problem {
                                 (MMA-bound)
      The fusion options do not apply to the weight-row tilings. */
   int32_t kernel;
+  /* Shared experts (moe_forward only; 0 elsewhere): S >= 0 experts, stored
+     after the E routed ones in w1/w2 (experts E .. E+S-1, same shapes), that
+     every token uses with weight 1 in addition to its k routed experts.  The
+     routing outputs then have k+S slots per token (the shared ones last, ids
+     E .. E+S-1, weight 1) and tokens_per_expert has E+S entries.  Needs
+     k+S <= MOE_MAX_TOPK and E+S <= MOE_MAX_EXPERTS. */
+  int32_t shared_experts;
 } moe_problem;
 
 #define MOE_FUSE_GATHER_A 1

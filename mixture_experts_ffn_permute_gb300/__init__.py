@@ -55,14 +55,15 @@ class Problem(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("glu_interleave", ctypes.c_int32),
                 ("swiglu_clamp", ctypes.c_float), ("precision", ctypes.c_int32),
-                ("fusion", ctypes.c_int32), ("kernel", ctypes.c_int32)]
+                ("fusion", ctypes.c_int32), ("kernel", ctypes.c_int32),
+                ("shared_experts", ctypes.c_int32)]
 
     @classmethod
     def make(cls, T, H, F, E, k, renormalize=True, glu_interleave=0, swiglu_clamp=0.0,
-             fusion=0, kernel=0, precision=0):
+             fusion=0, kernel=0, precision=0, shared_experts=0):
         return cls(int(T), int(H), int(F), int(E), int(k), int(bool(renormalize)),
                    int(glu_interleave), float(swiglu_clamp), int(precision), int(fusion),
-                   int(kernel))
+                   int(kernel), int(shared_experts))
 
 
 _lib = None

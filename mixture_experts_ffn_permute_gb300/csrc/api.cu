@@ -59,12 +59,23 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 // Byte offsets of every scratch region inside the caller's workspace.
+// The problem after routing: the S shared experts become experts E .. E+S-1
+// that every token selects in slots k .. k+S-1.
+moe_problem expanded(const moe_problem& p) {
+  moe_problem q = p;
+  q.E = p.E + p.shared_experts;
+  q.k = p.k + p.shared_experts;
+  q.shared_experts = 0;
+  return q;
+}
+
 struct Layout {
   size_t status, chunk_counts, tokens_per_expert, expert_offsets, mtile_prefix, topk_idx, topk_w,
       row_id_map, permuted_token, counters, x_perm, h, y, total;
 };
 
-Layout layout_of(const moe_problem& p) {
+Layout layout_of(const moe_problem& p0) {
+  const moe_problem p = expanded(p0);
   const size_t T = p.T, E = p.E, R = static_cast<size_t>(p.T) * p.k;
   const size_t nchunks = (T + kChunkTokens - 1) / kChunkTokens;
   Layout L;
@@ -101,10 +112,13 @@ bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u
 int check_routing(const moe_problem* p) {
   if (!p) return MOE_ERR_INVALID_ARG;
   if (p->T < 0 || p->E < 1 || p->k < 1 || p->k > p->E) return MOE_ERR_INVALID_ARG;
-  if (p->E > MOE_MAX_EXPERTS || p->k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (static_cast<long long>(p->T) * p->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (p->shared_experts < 0) return MOE_ERR_INVALID_ARG;
+  const int S = p->shared_experts;
+  if (p->E + S > MOE_MAX_EXPERTS || p->k + S > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(p->T) * (p->k + S) > (1LL << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
+
 
 int check_full(const moe_problem* p) {
   int rc = check_routing(p);
@@ -325,6 +339,7 @@ int moe_route_topk(const moe_problem* p, const float* logits, int32_t* topk_idx,
   (void)ws_bytes;
   int rc = check_routing(p);
   if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
   if (p->T == 0) { g_launches = 0; return MOE_OK; }
   MOE_REQUIRE_PTR(logits);
   MOE_REQUIRE_PTR(topk_idx);
@@ -342,6 +357,7 @@ int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, vo
                 int32_t* expert_offsets, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_routing(p);
   if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
   if (x_perm) {
     if (p->H <= 0 || p->H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     MOE_REQUIRE_PTR(x);
@@ -376,6 +392,7 @@ int moe_grouped_swiglu_mlp(const moe_problem* p, const void* x_perm,
                            void* y_perm, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_full(p);
   if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
   if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
   rc = check_ws(p, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
@@ -402,6 +419,7 @@ int moe_unpermute_combine(const moe_problem* p, const void* y_perm, const int32_
                           const float* topk_w, void* out, void* stream) {
   int rc = check_routing(p);
   if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
   if (p->H <= 0 || p->H % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (p->T == 0) { g_launches = 0; return MOE_OK; }
   MOE_REQUIRE_PTR(y_perm);
@@ -429,20 +447,23 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   if (topk_w_out && !aligned16(topk_w_out)) return MOE_ERR_MISALIGNED;
   if (tokens_per_expert_out && !aligned16(tokens_per_expert_out)) return MOE_ERR_MISALIGNED;
   const Layout L = layout_of(*p);
+  const moe_problem pe = expanded(*p);  // after routing: E+S experts, k+S slots
+  const moe_problem* q = &pe;
+  const int S = p->shared_experts;
   int launches = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* tpe = tokens_per_expert_out ? tokens_per_expert_out
                                        : at<int32_t>(ws, L.tokens_per_expert);
   if (p->T == 0) {
     if (tokens_per_expert_out)
-      MOE_LAUNCH(cudaMemsetAsync(tokens_per_expert_out, 0, sizeof(int32_t) * p->E, s));
+      MOE_LAUNCH(cudaMemsetAsync(tokens_per_expert_out, 0, sizeof(int32_t) * q->E, s));
     g_launches = launches;
     return MOE_OK;
   }
   MOE_REQUIRE_PTR(x);
   MOE_REQUIRE_PTR(logits);
   MOE_REQUIRE_PTR(out);
-  const int R = p->T * p->k;
+  const int R = q->T * q->k;
   int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.topk_idx);
   float* wts = topk_w_out ? topk_w_out : at<float>(ws, L.topk_w);
   int32_t* off = at<int32_t>(ws, L.expert_offsets);
@@ -454,32 +475,33 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   void* h = at<void>(ws, L.h);
   void* y = at<void>(ws, L.y);
   int32_t* counters = at<int32_t>(ws, L.counters);
-  const bool plain_tiles = use_weight_tiles(p) || gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_2CTA ||
-                           gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES_2CTA;
+  const bool plain_tiles = use_weight_tiles(q) || gemm_tiling(q) == MOE_KERNEL_TOKEN_TILES_2CTA ||
+                           gemm_tiling(q) == MOE_KERNEL_WEIGHT_TILES_2CTA;
   const bool fuse_gather = !plain_tiles && (p->fusion & MOE_FUSE_GATHER_A) != 0;
   const bool fuse_combine = !plain_tiles && (p->fusion & MOE_FUSE_COMBINE) != 0;
 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
   tm.mark(call, 0, s);
-  if (!fuse_combine && route_permute_tiny_fits(p->T, p->E, p->k)) {
+  if (!fuse_combine && route_permute_tiny_fits(p->T, p->E, p->k, S)) {
     // the smallest decode steps: routing, permutation and (few rows) the
     // gather in one block
     const bool gather_here = !fuse_gather && R <= kTinyGatherRoutes;
-    MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx,
+    MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, S, p->renormalize ? 1 : 0, idx,
                                          wts, tpe, off, mtp, rmap, ptok,
                                          gather_here ? x : nullptr, p->H, x_perm, s));
     for (int i = 1; i <= 4; ++i) tm.mark(call, i, s);
     if (!fuse_gather && !gather_here) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   } else {
-    MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
+    MOE_LAUNCH(
+        launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s, S));
     tm.mark(call, 1, s);
-    if (!fuse_combine && permute_small_fits(p->T, p->E, p->k)) {
+    if (!fuse_combine && permute_small_fits(q->T, q->E, q->k)) {
       // decode sizes: histogram + scan + scatter in one block
-      MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
+      MOE_LAUNCH(launch_permute_small(idx, q->T, q->E, q->k, tpe, off, mtp, rmap, ptok, s));
       for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
     } else {
-      rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2,
+      rc = run_permute(q, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2,
                        fuse_combine ? counters : nullptr, p->H / kBN);
       if (rc != MOE_OK) return rc;
     }
@@ -487,10 +509,10 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   }
   tm.mark(call, 5, s);
   const FusedIO fused{fuse_gather, fuse_combine, ptok, rmap, wts, counters, out};
-  rc = run_mlp(p, fuse_gather ? x : x_perm, off, mtp, w1, w2, h, y, status, s, launches, &tm,
+  rc = run_mlp(q, fuse_gather ? x : x_perm, off, mtp, w1, w2, h, y, status, s, launches, &tm,
                call, 6, &fused);
   if (rc != MOE_OK) return rc;
-  if (!fuse_combine) MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
+  if (!fuse_combine) MOE_LAUNCH(launch_combine(y, rmap, wts, q->T, q->H, q->k, out, s));
   tm.mark(call, 8, s);
   g_launches = launches;
   return MOE_OK;
@@ -501,6 +523,7 @@ int moe_forward_routed(const moe_problem* p, const void* x, const int32_t* topk_
                        int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_full(p);
   if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
   if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
   rc = check_ws(p, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
@@ -552,6 +575,7 @@ int moe_prepare_weights(const moe_problem* p, const uint8_t* w1_scale, const uin
                         void* prepared, size_t prepared_bytes, void* stream) {
   int rc = check_full(p);
   if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
   if (p->precision != MOE_PREC_FP8_NVFP4) return MOE_ERR_INVALID_ARG;
   MOE_REQUIRE_PTR(w1_scale);
   MOE_REQUIRE_PTR(w2_scale);
@@ -575,6 +599,7 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
                           void* stream) {
   int rc = check_full(p);
   if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
   if (p->precision != MOE_PREC_FP8_NVFP4) return MOE_ERR_INVALID_ARG;
   rc = check_ws(p, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
@@ -618,8 +643,8 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
   tm.mark(call, 0, s);
-  if (route_permute_tiny_fits(p->T, p->E, p->k)) {
-    MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx,
+  if (route_permute_tiny_fits(p->T, p->E, p->k, 0)) {
+    MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, 0, p->renormalize ? 1 : 0, idx,
                                          wts, tpe, off, mtp, rmap, ptok, nullptr, p->H, nullptr,
                                          s));
     for (int i = 1; i <= 4; ++i) tm.mark(call, i, s);
@@ -711,7 +736,8 @@ int moe_last_launch_count(void) { return g_launches; }
 int moe_selected_kernel(const moe_problem* p) {
   if (check_full(p) != MOE_OK) return -1;
   if (p->precision == MOE_PREC_FP8_NVFP4) return lowprec_tiling(p);
-  return gemm_tiling(p);
+  const moe_problem q = expanded(*p);
+  return gemm_tiling(&q);
 }
 
 int moe_stage_timing_begin(int n_calls) {

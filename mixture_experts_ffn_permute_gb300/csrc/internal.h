@@ -56,7 +56,7 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 
 // Step 1: routing.
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize,
-                              int32_t* topk_idx, float* topk_w, cudaStream_t s);
+                              int32_t* topk_idx, float* topk_w, cudaStream_t s, int S = 0);
 
 // Step 2a: per-chunk expert histogram of topk_idx (also validates indices).
 // When `counters` is not NULL the kernel also zeroes counters[t * ncnt ..
@@ -83,8 +83,9 @@ constexpr int kTinyTokens = 32;     // one routing warp per token
 constexpr int kTinyExperts = 256;   // staged logits: T * E floats of shared memory
 constexpr int kTinyRoutes = 256;
 constexpr int kTinyGatherRoutes = 64;  // rows one block gathers faster than a launch
-bool route_permute_tiny_fits(int T, int E, int k);
-cudaError_t launch_route_permute_tiny(const float* logits, int T, int E, int k, int renormalize,
+bool route_permute_tiny_fits(int T, int E, int k, int S);
+cudaError_t launch_route_permute_tiny(const float* logits, int T, int E, int k, int S,
+                                      int renormalize,
                                       int32_t* topk_idx, float* topk_w,
                                       int32_t* tokens_per_expert, int32_t* expert_offsets,
                                       int32_t* mtile_prefix, int32_t* row_id_map,

@@ -50,6 +50,7 @@ extern "C" int moe_permute_noalloc(const moe_problem* p, const int32_t* topk_idx
   using namespace moe;
   if (!p) return MOE_ERR_INVALID_ARG;
   if (p->T < 0 || p->E < 1 || p->k < 1 || p->k > p->E) return MOE_ERR_INVALID_ARG;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
   if (p->E > MOE_MAX_EXPERTS || p->k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<long long>(p->T) * p->k > (1LL << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long nchunks = (static_cast<long long>(p->T) + kChunkTokens - 1) / kChunkTokens;

@@ -52,10 +52,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Routes one token with one warp: its logits are staged in `row` (shared
 // memory) and each lane owns experts lane, lane+32, ... (at most 32 of them).
-// Writes the k expert ids (ties to the lowest id) and their weights, and the
-// ids to s_idx too when it is given.
+// Writes the k expert ids (ties to the lowest id) and their weights, then the
+// S shared experts (ids E .. E+S-1, weight 1), and the ids to s_idx too when
+// it is given.
 __device__ __forceinline__ void route_token(const float* __restrict__ src, float* row, int E,
-                                            int k, int renormalize, int lane,
+                                            int k, int S, int renormalize, int lane,
                                             int32_t* __restrict__ idx_out,
                                             float* __restrict__ w_out, int32_t* s_idx) {
   const int per_lane = (E + 31) >> 5;
@@ -93,20 +94,26 @@ __device__ __forceinline__ void route_token(const float* __restrict__ src, float
     w_out[lane] = ex / denom;
     if (s_idx) s_idx[lane] = mine.id;
   }
+  if (lane < S) {
+    idx_out[k + lane] = E + lane;
+    w_out[k + lane] = 1.0f;
+    if (s_idx) s_idx[k + lane] = E + lane;
+  }
   __syncwarp();
 }
 
 // One warp per token.
 __global__ void __launch_bounds__(kRouteWarps * 32)
-route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
+route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int S, int renormalize,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   pdl_enter();
   extern __shared__ float s_logits[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* row = s_logits + static_cast<size_t>(warp) * E;
+  const int slots = k + S;
   for (int t = blockIdx.x * kRouteWarps + warp; t < T; t += gridDim.x * kRouteWarps)
-    route_token(logits + static_cast<size_t>(t) * E, row, E, k, renormalize, lane,
-                topk_idx + static_cast<size_t>(t) * k, topk_w + static_cast<size_t>(t) * k,
+    route_token(logits + static_cast<size_t>(t) * E, row, E, k, S, renormalize, lane,
+                topk_idx + static_cast<size_t>(t) * slots, topk_w + static_cast<size_t>(t) * slots,
                 nullptr);
 }
 
@@ -434,9 +441,9 @@ permute_small_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
 // routing -- two kernel boundaries fewer than route + permute + gather.  Same
 // arithmetic as route_topk_kernel and permute_small_kernel (shared code).
 __global__ void __launch_bounds__(1024)
-route_permute_tiny_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
-                          int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                          int32_t* __restrict__ tokens_per_expert,
+route_permute_tiny_kernel(const float* __restrict__ logits, int T, int E, int k, int S,
+                          int renormalize, int32_t* __restrict__ topk_idx,
+                          float* __restrict__ topk_w, int32_t* __restrict__ tokens_per_expert,
                           int32_t* __restrict__ expert_offsets,
                           int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ row_id_map,
                           int32_t* __restrict__ permuted_token, const uint4* __restrict__ x,
@@ -445,19 +452,20 @@ route_permute_tiny_kernel(const float* __restrict__ logits, int T, int E, int k,
   extern __shared__ int32_t s_tiny[];
   __shared__ int s_warp[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int R = T * k;
+  const int slots = k + S, experts = E + S;  // routed + shared
+  const int R = T * slots;
   int32_t* s_idx = s_tiny;
   int32_t* s_cnt = s_idx + R;
-  int32_t* s_ptok = s_cnt + E;
+  int32_t* s_ptok = s_cnt + experts;
   float* s_rows = reinterpret_cast<float*>(s_ptok + R);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  for (int e = threadIdx.x; e < experts; e += blockDim.x) s_cnt[e] = 0;
   if (warp < T)
     route_token(logits + static_cast<size_t>(warp) * E, s_rows + static_cast<size_t>(warp) * E, E,
-                k, renormalize, lane, topk_idx + static_cast<size_t>(warp) * k,
-                topk_w + static_cast<size_t>(warp) * k, s_idx + warp * k);
+                k, S, renormalize, lane, topk_idx + static_cast<size_t>(warp) * slots,
+                topk_w + static_cast<size_t>(warp) * slots, s_idx + warp * slots);
   __syncthreads();
-  permute_block(s_idx, s_cnt, s_warp, T, E, k, tokens_per_expert, expert_offsets, mtile_prefix,
-                row_id_map, permuted_token, s_ptok);
+  permute_block(s_idx, s_cnt, s_warp, T, experts, slots, tokens_per_expert, expert_offsets,
+                mtile_prefix, row_id_map, permuted_token, s_ptok);
   if (x == nullptr) return;
   __syncthreads();
   for (int i = threadIdx.x; i < R * vecs_per_row; i += blockDim.x) {
@@ -469,7 +477,7 @@ route_permute_tiny_kernel(const float* __restrict__ logits, int T, int E, int k,
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int renormalize,
-                              int32_t* topk_idx, float* topk_w, cudaStream_t s) {
+                              int32_t* topk_idx, float* topk_w, cudaStream_t s, int S) {
   if (T == 0) return cudaSuccess;
   const size_t smem = sizeof(float) * kRouteWarps * E;
   if (smem > 48 * 1024) {
@@ -480,7 +488,7 @@ cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int reno
   }
   const int blocks = min(ceil_div(T, kRouteWarps), num_sms() * 8);
   return launch_kernel(route_topk_kernel, dim3(blocks), dim3(kRouteWarps * 32), smem, s, 1,
-                       logits, T, E, k, renormalize, topk_idx, topk_w);
+                       logits, T, E, k, S, renormalize, topk_idx, topk_w);
 }
 
 cudaError_t launch_chunk_histogram(const int32_t* topk_idx, int T, int E, int k,
@@ -539,21 +547,21 @@ cudaError_t launch_permute_small(const int32_t* topk_idx, int T, int E, int k,
                        permuted_token);
 }
 
-bool route_permute_tiny_fits(int T, int E, int k) {
-  return T > 0 && T <= kTinyTokens && E <= kTinyExperts && T * k <= kTinyRoutes;
+bool route_permute_tiny_fits(int T, int E, int k, int S) {
+  return T > 0 && T <= kTinyTokens && E + S <= kTinyExperts && T * (k + S) <= kTinyRoutes;
 }
 
-cudaError_t launch_route_permute_tiny(const float* logits, int T, int E, int k, int renormalize,
-                                      int32_t* topk_idx, float* topk_w,
+cudaError_t launch_route_permute_tiny(const float* logits, int T, int E, int k, int S,
+                                      int renormalize, int32_t* topk_idx, float* topk_w,
                                       int32_t* tokens_per_expert, int32_t* expert_offsets,
                                       int32_t* mtile_prefix, int32_t* row_id_map,
                                       int32_t* permuted_token, const void* x, int H,
                                       void* x_perm, cudaStream_t s) {
-  const int R = T * k;
-  const size_t smem = sizeof(int32_t) * (2 * static_cast<size_t>(R) + E) +
+  const int R = T * (k + S);
+  const size_t smem = sizeof(int32_t) * (2 * static_cast<size_t>(R) + E + S) +
                       sizeof(float) * static_cast<size_t>(T) * E;
   return launch_kernel(route_permute_tiny_kernel, dim3(1), dim3(1024), smem, s, 1, logits, T, E,
-                       k, renormalize, topk_idx, topk_w, tokens_per_expert, expert_offsets,
+                       k, S, renormalize, topk_idx, topk_w, tokens_per_expert, expert_offsets,
                        mtile_prefix, row_id_map, permuted_token, static_cast<const uint4*>(x),
                        H / 8, static_cast<uint4*>(x_perm));
 }

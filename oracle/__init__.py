@@ -253,6 +253,21 @@ def moe_forward_routed(x, topk_idx, topk_w, w1, w2, interleave: int = 0, clamp: 
     return {"out": out, **perm}
 
 
+def moe_forward_shared(x, logits, w1, w2, k: int, S: int, renormalize: bool = True,
+                       interleave: int = 0, clamp: float = 0.0):
+    """The layer with S shared experts: the last S experts of w1/w2, used by
+    every token with weight 1 after its k routed slots (this build's reading
+    of "Fuse shared expert MLP with grouped GEMM", a commit title in the
+    Megatron-LM change log on the pages; no formula is given there).  The
+    routing over the first E = logits.shape[1] experts is route_topk's."""
+    idx, w = route_topk(logits, k, renormalize)
+    T, E = idx.shape[0], _np(logits, np.float32).shape[1]
+    idx_all = np.concatenate([idx, np.tile(np.arange(E, E + S, dtype=np.int32), (T, 1))], axis=1)
+    w_all = np.concatenate([w, np.ones((T, S), np.float64)], axis=1)
+    res = moe_forward_routed(x, idx_all, w_all, w1, w2, interleave=interleave, clamp=clamp)
+    return {**res, "topk_idx": idx_all, "topk_w": w_all}
+
+
 def dense_bruteforce(x, topk_idx, topk_w, w1, w2, interleave: int = 0,
                      clamp: float = 0.0) -> np.ndarray:
     xb = _np(x, np.uint16)

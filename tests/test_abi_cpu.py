@@ -143,3 +143,21 @@ def test_forward_routed_validates(lib):
     assert f(ctypes.byref(p), a, a, a, a, a, a, None, a, moe.workspace_size(p) - 1, None) == 4
     lp = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, precision=moe.PREC_FP8_NVFP4)
     assert f(ctypes.byref(lp), a, a, a, a, a, a, None, a, big, None) == 1    # bf16 only
+
+
+def test_shared_experts_validation_and_workspace():
+    """Shared experts: moe_forward only; k+S and E+S within the limits; the
+    workspace grows with the k+S slots."""
+    lib = moe.load()
+    a = ctypes.c_void_p(1 << 20)
+    big = 1 << 40
+    p0 = moe.Problem.make(T=64, H=256, F=512, E=8, k=2)
+    p1 = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, shared_experts=1)
+    assert moe.workspace_size(p1) > moe.workspace_size(p0)
+    assert lib.moe_route_topk(ctypes.byref(p1), a, a, a, a, big, None) == 1
+    assert lib.moe_forward_routed(ctypes.byref(p1), a, a, a, a, a, a, None, a, big, None) == 1
+    bad = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, shared_experts=-1)
+    assert moe.workspace_size(bad) == 0
+    too_many = moe.Problem.make(T=64, H=256, F=512, E=8, k=8, shared_experts=25)
+    assert lib.moe_forward(ctypes.byref(too_many), a, a, a, a, a, None, None, None, a, big,
+                           None) == 2

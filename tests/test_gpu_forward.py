@@ -264,3 +264,40 @@ def test_forward_routed_invalid_indices_are_masked():
     assert moe.STATUS_NAMES[st] == "MOE_ERR_DEVICE_INDEX"
     assert_equal(tpe, ref["tokens_per_expert"], "tokens_per_expert")
     assert_bf16_close(out, ref["out"], "out (invalid routes masked)")
+
+
+# ---------------------------------------------------------------- shared experts
+
+SHARED_CASES = [(mi.MoEShape("shared-tiny-path", T=4, H=256, F=256, E=16, k=4), 2),
+                (mi.MoEShape("shared-small-permute", T=100, H=256, F=256, E=16, k=2), 1),
+                (mi.MoEShape("shared-multikernel", T=700, H=512, F=256, E=12, k=6), 2)]
+
+
+@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_TOKEN_TILES,
+                                    moe.KERNEL_WEIGHT_TILES_2CTA],
+                         ids=["auto", "token_tiles", "weight_tiles_2cta"])
+@pytest.mark.parametrize("case", SHARED_CASES, ids=lambda c: c[0].name)
+def test_forward_shared_experts(case, kernel):
+    """S shared experts (the last S of w1/w2) join every token with weight 1."""
+    shape, S = case
+    full = mi.MoEShape(shape.name, T=shape.T, H=shape.H, F=shape.F, E=shape.E + S, k=shape.k)
+    inp = mi.make_inputs(full, seed=8)
+    logits = mi.make_logits(shape, seed=8)
+    ref = oracle.moe_forward_shared(inp["x"], logits, inp["w1"], inp["w2"], shape.k, S)
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, kernel=kernel,
+                         shared_experts=S)
+    ws = moe.alloc_workspace(p)
+    moe.clear_device_status(ws)
+    slots = shape.k + S
+    out = torch.full((shape.T, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty(shape.T, slots, dtype=torch.int32, device=DEV)
+    w = torch.empty(shape.T, slots, dtype=torch.float32, device=DEV)
+    tpe = torch.empty(shape.E + S, dtype=torch.int32, device=DEV)
+    d = to_dev(inp)
+    moe.forward(p, d["x"], logits.to(DEV), d["w1"], d["w2"], out, ws, idx, w, tpe)
+    st = moe.get_device_status(ws)
+    assert st == 0, moe.STATUS_NAMES[st]
+    assert_equal(idx, ref["topk_idx"], "topk_idx (routed + shared slots)")
+    assert_equal(tpe, ref["tokens_per_expert"], "tokens_per_expert")
+    np.testing.assert_allclose(w.cpu().numpy(), ref["topk_w"], rtol=3e-6, atol=1e-7)
+    assert_bf16_close(out, ref["out"], f"out[{shape.name}, S={S}]")

@@ -153,3 +153,22 @@ def test_routed_composition_matches_bruteforce_with_masks():
     np.testing.assert_allclose(got["out"], ref, rtol=1e-12, atol=1e-12)
     assert not got["out"][5].any()
     assert int(got["tokens_per_expert"].sum()) == int((idx.numpy() >= 0).sum())
+
+
+def test_shared_experts_add_their_dense_mlp():
+    """With S shared experts the output is the routed layer's plus, for every
+    token, each shared expert's textbook SwiGLU MLP (numpy matmul) with weight
+    1; the routed slots are the plain routing's."""
+    E, S, k = 6, 2, 2
+    shape = mi.MoEShape("shared", T=30, H=64, F=96, E=E + S, k=k)
+    inp = mi.make_inputs(shape, seed=9)
+    logits = mi.make_logits(mi.MoEShape("routed-part", T=30, H=64, F=96, E=E, k=k), seed=9)
+    res = oracle.moe_forward_shared(inp["x"], logits, inp["w1"], inp["w2"], k, S)
+    base = oracle.moe_forward(inp["x"], logits, inp["w1"][:E], inp["w2"][:E], k)
+    x = _f64(inp["x"])
+    want = sum(dense_mlp(x, _f64(inp["w1"][E + s]), _f64(inp["w2"][E + s]), shape.F)
+               for s in range(S))
+    np.testing.assert_allclose(res["out"] - base["out"], want, rtol=1e-9, atol=1e-12)
+    assert (res["topk_idx"][:, :k] == base["topk_idx"]).all()
+    assert (res["topk_idx"][:, k:] == np.arange(E, E + S)).all()
+    assert (res["tokens_per_expert"][E:] == shape.T).all()
