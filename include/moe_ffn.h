@@ -227,6 +227,16 @@ MOE_API int moe_forward_routed(const moe_problem* p, const void* x, const int32_
                                int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes,
                                void* stream);
 
+/* Self-test of the bounded waits (the pages have no counterpart: this checks
+ * the library's own failure detection).  Launches one CTA that waits on an
+ * mbarrier nothing arrives on, through the same bounded wait every kernel
+ * uses, with a limit of limit_ns nanoseconds (1 .. 2e9); the wait runs out,
+ * MOE_ERR_DEVICE_TIMEOUT is recorded in the status word of `ws` (a workspace
+ * from moe_workspace_size; read it with moe_get_device_status) and the kernel
+ * returns normally, leaving the context usable.  Asynchronous on `stream`.
+ * Returns MOE_ERR_INVALID_ARG for a null ws or a limit out of range. */
+MOE_API int moe_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
+
 /* Capacity, in int32 entries, of the fixed device scratch that
  * moe_permute_noalloc uses: ceil(T / 64) * E + E + 1 must not exceed it. */
 #define MOE_NOALLOC_SCRATCH_INTS (1 << 18)

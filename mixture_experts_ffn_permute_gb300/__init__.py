@@ -89,6 +89,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_unpermute_combine": ([pp, vp, vp, vp, vp, vp], ci),
         "moe_forward": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_forward_routed": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_selftest_wait_timeout": ([vp, ctypes.c_uint64, vp], ci),
         "moe_get_device_status": ([vp, vp], ci),
         "moe_clear_device_status": ([vp, vp], ci),
         "moe_last_launch_count": ([], ci),
@@ -222,6 +223,12 @@ def forward_routed(p: Problem, x, topk_idx, topk_w, w1, w2, out, ws, tokens_per_
     """The layer with caller-supplied routing (int32 [T, k], -1 = masked; fp32 [T, k])."""
     _call("moe_forward_routed", ctypes.byref(p), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w1),
           _ptr(w2), _ptr(out), _ptr(tokens_per_expert), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def selftest_wait_timeout(ws, limit_ns: int, stream=None) -> None:
+    """Run the bounded-wait self-test: a wait that runs out after limit_ns and
+    records MOE_ERR_DEVICE_TIMEOUT in ws's status word."""
+    _call("moe_selftest_wait_timeout", _ptr(ws), int(limit_ns), _stream(stream))
 
 
 PREC_BF16 = 0

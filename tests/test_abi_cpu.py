@@ -161,3 +161,11 @@ def test_shared_experts_validation_and_workspace():
     too_many = moe.Problem.make(T=64, H=256, F=512, E=8, k=8, shared_experts=25)
     assert lib.moe_forward(ctypes.byref(too_many), a, a, a, a, a, None, None, None, a, big,
                            None) == 2
+
+
+def test_selftest_wait_timeout_validates(lib):
+    a = ctypes.c_void_p(1 << 20)
+    f = lib.moe_selftest_wait_timeout
+    assert f(None, 1000, None) == 1
+    assert f(a, 0, None) == 1
+    assert f(a, 3 * 10**9, None) == 1   # above the library's own 2 s wait limit
