@@ -212,23 +212,53 @@ def quantize_nvfp4(w: torch.Tensor):
     return packed, s8.view(torch.uint8).contiguous(), g.float().reshape(())
 
 
+def quantize_mxfp4(w: torch.Tensor):
+    """w [N, K] float -> (packed uint8 [N, K/2], E8M0 scale bytes uint8 [N, K/32]).
+
+    Per 32 values (the OCP microscaling recipe): shared exponent
+    s = floor(log2(amax)) - 2 (2 = the largest E2M1 exponent), scale byte
+    s + 127 (0 for an all-zero block); q = E2M1(w / 2^s) round-to-nearest-even,
+    saturating at 6.  Two codes per byte, the even index in the low nibble."""
+    N, K = w.shape
+    blocks = w.float().reshape(N, K // 32, 32)
+    amax = blocks.abs().amax(-1)
+    exp = torch.floor(torch.log2(torch.where(amax > 0, amax, torch.ones_like(amax)))) - 2
+    exp = torch.where(amax > 0, exp.clamp_(-127, 127), torch.full_like(exp, -127))
+    ratio = blocks / torch.exp2(exp)[..., None]
+    code = _e2m1_code(ratio.abs()) | (ratio < 0).to(torch.uint8) << 3
+    code = code.reshape(N, K)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).contiguous()
+    return packed, (exp + 127).to(torch.uint8).contiguous()
+
+
 def make_lowprec_inputs(shape: MoEShape, seed: int = 0, device="cpu",
-                        weights: bool = True) -> Dict[str, Optional[torch.Tensor]]:
-    """FP8 activations (+ fp32 scales), fp32 logits and NVFP4 weights."""
+                        weights: bool = True, wfmt: str = "nvfp4"
+                        ) -> Dict[str, Optional[torch.Tensor]]:
+    """FP8 activations (+ fp32 scales), fp32 logits and FP4 weights: NVFP4
+    (codes w?q, E4M3 scales per 16 w?s, fp32 expert scales w?g) or, with
+    wfmt="mxfp4", MXFP4 (codes w?q, E8M0 scales per 32 w?s) from the same
+    normal draws."""
     g = _gen(seed + 1, device)
     x = torch.randn(shape.T, shape.H, generator=g, device=device, dtype=torch.float32)
     xq, xs = quantize_fp8_rows(x)
     out = {"logits": make_logits(shape, seed, device), "xq": xq, "xs": xs}
     if weights:
+        blk = 32 if wfmt == "mxfp4" else 16
         for name, rows, cols, sd in (("w1", 2 * shape.F, shape.H, seed + 2),
                                      ("w2", shape.H, shape.F, seed + 3)):
             gw = _gen(sd, device)
             q = torch.empty(shape.E, rows, cols // 2, dtype=torch.uint8, device=device)
-            sc = torch.empty(shape.E, rows, cols // 16, dtype=torch.uint8, device=device)
+            sc = torch.empty(shape.E, rows, cols // blk, dtype=torch.uint8, device=device)
             gs = torch.empty(shape.E, dtype=torch.float32, device=device)
             for e in range(shape.E):
                 wf = torch.randn(rows, cols, generator=gw, device=device,
                                  dtype=torch.float32).mul_(1.0 / math.sqrt(cols))
-                q[e], sc[e], gs[e] = quantize_nvfp4(wf)
-            out[name + "q"], out[name + "s"], out[name + "g"] = q, sc, gs
+                if wfmt == "mxfp4":
+                    q[e], sc[e] = quantize_mxfp4(wf)
+                    gs[e] = 1.0
+                else:
+                    q[e], sc[e], gs[e] = quantize_nvfp4(wf)
+            out[name + "q"], out[name + "s"] = q, sc
+            if wfmt != "mxfp4":
+                out[name + "g"] = gs
     return out

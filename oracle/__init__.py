@@ -66,13 +66,14 @@ def _load():
                                              vp, vp], ci),
                 "oracle_e4m3_value": ([ctypes.c_uint8], cd),
                 "oracle_e2m1_value": ([ctypes.c_uint8], cd),
+                "oracle_e8m0_value": ([ctypes.c_uint8], cd),
                 "oracle_e4m3_encode": ([ctypes.c_float], ctypes.c_uint8),
                 "oracle_requant_fp8_block": ([vp, ci, vp], None),
                 "oracle_gemm1_swiglu_lowprec": ([cl, ci, ci, ci, ci, cd, vp, vp, vp, vp, vp, vp,
-                                                 ci, vp], ci),
-                "oracle_gemm2_lowprec": ([cl, ci, ci, ci, vp, vp, vp, vp, vp, vp], ci),
+                                                 ci, ci, vp], ci),
+                "oracle_gemm2_lowprec": ([cl, ci, ci, ci, vp, vp, vp, vp, vp, ci, vp], ci),
                 "oracle_moe_forward_lowprec": ([ci, ci, ci, ci, ci, ci, ci, cd, vp, vp, vp, vp,
-                                                vp, vp, vp, vp, vp, vp, vp, vp], ci),
+                                                vp, vp, vp, vp, vp, ci, vp, vp, vp], ci),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -296,6 +297,15 @@ def e2m1_value(code: int) -> float:
     return _load().oracle_e2m1_value(int(code))
 
 
+def e8m0_value(code: int) -> float:
+    return _load().oracle_e8m0_value(int(code))
+
+
+# weight formats of the low-precision functions
+WFMT_NVFP4 = 0  # E2M1 codes, E4M3 scale per 16 values, fp32 scale per expert tensor
+WFMT_MXFP4 = 1  # E2M1 codes, E8M0 scale per 32 values (the expert scales are unused)
+
+
 def e4m3_encode(x: float) -> int:
     return int(_load().oracle_e4m3_encode(float(x)))
 
@@ -322,7 +332,8 @@ def _byte_ptrs(ws):
 
 
 def gemm1_swiglu_lowprec(xq_perm, xs_perm, expert_offsets, w1q, w1s, g1, F: int,
-                         interleave: int = 0, clamp: float = 0.0, requant: bool = True):
+                         interleave: int = 0, clamp: float = 0.0, requant: bool = True,
+                         wfmt: int = WFMT_NVFP4):
     xq = _np(xq_perm, np.uint8)
     xs = _np(xs_perm, np.float32)
     off = _np(expert_offsets, np.int32)
@@ -333,12 +344,12 @@ def gemm1_swiglu_lowprec(xq_perm, xs_perm, expert_offsets, w1q, w1s, g1, F: int,
     h = np.empty((R, F), np.float64)
     _check(_load().oracle_gemm1_swiglu_lowprec(R, H, F, E, interleave, float(clamp), _p(off),
                                                _p(xq), _p(xs), _byte_ptrs(q), _byte_ptrs(sc),
-                                               _p(g), int(requant), _p(h)),
+                                               _p(g), int(requant), int(wfmt), _p(h)),
            "oracle_gemm1_swiglu_lowprec")
     return h
 
 
-def gemm2_lowprec(h, expert_offsets, w2q, w2s, g2, H: int):
+def gemm2_lowprec(h, expert_offsets, w2q, w2s, g2, H: int, wfmt: int = WFMT_NVFP4):
     hh = _np(h, np.float64)
     off = _np(expert_offsets, np.int32)
     E = off.shape[0] - 1
@@ -347,13 +358,16 @@ def gemm2_lowprec(h, expert_offsets, w2q, w2s, g2, H: int):
     g = _np(g2, np.float32)
     y = np.empty((R, H), np.float64)
     _check(_load().oracle_gemm2_lowprec(R, H, F, E, _p(off), _p(hh), _byte_ptrs(q),
-                                        _byte_ptrs(sc), _p(g), _p(y)), "oracle_gemm2_lowprec")
+                                        _byte_ptrs(sc), _p(g), int(wfmt), _p(y)),
+           "oracle_gemm2_lowprec")
     return y
 
 
 def moe_forward_lowprec(xq, xs, logits, w1q, w1s, g1, w2q, w2s, g2, k: int,
-                        renormalize: bool = True, interleave: int = 0, clamp: float = 0.0):
-    """The FP8-activation / NVFP4-weight layer on the given tokens.  Weight
+                        renormalize: bool = True, interleave: int = 0, clamp: float = 0.0,
+                        wfmt: int = WFMT_NVFP4):
+    """The FP8-activation / FP4-weight layer on the given tokens (NVFP4 or,
+    with wfmt=WFMT_MXFP4, MXFP4 weights; g1/g2 are then ignored).  Weight
     arguments are [E, ...] byte tensors or per-expert lists (None = unused)."""
     xqa = _np(xq, np.uint8)
     xsa = _np(xs, np.float32)
@@ -369,5 +383,6 @@ def moe_forward_lowprec(xq, xs, logits, w1q, w1s, g1, w2q, w2s, g2, k: int,
     _check(_load().oracle_moe_forward_lowprec(
         T, H, F, E, k, int(renormalize), interleave, float(clamp), _p(lg), _p(xqa), _p(xsa),
         _byte_ptrs(q1), _byte_ptrs(s1), _p(_np(g1, np.float32)), _byte_ptrs(q2), _byte_ptrs(s2),
-        _p(_np(g2, np.float32)), _p(out), _p(idx), _p(w)), "oracle_moe_forward_lowprec")
+        _p(_np(g2, np.float32)), int(wfmt), _p(out), _p(idx), _p(w)),
+        "oracle_moe_forward_lowprec")
     return {"out": out, "topk_idx": idx, "topk_w": w}

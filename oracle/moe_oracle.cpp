@@ -117,6 +117,24 @@ inline double nvfp4_value(const uint8_t* q_row, const uint8_t* s_row, long k, do
   return kCodes.e2m1[nib] * kCodes.e4m3[s_row[k >> 4]] * g;
 }
 
+// E8M0 scale byte: 2^(e - 127) (the byte 255 is not a number; out of contract).
+inline double e8m0_value(uint8_t e) { return std::ldexp(1.0, static_cast<int>(e) - 127); }
+
+// MXFP4 (the MegaMoE page's Usage: raw weight scales E8M0 per 32 values):
+// w = E2M1(q) * 2^(s - 127), s the scale byte of the 32-value block.
+inline double mxfp4_value(const uint8_t* q_row, const uint8_t* s_row, long k) {
+  const uint8_t byte = q_row[k >> 1];
+  const uint8_t nib = (k & 1) ? (byte >> 4) : (byte & 15);
+  return kCodes.e2m1[nib] * e8m0_value(s_row[k >> 5]);
+}
+
+// Weight formats of the low-precision oracle: 0 NVFP4 (E4M3 scale per 16 values
+// times the expert's fp32 scale g), 1 MXFP4 (E8M0 scale per 32 values; g unused).
+inline double fp4_value(int wfmt, const uint8_t* q_row, const uint8_t* s_row, long k, double g) {
+  return wfmt == 1 ? mxfp4_value(q_row, s_row, k) : nvfp4_value(q_row, s_row, k, g);
+}
+inline int scale_block(int wfmt) { return wfmt == 1 ? 32 : 16; }
+
 // clamp <= 0 or non-finite means "no clamp".
 inline double swiglu(double g, double u, double c) {
   if (c > 0 && std::isfinite(c)) {
@@ -403,6 +421,7 @@ int oracle_dense_bruteforce(int T, int H, int F, int E, int k, int interleave, d
 
 double oracle_e4m3_value(uint8_t c) { return e4m3_value(c); }
 double oracle_e2m1_value(uint8_t n) { return e2m1_value(n); }
+double oracle_e8m0_value(uint8_t e) { return e8m0_value(e); }
 uint8_t oracle_e4m3_encode(float x) { return e4m3_encode(x); }
 
 // Re-quantisation of one row block of h to FP8 (the split GEMM1 epilogue of
@@ -429,7 +448,8 @@ int oracle_gemm1_swiglu_lowprec(long R, int H, int F, int E, int interleave, dou
                                 const int32_t* expert_offsets, const uint8_t* xq_perm,
                                 const float* xs_perm, const uint8_t* const* w1q,
                                 const uint8_t* const* w1s, const float* g1, int requant,
-                                double* h) {
+                                int wfmt, double* h) {
+  const int sb = scale_block(wfmt);
   if (interleave > 0 && F % interleave != 0) return -1;
   if (H % 128 != 0 || F % 128 != 0) return -1;
   for (int e = 0; e < E; ++e)
@@ -451,13 +471,13 @@ int oracle_gemm1_swiglu_lowprec(long R, int H, int F, int E, int interleave, dou
         const double* xr = &xhat[(r - r0) * H];
         const long rg = gate_row(f, F, interleave), ru = up_row(f, F, interleave);
         const uint8_t* qg = w1q[e] + rg * (H / 2);
-        const uint8_t* sg = w1s[e] + rg * (H / 16);
+        const uint8_t* sg = w1s[e] + rg * (H / sb);
         const uint8_t* qu = w1q[e] + ru * (H / 2);
-        const uint8_t* su = w1s[e] + ru * (H / 16);
+        const uint8_t* su = w1s[e] + ru * (H / sb);
         double g = 0.0, u = 0.0;
         for (int c = 0; c < H; ++c) {
-          g += xr[c] * nvfp4_value(qg, sg, c, g1[e]);
-          u += xr[c] * nvfp4_value(qu, su, c, g1[e]);
+          g += xr[c] * fp4_value(wfmt, qg, sg, c, g1[e]);
+          u += xr[c] * fp4_value(wfmt, qu, su, c, g1[e]);
         }
         hraw[(r - r0) * F + f] = swiglu(g, u, clamp);
       }
@@ -478,7 +498,8 @@ int oracle_gemm1_swiglu_lowprec(long R, int H, int F, int E, int interleave, dou
 // w2q[e]: [H, F/2] bytes, w2s[e]: [H, F/16] bytes.
 int oracle_gemm2_lowprec(long R, int H, int F, int E, const int32_t* expert_offsets,
                          const double* h, const uint8_t* const* w2q, const uint8_t* const* w2s,
-                         const float* g2, double* y) {
+                         const float* g2, int wfmt, double* y) {
+  const int sb = scale_block(wfmt);
   for (int e = 0; e < E; ++e)
     if (expert_offsets[e + 1] > expert_offsets[e] && (!w2q[e] || !w2s[e])) return -2;
   for (long r = expert_offsets[E]; r < R; ++r)
@@ -490,9 +511,9 @@ int oracle_gemm2_lowprec(long R, int H, int F, int E, const int32_t* expert_offs
     for (long r = r0; r < r1; ++r) {
       for (int n = 0; n < H; ++n) {
         const uint8_t* q = w2q[e] + static_cast<long>(n) * (F / 2);
-        const uint8_t* sc = w2s[e] + static_cast<long>(n) * (F / 16);
+        const uint8_t* sc = w2s[e] + static_cast<long>(n) * (F / sb);
         double acc = 0.0;
-        for (int f = 0; f < F; ++f) acc += h[r * F + f] * nvfp4_value(q, sc, f, g2[e]);
+        for (int f = 0; f < F; ++f) acc += h[r * F + f] * fp4_value(wfmt, q, sc, f, g2[e]);
         y[r * H + n] = acc;
       }
     }
@@ -507,7 +528,7 @@ int oracle_moe_forward_lowprec(int T, int H, int F, int E, int k, int renormaliz
                                const uint8_t* xq, const float* xs, const uint8_t* const* w1q,
                                const uint8_t* const* w1s, const float* g1,
                                const uint8_t* const* w2q, const uint8_t* const* w2s,
-                               const float* g2, double* out, int32_t* topk_idx_out,
+                               const float* g2, int wfmt, double* out, int32_t* topk_idx_out,
                                double* topk_w_out) {
   const long R = static_cast<long>(T) * k;
   std::vector<int32_t> idx(R), row_id_map(R), permuted_token(R), counts(E), offsets(E + 1);
@@ -528,9 +549,9 @@ int oracle_moe_forward_lowprec(int T, int H, int F, int E, int k, int renormaliz
   }
   std::vector<double> h(static_cast<size_t>(R) * F), y(static_cast<size_t>(R) * H);
   rc = oracle_gemm1_swiglu_lowprec(R, H, F, E, interleave, clamp, offsets.data(), xq_perm.data(),
-                                   xs_perm.data(), w1q, w1s, g1, 1, h.data());
+                                   xs_perm.data(), w1q, w1s, g1, 1, wfmt, h.data());
   if (rc) return rc;
-  rc = oracle_gemm2_lowprec(R, H, F, E, offsets.data(), h.data(), w2q, w2s, g2, y.data());
+  rc = oracle_gemm2_lowprec(R, H, F, E, offsets.data(), h.data(), w2q, w2s, g2, wfmt, y.data());
   if (rc) return rc;
   oracle_unpermute_combine(T, H, k, y.data(), row_id_map.data(), w.data(), out);
   if (topk_idx_out) std::memcpy(topk_idx_out, idx.data(), sizeof(int32_t) * R);

@@ -156,3 +156,73 @@ def test_quantised_inputs_approximate_the_normal_draws():
     rel = (w_hat - w.double()).norm() / w.double().norm()
     assert rel < 0.15  # NVFP4 keeps about 2 significant bits
     assert (sc.view(torch.float8_e4m3fn).float() * 6 <= 448).all()
+
+
+# ---------------------------------------------------------------- MXFP4 weights
+
+def test_e8m0_decode_is_a_power_of_two():
+    assert [oracle.e8m0_value(e) for e in range(255)] == [math.ldexp(1.0, e - 127)
+                                                         for e in range(255)]
+
+
+def mx_dequant(q, s):
+    """Test-side MXFP4 decode: OCP E2M1 table x 2^(scale - 127) per 32 values."""
+    q, s = q.numpy(), s.numpy()
+    codes = np.stack([q & 15, q >> 4], axis=-1).reshape(q.shape[0], -1)
+    vals = np.array(E2M1_TABLE)[codes]
+    return vals * np.ldexp(1.0, s.astype(np.int64) - 127).repeat(32, axis=1)
+
+
+def test_mxfp4_gemm2_matches_numpy_on_decoded_weights():
+    g = torch.Generator().manual_seed(3)
+    E, H, F, R = 3, 64, 128, 20
+    w2 = torch.randn(E, H, F, generator=g) / 10
+    qs = [mi.quantize_mxfp4(w2[e]) for e in range(E)]
+    h = torch.randn(R, F, generator=g, dtype=torch.float64).numpy()
+    off = np.array([0, 7, 7, 20], np.int32)
+    got = oracle.gemm2_lowprec(h, off, [q for q, _ in qs], [s for _, s in qs], np.ones(E),
+                               H, wfmt=oracle.WFMT_MXFP4)
+    want = np.concatenate([h[off[e]:off[e + 1]] @ mx_dequant(*qs[e]).T for e in range(E)])
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-15)
+
+
+def e4m3_power_of_two(j):
+    """E4M3 code of 2^j for j in [-9, 8] (subnormal below 2^-6)."""
+    return (j + 7) << 3 if j >= -6 else 1 << (j + 9)
+
+
+@pytest.mark.parametrize("interleave", [0, 32])
+def test_mxfp4_equals_nvfp4_with_the_same_powers_of_two(interleave):
+    """MXFP4 scales written (by hand) as E4M3 powers of two for both 16-value
+    halves, expert scale 1, give the NVFP4 path's results exactly."""
+    shape = mi.MoEShape("mx", T=24, H=256, F=128, E=3, k=2, glu_interleave=interleave,
+                        swiglu_clamp=7.0, lowprec=True)
+    inp = mi.make_lowprec_inputs(shape, seed=2, wfmt="mxfp4")
+    assert int(inp["w1s"].min()) >= 127 - 9 and int(inp["w1s"].max()) <= 127 + 8
+    nv = {}
+    for n in ("w1", "w2"):
+        j = inp[n + "s"].to(torch.int64) - 127
+        codes = torch.tensor([e4m3_power_of_two(int(v)) for v in j.flatten()],
+                             dtype=torch.uint8).reshape(j.shape)
+        nv[n + "s"] = codes.repeat_interleave(2, dim=-1)
+    ones = torch.ones(shape.E)
+    mx = oracle.moe_forward_lowprec(inp["xq"], inp["xs"], inp["logits"], inp["w1q"], inp["w1s"],
+                                    ones, inp["w2q"], inp["w2s"], ones, shape.k,
+                                    interleave=interleave, clamp=7.0, wfmt=oracle.WFMT_MXFP4)
+    ref = oracle.moe_forward_lowprec(inp["xq"], inp["xs"], inp["logits"], inp["w1q"], nv["w1s"],
+                                     ones, inp["w2q"], nv["w2s"], ones, shape.k,
+                                     interleave=interleave, clamp=7.0)
+    np.testing.assert_array_equal(mx["out"], ref["out"])
+
+
+def test_mxfp4_quantiser_error_bound():
+    g = torch.Generator().manual_seed(5)
+    w = torch.randn(64, 256, generator=g) / 16
+    q, s = mi.quantize_mxfp4(w)
+    deq = mx_dequant(q, s)
+    scale = np.ldexp(1.0, s.numpy().astype(np.int64) - 127).repeat(32, axis=1)
+    err = np.abs(deq - w.double().numpy())
+    # rounding at most half the largest E2M1 step (1 at the top, times the scale),
+    # plus the clipping of magnitudes between 6 and 8 scale units
+    assert (err <= np.maximum(1.0, np.abs(w.double().numpy()) / scale - 6.0) * scale + 1e-12).all()
+    assert np.sqrt((err ** 2).mean() / (w.double().numpy() ** 2).mean()) < 0.15
