@@ -72,6 +72,8 @@ def parse_args(argv=None):
                     help="time CUDA-graph replays of one forward (stage times from an eager pass)")
     ap.add_argument("--kernel", type=int, default=0,
                     help="moe_problem.kernel: 0 auto, 1 token-row tiles, 2 weight-row tiles")
+    ap.add_argument("--wfmt", choices=["nvfp4", "mxfp4"], default="nvfp4",
+                    help="FP4 weight format of the lowprec workload")
     ap.add_argument("--fusion", type=int, default=0,
                     help="moe_problem.fusion bits: 1 = TMA-gather A rows, 2 = combine in GEMM2")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -96,15 +98,16 @@ def ncu_traffic(kernel_file: str, workload: str):
     return None
 
 
-def gemm1_algorithmic_bytes(shape, used_experts: int) -> float:
+def gemm1_algorithmic_bytes(shape, used_experts: int, scale_block: int = 16) -> float:
     """HBM bytes GEMM1 cannot avoid: the gate/up weights of every expert that
     received tokens, the permuted activation rows read once and h written once.
 
-    bf16: 2F*H*2 per expert, R*H*2 in, R*F*2 out.  FP8/NVFP4: 2F*H/2 packed
-    E2M1 + 2F*H/16 E4M3 block scales per expert; the rows come in as f16 (the
-    gather dequantises the E4M3 tokens), R*H*2, and h goes out as f16, R*F*2."""
+    bf16: 2F*H*2 per expert, R*H*2 in, R*F*2 out.  FP8/FP4: 2F*H/2 packed
+    E2M1 + 2F*H/scale_block scale bytes per expert (16 for NVFP4, 32 for MXFP4);
+    the rows come in as f16 (the gather dequantises the E4M3 tokens), R*H*2,
+    and h goes out as f16, R*F*2."""
     R, H, F = shape.R, shape.H, shape.F
-    w = (2 * F * H / 2 + 2 * F * H / 16) if shape.lowprec else 2 * F * H * 2
+    w = (2 * F * H / 2 + 2 * F * H / scale_block) if shape.lowprec else 2 * F * H * 2
     return used_experts * w + R * H * 2 + R * F * 2
 
 
@@ -226,7 +229,8 @@ def oracle_sample(shape, inp_host, n_tokens: int):
         h = inp_host
         oracle.moe_forward_lowprec(h["xq"][:n_tokens], h["xs"][:n_tokens], lg, h["w1q"], h["w1s"],
                                    h["w1g"], h["w2q"], h["w2s"], h["w2g"], shape.k,
-                                   interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
+                                   interleave=shape.glu_interleave, clamp=shape.swiglu_clamp,
+                                   wfmt=h.get("_wfmt", oracle.WFMT_NVFP4))
     else:
         oracle.moe_forward(inp_host["x"][:n_tokens], lg, inp_host["w1"], inp_host["w2"], shape.k,
                            interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
@@ -272,12 +276,18 @@ def bench_ours(args, shape, desc):
     ws = moe.alloc_workspace(p, dev)
     out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
+    mx = shape.lowprec and args.wfmt == "mxfp4"
     if shape.lowprec:
-        lp = mi.make_lowprec_inputs(shape, 0, dev)
+        lp = mi.make_lowprec_inputs(shape, 0, dev, wfmt=args.wfmt)
         if rank:
             lp.update({k: v for k, v in mi.make_lowprec_inputs(shape, rank, dev, weights=False).items()})
         prepared = torch.empty(moe.prepared_scales_size(p), dtype=torch.uint8, device=dev)
-        moe.prepare_weights(p, lp["w1s"], lp["w2s"], prepared)
+        if mx:  # MXFP4 scales re-encoded exactly, with per-expert fp32 scales
+            lp["w1g"] = torch.empty(shape.E, dtype=torch.float32, device=dev)
+            lp["w2g"] = torch.empty(shape.E, dtype=torch.float32, device=dev)
+            moe.prepare_weights_mxfp4(p, lp["w1s"], lp["w2s"], prepared, lp["w1g"], lp["w2g"])
+        else:
+            moe.prepare_weights(p, lp["w1s"], lp["w2s"], prepared)
         x, logits = lp["xq"], lp["logits"]
         xs = lp["xs"]
         weight_bytes = sum(lp[n].numel() for n in ("w1q", "w1s", "w2q", "w2s"))
@@ -394,10 +404,11 @@ def bench_ours(args, shape, desc):
     kid = moe.selected_kernel(p)
     kfile, kname = KERNEL_NAMES.get(kid, ("grouped_gemm_fp4.cu", "grouped_gemm_fp4_kernel<SwiGLU>"))
     if shape.lowprec:
-        kfile, kname = "grouped_gemm_fp4.cu", "grouped_gemm_fp4_kernel<SwiGLU> (GEMM1, NVFP4 weights)"
+        kfile, kname = "grouped_gemm_fp4.cu", "grouped_gemm_fp4_kernel<SwiGLU> (GEMM1, %s weights)" % (
+            "MXFP4" if mx else "NVFP4")
     gemm1_ms = stages.get("gemm1_swiglu", float("nan"))
     gemm1_flops = 4.0 * shape.R * shape.H * shape.F
-    gemm1_bytes = gemm1_algorithmic_bytes(shape, used_experts)
+    gemm1_bytes = gemm1_algorithmic_bytes(shape, used_experts, 32 if mx else 16)
     peak_key = "bf16_tflops_sustained"
     gemm1_s = gemm1_ms / 1e3
     t_tensor = gemm1_flops / (peaks[peak_key] * 1e12)
@@ -422,11 +433,12 @@ def bench_ours(args, shape, desc):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8xnvfp4->f16 mma" if shape.lowprec else "bf16",
+        "dtype": ("fp8xmxfp4->f16 mma" if mx else "fp8xnvfp4->f16 mma") if shape.lowprec else "bf16",
         "data": "synthetic",
         "config": {"workload": desc, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
                    "k": shape.k, "fusion": args.fusion, "kernel": args.kernel,
-                   "precision": "fp8-act/nvfp4-weight" if shape.lowprec else "bf16",
+                   "precision": ("fp8-act/mxfp4-weight" if mx else "fp8-act/nvfp4-weight")
+                   if shape.lowprec else "bf16",
                    "timing": "cuda-graph replay" if args.graph else "eager launches", "l2": "inputs larger than L2 (weights %.2f GB), no flush"
                    % (weight_bytes / 1e9)},
         "roofline": {"kernel": kname, "bound": main["bound"],
@@ -450,6 +462,7 @@ def bench_ours(args, shape, desc):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         if shape.lowprec:
             host = {k: v.cpu() for k, v in lp.items()}
+            host["_wfmt"] = 1 if mx else 0
         else:
             host = {"x": x.cpu(), "logits": logits.cpu(), "w1": w1.cpu(), "w2": w2.cpu()}
         line["cpu_baseline"] = cpu_baseline(shape, host, args.cpu_seconds)
@@ -534,6 +547,8 @@ def main(argv=None):
         desc = desc + f" (T={args.T})"
     elif args.workload == "decode":
         desc = desc + f" T={shape.T}"
+    if shape.lowprec and args.wfmt == "mxfp4":
+        desc = desc.replace("NVFP4", "MXFP4")
     if args.impl == "reference":
         bench_reference(args, shape, desc)
     else:

@@ -301,6 +301,25 @@ MOE_API int moe_prepare_weights(const moe_problem* p, const uint8_t* w1_scale,
                                 const uint8_t* w2_scale, void* prepared, size_t prepared_bytes,
                                 void* stream);
 
+/* MXFP4 weights (the MegaMoE page's Usage: raw weight scales E8M0 per 32
+ * values; the page prepares them with a weight transform before the call):
+ * re-encodes them exactly for moe_forward_fp8_nvfp4.  The packed E2M1 codes
+ * are used as they are (w1q / w2q); the scales become the prepared layout of
+ * moe_prepare_weights plus one fp32 scale per expert tensor:
+ *   w1_scale [E, 2F, H/32], w2_scale [E, H, F/32]: E8M0 bytes, 2^(s - 127);
+ *   prepared: moe_prepared_scales_size(p) bytes out;
+ *   w1_gscale_out [E], w2_gscale_out [E]: fp32 out, to pass to
+ *   moe_forward_fp8_nvfp4 as the expert scales.
+ * With e_max the expert tensor's largest scale byte, its fp32 scale is
+ * 2^(e_max - 135) and each block's scale becomes the E4M3 power of two
+ * 2^(s - e_max + 8) in [2^-9, 2^8], exact; a block more than 17 binades
+ * below e_max is set to zero.  The byte 255 (not a number) is out of contract.
+ * p->precision must be MOE_PREC_FP8_NVFP4. */
+MOE_API int moe_prepare_weights_mxfp4(const moe_problem* p, const uint8_t* w1_scale,
+                                      const uint8_t* w2_scale, void* prepared,
+                                      size_t prepared_bytes, float* w1_gscale_out,
+                                      float* w2_gscale_out, void* stream);
+
 /* The whole low-precision layer.
  *   xq [T, H] E4M3 codes, xs [T, H/128] fp32, logits [T, E] fp32
  *   w1q [E, 2F, H/2], w2q [E, H, F/2] packed E2M1 codes (GLU interleave as

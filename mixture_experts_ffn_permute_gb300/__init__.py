@@ -101,6 +101,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_permute_noalloc": ([pp, vp, vp, vp, vp, vp, vp, vp, vp], ci),
         "moe_prepared_scales_size": ([pp], sz),
         "moe_prepare_weights": ([pp, vp, vp, vp, sz, vp], ci),
+        "moe_prepare_weights_mxfp4": ([pp, vp, vp, vp, sz, vp, vp, vp], ci),
         "moe_forward_fp8_nvfp4": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                                    vp], ci),
     }
@@ -243,6 +244,15 @@ def prepare_weights(p: Problem, w1_scale, w2_scale, prepared, stream=None) -> No
     """Re-lay NVFP4 block scales into the order the low-precision kernels stream them."""
     _call("moe_prepare_weights", ctypes.byref(p), _ptr(w1_scale), _ptr(w2_scale), _ptr(prepared),
           prepared.numel() * prepared.element_size(), _stream(stream))
+
+
+def prepare_weights_mxfp4(p: Problem, w1_scale, w2_scale, prepared, w1_gscale, w2_gscale,
+                          stream=None) -> None:
+    """Re-encode MXFP4 E8M0 scales for forward_fp8_nvfp4 (prepared scales and the
+    per-expert fp32 scales w1_gscale / w2_gscale, both written)."""
+    _call("moe_prepare_weights_mxfp4", ctypes.byref(p), _ptr(w1_scale), _ptr(w2_scale),
+          _ptr(prepared), prepared.numel() * prepared.element_size(), _ptr(w1_gscale),
+          _ptr(w2_gscale), _stream(stream))
 
 
 def forward_fp8_nvfp4(p: Problem, xq, xs, logits, w1q, w1_gscale, w2q, w2_gscale, prepared,

@@ -591,6 +591,29 @@ int moe_prepare_weights(const moe_problem* p, const uint8_t* w1_scale, const uin
   return MOE_OK;
 }
 
+int moe_prepare_weights_mxfp4(const moe_problem* p, const uint8_t* w1_scale,
+                              const uint8_t* w2_scale, void* prepared, size_t prepared_bytes,
+                              float* w1_gscale_out, float* w2_gscale_out, void* stream) {
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
+  if (p->precision != MOE_PREC_FP8_NVFP4) return MOE_ERR_INVALID_ARG;
+  MOE_REQUIRE_PTR(w1_scale);
+  MOE_REQUIRE_PTR(w2_scale);
+  MOE_REQUIRE_PTR(prepared);
+  MOE_REQUIRE_PTR(w1_gscale_out);
+  MOE_REQUIRE_PTR(w2_gscale_out);
+  if (prepared_bytes < moe_prepared_scales_size(p)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* dst = static_cast<uint8_t*>(prepared);
+  MOE_LAUNCH(launch_prepare_mxfp4_scales(
+      w1_scale, w2_scale, dst, dst + static_cast<size_t>(p->E) * 2 * p->F * p->H / 16, p->E,
+      p->F, p->H, w1_gscale_out, w2_gscale_out, s));
+  g_launches = launches;
+  return MOE_OK;
+}
+
 int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* xs,
                           const float* logits, const uint8_t* w1q, const float* w1_gscale,
                           const uint8_t* w2q, const float* w2_gscale, const void* prepared_scales,

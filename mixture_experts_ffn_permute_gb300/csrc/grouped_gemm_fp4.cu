@@ -446,6 +446,57 @@ prepare_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst
   }
 }
 
+// MXFP4 scales -> the prepared E4M3 layout above, exactly: one CTA per (expert,
+// tensor).  With e_max the largest E8M0 byte of the expert's tensor, the
+// expert scale is g = 2^k, k = (e_max - 127) - 8, and each block's scale
+// 2^(e - 127) becomes the E4M3 power of two 2^(e - 127 - k) in [2^-9, 2^8]
+// (every power of two there is an E4M3 code), written for both 16-value
+// halves of its 32-value block.  A block more than 17 binades below e_max
+// gets scale 0 (its values are below 2^-17 of the expert's largest block).
+// The byte 255 (not a number) is out of contract and treated as 0.
+__device__ __forceinline__ uint32_t e4m3_power_of_two(int j) {  // j in [-9, 8]
+  return j >= -6 ? static_cast<uint32_t>(j + 7) << 3 : 1u << (j + 9);
+}
+
+__global__ void __launch_bounds__(512)
+prepare_mxfp4_scales_kernel(const uint8_t* __restrict__ s1, const uint8_t* __restrict__ s2,
+                            uint8_t* __restrict__ dst1, uint8_t* __restrict__ dst2, int F, int H,
+                            float* __restrict__ g1, float* __restrict__ g2) {
+  pdl_enter();
+  __shared__ int s_max[16];
+  const int e = blockIdx.x;
+  const bool second = blockIdx.y == 1;
+  const int N = second ? H : 2 * F, K = second ? F : H;
+  const uint8_t* src = (second ? s2 : s1) + static_cast<long>(e) * N * (K / 32);
+  uint8_t* dst = second ? dst2 : dst1;
+  const long nbytes = static_cast<long>(N) * (K / 32);
+  int m = 0;
+  for (long i = threadIdx.x; i < nbytes; i += blockDim.x) {
+    const int b = src[i];
+    if (b != 255) m = max(m, b);
+  }
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  int emax = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) emax = max(emax, s_max[w]);
+  const int k = min(127, max(-126, emax - 127 - 8));
+  if (threadIdx.x == 0) (second ? g2 : g1)[e] = ldexpf(1.0f, k);
+  const int kblocks = K / 64;
+  for (long i = threadIdx.x; i < static_cast<long>(N) * kblocks; i += blockDim.x) {
+    const int n = static_cast<int>(i / kblocks), kb = static_cast<int>(i % kblocks);
+    uint32_t word = 0;
+    for (int h = 0; h < 2; ++h) {
+      const int b = src[static_cast<long>(n) * (K / 32) + 2 * kb + h];
+      const int j = b - 127 - k;
+      const uint32_t c = (b == 255 || j < -9) ? 0u : e4m3_power_of_two(j);
+      word |= (c | (c << 8)) << (16 * h);
+    }
+    const long rb = static_cast<long>(e) * (N / 128) + n / 128;
+    *reinterpret_cast<uint32_t*>(dst + ((rb * kblocks + kb) * 128 + (n % 128)) * 4) = word;
+  }
+}
+
 // x_perm[r][c] = f16(E4M3(xq[t][c]) * xs[t][c / 128]), t = permuted_token[r]
 // (zero rows for -1); 8 values per thread.
 __global__ void __launch_bounds__(256)
@@ -520,6 +571,14 @@ cudaError_t launch_prepare_scales(const uint8_t* src, uint8_t* dst, int E, int N
   if (groups == 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<long>((groups + 255) / 256, num_sms() * 16L));
   return launch_kernel(prepare_scales_kernel, dim3(blocks), dim3(256), 0, s, 1, src, dst, E, N, K);
+}
+
+cudaError_t launch_prepare_mxfp4_scales(const uint8_t* s1, const uint8_t* s2, uint8_t* dst1,
+                                        uint8_t* dst2, int E, int F, int H, float* g1, float* g2,
+                                        cudaStream_t s) {
+  if (E == 0) return cudaSuccess;
+  return launch_kernel(prepare_mxfp4_scales_kernel, dim3(E, 2), dim3(512), 0, s, 1, s1, s2, dst1,
+                       dst2, F, H, g1, g2);
 }
 
 cudaError_t launch_gather_dequant_fp8(const uint8_t* xq, const float* xs,

@@ -178,6 +178,11 @@ cudaError_t launch_grouped_gemm_fp4_tmem(const GroupedGemmArgs& g, const uint8_t
 // [E][N][K/16] E4M3 scales -> [E][N/128][K/64][128][4]
 cudaError_t launch_prepare_scales(const uint8_t* src, uint8_t* dst, int E, int N, int K,
                                   cudaStream_t s);
+// MXFP4 E8M0 scales [E][2F][H/32] and [E][H][F/32] -> the prepared E4M3 layout
+// (exact powers of two) plus per-expert fp32 scales g1[E], g2[E].
+cudaError_t launch_prepare_mxfp4_scales(const uint8_t* s1, const uint8_t* s2, uint8_t* dst1,
+                                        uint8_t* dst2, int E, int F, int H, float* g1, float* g2,
+                                        cudaStream_t s);
 // FP8 rows (E4M3 codes + fp32 scales per 128) gathered by permuted_token into f16.
 cudaError_t launch_gather_dequant_fp8(const uint8_t* xq, const float* xs,
                                       const int32_t* permuted_token, int R, int H, void* x_perm,

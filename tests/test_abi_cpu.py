@@ -169,3 +169,14 @@ def test_selftest_wait_timeout_validates(lib):
     assert f(None, 1000, None) == 1
     assert f(a, 0, None) == 1
     assert f(a, 3 * 10**9, None) == 1   # above the library's own 2 s wait limit
+
+
+def test_prepare_weights_mxfp4_validates(lib):
+    a = ctypes.c_void_p(1 << 20)
+    big = 1 << 40
+    p = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, precision=moe.PREC_FP8_NVFP4)
+    f = lib.moe_prepare_weights_mxfp4
+    assert f(ctypes.byref(p), a, a, a, big, None, a, None) == 1
+    assert f(ctypes.byref(p), a, a, a, moe.prepared_scales_size(p) - 1, a, a, None) == 4
+    bf = moe.Problem.make(T=64, H=256, F=512, E=8, k=2)
+    assert f(ctypes.byref(bf), a, a, a, big, a, a, None) == 1

@@ -119,3 +119,98 @@ def test_lowprec_full_size_sampled(kernel):
                                      interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
     check(res["out"][ti], ref["out"], "lowprec sampled")
     assert torch.isfinite(res["out"].float()).all()
+
+
+# ---------------------------------------------------------------- MXFP4 weights
+
+def run_lowprec_mx(shape, inp, kernel=moe.KERNEL_AUTO):
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True, shape.glu_interleave,
+                         shape.swiglu_clamp, precision=moe.PREC_FP8_NVFP4, kernel=kernel)
+    prepared = torch.empty(moe.prepared_scales_size(p), dtype=torch.uint8, device=DEV)
+    g1 = torch.empty(shape.E, dtype=torch.float32, device=DEV)
+    g2 = torch.empty(shape.E, dtype=torch.float32, device=DEV)
+    moe.prepare_weights_mxfp4(p, inp["w1s"], inp["w2s"], prepared, g1, g2)
+    ws = moe.alloc_workspace(p)
+    moe.clear_device_status(ws)
+    out = torch.full((shape.T, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty(shape.T, shape.k, dtype=torch.int32, device=DEV)
+    moe.forward_fp8_nvfp4(p, inp["xq"], inp["xs"], inp["logits"], inp["w1q"], g1, inp["w2q"], g2,
+                          prepared, out, ws, idx)
+    st = moe.get_device_status(ws)
+    assert st == 0, moe.STATUS_NAMES[st]
+    return {"out": out, "topk_idx": idx, "prepared": prepared, "g1": g1, "g2": g2}
+
+
+@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_WIDE],
+                         ids=["token_tiles", "weight_tiles_tmem"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
+def test_mxfp4_forward_small(shape, kernel):
+    inp = mi.make_lowprec_inputs(shape, seed=0, wfmt="mxfp4")
+    ones = torch.ones(shape.E)
+    ref = oracle.moe_forward_lowprec(inp["xq"], inp["xs"], inp["logits"], inp["w1q"], inp["w1s"],
+                                     ones, inp["w2q"], inp["w2s"], ones, shape.k,
+                                     interleave=shape.glu_interleave, clamp=shape.swiglu_clamp,
+                                     wfmt=oracle.WFMT_MXFP4)
+    res = run_lowprec_mx(shape, {k: v.to(DEV) for k, v in inp.items()}, kernel)
+    assert_equal(res["topk_idx"], ref["topk_idx"], "topk_idx")
+    check(res["out"], ref["out"], shape.name + " (MXFP4)")
+
+
+def test_mxfp4_prepare_is_exact_and_flushes_below_its_window():
+    """prepared E4M3 code x expert scale == 2^(s - 127) for every block within 17
+    binades of the expert's largest scale; blocks further down become 0."""
+    shape = SHAPES[1]
+    E, N1, K1 = shape.E, 2 * shape.F, shape.H
+    g = torch.Generator().manual_seed(11)
+    s1 = torch.randint(118, 136, (E, N1, K1 // 32), generator=g, dtype=torch.uint8)
+    s2 = torch.randint(100, 128, (E, shape.H, shape.F // 32), generator=g, dtype=torch.uint8)
+    s1[2, 5, 3] = int(s1[2].max()) - 20      # below the window of expert 2
+    p = moe.Problem.make(shape.T, shape.H, shape.F, E, shape.k, precision=moe.PREC_FP8_NVFP4)
+    prepared = torch.empty(moe.prepared_scales_size(p), dtype=torch.uint8, device=DEV)
+    g1 = torch.empty(E, dtype=torch.float32, device=DEV)
+    g2 = torch.empty(E, dtype=torch.float32, device=DEV)
+    moe.prepare_weights_mxfp4(p, s1.to(DEV), s2.to(DEV), prepared, g1, g2)
+    torch.cuda.synchronize()
+    pre = prepared.cpu()
+    n1 = E * N1 * (K1 // 16)
+
+    def unrelay(flat, N, K):  # [E, N/128, K/64, 128, 4] -> [E, N, K/16]
+        return flat.reshape(E, N // 128, K // 64, 128, 4).permute(0, 1, 3, 2, 4).reshape(E, N, K // 16)
+
+    for flat, src, gs, N, K in ((pre[:n1], s1, g1.cpu(), N1, K1),
+                                (pre[n1:], s2, g2.cpu(), shape.H, shape.F)):
+        codes = unrelay(flat, N, K)
+        assert torch.equal(codes[..., 0::2], codes[..., 1::2])   # both 16-value halves
+        val = codes[..., 0::2].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+        val = val * gs.to(torch.float64)[:, None, None]
+        want = torch.ldexp(torch.ones_like(val), src.to(torch.int64) - 127)
+        emax = src.reshape(E, -1).max(1).values.to(torch.int64)[:, None, None]
+        inside = src.to(torch.int64) >= emax - 17
+        assert torch.equal(val[inside], want[inside])
+        assert (val[~inside] == 0).all()
+    assert not bool((s1[2].to(torch.int64) >= int(s1[2].max()) - 17)[5, 3])
+
+
+@pytest.mark.slow
+def test_mxfp4_full_size_sampled():
+    shape = mi.LOWPREC
+    inp = mi.make_lowprec_inputs(shape, seed=0, device=DEV, wfmt="mxfp4")
+    res = run_lowprec_mx(shape, inp)
+    logits_h = inp["logits"].cpu()
+    idx_ref, _ = oracle.route_topk(logits_h, shape.k)
+    assert_equal(res["topk_idx"], idx_ref, "topk_idx")
+    g = np.random.default_rng(8)
+    toks = np.sort(g.choice(shape.T, size=4, replace=False))
+    used = sorted(set(idx_ref[toks].ravel().tolist()))
+    lists = {n: [None] * shape.E for n in ("w1q", "w1s", "w2q", "w2s")}
+    for e in used:
+        for n in lists:
+            lists[n][e] = inp[n][e].cpu()
+    ti = torch.from_numpy(toks).to(DEV)
+    ones = torch.ones(shape.E)
+    ref = oracle.moe_forward_lowprec(inp["xq"][ti].cpu(), inp["xs"][ti].cpu(), logits_h[toks],
+                                     lists["w1q"], lists["w1s"], ones, lists["w2q"],
+                                     lists["w2s"], ones, shape.k,
+                                     interleave=shape.glu_interleave, clamp=shape.swiglu_clamp,
+                                     wfmt=oracle.WFMT_MXFP4)
+    check(res["out"][ti], ref["out"], "MXFP4 sampled")
