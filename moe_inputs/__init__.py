@@ -25,6 +25,8 @@ size):
     b_e = -s * ln(rank_e) is added, rank = a seeded random permutation of
     1..E and s = 1.1 (Zipf-law expert popularity)
   * W1 [E, 2F, H] ~ N(0, 1/H), W2 [E, H, F] ~ N(0, 1/F), rounded to bf16.
+  * backward: the output gradient dOut [T, H] ~ N(0, 1), rounded to bf16,
+    from its own generator (seed + 4).
 
 Full-size weights are drawn directly on the device given (``device='cuda'``)
 because they are gigabytes; the oracle is then handed host copies of exactly
@@ -131,6 +133,13 @@ def make_inputs(shape: MoEShape, seed: int = 0, device="cpu",
         "w2": make_w2(shape, seed, device) if weights else None,
     }
     return out
+
+
+def make_grad_out(shape: MoEShape, seed: int = 0, device="cpu") -> torch.Tensor:
+    """The gradient of the loss with respect to the layer's output, [T, H] bf16."""
+    g = _gen(seed + 4, device)
+    return torch.randn(shape.T, shape.H, generator=g, device=device,
+                       dtype=torch.float32).to(torch.bfloat16)
 
 
 def bf16_bits(t: torch.Tensor):

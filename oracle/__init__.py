@@ -74,6 +74,15 @@ def _load():
                 "oracle_gemm2_lowprec": ([cl, ci, ci, ci, vp, vp, vp, vp, vp, ci, vp], ci),
                 "oracle_moe_forward_lowprec": ([ci, ci, ci, ci, ci, ci, ci, cd, vp, vp, vp, vp,
                                                 vp, vp, vp, vp, vp, ci, vp, vp, vp], ci),
+                "oracle_moe_backward": ([ci, ci, ci, ci, ci, ci, cd, ci, vp, vp, vp, vp, vp,
+                                         vp, vp, vp, vp, vp], ci),
+                "oracle_backward_tokens": ([ci, ci, ci, ci, ci, ci, cd, ci, vp, vp, vp, vp,
+                                            vp, vp, ci, vp, vp, vp], ci),
+                "oracle_backward_dw1_rows": ([ci, ci, ci, ci, ci, ci, cd, ci, vp, vp, vp, vp,
+                                              vp, vp, ci, vp, vp], ci),
+                "oracle_backward_dw2_cols": ([ci, ci, ci, ci, ci, ci, cd, ci, vp, vp, vp, vp,
+                                              vp, ci, vp, vp], ci),
+                "oracle_router_backward": ([ci, ci, ci, ci, ci, vp, vp, vp, vp, vp], ci),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -386,3 +395,127 @@ def moe_forward_lowprec(xq, xs, logits, w1q, w1s, g1, w2q, w2s, g2, k: int,
         _p(_np(g2, np.float32)), int(wfmt), _p(out), _p(idx), _p(w)),
         "oracle_moe_forward_lowprec")
     return {"out": out, "topk_idx": idx, "topk_w": w}
+
+
+# ---------------------------------------------------------------- backward
+
+def routes_with_shared(logits, k: int, S: int = 0, renormalize: bool = True):
+    """route_topk's routes plus S shared-expert slots (experts E .. E+S-1,
+    weight 1) after the k routed ones, as [T, k+S] arrays."""
+    idx, w = route_topk(logits, k, renormalize)
+    if S:
+        T, E = idx.shape[0], _np(logits, np.float32).shape[1]
+        idx = np.concatenate([idx, np.tile(np.arange(E, E + S, dtype=np.int32), (T, 1))], axis=1)
+        w = np.concatenate([w, np.ones((T, S), np.float64)], axis=1)
+    return np.ascontiguousarray(idx), np.ascontiguousarray(w)
+
+
+def _bwd_args(x, topk_idx, topk_w, w1, w2, d_out):
+    xb = _np(x, np.uint16)
+    gb = _np(d_out, np.uint16)
+    ix = _np(topk_idx, np.int32)
+    ww = _np(topk_w, np.float64)
+    if isinstance(w1, (list, tuple)):
+        E = len(w1)
+    else:
+        E = int(w1.shape[0])
+    w1s, w2s = _experts(w1, E), _experts(w2, E)
+    F = next(m for m in w2s if m is not None).shape[1]
+    return xb, gb, ix, ww, w1s, w2s, E, F
+
+
+def expert_backward(x, topk_idx, topk_w, w1, w2, d_out, interleave: int = 0,
+                    clamp: float = 0.0, mask_bf16: bool = False) -> Dict[str, np.ndarray]:
+    """Gradients of sum(d_out * out) through the expert MLPs for the given
+    routes ([T, slots] indices, -1 masked, and weights): dx [T, H],
+    dw_route [T, slots] (d loss / d weight of each route), dw1 [E, 2F, H] and
+    dw2 [E, H, F], all fp64."""
+    xb, gb, ix, ww, w1s, w2s, E, F = _bwd_args(x, topk_idx, topk_w, w1, w2, d_out)
+    T, H = xb.shape
+    slots = ix.shape[1]
+    dx = np.empty((T, H), np.float64)
+    dwr = np.empty((T, slots), np.float64)
+    dw1 = np.empty((E, 2 * F, H), np.float64)
+    dw2 = np.empty((E, H, F), np.float64)
+    _check(_load().oracle_moe_backward(T, H, F, E, slots, interleave, float(clamp),
+                                       int(mask_bf16), _p(ix), _p(ww), _p(xb),
+                                       _expert_ptrs(w1s), _expert_ptrs(w2s), _p(gb), _p(dx),
+                                       _p(dwr), _p(dw1), _p(dw2)), "oracle_moe_backward")
+    return {"dx": dx, "dw_route": dwr, "dw1": dw1, "dw2": dw2}
+
+
+def router_backward(logits, topk_idx, topk_w, dw_route, k: int,
+                    renormalize: bool = True) -> np.ndarray:
+    """d loss / d logits [T, E] from the per-route weight gradients (the
+    first k slots are the routed ones; later slots are shared experts)."""
+    lg = _np(logits, np.float32)
+    ix = _np(topk_idx, np.int32)
+    ww = _np(topk_w, np.float64)
+    dw = _np(dw_route, np.float64)
+    T, E = lg.shape
+    slots = ix.shape[1]
+    dl = np.empty((T, E), np.float64)
+    _check(_load().oracle_router_backward(T, E, k, slots, int(renormalize), _p(lg), _p(ix),
+                                          _p(ww), _p(dw), _p(dl)), "oracle_router_backward")
+    return dl
+
+
+def moe_backward(x, logits, w1, w2, d_out, k: int, renormalize: bool = True,
+                 interleave: int = 0, clamp: float = 0.0, shared_experts: int = 0,
+                 mask_bf16: bool = False) -> Dict[str, np.ndarray]:
+    """Gradients of sum(d_out * out) for the whole layer (route_topk's
+    routing, optional shared experts): dx, dlogits, dw1, dw2 plus the
+    routes."""
+    idx, w = routes_with_shared(logits, k, shared_experts, renormalize)
+    res = expert_backward(x, idx, w, w1, w2, d_out, interleave, clamp, mask_bf16)
+    res["dlogits"] = router_backward(logits, idx, w, res["dw_route"], k, renormalize)
+    res["topk_idx"], res["topk_w"] = idx, w
+    return res
+
+
+def backward_tokens(x, topk_idx, topk_w, w1, w2, d_out, tokens, interleave: int = 0,
+                    clamp: float = 0.0, mask_bf16: bool = False):
+    """dx rows [n, H] and per-route weight gradients [n, slots] of the listed
+    tokens (expert_backward's definitions, only those rows)."""
+    xb, gb, ix, ww, w1s, w2s, E, F = _bwd_args(x, topk_idx, topk_w, w1, w2, d_out)
+    T, H = xb.shape
+    slots = ix.shape[1]
+    tk = np.ascontiguousarray(np.asarray(tokens, np.int32))
+    dx = np.empty((tk.shape[0], H), np.float64)
+    dw = np.empty((tk.shape[0], slots), np.float64)
+    _check(_load().oracle_backward_tokens(T, H, F, E, slots, interleave, float(clamp),
+                                          int(mask_bf16), _p(ix), _p(ww), _p(xb),
+                                          _expert_ptrs(w1s), _expert_ptrs(w2s), _p(gb),
+                                          tk.shape[0], _p(tk), _p(dx), _p(dw)),
+           "oracle_backward_tokens")
+    return dx, dw
+
+
+def backward_dw1_rows(x, topk_idx, topk_w, w1, w2, d_out, pairs, interleave: int = 0,
+                      clamp: float = 0.0, mask_bf16: bool = False) -> np.ndarray:
+    """Rows dw1[e, row, :] for the listed (e, row) pairs, [n, H]."""
+    xb, gb, ix, ww, w1s, w2s, E, F = _bwd_args(x, topk_idx, topk_w, w1, w2, d_out)
+    T, H = xb.shape
+    pr = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+    rows = np.empty((pr.shape[0], H), np.float64)
+    _check(_load().oracle_backward_dw1_rows(T, H, F, E, ix.shape[1], interleave, float(clamp),
+                                            int(mask_bf16), _p(ix), _p(ww), _p(xb),
+                                            _expert_ptrs(w1s), _expert_ptrs(w2s), _p(gb),
+                                            pr.shape[0], _p(pr), _p(rows)),
+           "oracle_backward_dw1_rows")
+    return rows
+
+
+def backward_dw2_cols(x, topk_idx, topk_w, w1, w2, d_out, pairs, interleave: int = 0,
+                      clamp: float = 0.0, mask_bf16: bool = False) -> np.ndarray:
+    """Columns dw2[e, :, f] for the listed (e, f) pairs, [n, H]."""
+    xb, gb, ix, ww, w1s, w2s, E, F = _bwd_args(x, topk_idx, topk_w, w1, w2, d_out)
+    T, H = xb.shape
+    pr = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+    cols = np.empty((pr.shape[0], H), np.float64)
+    _check(_load().oracle_backward_dw2_cols(T, H, F, E, ix.shape[1], interleave, float(clamp),
+                                            int(mask_bf16), _p(ix), _p(ww), _p(xb),
+                                            _expert_ptrs(w1s), _p(gb), pr.shape[0], _p(pr),
+                                            _p(cols)),
+           "oracle_backward_dw2_cols")
+    return cols

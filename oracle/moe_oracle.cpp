@@ -560,3 +560,371 @@ int oracle_moe_forward_lowprec(int T, int H, int F, int E, int k, int renormaliz
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward of the layer.  The Megatron-LM pages ("add permute fusion into
+// hybrid ep", "Support GEMM + Swiglu fused MLP") use the layer in training,
+// where the gradients of its inputs are needed; the pages print no backward
+// formulas, so these are the derivatives of the forward above, taken route by
+// route.  For a route (token t, slot j) to expert e with weight w:
+//   g_f, u_f = rows gate_row(f), up_row(f) of W1_e times x_t
+//   gc_f = min(g_f, c), uc_f = clamp(u_f, -c, c), h_f = silu(gc_f) uc_f
+//   y = W2_e h,  out_t = sum over the token's routes of w y
+// and with G = dL/d out_t:
+//   dy = w G,  dw = <G, y>
+//   dh_f = sum_n W2_e[n][f] dy[n]
+//   du_f = dh_f silu(gc_f)          where -c <= u_f <= c, else 0
+//   dg_f = dh_f uc_f silu'(gc_f)    where g_f <= c, else 0
+//   silu'(z) = s (1 + z (1 - s)),  s = 1 / (1 + exp(-z))
+//   dW2_e[n][f] += dy[n] h_f
+//   dW1_e[gate_row(f)][:] += dg_f x_t,  dW1_e[up_row(f)][:] += du_f x_t
+//   dx_t += sum_f dg_f W1_e[gate_row(f)] + du_f W1_e[up_row(f)]
+// Without a clamp both masks are 1.  The top-k selection is piecewise
+// constant and passes no gradient; the routing weights do (router backward
+// below).  mask_bf16 = 1 takes the two clamp decisions on g and u rounded to
+// bf16 (the precision a caller may keep the pre-activations in); 0 takes
+// them on the exact values.
+namespace {
+
+// Nearest bf16 value (8 significant bits), ties to even; normal range only.
+inline double round_bf16(double v) {
+  if (v == 0.0 || !std::isfinite(v)) return v;
+  int e = 0;
+  const double m = std::frexp(v, &e);  // |m| in [0.5, 1)
+  return std::ldexp(std::nearbyint(std::ldexp(m, 8)), e - 8);
+}
+
+inline double silu_grad(double z) {
+  const double s = 1.0 / (1.0 + std::exp(-z));
+  return s * (1.0 + z * (1.0 - s));
+}
+
+// Column f of the SwiGLU and its backward for one route.
+inline void swiglu_backward(double g, double u, double dh, double c, int mask_bf16, double* h,
+                            double* dg, double* du) {
+  double gc = g, uc = u;
+  bool pass_g = true, pass_u = true;
+  if (c > 0 && std::isfinite(c)) {
+    const double gm = mask_bf16 ? round_bf16(g) : g;
+    const double um = mask_bf16 ? round_bf16(u) : u;
+    pass_g = gm <= c;
+    pass_u = um >= -c && um <= c;
+    gc = std::fmin(g, c);
+    uc = std::fmax(std::fmin(u, c), -c);
+  }
+  *h = silu(gc) * uc;
+  *du = pass_u ? dh * silu(gc) : 0.0;
+  *dg = pass_g ? dh * uc * silu_grad(gc) : 0.0;
+}
+
+// Which output column f (and gate or up) row `row` of W1 holds: the inverse
+// of gate_row / up_row.
+inline long w1_row_column(long row, long F, long I, bool* is_gate) {
+  if (I == 0) {
+    *is_gate = row < F;
+    return row < F ? row : row - F;
+  }
+  const long block = row / I;
+  *is_gate = (block % 2) == 0;
+  return (block / 2) * I + row % I;
+}
+
+// Gate and up pre-activations of column f for the widened row xr.
+inline void preact(const double* xr, const uint16_t* W1, long H, long F, long I, long f,
+                   double* g, double* u) {
+  const uint16_t* wg = W1 + gate_row(f, F, I) * H;
+  const uint16_t* wu = W1 + up_row(f, F, I) * H;
+  double a = 0.0, b = 0.0;
+  for (long c = 0; c < H; ++c) {
+    a += xr[c] * bf16_value(wg[c]);
+    b += xr[c] * bf16_value(wu[c]);
+  }
+  *g = a;
+  *u = b;
+}
+
+// dh_f = sum_n W2[n][f] dy[n].
+inline double dh_at(const double* dy, const uint16_t* W2, long H, long F, long f) {
+  double acc = 0.0;
+  for (long n = 0; n < H; ++n) acc += bf16_value(W2[n * F + f]) * dy[n];
+  return acc;
+}
+
+// Every backward quantity of one route: the W1-row-ordered dA (2F), h (F),
+// dy (H) and dw = <G, y>.  Optionally adds the route's dx contribution.
+void route_backward(long H, long F, long I, double c, int mask_bf16, double w,
+                    const uint16_t* x_row, const uint16_t* g_row, const uint16_t* W1,
+                    const uint16_t* W2, double* dA, double* h, double* dy, double* dw,
+                    double* dx_add) {
+  std::vector<double> xr(H), G(H), gv(F), uv(F), y(H);
+  for (long c2 = 0; c2 < H; ++c2) {
+    xr[c2] = bf16_value(x_row[c2]);
+    G[c2] = bf16_value(g_row[c2]);
+  }
+  for (long f = 0; f < F; ++f) {
+    preact(xr.data(), W1, H, F, I, f, &gv[f], &uv[f]);
+    double hf, dg, du;
+    swiglu_backward(gv[f], uv[f], 0.0, c, mask_bf16, &hf, &dg, &du);
+    h[f] = hf;
+  }
+  double d = 0.0;
+  for (long n = 0; n < H; ++n) {
+    double acc = 0.0;
+    for (long f = 0; f < F; ++f) acc += bf16_value(W2[n * F + f]) * h[f];
+    y[n] = acc;
+    d += G[n] * acc;
+  }
+  *dw = d;
+  for (long n = 0; n < H; ++n) dy[n] = w * G[n];
+  for (long f = 0; f < F; ++f) {
+    const double dh = dh_at(dy, W2, H, F, f);
+    double hf, dg, du;
+    swiglu_backward(gv[f], uv[f], dh, c, mask_bf16, &hf, &dg, &du);
+    dA[gate_row(f, F, I)] = dg;
+    dA[up_row(f, F, I)] = du;
+  }
+  if (dx_add) {
+    for (long row = 0; row < 2 * F; ++row) {
+      const double a = dA[row];
+      if (a == 0.0) continue;
+      const uint16_t* wr = W1 + row * H;
+      for (long c2 = 0; c2 < H; ++c2) dx_add[c2] += a * bf16_value(wr[c2]);
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+// Expert backward for given routes.  topk_idx / topk_w are [T, slots] (-1 =
+// masked slot); expert e uses w1_experts[e] [2F, H] and w2_experts[e] [H, F]
+// (NULL allowed for an expert no route selects); d_out is G as bf16 [T, H].
+// Outputs (fp64): dx [T, H], dw_route [T, slots] (= <G_t, y> per route, 0 for
+// a masked slot), dw1 [E, 2F, H], dw2 [E, H, F].  Returns 0, -1 on bad sizes,
+// -2 on a route to an expert without weights or outside [-1, E).
+int oracle_moe_backward(int T, int H, int F, int E, int slots, int interleave, double clamp,
+                        int mask_bf16, const int32_t* topk_idx, const double* topk_w,
+                        const uint16_t* x, const uint16_t* const* w1_experts,
+                        const uint16_t* const* w2_experts, const uint16_t* d_out, double* dx,
+                        double* dw_route, double* dw1, double* dw2) {
+  if (T < 0 || H <= 0 || F <= 0 || E <= 0 || slots <= 0) return -1;
+  const long R = static_cast<long>(T) * slots, HH = H, FF = F;
+  for (long r = 0; r < R; ++r) {
+    const int e = topk_idx[r];
+    if (e < -1 || e >= E) return -2;
+    if (e >= 0 && (w1_experts[e] == nullptr || w2_experts[e] == nullptr)) return -2;
+  }
+  std::vector<double> dA(static_cast<size_t>(R) * 2 * FF, 0.0), hr(static_cast<size_t>(R) * FF, 0.0),
+      dy(static_cast<size_t>(R) * HH, 0.0), dxr(static_cast<size_t>(R) * HH, 0.0);
+#pragma omp parallel for schedule(dynamic)
+  for (long r = 0; r < R; ++r) {
+    const int e = topk_idx[r];
+    dw_route[r] = 0.0;
+    if (e < 0) continue;
+    const long t = r / slots;
+    route_backward(HH, FF, interleave, clamp, mask_bf16, topk_w[r], x + t * HH, d_out + t * HH,
+                   w1_experts[e], w2_experts[e], &dA[r * 2 * FF], &hr[r * FF], &dy[r * HH],
+                   &dw_route[r], &dxr[r * HH]);
+  }
+#pragma omp parallel for
+  for (long t = 0; t < T; ++t)
+    for (long c = 0; c < HH; ++c) {
+      double acc = 0.0;
+      for (int j = 0; j < slots; ++j) acc += dxr[(t * slots + j) * HH + c];
+      dx[t * HH + c] = acc;
+    }
+#pragma omp parallel for schedule(dynamic)
+  for (long er = 0; er < static_cast<long>(E) * 2 * FF; ++er) {
+    const long e = er / (2 * FF), row = er % (2 * FF);
+    double* out = dw1 + er * HH;
+    for (long c = 0; c < HH; ++c) out[c] = 0.0;
+    for (long r = 0; r < R; ++r) {
+      if (topk_idx[r] != e) continue;
+      const double a = dA[r * 2 * FF + row];
+      const uint16_t* xr = x + (r / slots) * HH;
+      for (long c = 0; c < HH; ++c) out[c] += a * bf16_value(xr[c]);
+    }
+  }
+#pragma omp parallel for schedule(dynamic)
+  for (long en = 0; en < static_cast<long>(E) * HH; ++en) {
+    const long e = en / HH, n = en % HH;
+    double* out = dw2 + en * FF;
+    for (long f = 0; f < FF; ++f) out[f] = 0.0;
+    for (long r = 0; r < R; ++r) {
+      if (topk_idx[r] != e) continue;
+      const double d = dy[r * HH + n];
+      for (long f = 0; f < FF; ++f) out[f] += d * hr[r * FF + f];
+    }
+  }
+  return 0;
+}
+
+// dx rows and per-route dw of the listed tokens only (the same definitions as
+// oracle_moe_backward, for sizes where the whole backward is too slow).
+//   tokens [n], dx_rows [n, H] (slots summed in order j = 0, 1, ...),
+//   dw_rows [n, slots].
+int oracle_backward_tokens(int T, int H, int F, int E, int slots, int interleave, double clamp,
+                           int mask_bf16, const int32_t* topk_idx, const double* topk_w,
+                           const uint16_t* x, const uint16_t* const* w1_experts,
+                           const uint16_t* const* w2_experts, const uint16_t* d_out, int n,
+                           const int32_t* tokens, double* dx_rows, double* dw_rows) {
+  if (T < 0 || H <= 0 || F <= 0 || E <= 0 || slots <= 0 || n < 0) return -1;
+  const long HH = H, FF = F;
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= T) return -1;
+  std::vector<double> part(static_cast<size_t>(n) * slots * HH, 0.0);
+#pragma omp parallel for schedule(dynamic)
+  for (long q = 0; q < static_cast<long>(n) * slots; ++q) {
+    const long i = q / slots, j = q % slots, t = tokens[i], r = t * slots + j;
+    dw_rows[q] = 0.0;
+    const int e = topk_idx[r];
+    if (e < 0 || e >= E || !w1_experts[e] || !w2_experts[e]) continue;
+    std::vector<double> dA(2 * FF), h(FF), dy(HH);
+    route_backward(HH, FF, interleave, clamp, mask_bf16, topk_w[r], x + t * HH, d_out + t * HH,
+                   w1_experts[e], w2_experts[e], dA.data(), h.data(), dy.data(), &dw_rows[q],
+                   &part[q * HH]);
+  }
+  for (long i = 0; i < n; ++i)
+    for (long c = 0; c < HH; ++c) {
+      double acc = 0.0;
+      for (long j = 0; j < slots; ++j) acc += part[(i * slots + j) * HH + c];
+      dx_rows[i * HH + c] = acc;
+    }
+  return 0;
+}
+
+// Whole rows of dW1 for the listed (expert, W1 row) pairs:
+//   dW1_e[row][:] = sum over the routes of e of dA[row] x_t   (rows [n, H]).
+int oracle_backward_dw1_rows(int T, int H, int F, int E, int slots, int interleave,
+                             double clamp, int mask_bf16, const int32_t* topk_idx,
+                             const double* topk_w, const uint16_t* x,
+                             const uint16_t* const* w1_experts,
+                             const uint16_t* const* w2_experts, const uint16_t* d_out, int n,
+                             const int32_t* pairs, double* rows) {
+  if (T < 0 || H <= 0 || F <= 0 || E <= 0 || slots <= 0 || n < 0) return -1;
+  const long HH = H, FF = F, R = static_cast<long>(T) * slots;
+  for (int i = 0; i < n; ++i) {
+    const int e = pairs[2 * i], row = pairs[2 * i + 1];
+    if (e < 0 || e >= E || row < 0 || row >= 2 * F) return -1;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int e = pairs[2 * i];
+    const long row = pairs[2 * i + 1];
+    bool is_gate = true;
+    const long f = w1_row_column(row, FF, interleave, &is_gate);
+    std::vector<long> routes;
+    for (long r = 0; r < R; ++r)
+      if (topk_idx[r] == e) routes.push_back(r);
+    std::vector<double> a(routes.size(), 0.0);
+    if (!routes.empty() && (!w1_experts[e] || !w2_experts[e])) return -2;
+#pragma omp parallel for schedule(dynamic)
+    for (long q = 0; q < static_cast<long>(routes.size()); ++q) {
+      const long r = routes[q], t = r / slots;
+      std::vector<double> xr(HH), dy(HH);
+      for (long c = 0; c < HH; ++c) {
+        xr[c] = bf16_value(x[t * HH + c]);
+        dy[c] = topk_w[r] * bf16_value(d_out[t * HH + c]);
+      }
+      double g, u, h, dg, du;
+      preact(xr.data(), w1_experts[e], HH, FF, interleave, f, &g, &u);
+      swiglu_backward(g, u, dh_at(dy.data(), w2_experts[e], HH, FF, f), clamp, mask_bf16, &h,
+                      &dg, &du);
+      a[q] = is_gate ? dg : du;
+    }
+#pragma omp parallel for
+    for (long c = 0; c < HH; ++c) {
+      double acc = 0.0;
+      for (size_t q = 0; q < routes.size(); ++q)
+        acc += a[q] * bf16_value(x[(routes[q] / slots) * HH + c]);
+      rows[i * HH + c] = acc;
+    }
+  }
+  return 0;
+}
+
+// Whole columns of dW2 for the listed (expert, f) pairs:
+//   dW2_e[:][f] = sum over the routes of e of w G_t h_f   (cols [n, H]).
+int oracle_backward_dw2_cols(int T, int H, int F, int E, int slots, int interleave,
+                             double clamp, int mask_bf16, const int32_t* topk_idx,
+                             const double* topk_w, const uint16_t* x,
+                             const uint16_t* const* w1_experts, const uint16_t* d_out, int n,
+                             const int32_t* pairs, double* cols) {
+  if (T < 0 || H <= 0 || F <= 0 || E <= 0 || slots <= 0 || n < 0) return -1;
+  const long HH = H, FF = F, R = static_cast<long>(T) * slots;
+  for (int i = 0; i < n; ++i) {
+    const int e = pairs[2 * i], f = pairs[2 * i + 1];
+    if (e < 0 || e >= E || f < 0 || f >= F) return -1;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int e = pairs[2 * i];
+    const long f = pairs[2 * i + 1];
+    std::vector<long> routes;
+    for (long r = 0; r < R; ++r)
+      if (topk_idx[r] == e) routes.push_back(r);
+    if (!routes.empty() && !w1_experts[e]) return -2;
+    std::vector<double> wh(routes.size(), 0.0);
+#pragma omp parallel for schedule(dynamic)
+    for (long q = 0; q < static_cast<long>(routes.size()); ++q) {
+      const long r = routes[q], t = r / slots;
+      std::vector<double> xr(HH);
+      for (long c = 0; c < HH; ++c) xr[c] = bf16_value(x[t * HH + c]);
+      double g, u, h, dg, du;
+      preact(xr.data(), w1_experts[e], HH, FF, interleave, f, &g, &u);
+      swiglu_backward(g, u, 0.0, clamp, mask_bf16, &h, &dg, &du);
+      wh[q] = topk_w[r] * h;
+    }
+#pragma omp parallel for
+    for (long nn = 0; nn < HH; ++nn) {
+      double acc = 0.0;
+      for (size_t q = 0; q < routes.size(); ++q)
+        acc += bf16_value(d_out[(routes[q] / slots) * HH + nn]) * wh[q];
+      cols[i * HH + nn] = acc;
+    }
+  }
+  return 0;
+}
+
+// Router backward: the gradient of the loss with respect to the logits given
+// dw = dL/d topk_w for the first k slots of each token (slots >= k are shared
+// experts with the constant weight 1 and pass nothing).
+//   renormalize = 1: dl_{e_j} = w_j (dw_j - sum_i w_i dw_i), 0 elsewhere;
+//   renormalize = 0: dl_e = p_e ([e selected by slot j] dw_j - sum_i w_i dw_i),
+//                    p = softmax of the token's E logits (fp64).
+// A masked slot (-1) is left out of both sums.  dlogits [T, E] fp64.
+int oracle_router_backward(int T, int E, int k, int slots, int renormalize, const float* logits,
+                           const int32_t* topk_idx, const double* topk_w, const double* dw,
+                           double* dlogits) {
+  if (T < 0 || E <= 0 || k <= 0 || slots < k) return -1;
+#pragma omp parallel for
+  for (long t = 0; t < T; ++t) {
+    double* dl = dlogits + t * E;
+    for (int e = 0; e < E; ++e) dl[e] = 0.0;
+    double s = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const long r = t * slots + j;
+      if (topk_idx[r] >= 0) s += topk_w[r] * dw[r];
+    }
+    if (renormalize) {
+      for (int j = 0; j < k; ++j) {
+        const long r = t * slots + j;
+        if (topk_idx[r] >= 0) dl[topk_idx[r]] = topk_w[r] * (dw[r] - s);
+      }
+    } else {
+      const float* l = logits + t * E;
+      double lmax = l[0];
+      for (int e = 1; e < E; ++e) lmax = std::fmax(lmax, static_cast<double>(l[e]));
+      double denom = 0.0;
+      for (int e = 0; e < E; ++e) denom += std::exp(static_cast<double>(l[e]) - lmax);
+      for (int e = 0; e < E; ++e) dl[e] = -(std::exp(static_cast<double>(l[e]) - lmax) / denom) * s;
+      for (int j = 0; j < k; ++j) {
+        const long r = t * slots + j;
+        const int e = topk_idx[r];
+        if (e >= 0) dl[e] += std::exp(static_cast<double>(l[e]) - lmax) / denom * dw[r];
+      }
+    }
+  }
+  return 0;
+}
+
+}  // extern "C"
