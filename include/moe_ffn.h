@@ -227,6 +227,36 @@ MOE_API int moe_forward_routed(const moe_problem* p, const void* x, const int32_
                                int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes,
                                void* stream);
 
+/* ---- Backward (bf16 precision) -------------------------------------------
+ * Gradients of a scalar loss L given G = dL/d out, for the layer moe_forward
+ * computes (training use: the Megatron-LM pages, "add permute fusion into
+ * hybrid ep" and "Support GEMM + Swiglu fused MLP", place the layer in
+ * training; they print no backward formulas, so these are the derivatives of
+ * the forward).  Per route (token t, expert e, weight w), with g, u the gate
+ * and up pre-activations, gc = min(g, c), uc = clamp(u, -c, c) and
+ * h = silu(gc) uc:
+ *   dh = W2_e^T (w G_t);  du = dh silu(gc) [-c <= u <= c];
+ *   dg = dh uc silu'(gc) [g <= c];  dW2_e += (w G_t) h^T;
+ *   dW1_e += [dg | du] x_t^T (rows per glu_interleave);  dx_t += W1_e^T [dg | du];
+ *   d w = <G_t, y>, then the softmax backward of the routing weights
+ *   (renormalize = 1: over the selected logits; 0: over all E).
+ * The top-k selection passes no gradient.  The forward's intermediates are
+ * recomputed, not stored: the pre-activations x W1_e^T are recomputed in fp32
+ * and the clamp decisions are taken on those fp32 values.  Every output is
+ * written by one thread in a fixed order (no atomics): bitwise reproducible.
+ *   x [T, H] bf16, logits [T, E] fp32, w1 [E+S, 2F, H] bf16,
+ *   w2 [E+S, H, F] bf16, d_out [T, H] bf16 (G);
+ *   dx [T, H] bf16 out; d_logits [T, E] fp32 out (NULL to skip);
+ *   dw1 [E+S, 2F, H] bf16 out, dw2 [E+S, H, F] bf16 out (shared experts
+ *   included; an expert no token selects gets zero gradients);
+ *   ws of at least moe_backward_workspace_size(p) bytes.
+ * p->precision must be MOE_PREC_BF16; p->fusion and p->kernel are ignored. */
+MOE_API size_t moe_backward_workspace_size(const moe_problem* p);
+MOE_API int moe_backward(const moe_problem* p, const void* x, const float* logits,
+                         const void* w1, const void* w2, const void* d_out, void* dx,
+                         float* d_logits, void* dw1, void* dw2, void* ws, size_t ws_bytes,
+                         void* stream);
+
 /* Self-test of the bounded waits (the pages have no counterpart: this checks
  * the library's own failure detection).  Launches one CTA that waits on an
  * mbarrier nothing arrives on, through the same bounded wait every kernel
@@ -349,13 +379,15 @@ MOE_API int moe_selected_kernel(const moe_problem* p);
  * enqueued (for launch accounting in benchmarks). */
 MOE_API int moe_last_launch_count(void);
 
-/* Per-stage timing of moe_forward with CUDA events (for benchmarks).
- * moe_stage_timing_begin(n) makes the next n moe_forward calls on this
- * thread record an event on their stream before each stage and after the
- * last (events created once, reused); moe_stage_timing_end synchronises the
- * device, writes the average milliseconds of each stage over the recorded
- * calls into ms[0 .. *n_stages) (at most max_stages entries) and stops
- * recording.  Stage i is named by moe_stage_name(i).  Returns a status. */
+/* Per-stage timing of moe_forward / moe_backward with CUDA events (for
+ * benchmarks).  moe_stage_timing_begin(n) makes the next n moe_forward or
+ * moe_backward calls on this thread record an event on their stream before
+ * each stage and after the last (events created once, reused);
+ * moe_stage_timing_end synchronises the device, writes the average
+ * milliseconds of each stage over the recorded calls into ms[0 .. *n_stages)
+ * (at most max_stages entries) and stops recording.  Stage i is named by
+ * moe_stage_name(i), for the entry point recorded last (time one kind of
+ * call per session).  Returns a status. */
 MOE_API int moe_stage_timing_begin(int n_calls);
 MOE_API int moe_stage_timing_end(float* ms, int max_stages, int* n_stages, int* n_calls);
 MOE_API const char* moe_stage_name(int i);

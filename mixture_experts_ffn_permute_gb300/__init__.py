@@ -90,6 +90,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_forward": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_forward_routed": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_selftest_wait_timeout": ([vp, ctypes.c_uint64, vp], ci),
+        "moe_backward_workspace_size": ([pp], sz),
+        "moe_backward": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_get_device_status": ([vp, vp], ci),
         "moe_clear_device_status": ([vp, vp], ci),
         "moe_last_launch_count": ([], ci),
@@ -224,6 +226,29 @@ def forward_routed(p: Problem, x, topk_idx, topk_w, w1, w2, out, ws, tokens_per_
     """The layer with caller-supplied routing (int32 [T, k], -1 = masked; fp32 [T, k])."""
     _call("moe_forward_routed", ctypes.byref(p), _ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(w1),
           _ptr(w2), _ptr(out), _ptr(tokens_per_expert), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def backward_workspace_size(p: Problem) -> int:
+    return int(load().moe_backward_workspace_size(ctypes.byref(p)))
+
+
+def alloc_backward_workspace(p: Problem, device="cuda") -> torch.Tensor:
+    """A uint8 device tensor sized by moe_backward_workspace_size (256-byte aligned)."""
+    n = backward_workspace_size(p)
+    if n == 0:
+        raise MoEError("moe_backward_workspace_size", 1)
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def backward(p: Problem, x, logits, w1, w2, d_out, dx, dw1, dw2, ws, d_logits=None,
+             stream=None) -> None:
+    """Gradients of the layer given d_out = dL/d out: dx [T, H] bf16,
+    d_logits [T, E] fp32 (optional), dw1 / dw2 bf16 in the weights' shapes."""
+    _call("moe_backward", ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(w1), _ptr(w2),
+          _ptr(d_out), _ptr(dx), _ptr(d_logits), _ptr(dw1), _ptr(dw2), _ptr(ws), ws.numel(),
+          _stream(stream))
 
 
 def selftest_wait_timeout(ws, limit_ns: int, stream=None) -> None:

@@ -35,21 +35,28 @@ namespace {
 
 thread_local int g_launches = 0;
 
-// Stage names of moe_forward, in launch order.
-constexpr int kNumStages = 8;
-const char* const kStageNames[kNumStages] = {"route_topk", "chunk_histogram", "scan",
+// Stage names of moe_forward and moe_backward, in launch order.
+constexpr int kFwdStages = 8;
+constexpr int kBwdStages = 10;
+constexpr int kMaxStages = 10;
+const char* const kStageNames[kFwdStages] = {"route_topk", "chunk_histogram", "scan",
                                              "scatter",    "gather_rows",     "gemm1_swiglu",
                                              "gemm2",      "combine"};
+const char* const kBwdStageNames[kBwdStages] = {
+    "route_topk",    "permute", "gather_rows", "gemm1_recompute", "dgrad_h_swiglu",
+    "wgrad_w2",      "dgrad_x", "wgrad_w1",    "combine_dx",      "router_backward"};
 
-// Event ring for moe_stage_timing_begin/end (one row of kNumStages+1 events
-// per recorded call).
+// Event ring for moe_stage_timing_begin/end (one row of kMaxStages+1 events
+// per recorded call).  `kind` is the entry point last recorded (0 forward,
+// 1 backward).
 struct StageTimer {
   bool on = false;
   int capacity = 0;
   int used = 0;
+  int kind = 0;
   cudaEvent_t* ev = nullptr;
   void mark(int call, int i, cudaStream_t s) {
-    if (on && call < capacity) cudaEventRecord(ev[call * (kNumStages + 1) + i], s);
+    if (on && call < capacity) cudaEventRecord(ev[call * (kMaxStages + 1) + i], s);
   }
 };
 thread_local StageTimer g_timer;
@@ -100,6 +107,34 @@ Layout layout_of(const moe_problem& p0) {
   L.y = take(2 * R * static_cast<size_t>(p.H));
   L.total = o;
   return L;
+}
+
+// The backward's workspace: the forward's regions (routing, x_perm; y holds
+// the permuted output gradient, h the weighted activations w*h) plus the fp32
+// pre-activations, their bf16 gradient, the routing weight of each permuted
+// row and the per-(row, 256-column tile) partials of the router gradient.
+struct BwdLayout {
+  Layout f;
+  size_t act, dact, w_perm, dw_part, total;
+};
+
+BwdLayout bwd_layout_of(const moe_problem& p0) {
+  const moe_problem p = expanded(p0);
+  const size_t R = static_cast<size_t>(p.T) * p.k, F = p.F;
+  BwdLayout B;
+  B.f = layout_of(p0);
+  size_t o = B.f.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  B.act = take(sizeof(float) * R * 2 * F);
+  B.dact = take(2 * R * 2 * F);
+  B.w_perm = take(sizeof(float) * R);
+  B.dw_part = take(sizeof(float) * R * ((F + kBN - 1) / kBN));
+  B.total = o;
+  return B;
 }
 
 template <typename T>
@@ -482,6 +517,7 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
+  if (tm.on) tm.kind = 0;
   tm.mark(call, 0, s);
   if (!fuse_combine && route_permute_tiny_fits(p->T, p->E, p->k, S)) {
     // the smallest decode steps: routing, permutation and (few rows) the
@@ -561,6 +597,173 @@ int moe_forward_routed(const moe_problem* p, const void* x, const int32_t* topk_
   rc = run_mlp(p, x_perm, off, mtp, w1, w2, h, y, status, s, launches);
   if (rc != MOE_OK) return rc;
   MOE_LAUNCH(launch_combine(y, rmap, topk_w, p->T, p->H, p->k, out, s));
+  g_launches = launches;
+  return MOE_OK;
+}
+
+size_t moe_backward_workspace_size(const moe_problem* p) {
+  if (check_full(p) != MOE_OK || p->precision != MOE_PREC_BF16) return 0;
+  return bwd_layout_of(*p).total;
+}
+
+int moe_backward(const moe_problem* p, const void* x, const float* logits, const void* w1,
+                 const void* w2, const void* d_out, void* dx, float* d_logits, void* dw1,
+                 void* dw2, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
+  const BwdLayout B = bwd_layout_of(*p);
+  if (ws_bytes < B.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  MOE_REQUIRE_PTR(w1);
+  MOE_REQUIRE_PTR(w2);
+  MOE_REQUIRE_PTR(dw1);
+  MOE_REQUIRE_PTR(dw2);
+  if (d_logits && !aligned16(d_logits)) return MOE_ERR_MISALIGNED;
+  const Layout& L = B.f;
+  const moe_problem pe = expanded(*p);  // after routing: E+S experts, k+S slots
+  const moe_problem* q = &pe;
+  const int S = p->shared_experts;
+  int launches = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t w1_bytes = sizeof(uint16_t) * q->E * 2 * static_cast<size_t>(q->F) * q->H;
+  const size_t w2_bytes = sizeof(uint16_t) * q->E * static_cast<size_t>(q->H) * q->F;
+  if (p->T == 0) {  // no routes: the weight gradients are zero
+    MOE_LAUNCH(cudaMemsetAsync(dw1, 0, w1_bytes, s));
+    MOE_LAUNCH(cudaMemsetAsync(dw2, 0, w2_bytes, s));
+    g_launches = launches;
+    return MOE_OK;
+  }
+  MOE_REQUIRE_PTR(x);
+  MOE_REQUIRE_PTR(logits);
+  MOE_REQUIRE_PTR(d_out);
+  MOE_REQUIRE_PTR(dx);
+  const int R = q->T * q->k;
+  const int H = q->H, F = q->F;
+  int32_t* idx = at<int32_t>(ws, L.topk_idx);
+  float* wts = at<float>(ws, L.topk_w);
+  int32_t* tpe = at<int32_t>(ws, L.tokens_per_expert);
+  int32_t* off = at<int32_t>(ws, L.expert_offsets);
+  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
+  int32_t* rmap = at<int32_t>(ws, L.row_id_map);
+  int32_t* ptok = at<int32_t>(ws, L.permuted_token);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* hw = at<void>(ws, L.h);      // [R, F] w * h
+  void* dy = at<void>(ws, L.y);      // [R, H] permuted output gradient, later dXp
+  float* act = at<float>(ws, B.act);  // [R, 2F] fp32 pre-activations
+  void* dact = at<void>(ws, B.dact);  // [R, 2F] bf16 their gradient
+  float* w_perm = at<float>(ws, B.w_perm);
+  float* dw_part = at<float>(ws, B.dw_part);
+  const int n_parts = ceil_div(F, kBN);
+
+  const int call = g_timer.on ? g_timer.used++ : 0;
+  StageTimer& tm = g_timer;
+  if (tm.on) tm.kind = 1;
+  tm.mark(call, 0, s);
+  // the forward's routing and permutation
+  MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s, S));
+  tm.mark(call, 1, s);
+  if (permute_small_fits(q->T, q->E, q->k)) {
+    MOE_LAUNCH(launch_permute_small(idx, q->T, q->E, q->k, tpe, off, mtp, rmap, ptok, s));
+  } else {
+    rc = run_permute(q, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches);
+    if (rc != MOE_OK) return rc;
+  }
+  tm.mark(call, 2, s);
+  MOE_LAUNCH(launch_gather_rows(x, ptok, R, H, x_perm, s));
+  MOE_LAUNCH(launch_gather_rows(d_out, ptok, R, H, dy, s));
+  MOE_LAUNCH(launch_weights_to_rows(rmap, wts, R, w_perm, s));
+  tm.mark(call, 3, s);
+  // pre-activations a = x W1_e^T in fp32, recomputed rather than kept from
+  // the forward
+  BwdGemmArgs ga{};
+  ga.mode = kBwdPreact;
+  ga.a = x_perm;
+  ga.b = w1;
+  ga.R = R;
+  ga.E = q->E;
+  ga.K = H;
+  ga.N = 2 * F;
+  ga.expert_offsets = off;
+  ga.mtile_prefix = mtp;
+  ga.out = act;
+  ga.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(ga, s));
+  tm.mark(call, 4, s);
+  // dh = dY W2_e, then the SwiGLU backward: dA, w*h, router partials
+  BwdGemmArgs g{};
+  g.mode = kBwdDataSwiGLU;
+  g.a = dy;
+  g.b = w2;
+  g.R = R;
+  g.E = q->E;
+  g.K = H;
+  g.N = F;
+  g.expert_offsets = off;
+  g.mtile_prefix = mtp;
+  g.act = act;
+  g.dact = dact;
+  g.hw = hw;
+  g.dw_part = dw_part;
+  g.w_perm = w_perm;
+  g.F = F;
+  g.interleave = p->glu_interleave;
+  g.clamp = clamp_of(p);
+  g.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(g, s));
+  tm.mark(call, 5, s);
+  // dW2_e = dY_e^T (w h)_e
+  BwdGemmArgs gw2{};
+  gw2.mode = kBwdWeight;
+  gw2.a = dy;
+  gw2.b = hw;
+  gw2.R = R;
+  gw2.E = q->E;
+  gw2.M = H;
+  gw2.N = F;
+  gw2.expert_offsets = off;
+  gw2.out = dw2;
+  gw2.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(gw2, s));
+  tm.mark(call, 6, s);
+  // dXp = dA W1_e (into dY's region, no longer needed)
+  BwdGemmArgs gx{};
+  gx.mode = kBwdDataPlain;
+  gx.a = dact;
+  gx.b = w1;
+  gx.R = R;
+  gx.E = q->E;
+  gx.K = 2 * F;
+  gx.N = H;
+  gx.expert_offsets = off;
+  gx.mtile_prefix = mtp;
+  gx.out = dy;
+  gx.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(gx, s));
+  tm.mark(call, 7, s);
+  // dW1_e = dA_e^T x_e
+  BwdGemmArgs gw1{};
+  gw1.mode = kBwdWeight;
+  gw1.a = dact;
+  gw1.b = x_perm;
+  gw1.R = R;
+  gw1.E = q->E;
+  gw1.M = 2 * F;
+  gw1.N = H;
+  gw1.expert_offsets = off;
+  gw1.out = dw1;
+  gw1.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(gw1, s));
+  tm.mark(call, 8, s);
+  // dx_t = sum over the token's routes of dXp (weights already applied)
+  MOE_LAUNCH(launch_combine(dy, rmap, nullptr, q->T, H, q->k, dx, s));
+  tm.mark(call, 9, s);
+  if (d_logits)
+    MOE_LAUNCH(launch_router_backward(logits, idx, wts, rmap, dw_part, n_parts, p->T, p->E,
+                                      p->k, q->k, p->renormalize ? 1 : 0, d_logits, s));
+  tm.mark(call, 10, s);
   g_launches = launches;
   return MOE_OK;
 }
@@ -768,11 +971,11 @@ int moe_stage_timing_begin(int n_calls) {
   StageTimer& t = g_timer;
   if (n_calls > t.capacity) {
     if (t.ev) {
-      for (int i = 0; i < t.capacity * (kNumStages + 1); ++i) cudaEventDestroy(t.ev[i]);
+      for (int i = 0; i < t.capacity * (kMaxStages + 1); ++i) cudaEventDestroy(t.ev[i]);
       delete[] t.ev;
     }
-    t.ev = new cudaEvent_t[n_calls * (kNumStages + 1)];
-    for (int i = 0; i < n_calls * (kNumStages + 1); ++i)
+    t.ev = new cudaEvent_t[n_calls * (kMaxStages + 1)];
+    for (int i = 0; i < n_calls * (kMaxStages + 1); ++i)
       if (cudaEventCreate(&t.ev[i]) != cudaSuccess) return MOE_ERR_CUDA;
     t.capacity = n_calls;
   }
@@ -786,14 +989,15 @@ int moe_stage_timing_end(float* ms, int max_stages, int* n_stages, int* n_calls)
   t.on = false;
   const int calls = t.used < t.capacity ? t.used : t.capacity;
   if (n_calls) *n_calls = calls;
-  if (n_stages) *n_stages = kNumStages;
+  const int nst = t.kind ? kBwdStages : kFwdStages;
+  if (n_stages) *n_stages = nst;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
-  for (int i = 0; i < kNumStages && i < max_stages; ++i) {
+  for (int i = 0; i < nst && i < max_stages; ++i) {
     double acc = 0.0;
     for (int c = 0; c < calls; ++c) {
       float v = 0.f;
-      if (cudaEventElapsedTime(&v, t.ev[c * (kNumStages + 1) + i],
-                               t.ev[c * (kNumStages + 1) + i + 1]) != cudaSuccess)
+      if (cudaEventElapsedTime(&v, t.ev[c * (kMaxStages + 1) + i],
+                               t.ev[c * (kMaxStages + 1) + i + 1]) != cudaSuccess)
         return MOE_ERR_CUDA;
       acc += v;
     }
@@ -803,7 +1007,8 @@ int moe_stage_timing_end(float* ms, int max_stages, int* n_stages, int* n_calls)
 }
 
 const char* moe_stage_name(int i) {
-  return (i >= 0 && i < kNumStages) ? kStageNames[i] : "";
+  if (g_timer.kind) return (i >= 0 && i < kBwdStages) ? kBwdStageNames[i] : "";
+  return (i >= 0 && i < kFwdStages) ? kStageNames[i] : "";
 }
 
 }  // extern "C"

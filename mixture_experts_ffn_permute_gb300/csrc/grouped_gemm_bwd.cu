@@ -1,0 +1,568 @@
+// Grouped GEMMs of the layer's backward on the sm_103a tensor cores (tcgen05
+// + TMEM + TMA).  The backward needs every operand in the layout the forward
+// stored it in, so the tiles are read as the MMA wants them instead of being
+// transposed in memory first:
+//
+//   recomputed forward (ragged M)
+//     a   = Xp W1_e^T A = Xp [R, H], B = W1_e [2F, H], both K-major; the
+//                     pre-activations are kept in fp32
+//   data gradients (ragged M: the permuted rows of each expert)
+//     dH  = dY W2_e   A = dY [R, H] K-major; B = W2_e [H, F] read MN-major
+//                     epilogue: SwiGLU backward -- reads the fp32
+//                     pre-activations, writes dA (bf16), h_w = w h, and the
+//                     per-route partial <dh, h> of the router gradient
+//     dXp = dA W1_e   A = dA [R, 2F] K-major; B = W1_e [2F, H] read MN-major
+//   weight gradients (ragged K: the contraction runs over an expert's rows)
+//     dW2_e = dY_e^T h_w_e   A = dY [R, H], B = h_w [R, F], both read MN-major
+//     dW1_e = dA_e^T Xp_e    A = dA [R, 2F], B = Xp [R, H], both read MN-major
+//
+// An MN-major operand tile comes from a row-major [K rows, MN cols] matrix as
+// TMA boxes of 64 columns x 64 rows with the 128-byte swizzle: 128-byte rows
+// hold 64 consecutive MN elements of one k, 8-row groups are 1024 bytes apart
+// (the descriptor's stride offset) and the next 64 MN columns sit one box
+// (8 KB) further (its leading offset).  One K=16 MMA step is 16 rows = 2 KB.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over the tile list):
+//   warp 0      TMA producer, 4-stage ring of 48 KB (A 16 KB + B 32 KB)
+//   warp 1      TMEM allocation + MMA issue (lane 0); in the weight-gradient
+//               kernel the whole warp first zeroes the rows of a ragged last
+//               K step that belong to the next expert
+//   warps 2..5  epilogue (TMEM lanes 32*(warp%4) ..), two 256-column
+//               accumulators so a tile's epilogue overlaps the next mainloop
+// Every wait is bounded (ptx.cuh).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "../../include/moe_ffn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+// 2-D bf16 tensor map, boxes of 64 columns x box_rows rows, 128-byte swizzle
+// (grouped_gemm.cu).
+bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);
+
+namespace {
+
+constexpr int kStagesB = 4;
+constexpr int kThreadsB = 192;
+constexpr uint32_t kABytesB = kBM * kBK * 2;             // 16 KB
+constexpr uint32_t kBBytesB = kBN * kBK * 2;             // 32 KB
+constexpr uint32_t kStageBytesB = kABytesB + kBBytesB;   // 48 KB
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;              // one MN-major box, 8 KB
+constexpr uint32_t kStepBytesMN = 16 * 128;              // one K=16 step of an MN-major tile
+constexpr uint32_t kTmemColsB = 2 * kBN;
+constexpr int kMaxEB = MOE_MAX_EXPERTS;
+static_assert((2 * kStagesB + 5) * 8 + 8 <= 256, "barrier area");
+constexpr size_t kSmemBytesB = 1024 + kStagesB * kStageBytesB + 256 +
+                               2 * (kMaxEB + 1) * sizeof(int32_t);
+static_assert(kSmemBytesB <= 232448, "shared memory budget");
+
+enum class BwdMode : int { kDataPlain = 0, kDataSwiGLU = 1, kWeight = 2, kPreact = 3 };
+
+struct BwdParams {
+  const int32_t* expert_offsets;  // [E + 1]
+  const int32_t* mtile_prefix;    // [E + 1] (data gradients)
+  int E;
+  int K;        // data gradients: contraction length (rows of B per expert)
+  int N;        // output columns
+  int n_tiles;  // ceil(N / 256)
+  int M;        // weight gradients: output rows per expert
+  int m_tiles;  // M / 128
+  uint4* out;   // data: [R, N] bf16; weight: [E, M, N] bf16; pre-activations [R, N] fp32
+  int ldo_vec;  // N / 8 (bf16) or N / 4 (fp32)
+  // SwiGLU backward
+  const float4* act;     // [R, 2F] fp32 pre-activations
+  int act_vec;           // 2F / 4
+  uint4* dact;           // [R, 2F] bf16 out: dA
+  int dact_vec;          // 2F / 8
+  uint4* hw;             // [R, F] bf16: w * h
+  float* dw_part;        // [R, n_tiles]: partial <dh, h>
+  const float* w_perm;   // [R] routing weight of each permuted row
+  int F, interleave;
+  float clamp;           // > 0: clamp value, else none
+  uint32_t* status;
+};
+
+struct BTile {
+  int e, m, n;
+};
+
+__device__ __forceinline__ int find_expert_b(const int32_t* mtp, int E, int q) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (mtp[mid] <= q) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <BwdMode kMode>
+__device__ __forceinline__ BTile decode_btile(int tile, const int32_t* mtp, const BwdParams& p) {
+  BTile t;
+  if (kMode == BwdMode::kWeight) {
+    const int per = p.m_tiles * p.n_tiles;
+    t.e = tile / per;
+    const int local = tile - t.e * per;
+    t.n = local / p.m_tiles;  // m-tiles of one n-tile adjacent: B columns shared from L2
+    t.m = local - t.n * p.m_tiles;
+  } else {
+    const int q = tile / p.n_tiles;
+    t.e = find_expert_b(mtp, p.E, q);
+    const int mt = mtp[t.e + 1] - mtp[t.e];
+    const int local = tile - mtp[t.e] * p.n_tiles;
+    t.n = local / mt;  // m-tiles of one n-tile adjacent: the weight tile is reused from L2
+    t.m = local - t.n * mt;
+  }
+  return t;
+}
+
+// Shared-memory descriptor of an MN-major tile stored as 64-column boxes with
+// the 128-byte swizzle (see the file comment): leading offset = one box,
+// stride offset = 8 rows of 128 bytes.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(kBoxBytes >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// Instruction descriptor with the MN-major (transposed) operand bits.
+__host__ __device__ constexpr uint32_t idesc_bwd(bool a_mn, bool b_mn) {
+  return idesc_bf16_f32(kBM, kBN) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16);
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Column of W1 (and of the pre-activation row) holding gate (resp. up) output
+// f: interleave 0 -> [gate | up] halves; I -> blocks of I gate then I up.
+__device__ __forceinline__ int gate_col(int f, int F, int I) {
+  return I == 0 ? f : (f / I) * 2 * I + f % I;
+}
+__device__ __forceinline__ int up_col(int f, int F, int I) {
+  return I == 0 ? F + f : (f / I) * 2 * I + f % I + I;
+}
+
+template <BwdMode kMode>
+__global__ void __launch_bounds__(kThreadsB, 1)
+grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_b, const BwdParams p) {
+  pdl_enter();
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStagesB * kABytesB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStagesB * kBBytesB);
+  uint64_t* empty = full + kStagesB;
+  uint64_t* tfull = empty + kStagesB;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStagesB * kStageBytesB + 256);
+  int32_t* s_mtp = s_off + (p.E + 1);
+
+  constexpr bool kWeightGrad = kMode == BwdMode::kWeight;
+  constexpr bool kBKMajor = kMode == BwdMode::kPreact;  // B = weight rows, K-major
+  constexpr uint32_t kIdescB = idesc_bwd(kWeightGrad, !kBKMajor);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i <= p.E; i += kThreadsB) {
+    s_off[i] = p.expert_offsets[i];
+    s_mtp[i] = kWeightGrad ? 0 : p.mtile_prefix[i];
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesB; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&map_a);
+    prefetch_tensormap(&map_b);
+  }
+  if (warp == 1) tmem_alloc<kTmemColsB>(tmem_slot);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_tiles = kWeightGrad ? p.E * p.m_tiles * p.n_tiles : s_mtp[p.E] * p.n_tiles;
+  auto rows_of = [&](int e) { return s_off[e + 1] - s_off[e]; };
+  auto ksteps = [&](const BTile& t) {
+    return kWeightGrad ? (rows_of(t.e) + kBK - 1) / kBK : p.K / kBK;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        if (*abort_flag) break;
+        const BTile t = decode_btile<kMode>(tile, s_mtp, p);
+        const int nk = ksteps(t);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], kStageBytesB);
+          uint8_t* a_dst = sA + stage * kABytesB;
+          uint8_t* b_dst = sB + stage * kBBytesB;
+          int brow;
+          if (kWeightGrad) {
+            brow = s_off[t.e] + kb * kBK;  // the expert's rows are the contraction
+            tma_load_2d(a_dst, &map_a, t.m * kBM, brow, &full[stage], pol);
+            tma_load_2d(a_dst + kBoxBytes, &map_a, t.m * kBM + 64, brow, &full[stage], pol);
+          } else {
+            tma_load_2d(a_dst, &map_a, kb * kBK, s_off[t.e] + t.m * kBM, &full[stage], pol);
+            brow = t.e * p.K + kb * kBK;  // rows of the expert's weight matrix
+          }
+          if (kBKMajor) {  // 256 weight rows x 64 K in one box
+            tma_load_2d(b_dst, &map_b, kb * kBK, t.e * p.N + t.n * kBN, &full[stage], pol);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              tma_load_2d(b_dst + i * kBoxBytes, &map_b, t.n * kBN + 64 * i, brow, &full[stage],
+                          pol);
+          }
+          ++issued;
+          if (++stage == kStagesB) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) { *abort_flag = 1; break; }
+      }
+      // Leave no bulk copy in flight: wait for the last fill of every stage.
+      for (int i = 1; i <= kStagesB && i <= issued; ++i) {
+        int s = stage - i;
+        uint32_t ph = phase;
+        if (s < 0) { s += kStagesB; ph ^= 1; }
+        mbar_wait(&full[s], ph, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const int buf = local & 1;
+      const uint32_t tph = (local >> 1) & 1;
+      const BTile t = decode_btile<kMode>(tile, s_mtp, p);
+      const int nk = ksteps(t);
+      int ok = lane == 0 ? (mbar_wait(&tempty[buf], tph ^ 1, p.status) ? 1 : 0) : 1;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * kBN;
+      for (int kb = 0; kb < nk; ++kb) {
+        ok = lane == 0 ? (mbar_wait(&full[stage], phase, p.status) ? 1 : 0) : 1;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (kWeightGrad) {
+          const int valid = rows_of(t.e) - kb * kBK;
+          if (valid < kBK) {
+            // rows valid..63 of each of the six boxes are the next expert's
+            // (or past the matrix): zero them, then hand the writes to the
+            // async proxy the MMA reads through
+            __syncwarp();
+            const int per_box = (kBK - valid) * 8;  // 16-byte vectors per box
+            for (int i = lane; i < 6 * per_box; i += 32) {
+              const int b = i / per_box, v = i - b * per_box;
+              uint8_t* box = b < 2 ? sA + stage * kABytesB + b * kBoxBytes
+                                   : sB + stage * kBBytesB + (b - 2) * kBoxBytes;
+              reinterpret_cast<uint4*>(box + valid * 128)[v] = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_shared();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * kABytesB);
+          const uint32_t b_addr = smem_u32(sB + stage * kBBytesB);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t a_desc = kWeightGrad
+                                        ? sw128_mnmajor_desc(a_addr + kk * kStepBytesMN)
+                                        : sw128_kmajor_desc(a_addr) + 2 * kk;
+            const uint64_t b_desc = kBKMajor ? sw128_kmajor_desc(b_addr) + 2 * kk
+                                             : sw128_mnmajor_desc(b_addr + kk * kStepBytesMN);
+            mma_bf16_ss(d_tmem, a_desc, b_desc, kIdescB, (kb | kk) != 0);
+          }
+          mma_commit(&empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == kStagesB) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      // an expert without rows commits no MMA: the epilogue writes zeros
+      if (lane == 0) mma_commit(&tfull[buf]);
+      __syncwarp();
+    }
+    if (lane == 0) {
+      // All MMAs of this CTA done before TMEM is released.
+      mma_commit(drain);
+      mbar_wait(drain, 0, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quad * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      const int buf = local & 1;
+      const uint32_t tph = (local >> 1) & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], tph, p.status));
+      if (!ok) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const BTile t = decode_btile<kMode>(tile, s_mtp, p);
+      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN;
+      const int col0 = t.n * kBN;
+      if (kMode == BwdMode::kWeight) {
+        const long orow = static_cast<long>(t.e) * p.M + t.m * kBM + row_in_tile;
+        uint4* dst = p.out + orow * p.ldo_vec + col0 / 8;
+        const bool none = rows_of(t.e) == 0;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
+          uint32_t a[32];
+          if (none) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = 0u;
+          } else {
+            tmem_ld_32x32b_x32(t_lane + c * 32, a);
+            tmem_ld_wait();
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[c * 4 + v] = make_uint4(
+                pack2_bf16(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
+                pack2_bf16(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3])),
+                pack2_bf16(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5])),
+                pack2_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
+        }
+      } else {
+        const bool row_ok = t.m * kBM + row_in_tile < rows_of(t.e);
+        const long out_row = static_cast<long>(s_off[t.e]) + t.m * kBM + row_in_tile;
+        if (kMode == BwdMode::kPreact) {
+          float4* dst = reinterpret_cast<float4*>(p.out) + out_row * p.ldo_vec + col0 / 4;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
+            uint32_t a[32];
+            tmem_ld_32x32b_x32(t_lane + c * 32, a);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[c * 8 + v] = make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
+                                             __uint_as_float(a[4 * v + 2]),
+                                             __uint_as_float(a[4 * v + 3]));
+            }
+          }
+        } else if (kMode == BwdMode::kDataPlain) {
+          uint4* dst = p.out + out_row * p.ldo_vec + col0 / 8;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
+            uint32_t a[32];
+            tmem_ld_32x32b_x32(t_lane + c * 32, a);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[c * 4 + v] = make_uint4(
+                    pack2_bf16(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
+                    pack2_bf16(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3])),
+                    pack2_bf16(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5])),
+                    pack2_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
+            }
+          }
+        } else {
+          // SwiGLU backward of 32 columns f at a time: dh (unweighted) from
+          // TMEM, g and u from the fp32 pre-activations (the clamp decisions
+          // are taken on exactly these values)
+          const float w = row_ok ? __ldg(p.w_perm + out_row) : 0.f;
+          const bool clamped = p.clamp > 0.f;
+          const float cl = p.clamp;
+          const float4* arow = p.act + out_row * p.act_vec;
+          uint4* drow = p.dact + out_row * p.dact_vec;
+          uint4* hrow = p.hw + out_row * (p.F / 8);
+          float dw_acc = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
+            const int f0 = col0 + c * 32;
+            uint32_t d[32];
+            tmem_ld_32x32b_x32(t_lane + c * 32, d);
+            tmem_ld_wait();
+            if (!row_ok) continue;
+            const int gc0 = gate_col(f0, p.F, p.interleave);
+            const int uc0 = up_col(f0, p.F, p.interleave);
+            uint32_t dgp[16], dup[16], hp[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {  // 4 columns per step
+              const float4 g4 = __ldg(arow + gc0 / 4 + q4);
+              const float4 u4 = __ldg(arow + uc0 / 4 + q4);
+              const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+              const float us[4] = {u4.x, u4.y, u4.z, u4.w};
+              float dg[4], du[4], hh[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float g = gs[q], u = us[q];
+                const float dh = __uint_as_float(d[4 * q4 + q]);
+                float gc = g, uc = u, mg = 1.f, mu = 1.f;
+                if (clamped) {
+                  mg = g <= cl ? 1.f : 0.f;
+                  mu = (u >= -cl && u <= cl) ? 1.f : 0.f;
+                  gc = fminf(g, cl);
+                  uc = fminf(fmaxf(u, -cl), cl);
+                }
+                const float sg = 1.f / (1.f + expf(-gc));
+                const float si = gc * sg;
+                const float h = si * uc;
+                const float dhw = w * dh;
+                dg[q] = mg * dhw * uc * (sg * (1.f + gc * (1.f - sg)));
+                du[q] = mu * dhw * si;
+                hh[q] = w * h;
+                dw_acc = fmaf(dh, h, dw_acc);
+              }
+              dgp[2 * q4] = pack2_bf16(dg[0], dg[1]);
+              dgp[2 * q4 + 1] = pack2_bf16(dg[2], dg[3]);
+              dup[2 * q4] = pack2_bf16(du[0], du[1]);
+              dup[2 * q4 + 1] = pack2_bf16(du[2], du[3]);
+              hp[2 * q4] = pack2_bf16(hh[0], hh[1]);
+              hp[2 * q4 + 1] = pack2_bf16(hh[2], hh[3]);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              drow[gc0 / 8 + v] = make_uint4(dgp[4 * v], dgp[4 * v + 1], dgp[4 * v + 2], dgp[4 * v + 3]);
+              drow[uc0 / 8 + v] = make_uint4(dup[4 * v], dup[4 * v + 1], dup[4 * v + 2], dup[4 * v + 3]);
+              hrow[f0 / 8 + v] = make_uint4(hp[4 * v], hp[4 * v + 1], hp[4 * v + 2], hp[4 * v + 3]);
+            }
+          }
+          if (row_ok) p.dw_part[out_row * p.n_tiles + t.n] = dw_acc;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<kTmemColsB>(tmem_base);
+  }
+}
+
+template <BwdMode kMode>
+cudaError_t launch_bwd_impl(const CUtensorMap& ma, const CUtensorMap& mb, const BwdParams& kp,
+                            int grid, cudaStream_t s) {
+  auto kern = grouped_gemm_bwd_kernel<kMode>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytesB));
+  if (err != cudaSuccess) return err;
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsB), kSmemBytesB, s,
+                       1, ma, mb, kp);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s) {
+  if (g.R == 0 || g.E == 0) return cudaSuccess;
+  if (g.N % 32 != 0 || g.E > kMaxEB) return cudaErrorInvalidValue;
+  const bool weight = g.mode == kBwdWeight;
+  if (weight && g.M % kBM != 0) return cudaErrorInvalidValue;
+  if (!weight && g.K % kBK != 0) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  // A: data gradients [R, K] in 128-row K-major boxes; weight gradients
+  // [R, M] in 64-row MN-major boxes.  B: 64-row MN-major boxes over the
+  // stacked weights [E * K, N] or the activations [R, N].
+  if (!make_map_2d(&ma, g.a, static_cast<uint64_t>(g.R),
+                   static_cast<uint64_t>(weight ? g.M : g.K), weight ? 64u : static_cast<uint32_t>(kBM)))
+    return cudaErrorInvalidValue;
+  const bool preact = g.mode == kBwdPreact;
+  if (preact) {  // the stacked weight rows [E * N, K], 256-row K-major boxes
+    if (g.N % kBN != 0 ||
+        !make_map_2d(&mb, g.b, static_cast<uint64_t>(g.E) * static_cast<uint64_t>(g.N),
+                     static_cast<uint64_t>(g.K), static_cast<uint32_t>(kBN)))
+      return cudaErrorInvalidValue;
+  } else if (!make_map_2d(&mb, g.b,
+                          weight ? static_cast<uint64_t>(g.R)
+                                 : static_cast<uint64_t>(g.E) * static_cast<uint64_t>(g.K),
+                          static_cast<uint64_t>(g.N), 64u)) {
+    return cudaErrorInvalidValue;
+  }
+  BwdParams kp{};
+  kp.expert_offsets = g.expert_offsets;
+  kp.mtile_prefix = g.mtile_prefix;
+  kp.E = g.E;
+  kp.K = g.K;
+  kp.N = g.N;
+  kp.n_tiles = ceil_div(g.N, kBN);
+  kp.M = g.M;
+  kp.m_tiles = weight ? g.M / kBM : 0;
+  kp.out = static_cast<uint4*>(g.out);
+  kp.ldo_vec = preact ? g.N / 4 : g.N / 8;
+  kp.act = static_cast<const float4*>(g.act);
+  kp.act_vec = g.F * 2 / 4;
+  kp.dact = static_cast<uint4*>(g.dact);
+  kp.dact_vec = g.F * 2 / 8;
+  kp.hw = static_cast<uint4*>(g.hw);
+  kp.dw_part = g.dw_part;
+  kp.w_perm = g.w_perm;
+  kp.F = g.F;
+  kp.interleave = g.interleave;
+  kp.clamp = g.clamp;
+  kp.status = g.status;
+  long max_tiles;
+  if (weight) {
+    max_tiles = static_cast<long>(g.E) * kp.m_tiles * kp.n_tiles;
+  } else {
+    max_tiles = (ceil_div(g.R, kBM) + std::min(g.E, g.R)) * static_cast<long>(kp.n_tiles);
+  }
+  const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
+  switch (g.mode) {
+    case kBwdDataPlain: return launch_bwd_impl<BwdMode::kDataPlain>(ma, mb, kp, grid, s);
+    case kBwdDataSwiGLU: return launch_bwd_impl<BwdMode::kDataSwiGLU>(ma, mb, kp, grid, s);
+    case kBwdWeight: return launch_bwd_impl<BwdMode::kWeight>(ma, mb, kp, grid, s);
+    case kBwdPreact: return launch_bwd_impl<BwdMode::kPreact>(ma, mb, kp, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

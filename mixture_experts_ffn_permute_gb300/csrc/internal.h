@@ -111,7 +111,8 @@ cudaError_t launch_mtile_prefix_from_offsets(const int32_t* expert_offsets, int 
                                              int32_t* mtile_prefix, uint32_t* status,
                                              cudaStream_t s);
 
-// Step 6: out[t] = sum_j w[t][j] * y[row_id_map[t][j]] in slot order.
+// Step 6: out[t] = sum_j w[t][j] * y[row_id_map[t][j]] in slot order (w = 1
+// when topk_w is null).
 cudaError_t launch_combine(const void* y, const int32_t* row_id_map, const float* topk_w,
                            int T, int H, int k, void* out, cudaStream_t s);
 
@@ -183,6 +184,53 @@ cudaError_t launch_prepare_scales(const uint8_t* src, uint8_t* dst, int E, int N
 cudaError_t launch_prepare_mxfp4_scales(const uint8_t* s1, const uint8_t* s2, uint8_t* dst1,
                                         uint8_t* dst2, int E, int F, int H, float* g1, float* g2,
                                         cudaStream_t s);
+// ---- backward -------------------------------------------------------------
+// Grouped GEMMs of the backward (grouped_gemm_bwd.cu):
+//   kBwdDataPlain   out[r, :N] = a[r, :K] b_e[K, N]       (b read MN-major)
+//   kBwdDataSwiGLU  the same product dh, then the SwiGLU backward epilogue
+//                   over act (pre-activations -> dA in place), hw and dw_part
+//   kBwdWeight      out[e, :M, :N] = a_e^T b_e over the rows of expert e
+//   kBwdPreact      out[r, :N] = a[r, :K] b_e[N, K]^T in fp32 (the forward's
+//                   GEMM1 without its activation; b read K-major)
+constexpr int kBwdDataPlain = 0;
+constexpr int kBwdDataSwiGLU = 1;
+constexpr int kBwdWeight = 2;
+constexpr int kBwdPreact = 3;
+
+struct BwdGemmArgs {
+  int mode;
+  const void* a;  // data: [R, K]; weight: [R, M] bf16
+  const void* b;  // data: [E * K, N] stacked weights; weight: [R, N] bf16;
+                  // pre-activations: [E * N, K] weights
+  int R, E, K, N, M;
+  const int32_t* expert_offsets;  // [E + 1]
+  const int32_t* mtile_prefix;    // [E + 1] (data modes)
+  void* out;                      // data: [R, N]; weight: [E, M, N] bf16; [R, N] fp32
+  // kBwdDataSwiGLU
+  const void* act = nullptr;      // [R, 2F] fp32 pre-activations
+  void* dact = nullptr;           // [R, 2F] bf16 out: their gradient dA
+  void* hw = nullptr;             // [R, F] bf16 out: w * h
+  float* dw_part = nullptr;       // [R, ceil(N / 256)] fp32 out
+  const float* w_perm = nullptr;  // [R] routing weight per permuted row
+  int F = 0, interleave = 0;
+  float clamp = 0.f;
+  uint32_t* status = nullptr;
+};
+
+cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s);
+
+// w_perm[row_id_map[t][j]] = topk_w[t][j] for every valid route.
+cudaError_t launch_weights_to_rows(const int32_t* row_id_map, const float* topk_w, long routes,
+                                   float* w_perm, cudaStream_t s);
+
+// Router backward, one warp per token: dw_j = sum of the dw_part row of the
+// route (fixed order), then the softmax backward over the first k slots of
+// the `slots` per token into dlogits [T, E] fp32.
+cudaError_t launch_router_backward(const float* logits, const int32_t* topk_idx,
+                                   const float* topk_w, const int32_t* row_id_map,
+                                   const float* dw_part, int n_parts, int T, int E, int k,
+                                   int slots, int renormalize, float* dlogits, cudaStream_t s);
+
 // FP8 rows (E4M3 codes + fp32 scales per 128) gathered by permuted_token into f16.
 cudaError_t launch_gather_dequant_fp8(const uint8_t* xq, const float* xs,
                                       const int32_t* permuted_token, int R, int H, void* x_perm,

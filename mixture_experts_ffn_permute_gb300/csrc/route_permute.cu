@@ -328,7 +328,8 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   }
 }
 
-// out[t][c..c+8) = sum_{j} w[t][j] * y[row][c..c+8), fp32 in slot order.
+// out[t][c..c+8) = sum_{j} w[t][j] * y[row][c..c+8), fp32 in slot order
+// (w = 1 when topk_w is null: the plain sum of the token's rows).
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_id_map,
                const float* __restrict__ topk_w, int T, int vecs_per_row, int k,
@@ -343,7 +344,7 @@ combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_id_m
   for (int j = 0; j < k; ++j) {
     const int row = __ldg(row_id_map + static_cast<size_t>(t) * k + j);
     if (row < 0) continue;
-    const float w = __ldg(topk_w + static_cast<size_t>(t) * k + j);
+    const float w = topk_w ? __ldg(topk_w + static_cast<size_t>(t) * k + j) : 1.f;
     float f[8];
     bf16x8_to_f32(__ldg(y + static_cast<size_t>(row) * vecs_per_row + v), f);
 #pragma unroll

@@ -74,15 +74,15 @@ def _load():
                 "oracle_gemm2_lowprec": ([cl, ci, ci, ci, vp, vp, vp, vp, vp, ci, vp], ci),
                 "oracle_moe_forward_lowprec": ([ci, ci, ci, ci, ci, ci, ci, cd, vp, vp, vp, vp,
                                                 vp, vp, vp, vp, vp, ci, vp, vp, vp], ci),
-                "oracle_moe_backward": ([ci, ci, ci, ci, ci, ci, cd, ci, vp, vp, vp, vp, vp,
-                                         vp, vp, vp, vp, vp], ci),
-                "oracle_backward_tokens": ([ci, ci, ci, ci, ci, ci, cd, ci, vp, vp, vp, vp,
+                "oracle_moe_backward": ([ci, ci, ci, ci, ci, ci, cd, ci, ci, vp, vp, vp, vp,
+                                         vp, vp, vp, vp, vp, vp], ci),
+                "oracle_backward_tokens": ([ci, ci, ci, ci, ci, ci, cd, ci, ci, vp, vp, vp, vp,
                                             vp, vp, ci, vp, vp, vp], ci),
-                "oracle_backward_dw1_rows": ([ci, ci, ci, ci, ci, ci, cd, ci, vp, vp, vp, vp,
+                "oracle_backward_dw1_rows": ([ci, ci, ci, ci, ci, ci, cd, ci, ci, vp, vp, vp,
+                                              vp, vp, vp, ci, vp, vp], ci),
+                "oracle_backward_dw2_cols": ([ci, ci, ci, ci, ci, ci, cd, ci, ci, vp, vp, vp,
                                               vp, vp, ci, vp, vp], ci),
-                "oracle_backward_dw2_cols": ([ci, ci, ci, ci, ci, ci, cd, ci, vp, vp, vp, vp,
-                                              vp, ci, vp, vp], ci),
-                "oracle_router_backward": ([ci, ci, ci, ci, ci, vp, vp, vp, vp, vp], ci),
+                "oracle_router_backward": ([ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp], ci),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(lib, name)
@@ -425,11 +425,14 @@ def _bwd_args(x, topk_idx, topk_w, w1, w2, d_out):
 
 
 def expert_backward(x, topk_idx, topk_w, w1, w2, d_out, interleave: int = 0,
-                    clamp: float = 0.0, mask_bf16: bool = False) -> Dict[str, np.ndarray]:
+                    clamp: float = 0.0, mask_f32: bool = False,
+                    magnitude: bool = False) -> Dict[str, np.ndarray]:
     """Gradients of sum(d_out * out) through the expert MLPs for the given
     routes ([T, slots] indices, -1 masked, and weights): dx [T, H],
     dw_route [T, slots] (d loss / d weight of each route), dw1 [E, 2F, H] and
-    dw2 [E, H, F], all fp64."""
+    dw2 [E, H, F], all fp64.  ``mask_f32`` takes the clamp decisions on the
+    pre-activations rounded to fp32; ``magnitude`` returns for every output
+    the sum of the absolute values of its terms instead."""
     xb, gb, ix, ww, w1s, w2s, E, F = _bwd_args(x, topk_idx, topk_w, w1, w2, d_out)
     T, H = xb.shape
     slots = ix.shape[1]
@@ -438,16 +441,17 @@ def expert_backward(x, topk_idx, topk_w, w1, w2, d_out, interleave: int = 0,
     dw1 = np.empty((E, 2 * F, H), np.float64)
     dw2 = np.empty((E, H, F), np.float64)
     _check(_load().oracle_moe_backward(T, H, F, E, slots, interleave, float(clamp),
-                                       int(mask_bf16), _p(ix), _p(ww), _p(xb),
+                                       int(mask_f32), int(magnitude), _p(ix), _p(ww), _p(xb),
                                        _expert_ptrs(w1s), _expert_ptrs(w2s), _p(gb), _p(dx),
                                        _p(dwr), _p(dw1), _p(dw2)), "oracle_moe_backward")
     return {"dx": dx, "dw_route": dwr, "dw1": dw1, "dw2": dw2}
 
 
 def router_backward(logits, topk_idx, topk_w, dw_route, k: int,
-                    renormalize: bool = True) -> np.ndarray:
+                    renormalize: bool = True, magnitude: bool = False) -> np.ndarray:
     """d loss / d logits [T, E] from the per-route weight gradients (the
-    first k slots are the routed ones; later slots are shared experts)."""
+    first k slots are the routed ones; later slots are shared experts).  With
+    ``magnitude`` dw_route holds magnitudes and so does the result."""
     lg = _np(logits, np.float32)
     ix = _np(topk_idx, np.int32)
     ww = _np(topk_w, np.float64)
@@ -455,26 +459,27 @@ def router_backward(logits, topk_idx, topk_w, dw_route, k: int,
     T, E = lg.shape
     slots = ix.shape[1]
     dl = np.empty((T, E), np.float64)
-    _check(_load().oracle_router_backward(T, E, k, slots, int(renormalize), _p(lg), _p(ix),
+    _check(_load().oracle_router_backward(T, E, k, slots, int(renormalize), int(magnitude),
+                                          _p(lg), _p(ix),
                                           _p(ww), _p(dw), _p(dl)), "oracle_router_backward")
     return dl
 
 
 def moe_backward(x, logits, w1, w2, d_out, k: int, renormalize: bool = True,
                  interleave: int = 0, clamp: float = 0.0, shared_experts: int = 0,
-                 mask_bf16: bool = False) -> Dict[str, np.ndarray]:
+                 mask_f32: bool = False, magnitude: bool = False) -> Dict[str, np.ndarray]:
     """Gradients of sum(d_out * out) for the whole layer (route_topk's
     routing, optional shared experts): dx, dlogits, dw1, dw2 plus the
     routes."""
     idx, w = routes_with_shared(logits, k, shared_experts, renormalize)
-    res = expert_backward(x, idx, w, w1, w2, d_out, interleave, clamp, mask_bf16)
-    res["dlogits"] = router_backward(logits, idx, w, res["dw_route"], k, renormalize)
+    res = expert_backward(x, idx, w, w1, w2, d_out, interleave, clamp, mask_f32, magnitude)
+    res["dlogits"] = router_backward(logits, idx, w, res["dw_route"], k, renormalize, magnitude)
     res["topk_idx"], res["topk_w"] = idx, w
     return res
 
 
 def backward_tokens(x, topk_idx, topk_w, w1, w2, d_out, tokens, interleave: int = 0,
-                    clamp: float = 0.0, mask_bf16: bool = False):
+                    clamp: float = 0.0, mask_f32: bool = False, magnitude: bool = False):
     """dx rows [n, H] and per-route weight gradients [n, slots] of the listed
     tokens (expert_backward's definitions, only those rows)."""
     xb, gb, ix, ww, w1s, w2s, E, F = _bwd_args(x, topk_idx, topk_w, w1, w2, d_out)
@@ -484,7 +489,7 @@ def backward_tokens(x, topk_idx, topk_w, w1, w2, d_out, tokens, interleave: int 
     dx = np.empty((tk.shape[0], H), np.float64)
     dw = np.empty((tk.shape[0], slots), np.float64)
     _check(_load().oracle_backward_tokens(T, H, F, E, slots, interleave, float(clamp),
-                                          int(mask_bf16), _p(ix), _p(ww), _p(xb),
+                                          int(mask_f32), int(magnitude), _p(ix), _p(ww), _p(xb),
                                           _expert_ptrs(w1s), _expert_ptrs(w2s), _p(gb),
                                           tk.shape[0], _p(tk), _p(dx), _p(dw)),
            "oracle_backward_tokens")
@@ -492,14 +497,15 @@ def backward_tokens(x, topk_idx, topk_w, w1, w2, d_out, tokens, interleave: int 
 
 
 def backward_dw1_rows(x, topk_idx, topk_w, w1, w2, d_out, pairs, interleave: int = 0,
-                      clamp: float = 0.0, mask_bf16: bool = False) -> np.ndarray:
+                      clamp: float = 0.0, mask_f32: bool = False,
+                      magnitude: bool = False) -> np.ndarray:
     """Rows dw1[e, row, :] for the listed (e, row) pairs, [n, H]."""
     xb, gb, ix, ww, w1s, w2s, E, F = _bwd_args(x, topk_idx, topk_w, w1, w2, d_out)
     T, H = xb.shape
     pr = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
     rows = np.empty((pr.shape[0], H), np.float64)
     _check(_load().oracle_backward_dw1_rows(T, H, F, E, ix.shape[1], interleave, float(clamp),
-                                            int(mask_bf16), _p(ix), _p(ww), _p(xb),
+                                            int(mask_f32), int(magnitude), _p(ix), _p(ww), _p(xb),
                                             _expert_ptrs(w1s), _expert_ptrs(w2s), _p(gb),
                                             pr.shape[0], _p(pr), _p(rows)),
            "oracle_backward_dw1_rows")
@@ -507,14 +513,15 @@ def backward_dw1_rows(x, topk_idx, topk_w, w1, w2, d_out, pairs, interleave: int
 
 
 def backward_dw2_cols(x, topk_idx, topk_w, w1, w2, d_out, pairs, interleave: int = 0,
-                      clamp: float = 0.0, mask_bf16: bool = False) -> np.ndarray:
+                      clamp: float = 0.0, mask_f32: bool = False,
+                      magnitude: bool = False) -> np.ndarray:
     """Columns dw2[e, :, f] for the listed (e, f) pairs, [n, H]."""
     xb, gb, ix, ww, w1s, w2s, E, F = _bwd_args(x, topk_idx, topk_w, w1, w2, d_out)
     T, H = xb.shape
     pr = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
     cols = np.empty((pr.shape[0], H), np.float64)
     _check(_load().oracle_backward_dw2_cols(T, H, F, E, ix.shape[1], interleave, float(clamp),
-                                            int(mask_bf16), _p(ix), _p(ww), _p(xb),
+                                            int(mask_f32), int(magnitude), _p(ix), _p(ww), _p(xb),
                                             _expert_ptrs(w1s), _p(gb), pr.shape[0], _p(pr),
                                             _p(cols)),
            "oracle_backward_dw2_cols")

@@ -581,18 +581,14 @@ int oracle_moe_forward_lowprec(int T, int H, int F, int E, int k, int renormaliz
 //   dx_t += sum_f dg_f W1_e[gate_row(f)] + du_f W1_e[up_row(f)]
 // Without a clamp both masks are 1.  The top-k selection is piecewise
 // constant and passes no gradient; the routing weights do (router backward
-// below).  mask_bf16 = 1 takes the two clamp decisions on g and u rounded to
-// bf16 (the precision a caller may keep the pre-activations in); 0 takes
+// below).  mask_f32 = 1 takes the two clamp decisions on g and u rounded to
+// fp32 (the precision a caller may keep the pre-activations in); 0 takes
 // them on the exact values.
+// magnitude = 1 returns, instead of each output, the sum of the absolute
+// values of the terms that make it up (|a| |b| for every product a b of the
+// sums above): the scale of the rounding error a finite-precision evaluation
+// of the same sums may make.
 namespace {
-
-// Nearest bf16 value (8 significant bits), ties to even; normal range only.
-inline double round_bf16(double v) {
-  if (v == 0.0 || !std::isfinite(v)) return v;
-  int e = 0;
-  const double m = std::frexp(v, &e);  // |m| in [0.5, 1)
-  return std::ldexp(std::nearbyint(std::ldexp(m, 8)), e - 8);
-}
 
 inline double silu_grad(double z) {
   const double s = 1.0 / (1.0 + std::exp(-z));
@@ -600,13 +596,13 @@ inline double silu_grad(double z) {
 }
 
 // Column f of the SwiGLU and its backward for one route.
-inline void swiglu_backward(double g, double u, double dh, double c, int mask_bf16, double* h,
+inline void swiglu_backward(double g, double u, double dh, double c, int mask_f32, double* h,
                             double* dg, double* du) {
   double gc = g, uc = u;
   bool pass_g = true, pass_u = true;
   if (c > 0 && std::isfinite(c)) {
-    const double gm = mask_bf16 ? round_bf16(g) : g;
-    const double um = mask_bf16 ? round_bf16(u) : u;
+    const double gm = mask_f32 ? static_cast<double>(static_cast<float>(g)) : g;
+    const double um = mask_f32 ? static_cast<double>(static_cast<float>(u)) : u;
     pass_g = gm <= c;
     pass_u = um >= -c && um <= c;
     gc = std::fmin(g, c);
@@ -651,8 +647,9 @@ inline double dh_at(const double* dy, const uint16_t* W2, long H, long F, long f
 }
 
 // Every backward quantity of one route: the W1-row-ordered dA (2F), h (F),
-// dy (H) and dw = <G, y>.  Optionally adds the route's dx contribution.
-void route_backward(long H, long F, long I, double c, int mask_bf16, double w,
+// dy (H) and dw = <G, y> (its magnitude sum |G| |y| when `magnitude`).
+// Optionally adds the route's dx contribution (|dA| |W1| when `magnitude`).
+void route_backward(long H, long F, long I, double c, int mask_f32, int magnitude, double w,
                     const uint16_t* x_row, const uint16_t* g_row, const uint16_t* W1,
                     const uint16_t* W2, double* dA, double* h, double* dy, double* dw,
                     double* dx_add) {
@@ -664,7 +661,7 @@ void route_backward(long H, long F, long I, double c, int mask_bf16, double w,
   for (long f = 0; f < F; ++f) {
     preact(xr.data(), W1, H, F, I, f, &gv[f], &uv[f]);
     double hf, dg, du;
-    swiglu_backward(gv[f], uv[f], 0.0, c, mask_bf16, &hf, &dg, &du);
+    swiglu_backward(gv[f], uv[f], 0.0, c, mask_f32, &hf, &dg, &du);
     h[f] = hf;
   }
   double d = 0.0;
@@ -672,14 +669,14 @@ void route_backward(long H, long F, long I, double c, int mask_bf16, double w,
     double acc = 0.0;
     for (long f = 0; f < F; ++f) acc += bf16_value(W2[n * F + f]) * h[f];
     y[n] = acc;
-    d += G[n] * acc;
+    d += magnitude ? std::fabs(G[n] * acc) : G[n] * acc;
   }
   *dw = d;
   for (long n = 0; n < H; ++n) dy[n] = w * G[n];
   for (long f = 0; f < F; ++f) {
     const double dh = dh_at(dy, W2, H, F, f);
     double hf, dg, du;
-    swiglu_backward(gv[f], uv[f], dh, c, mask_bf16, &hf, &dg, &du);
+    swiglu_backward(gv[f], uv[f], dh, c, mask_f32, &hf, &dg, &du);
     dA[gate_row(f, F, I)] = dg;
     dA[up_row(f, F, I)] = du;
   }
@@ -688,7 +685,8 @@ void route_backward(long H, long F, long I, double c, int mask_bf16, double w,
       const double a = dA[row];
       if (a == 0.0) continue;
       const uint16_t* wr = W1 + row * H;
-      for (long c2 = 0; c2 < H; ++c2) dx_add[c2] += a * bf16_value(wr[c2]);
+      for (long c2 = 0; c2 < H; ++c2)
+        dx_add[c2] += magnitude ? std::fabs(a * bf16_value(wr[c2])) : a * bf16_value(wr[c2]);
     }
   }
 }
@@ -704,7 +702,8 @@ extern "C" {
 // a masked slot), dw1 [E, 2F, H], dw2 [E, H, F].  Returns 0, -1 on bad sizes,
 // -2 on a route to an expert without weights or outside [-1, E).
 int oracle_moe_backward(int T, int H, int F, int E, int slots, int interleave, double clamp,
-                        int mask_bf16, const int32_t* topk_idx, const double* topk_w,
+                        int mask_f32, int magnitude, const int32_t* topk_idx,
+                        const double* topk_w,
                         const uint16_t* x, const uint16_t* const* w1_experts,
                         const uint16_t* const* w2_experts, const uint16_t* d_out, double* dx,
                         double* dw_route, double* dw1, double* dw2) {
@@ -723,9 +722,9 @@ int oracle_moe_backward(int T, int H, int F, int E, int slots, int interleave, d
     dw_route[r] = 0.0;
     if (e < 0) continue;
     const long t = r / slots;
-    route_backward(HH, FF, interleave, clamp, mask_bf16, topk_w[r], x + t * HH, d_out + t * HH,
-                   w1_experts[e], w2_experts[e], &dA[r * 2 * FF], &hr[r * FF], &dy[r * HH],
-                   &dw_route[r], &dxr[r * HH]);
+    route_backward(HH, FF, interleave, clamp, mask_f32, magnitude, topk_w[r], x + t * HH,
+                   d_out + t * HH, w1_experts[e], w2_experts[e], &dA[r * 2 * FF], &hr[r * FF],
+                   &dy[r * HH], &dw_route[r], &dxr[r * HH]);
   }
 #pragma omp parallel for
   for (long t = 0; t < T; ++t)
@@ -743,7 +742,8 @@ int oracle_moe_backward(int T, int H, int F, int E, int slots, int interleave, d
       if (topk_idx[r] != e) continue;
       const double a = dA[r * 2 * FF + row];
       const uint16_t* xr = x + (r / slots) * HH;
-      for (long c = 0; c < HH; ++c) out[c] += a * bf16_value(xr[c]);
+      for (long c = 0; c < HH; ++c)
+        out[c] += magnitude ? std::fabs(a * bf16_value(xr[c])) : a * bf16_value(xr[c]);
     }
   }
 #pragma omp parallel for schedule(dynamic)
@@ -754,7 +754,8 @@ int oracle_moe_backward(int T, int H, int F, int E, int slots, int interleave, d
     for (long r = 0; r < R; ++r) {
       if (topk_idx[r] != e) continue;
       const double d = dy[r * HH + n];
-      for (long f = 0; f < FF; ++f) out[f] += d * hr[r * FF + f];
+      for (long f = 0; f < FF; ++f)
+        out[f] += magnitude ? std::fabs(d * hr[r * FF + f]) : d * hr[r * FF + f];
     }
   }
   return 0;
@@ -765,7 +766,8 @@ int oracle_moe_backward(int T, int H, int F, int E, int slots, int interleave, d
 //   tokens [n], dx_rows [n, H] (slots summed in order j = 0, 1, ...),
 //   dw_rows [n, slots].
 int oracle_backward_tokens(int T, int H, int F, int E, int slots, int interleave, double clamp,
-                           int mask_bf16, const int32_t* topk_idx, const double* topk_w,
+                           int mask_f32, int magnitude, const int32_t* topk_idx,
+                           const double* topk_w,
                            const uint16_t* x, const uint16_t* const* w1_experts,
                            const uint16_t* const* w2_experts, const uint16_t* d_out, int n,
                            const int32_t* tokens, double* dx_rows, double* dw_rows) {
@@ -781,9 +783,9 @@ int oracle_backward_tokens(int T, int H, int F, int E, int slots, int interleave
     const int e = topk_idx[r];
     if (e < 0 || e >= E || !w1_experts[e] || !w2_experts[e]) continue;
     std::vector<double> dA(2 * FF), h(FF), dy(HH);
-    route_backward(HH, FF, interleave, clamp, mask_bf16, topk_w[r], x + t * HH, d_out + t * HH,
-                   w1_experts[e], w2_experts[e], dA.data(), h.data(), dy.data(), &dw_rows[q],
-                   &part[q * HH]);
+    route_backward(HH, FF, interleave, clamp, mask_f32, magnitude, topk_w[r], x + t * HH,
+                   d_out + t * HH, w1_experts[e], w2_experts[e], dA.data(), h.data(), dy.data(),
+                   &dw_rows[q], &part[q * HH]);
   }
   for (long i = 0; i < n; ++i)
     for (long c = 0; c < HH; ++c) {
@@ -797,8 +799,8 @@ int oracle_backward_tokens(int T, int H, int F, int E, int slots, int interleave
 // Whole rows of dW1 for the listed (expert, W1 row) pairs:
 //   dW1_e[row][:] = sum over the routes of e of dA[row] x_t   (rows [n, H]).
 int oracle_backward_dw1_rows(int T, int H, int F, int E, int slots, int interleave,
-                             double clamp, int mask_bf16, const int32_t* topk_idx,
-                             const double* topk_w, const uint16_t* x,
+                             double clamp, int mask_f32, int magnitude,
+                             const int32_t* topk_idx, const double* topk_w, const uint16_t* x,
                              const uint16_t* const* w1_experts,
                              const uint16_t* const* w2_experts, const uint16_t* d_out, int n,
                              const int32_t* pairs, double* rows) {
@@ -828,15 +830,18 @@ int oracle_backward_dw1_rows(int T, int H, int F, int E, int slots, int interlea
       }
       double g, u, h, dg, du;
       preact(xr.data(), w1_experts[e], HH, FF, interleave, f, &g, &u);
-      swiglu_backward(g, u, dh_at(dy.data(), w2_experts[e], HH, FF, f), clamp, mask_bf16, &h,
+      swiglu_backward(g, u, dh_at(dy.data(), w2_experts[e], HH, FF, f), clamp, mask_f32, &h,
                       &dg, &du);
       a[q] = is_gate ? dg : du;
+      if (magnitude) a[q] = std::fabs(a[q]);
     }
 #pragma omp parallel for
     for (long c = 0; c < HH; ++c) {
       double acc = 0.0;
-      for (size_t q = 0; q < routes.size(); ++q)
-        acc += a[q] * bf16_value(x[(routes[q] / slots) * HH + c]);
+      for (size_t q = 0; q < routes.size(); ++q) {
+        const double xv = bf16_value(x[(routes[q] / slots) * HH + c]);
+        acc += a[q] * (magnitude ? std::fabs(xv) : xv);
+      }
       rows[i * HH + c] = acc;
     }
   }
@@ -846,8 +851,8 @@ int oracle_backward_dw1_rows(int T, int H, int F, int E, int slots, int interlea
 // Whole columns of dW2 for the listed (expert, f) pairs:
 //   dW2_e[:][f] = sum over the routes of e of w G_t h_f   (cols [n, H]).
 int oracle_backward_dw2_cols(int T, int H, int F, int E, int slots, int interleave,
-                             double clamp, int mask_bf16, const int32_t* topk_idx,
-                             const double* topk_w, const uint16_t* x,
+                             double clamp, int mask_f32, int magnitude,
+                             const int32_t* topk_idx, const double* topk_w, const uint16_t* x,
                              const uint16_t* const* w1_experts, const uint16_t* d_out, int n,
                              const int32_t* pairs, double* cols) {
   if (T < 0 || H <= 0 || F <= 0 || E <= 0 || slots <= 0 || n < 0) return -1;
@@ -871,14 +876,16 @@ int oracle_backward_dw2_cols(int T, int H, int F, int E, int slots, int interlea
       for (long c = 0; c < HH; ++c) xr[c] = bf16_value(x[t * HH + c]);
       double g, u, h, dg, du;
       preact(xr.data(), w1_experts[e], HH, FF, interleave, f, &g, &u);
-      swiglu_backward(g, u, 0.0, clamp, mask_bf16, &h, &dg, &du);
-      wh[q] = topk_w[r] * h;
+      swiglu_backward(g, u, 0.0, clamp, mask_f32, &h, &dg, &du);
+      wh[q] = magnitude ? std::fabs(topk_w[r] * h) : topk_w[r] * h;
     }
 #pragma omp parallel for
     for (long nn = 0; nn < HH; ++nn) {
       double acc = 0.0;
-      for (size_t q = 0; q < routes.size(); ++q)
-        acc += bf16_value(d_out[(routes[q] / slots) * HH + nn]) * wh[q];
+      for (size_t q = 0; q < routes.size(); ++q) {
+        const double gv = bf16_value(d_out[(routes[q] / slots) * HH + nn]);
+        acc += (magnitude ? std::fabs(gv) : gv) * wh[q];
+      }
       cols[i * HH + nn] = acc;
     }
   }
@@ -892,9 +899,13 @@ int oracle_backward_dw2_cols(int T, int H, int F, int E, int slots, int interlea
 //   renormalize = 0: dl_e = p_e ([e selected by slot j] dw_j - sum_i w_i dw_i),
 //                    p = softmax of the token's E logits (fp64).
 // A masked slot (-1) is left out of both sums.  dlogits [T, E] fp64.
-int oracle_router_backward(int T, int E, int k, int slots, int renormalize, const float* logits,
-                           const int32_t* topk_idx, const double* topk_w, const double* dw,
-                           double* dlogits) {
+// magnitude = 1: dw holds the magnitudes m_j of the per-route gradients and
+// the result is the magnitude of each logit's gradient, the two sums added
+// instead of subtracted: w_j (m_j + sum_i w_i m_i), resp.
+// p_e ([e = e_j] m_j + sum_i w_i m_i).
+int oracle_router_backward(int T, int E, int k, int slots, int renormalize, int magnitude,
+                           const float* logits, const int32_t* topk_idx, const double* topk_w,
+                           const double* dw, double* dlogits) {
   if (T < 0 || E <= 0 || k <= 0 || slots < k) return -1;
 #pragma omp parallel for
   for (long t = 0; t < T; ++t) {
@@ -908,7 +919,7 @@ int oracle_router_backward(int T, int E, int k, int slots, int renormalize, cons
     if (renormalize) {
       for (int j = 0; j < k; ++j) {
         const long r = t * slots + j;
-        if (topk_idx[r] >= 0) dl[topk_idx[r]] = topk_w[r] * (dw[r] - s);
+        if (topk_idx[r] >= 0) dl[topk_idx[r]] = topk_w[r] * (magnitude ? dw[r] + s : dw[r] - s);
       }
     } else {
       const float* l = logits + t * E;
@@ -916,7 +927,8 @@ int oracle_router_backward(int T, int E, int k, int slots, int renormalize, cons
       for (int e = 1; e < E; ++e) lmax = std::fmax(lmax, static_cast<double>(l[e]));
       double denom = 0.0;
       for (int e = 0; e < E; ++e) denom += std::exp(static_cast<double>(l[e]) - lmax);
-      for (int e = 0; e < E; ++e) dl[e] = -(std::exp(static_cast<double>(l[e]) - lmax) / denom) * s;
+      for (int e = 0; e < E; ++e)
+        dl[e] = (magnitude ? 1.0 : -1.0) * (std::exp(static_cast<double>(l[e]) - lmax) / denom) * s;
       for (int j = 0; j < k; ++j) {
         const long r = t * slots + j;
         const int e = topk_idx[r];

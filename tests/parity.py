@@ -5,6 +5,15 @@ Floating-point contract (bf16 path): per element
 and over the whole tensor
     RMS relative error sqrt(sum (gpu - oracle)^2 / sum oracle^2) <= 5e-3.
 Routing indices, row maps and counts are compared bit for bit.
+
+Gradients (the backward): each output is a sum of products in which exactly
+one factor was rounded to bf16 (relative error <= 2^-9) and the result is
+rounded once more to bf16 (<= 2^-9 of its value); fp32 accumulation adds far
+less.  So per element
+    |gpu - oracle| <= 2^-7 * M
+where M is the oracle's sum of the absolute values of that element's terms
+(the dot-product error bound, with a factor 2 to spare), and over the whole
+tensor the RMS relative error <= 5e-3.
 """
 import numpy as np
 import torch
@@ -53,3 +62,27 @@ def assert_equal(gpu, ref, what: str = ""):
         d = np.argwhere(g != r)
         raise AssertionError(f"{what}: {len(d)} mismatches, first at {tuple(d[0])}: "
                              f"gpu={g[tuple(d[0])]} oracle={r[tuple(d[0])]}")
+
+
+
+TAU_GRAD = 2.0 ** -7
+
+
+def assert_grad_bound(gpu, ref, mag, what: str = "", rms: float = RMS_BF16, tau: float = TAU_GRAD):
+    """Gradient parity: per element within tau times the magnitude of its
+    terms (``mag``, from the oracle), and RMS relative error <= rms."""
+    g = to_f64(gpu)
+    r = np.asarray(ref, np.float64)
+    m = np.asarray(mag, np.float64)
+    assert g.shape == r.shape == m.shape, (what, g.shape, r.shape, m.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    err = np.abs(g - r)
+    bound = tau * m
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; worst at {i}: "
+                             f"gpu={g[i]!r} oracle={r[i]!r} magnitude={m[i]!r}")
+    e = rms_rel(g, r)
+    assert e <= rms, f"{what}: RMS relative error {e:.3e} > {rms:.1e}"
+    return e

@@ -180,3 +180,27 @@ def test_prepare_weights_mxfp4_validates(lib):
     assert f(ctypes.byref(p), a, a, a, moe.prepared_scales_size(p) - 1, a, a, None) == 4
     bf = moe.Problem.make(T=64, H=256, F=512, E=8, k=2)
     assert f(ctypes.byref(bf), a, a, a, big, a, a, None) == 1
+
+
+def test_backward_validates(lib):
+    """moe_backward's host checks (no GPU work is enqueued on any of these)."""
+    p = P()
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    big = 1 << 40
+    f = lib.moe_backward
+    need = moe.backward_workspace_size(p)
+    assert need > moe.workspace_size(p)  # adds the pre-activations and router partials
+    assert f(ctypes.byref(p), a, a, a, a, a, a, a, a, a, a, need - 1, None) == 4
+    assert f(ctypes.byref(p), a, a, a, a, a, a, a, a, a, None, big, None) == 1      # ws
+    assert f(ctypes.byref(p), a, a, a, a, a, a, a, None, a, a, big, None) == 1      # dw1
+    assert f(ctypes.byref(p), a, a, a, a, a, a, a, a, mis, a, big, None) == 3      # dw2
+    assert f(ctypes.byref(p), a, a, a, a, a, a, mis, a, a, a, big, None) == 3      # d_logits
+    assert f(ctypes.byref(p), a, a, a, a, None, a, a, a, a, a, big, None) == 1     # d_out
+    assert f(ctypes.byref(P(H=200)), a, a, a, a, a, a, a, a, a, a, big, None) == 2
+    lp = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, precision=moe.PREC_FP8_NVFP4)
+    assert f(ctypes.byref(lp), a, a, a, a, a, a, a, a, a, a, big, None) == 1        # bf16 only
+    assert moe.backward_workspace_size(lp) == 0
+    # shared experts widen the workspace like the forward's
+    ps = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, shared_experts=1)
+    assert moe.backward_workspace_size(ps) > need

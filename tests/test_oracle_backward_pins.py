@@ -174,32 +174,62 @@ def test_masked_routes_contribute_nothing():
     assert (a["dw_route"][~keep] == 0).all()
 
 
+@pytest.mark.parametrize("magnitude", [False, True])
 @pytest.mark.parametrize("I,c", [(0, 0.0), (8, 0.7)])
-def test_sampled_forms_match_the_whole_backward(I, c):
+def test_sampled_forms_match_the_whole_backward(I, c, magnitude):
     x, logits, w1, w2, g = _case(T=16, E=4, k=2, seed=2)
     idx, w = oracle.route_topk(logits, 2)
-    full = oracle.expert_backward(x, idx, w, w1, w2, g, interleave=I, clamp=c, mask_bf16=True)
+    full = oracle.expert_backward(x, idx, w, w1, w2, g, interleave=I, clamp=c, mask_f32=True, magnitude=magnitude)
     toks = [0, 5, 15]
     dx, dw = oracle.backward_tokens(x, idx, w, w1, w2, g, toks, interleave=I, clamp=c,
-                                    mask_bf16=True)
+                                    mask_f32=True, magnitude=magnitude)
     np.testing.assert_allclose(dx, full["dx"][toks], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(dw, full["dw_route"][toks], rtol=1e-12, atol=1e-14)
     pairs = [(0, 0), (1, 17), (3, 31), (2, 8)]
     rows = oracle.backward_dw1_rows(x, idx, w, w1, w2, g, pairs, interleave=I, clamp=c,
-                                    mask_bf16=True)
+                                    mask_f32=True, magnitude=magnitude)
     for i, (e, r) in enumerate(pairs):
         np.testing.assert_allclose(rows[i], full["dw1"][e, r], rtol=1e-12, atol=1e-14)
     pairs = [(0, 0), (1, 15), (3, 7)]
     cols = oracle.backward_dw2_cols(x, idx, w, w1, w2, g, pairs, interleave=I, clamp=c,
-                                    mask_bf16=True)
+                                    mask_f32=True, magnitude=magnitude)
     for i, (e, f) in enumerate(pairs):
         np.testing.assert_allclose(cols[i], full["dw2"][e, :, f], rtol=1e-12, atol=1e-14)
 
 
-def test_bf16_masks_differ_only_at_the_clamp_boundary():
-    # without a clamp the mask precision cannot matter
+def test_mask_precision_matters_only_with_a_clamp():
     x, logits, w1, w2, g = _case(seed=4)
-    a = oracle.moe_backward(x, logits, w1, w2, g, 2, mask_bf16=False)
-    b = oracle.moe_backward(x, logits, w1, w2, g, 2, mask_bf16=True)
+    a = oracle.moe_backward(x, logits, w1, w2, g, 2, mask_f32=False)
+    b = oracle.moe_backward(x, logits, w1, w2, g, 2, mask_f32=True)
     for name in ("dx", "dw1", "dw2"):
         np.testing.assert_array_equal(a[name], b[name])
+    # with a clamp, values more than an fp32 rounding away from it decide alike
+    a = oracle.moe_backward(x, logits, w1, w2, g, 2, clamp=0.8, mask_f32=False)
+    b = oracle.moe_backward(x, logits, w1, w2, g, 2, clamp=0.8, mask_f32=True)
+    for name in ("dx", "dw1", "dw2"):
+        np.testing.assert_array_equal(a[name], b[name])
+
+
+@pytest.mark.parametrize("renormalize", [True, False])
+def test_magnitudes_bound_the_gradients(renormalize):
+    x, logits, w1, w2, g = _case(T=14, E=5, k=2, S=1, seed=12)
+    kw = dict(renormalize=renormalize, interleave=8, clamp=0.8, shared_experts=1)
+    v = oracle.moe_backward(x, logits, w1, w2, g, 2, **kw)
+    m = oracle.moe_backward(x, logits, w1, w2, g, 2, magnitude=True, **kw)
+    for name in ("dx", "dlogits", "dw1", "dw2", "dw_route"):
+        assert (m[name] >= np.abs(v[name]) * (1 - 1e-12)).all(), name
+        assert (m[name] >= 0).all(), name
+    # the magnitudes do not see the sign of the output gradient
+    mneg = oracle.moe_backward(x, logits, w1, w2, (-g.float()).to(torch.bfloat16), 2,
+                               magnitude=True, **kw)
+    for name in ("dx", "dlogits", "dw1", "dw2"):
+        np.testing.assert_allclose(mneg[name], m[name], rtol=1e-12, atol=0)
+
+
+def test_magnitude_of_a_single_term_is_its_absolute_value():
+    # one token, one expert: every dW element is a single product
+    x, logits, w1, w2, g = _case(T=1, E=1, k=1, seed=13)
+    v = oracle.moe_backward(x, logits, w1, w2, g, 1, clamp=0.8)
+    m = oracle.moe_backward(x, logits, w1, w2, g, 1, clamp=0.8, magnitude=True)
+    np.testing.assert_allclose(m["dw1"], np.abs(v["dw1"]), rtol=1e-12, atol=0)
+    np.testing.assert_allclose(m["dw2"], np.abs(v["dw2"]), rtol=1e-12, atol=0)
