@@ -7,7 +7,7 @@ top-2, bf16).  Its 2.8 GB of weights exceed the 129 MB L2, so no flush is
 needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload mixtral|skewed|decode|tiny] [--T T]
+                  [--workload mixtral|skewed|decode|tiny] [--T T] [--backward]
 
 Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
 own batch of T tokens with the same weights (weak scaling, no data-path
@@ -15,6 +15,9 @@ collective); the step time is the maximum over ranks.
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload on this machine's host cores (rank 0 only).
+
+--backward times moe_backward instead (dx, logit, dW1 and dW2 gradients of
+the same workload, bf16), with its own metric line.
 """
 from __future__ import annotations
 
@@ -36,6 +39,13 @@ import torch  # noqa: E402
 import moe_inputs as mi  # noqa: E402
 
 METRIC = "MoE layer fwd TFLOP/s & tokens/s at 1 GB300; % of tensor/HBM roofline"
+METRIC_BWD = "MoE layer bwd TFLOP/s & tokens/s at 1 GB300; % of tensor roofline"
+# Backward stages that are grouped GEMMs, with their algorithmic FLOPs in
+# units of R*H*F (the pre-activation recompute is the backward's own choice:
+# timed, but not counted in the layer's backward FLOPs)
+BWD_GEMMS = {"gemm1_recompute": 4.0, "dgrad_h_swiglu": 2.0, "wgrad_w2": 2.0, "dgrad_x": 4.0,
+             "wgrad_w1": 4.0}
+BWD_KERNEL = ("grouped_gemm_bwd.cu", "grouped_gemm_bwd_kernel")
 # GEMM kernel (file and instance) behind each moe_problem.kernel value
 KERNEL_NAMES = {1: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU> (GEMM1, 1-CTA 128x256 tiles)"),
                 2: ("grouped_gemm_swap.cu", "grouped_gemm_swap_kernel<SwiGLU,32> (GEMM1)"),
@@ -76,6 +86,8 @@ def parse_args(argv=None):
                     help="FP4 weight format of the lowprec workload")
     ap.add_argument("--fusion", type=int, default=0,
                     help="moe_problem.fusion bits: 1 = TMA-gather A rows, 2 = combine in GEMM2")
+    ap.add_argument("--backward", action="store_true",
+                    help="time moe_backward (the layer's gradients) instead of the forward")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args(argv)
@@ -473,6 +485,230 @@ def bench_ours(args, shape, desc):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ backward
+
+def bwd_flops(shape) -> float:
+    """Algorithmic FLOPs of the backward: dH 2RHF + dX 4RHF + dW2 2RHF + dW1 4RHF."""
+    return 12.0 * shape.R * shape.H * shape.F
+
+
+def oracle_bwd_sample(shape, host, n_tokens: int):
+    """The oracle's per-token backward (recomputed forward, dh, dx and the
+    route-weight gradients) on the first n tokens; returns (seconds, flops
+    performed: 12 H F per route)."""
+    import oracle
+    idx, w = oracle.route_topk(host["logits"][:n_tokens], shape.k)
+    t0 = time.perf_counter()
+    oracle.backward_tokens(host["x"][:n_tokens], idx, w, host["w1"], host["w2"],
+                           host["g"][:n_tokens], list(range(n_tokens)),
+                           interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
+    return time.perf_counter() - t0, 12.0 * n_tokens * shape.k * shape.H * shape.F
+
+
+def cpu_baseline_bwd(shape, host, target_s: float):
+    import oracle
+    oracle.build()
+    n = 1
+    while True:
+        dt, flops = oracle_bwd_sample(shape, host, n)
+        if dt >= target_s / 3 or n >= shape.T:
+            break
+        n = int(min(shape.T, max(2 * n, n * 0.8 * target_s / max(dt, 1e-6))))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"dx and route-weight gradients of the first {n} of {shape.T} tokens "
+                      f"(fp64 oracle per-token backward, {dt:.1f} s)"}
+
+
+def bench_backward(args, shape, desc):
+    import mixture_experts_ffn_permute_gb300 as moe
+    from mixture_experts_ffn_permute_gb300 import _build
+
+    rank, world, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    _build.build()
+    moe.load()
+    peaks, peak_src = load_peaks()
+    if shape.lowprec:
+        raise SystemExit("the backward is bf16 only")
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True,
+                         shape.glu_interleave, shape.swiglu_clamp)
+    ws = moe.alloc_backward_workspace(p, dev)
+    stream = torch.cuda.current_stream(dev)
+    w1 = mi.make_w1(shape, 0, dev)
+    w2 = mi.make_w2(shape, 0, dev)
+    x = mi.make_x(shape, rank, dev)
+    logits = mi.make_logits(shape, rank, dev)
+    g = mi.make_grad_out(shape, rank, dev)
+    dx = torch.empty_like(x)
+    dl = torch.empty(shape.T, shape.E, dtype=torch.float32, device=dev)
+    dw1 = torch.empty_like(w1)
+    dw2 = torch.empty_like(w2)
+    weight_bytes = 2 * (w1.numel() + w2.numel())
+
+    def bwd(xx, ll, gg):
+        moe.backward(p, xx, ll, w1, w2, gg, dx, dw1, dw2, ws, d_logits=dl)
+
+    moe.clear_device_status(ws)
+    for _ in range(max(args.warmup, 3)):
+        bwd(x, logits, g)
+    torch.cuda.synchronize()
+    launches_per_step = moe.last_launch_count()
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        moe.stage_timing_begin(K)
+        ev0.record(stream)
+        for _ in range(K):
+            bwd(x, logits, g)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        stages = moe.stage_timing_end()
+        barrier(world)
+    status = moe.get_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status, status)}")
+    ms = reduce_max(ev0.elapsed_time(ev1) / K, world, dev)
+    sec = ms / 1e3
+
+    # end to end: x, logits and dOut from pinned host memory each step, dx and
+    # the logit gradient back; the weight gradients stay on the device (the
+    # optimizer's input)
+    step_inputs = [x, logits, g]
+    hosts = [t.cpu().pin_memory() for t in step_inputs]
+    devs = [torch.empty_like(t) for t in step_inputs]
+    outs = [dx, dl]
+    out_h = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+
+    def e2e_step():
+        for hsrc, ddst in zip(hosts, devs):
+            ddst.copy_(hsrc, non_blocking=True)
+        bwd(*devs)
+        for src, dst in zip(outs, out_h):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    K2 = max(3, K // 2)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / K2, world, dev)
+
+    flops = bwd_flops(shape)
+    rhf = float(shape.R) * shape.H * shape.F
+    gemm_ms = {k: stages[k] for k in BWD_GEMMS if k in stages}
+    top = max(gemm_ms, key=gemm_ms.get)
+    top_flops = BWD_GEMMS[top] * rhf
+    peak_key = "bf16_tflops_sustained"
+    achieved = top_flops / (gemm_ms[top] / 1e3) / 1e12
+    wl = ("backward-" + args.workload) if not args.T and not args.E and not args.k else "custom"
+    line = {
+        "metric": METRIC_BWD,
+        "value": world * flops / sec / 1e12,
+        "unit": "TFLOP/s",
+        "tokens_per_s": world * shape.T / sec,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": desc + " -- backward (dx, d logits, dW1, dW2)", "T": shape.T,
+                   "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k,
+                   "timing": "eager launches",
+                   "l2": "inputs larger than L2 (weights %.2f GB), no flush" % (weight_bytes / 1e9),
+                   "flops": "12*R*H*F (dH 2, dX 4, dW2 2, dW1 4); the 4*R*H*F recompute of "
+                            "the pre-activations is timed but not counted"},
+        "roofline": {"kernel": f"{BWD_KERNEL[1]} ({top})", "bound": "tensor",
+                     "achieved": achieved, "peak": peaks[peak_key], "unit": "TFLOP/s",
+                     "frac": achieved / peaks[peak_key],
+                     "traffic": ncu_traffic(BWD_KERNEL[0], wl + ":" + top),
+                     "peak_source": f"{peak_key} ({peak_src})",
+                     "algorithmic": {"flops": top_flops}},
+        "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in step_inputs),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+        "stages_ms": {k: round(v, 5) for k, v in stages.items() if not k.startswith("_")},
+        "stage_tflops": {k: round(BWD_GEMMS[k] * rhf / (v / 1e3) / 1e12, 1)
+                         for k, v in gemm_ms.items()},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {"x": x.cpu(), "logits": logits.cpu(), "w1": w1.cpu(), "w2": w2.cpu(),
+                "g": g.cpu()}
+        line["cpu_baseline"] = cpu_baseline_bwd(shape, host, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def bench_reference_backward(args, shape, desc):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    n_max = 16
+    logits = mi.make_logits(shape, 0)[:n_max]
+    idx, _ = oracle.route_topk(logits, shape.k)
+    used = sorted(set(idx.ravel().tolist()))
+    w1 = [None] * shape.E
+    w2 = [None] * shape.E
+    for e in used:  # same distributions as moe_inputs, drawn per used expert
+        gen = torch.Generator().manual_seed(1000 + e)
+        w1[e] = torch.randn(2 * shape.F, shape.H, generator=gen).mul_(
+            1 / math.sqrt(shape.H)).to(torch.bfloat16)
+        w2[e] = torch.randn(shape.H, shape.F, generator=gen).mul_(
+            1 / math.sqrt(shape.F)).to(torch.bfloat16)
+    host = {"x": mi.make_x(shape.with_T(n_max), 0), "logits": logits, "w1": w1, "w2": w2,
+            "g": mi.make_grad_out(shape.with_T(n_max), 0)}
+    steps, warm = args.steps, max(args.warmup, 1)
+    dt1, _ = oracle_bwd_sample(shape, host, 1)
+    budget = 150.0 / (steps + warm)
+    n = int(max(1, min(n_max, math.floor(budget / max(dt1, 1e-6)))))
+    for _ in range(warm - 1):
+        oracle_bwd_sample(shape, host, n)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(steps):
+        _, flops = oracle_bwd_sample(shape, host, n)
+    dt = (time.perf_counter() - t0) / steps
+    val = flops / dt / 1e12
+    line = {
+        "metric": METRIC_BWD, "impl": "reference", "value": val, "unit": "TFLOP/s",
+        "tokens_per_s": n / dt, "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc + " -- backward (dx, d logits, dW1, dW2)", "T": shape.T,
+                   "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"dx and route-weight gradients of the first {n} of "
+                                   f"{shape.T} tokens per step (fp64 oracle)"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm
 
 def bench_reference(args, shape, desc):
@@ -549,7 +785,10 @@ def main(argv=None):
         desc = desc + f" T={shape.T}"
     if shape.lowprec and args.wfmt == "mxfp4":
         desc = desc.replace("NVFP4", "MXFP4")
-    if args.impl == "reference":
+    if args.backward:
+        (bench_reference_backward if args.impl == "reference" else bench_backward)(
+            args, shape, desc)
+    elif args.impl == "reference":
         bench_reference(args, shape, desc)
     else:
         bench_ours(args, shape, desc)
