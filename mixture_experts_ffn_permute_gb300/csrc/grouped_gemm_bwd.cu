@@ -47,10 +47,14 @@ namespace moe {
 // (grouped_gemm.cu).
 bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
+bool make_map_2d_plain(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint32_t box_cols, uint32_t box_rows);
 
 namespace {
 
-constexpr int kStagesB = 4;
+// pipeline depth: the weight gradients trade a stage for output staging
+template <int kMode>
+__host__ __device__ constexpr int stages_of() { return kMode == 2 ? 3 : 4; }
 constexpr int kThreadsB = 192;
 constexpr uint32_t kABytesB = kBM * kBK * 2;             // 16 KB
 constexpr uint32_t kBBytesB = kBN * kBK * 2;             // 32 KB
@@ -59,12 +63,39 @@ constexpr uint32_t kBoxBytes = 64 * 64 * 2;              // one MN-major box, 8 
 constexpr uint32_t kStepBytesMN = 16 * 128;              // one K=16 step of an MN-major tile
 constexpr uint32_t kTmemColsB = 2 * kBN;
 constexpr int kMaxEB = MOE_MAX_EXPERTS;
-static_assert((2 * kStagesB + 5) * 8 + 8 <= 256, "barrier area");
-constexpr size_t kSmemBytesB = 1024 + kStagesB * kStageBytesB + 256 +
-                               2 * (kMaxEB + 1) * sizeof(int32_t);
-static_assert(kSmemBytesB <= 232448, "shared memory budget");
+// weight-gradient output staging, in 64-column x 32-row boxes with the
+// 128-byte swizzle: experts with few rows (short K loops, mode 2) stage 128
+// columns per step in two buffers per epilogue warp (64 KB, 3 pipeline
+// stages); experts with many rows (mode 4) keep 4 pipeline stages and stage 64
+// columns per step in one buffer per warp (16 KB)
+constexpr uint32_t kOutBoxBytes = 32 * 128;  // 32 rows x 64 bf16
+template <int kMode>
+__host__ __device__ constexpr int out_step_cols() { return kMode == 2 ? 128 : 64; }
+template <int kMode>
+__host__ __device__ constexpr int out_buffers() { return kMode == 2 ? 2 : 1; }
+template <int kMode>
+__host__ __device__ constexpr uint32_t out_stage_bytes() {
+  return (kMode == 2 || kMode == 4)
+             ? 4 * out_buffers<kMode>() * (out_step_cols<kMode>() / 64) * kOutBoxBytes
+             : 0;
+}
+template <int kMode>
+constexpr size_t smem_bytes_of() {
+  return 1024 + stages_of<kMode>() * kStageBytesB + out_stage_bytes<kMode>() + 256 +
+         2 * (kMaxEB + 1) * sizeof(int32_t);
+}
+static_assert((2 * 4 + 5) * 8 + 8 <= 256, "barrier area");
+static_assert(smem_bytes_of<0>() <= 232448 && smem_bytes_of<2>() <= 232448 &&
+                  smem_bytes_of<4>() <= 232448,
+              "shared memory budget");
 
-enum class BwdMode : int { kDataPlain = 0, kDataSwiGLU = 1, kWeight = 2, kPreact = 3 };
+enum class BwdMode : int {
+  kDataPlain = 0,
+  kDataSwiGLU = 1,
+  kWeight = 2,      // weight gradients, experts with few rows
+  kPreact = 3,
+  kWeightLong = 4   // weight gradients, experts with many rows
+};
 
 struct BwdParams {
   const int32_t* expert_offsets;  // [E + 1]
@@ -106,7 +137,7 @@ __device__ __forceinline__ int find_expert_b(const int32_t* mtp, int E, int q) {
 template <BwdMode kMode>
 __device__ __forceinline__ BTile decode_btile(int tile, const int32_t* mtp, const BwdParams& p) {
   BTile t;
-  if (kMode == BwdMode::kWeight) {
+  if (kMode == BwdMode::kWeight || kMode == BwdMode::kWeightLong) {
     const int per = p.m_tiles * p.n_tiles;
     t.e = tile / per;
     const int local = tile - t.e * per;
@@ -163,23 +194,28 @@ __device__ __forceinline__ int up_col(int f, int F, int I) {
 template <BwdMode kMode>
 __global__ void __launch_bounds__(kThreadsB, 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
-                        const __grid_constant__ CUtensorMap map_b, const BwdParams p) {
+                        const __grid_constant__ CUtensorMap map_b,
+                        const __grid_constant__ CUtensorMap map_out, const BwdParams p) {
   pdl_enter();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;
+  constexpr int kStagesB = stages_of<static_cast<int>(kMode)>();
+  constexpr uint32_t kOutStageBytes = out_stage_bytes<static_cast<int>(kMode)>();
   uint8_t* sB = smem + kStagesB * kABytesB;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStagesB * kBBytesB);
+  uint8_t* s_out = sB + kStagesB * kBBytesB;  // kWeight: output staging (1024-aligned)
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_out + kOutStageBytes);
   uint64_t* empty = full + kStagesB;
   uint64_t* tfull = empty + kStagesB;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStagesB * kStageBytesB + 256);
+  int32_t* s_off =
+      reinterpret_cast<int32_t*>(smem + kStagesB * kStageBytesB + kOutStageBytes + 256);
   int32_t* s_mtp = s_off + (p.E + 1);
 
-  constexpr bool kWeightGrad = kMode == BwdMode::kWeight;
+  constexpr bool kWeightGrad = kMode == BwdMode::kWeight || kMode == BwdMode::kWeightLong;
   constexpr bool kBKMajor = kMode == BwdMode::kPreact;  // B = weight rows, K-major
   constexpr uint32_t kIdescB = idesc_bwd(kWeightGrad, !kBKMajor);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -203,6 +239,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&map_a);
     prefetch_tensormap(&map_b);
+    if (kWeightGrad) prefetch_tensormap(&map_out);
   }
   if (warp == 1) tmem_alloc<kTmemColsB>(tmem_slot);
   tc_fence_before();
@@ -286,21 +323,26 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
         ok = lane == 0 ? (mbar_wait(&full[stage], phase, p.status) ? 1 : 0) : 1;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        int nkk = kBK / 16;  // K=16 MMA steps of this stage
         if (kWeightGrad) {
           const int valid = rows_of(t.e) - kb * kBK;
           if (valid < kBK) {
-            // rows valid..63 of each of the six boxes are the next expert's
-            // (or past the matrix): zero them, then hand the writes to the
-            // async proxy the MMA reads through
-            __syncwarp();
-            const int per_box = (kBK - valid) * 8;  // 16-byte vectors per box
-            for (int i = lane; i < 6 * per_box; i += 32) {
-              const int b = i / per_box, v = i - b * per_box;
-              uint8_t* box = b < 2 ? sA + stage * kABytesB + b * kBoxBytes
-                                   : sB + stage * kBBytesB + (b - 2) * kBoxBytes;
-              reinterpret_cast<uint4*>(box + valid * 128)[v] = make_uint4(0, 0, 0, 0);
+            // the MMAs read rows 0 .. 16*nkk-1; rows valid .. 16*nkk-1 of each
+            // of the six boxes are the next expert's (or past the matrix):
+            // zero them, then hand the writes to the async proxy the MMA reads
+            nkk = (valid + 15) / 16;
+            const int zrows = 16 * nkk - valid;
+            if (zrows > 0) {
+              __syncwarp();
+              const int per_box = zrows * 8;  // 16-byte vectors per box
+              for (int i = lane; i < 6 * per_box; i += 32) {
+                const int b = i / per_box, v = i - b * per_box;
+                uint8_t* box = b < 2 ? sA + stage * kABytesB + b * kBoxBytes
+                                     : sB + stage * kBBytesB + (b - 2) * kBoxBytes;
+                reinterpret_cast<uint4*>(box + valid * 128)[v] = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_shared();
             }
-            fence_proxy_async_shared();
           }
           __syncwarp();
         }
@@ -310,6 +352,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
           const uint32_t b_addr = smem_u32(sB + stage * kBBytesB);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
+            if (kk >= nkk) break;
             const uint64_t a_desc = kWeightGrad
                                         ? sw128_mnmajor_desc(a_addr + kk * kStepBytesMN)
                                         : sw128_kmajor_desc(a_addr) + 2 * kk;
@@ -341,6 +384,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
     const int quad = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quad * 32 + lane;
     int local = 0;
+    int n_stores = 0;  // bulk-tensor stores this warp issued (kWeight)
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const int buf = local & 1;
@@ -354,63 +398,109 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
       const BTile t = decode_btile<kMode>(tile, s_mtp, p);
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN;
       const int col0 = t.n * kBN;
-      if (kMode == BwdMode::kWeight) {
-        const long orow = static_cast<long>(t.e) * p.M + t.m * kBM + row_in_tile;
-        uint4* dst = p.out + orow * p.ldo_vec + col0 / 8;
-        const bool none = rows_of(t.e) == 0;
+      // chunks of 32 columns, read from TMEM two at a time (one wait per pair)
+      const int nch = min(kBN / 32, (p.N - col0) / 32);
+      auto chunk_pairs = [&](bool zeros, auto&& handle) {
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
-          uint32_t a[32];
-          if (none) {
+        for (int c = 0; c < nch; c += 2) {
+          uint32_t a0[32], a1[32];
+          const bool two = c + 1 < nch;
+          if (zeros) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = 0u;
+            for (int i = 0; i < 32; ++i) a0[i] = a1[i] = 0u;
           } else {
-            tmem_ld_32x32b_x32(t_lane + c * 32, a);
+            tmem_ld_32x32b_x32(t_lane + c * 32, a0);
+            if (two) tmem_ld_32x32b_x32(t_lane + (c + 1) * 32, a1);
             tmem_ld_wait();
           }
+          handle(c, a0);
+          if (two) handle(c + 1, a1);
+        }
+      };
+      if (kWeightGrad) {
+        // each warp's 32 rows x kStep columns staged in shared memory as
+        // 64-column boxes with the 128-byte swizzle (lane r puts 16-byte
+        // chunk j of its row at slot j ^ (r % 8): no bank conflicts), then
+        // bulk-tensor stores; kNB buffers per warp alternate
+        constexpr int kStep = out_step_cols<static_cast<int>(kMode)>();
+        constexpr int kNB = out_buffers<static_cast<int>(kMode)>();
+        constexpr uint32_t kBufBytes = (kStep / 64) * kOutBoxBytes;
+        const int orow0 = t.e * p.M + t.m * kBM + quad * 32;
+        const bool none = rows_of(t.e) == 0;
+        uint8_t* stg = s_out + (warp - 2) * kNB * kBufBytes;
+        const int rsw = lane & 7;
+#pragma unroll 1
+        for (int h = 0; h < kBN / kStep; ++h) {
+          const int c0 = col0 + h * kStep;
+          if (c0 >= p.N) break;
+          const int nq = min(kStep / 32, (p.N - c0) / 32);
+          uint8_t* buf = stg + (n_stores % kNB) * kBufBytes;
+          if (lane == 0) bulk_wait_group_read<kNB - 1>();  // the buffer's last stores read it
+          __syncwarp();
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[c * 4 + v] = make_uint4(
-                pack2_bf16(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
-                pack2_bf16(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3])),
-                pack2_bf16(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5])),
-                pack2_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
+          for (int qp = 0; qp < kStep / 32; qp += 2) {  // two 32-column chunks per TMEM wait
+            if (qp >= nq) break;
+            uint32_t a[2][32];
+            if (none) {
+#pragma unroll
+              for (int i2 = 0; i2 < 32; ++i2) a[0][i2] = a[1][i2] = 0u;
+            } else {
+              tmem_ld_32x32b_x32(t_lane + h * kStep + qp * 32, a[0]);
+              if (qp + 1 < nq) tmem_ld_32x32b_x32(t_lane + h * kStep + (qp + 1) * 32, a[1]);
+              tmem_ld_wait();
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int q = qp + u;
+              if (q < nq) {
+                uint8_t* row = buf + (q >> 1) * kOutBoxBytes + lane * 128;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  const int jj = (q & 1) * 4 + v;
+                  *reinterpret_cast<uint4*>(row + ((jj ^ rsw) << 4)) = make_uint4(
+                      pack2_bf16(__uint_as_float(a[u][8 * v + 0]), __uint_as_float(a[u][8 * v + 1])),
+                      pack2_bf16(__uint_as_float(a[u][8 * v + 2]), __uint_as_float(a[u][8 * v + 3])),
+                      pack2_bf16(__uint_as_float(a[u][8 * v + 4]), __uint_as_float(a[u][8 * v + 5])),
+                      pack2_bf16(__uint_as_float(a[u][8 * v + 6]), __uint_as_float(a[u][8 * v + 7])));
+                }
+              }
+            }
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < kStep / 64; ++b)
+              if (c0 + 64 * b < p.N) tma_store_2d(&map_out, buf + b * kOutBoxBytes, c0 + 64 * b, orow0);
+            bulk_commit_group();
+          }
+          ++n_stores;
         }
       } else {
         const bool row_ok = t.m * kBM + row_in_tile < rows_of(t.e);
         const long out_row = static_cast<long>(s_off[t.e]) + t.m * kBM + row_in_tile;
         if (kMode == BwdMode::kPreact) {
           float4* dst = reinterpret_cast<float4*>(p.out) + out_row * p.ldo_vec + col0 / 4;
-#pragma unroll 1
-          for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
-            uint32_t a[32];
-            tmem_ld_32x32b_x32(t_lane + c * 32, a);
-            tmem_ld_wait();
-            if (row_ok) {
+          chunk_pairs(false, [&](int c, const uint32_t(&a)[32]) {
+            if (!row_ok) return;
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[c * 8 + v] = make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
-                                             __uint_as_float(a[4 * v + 2]),
-                                             __uint_as_float(a[4 * v + 3]));
-            }
-          }
+            for (int v = 0; v < 8; ++v)
+              dst[c * 8 + v] = make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
+                                           __uint_as_float(a[4 * v + 2]),
+                                           __uint_as_float(a[4 * v + 3]));
+          });
         } else if (kMode == BwdMode::kDataPlain) {
           uint4* dst = p.out + out_row * p.ldo_vec + col0 / 8;
-#pragma unroll 1
-          for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
-            uint32_t a[32];
-            tmem_ld_32x32b_x32(t_lane + c * 32, a);
-            tmem_ld_wait();
-            if (row_ok) {
+          chunk_pairs(false, [&](int c, const uint32_t(&a)[32]) {
+            if (!row_ok) return;
 #pragma unroll
-              for (int v = 0; v < 4; ++v)
-                dst[c * 4 + v] = make_uint4(
-                    pack2_bf16(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
-                    pack2_bf16(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3])),
-                    pack2_bf16(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5])),
-                    pack2_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
-            }
-          }
+            for (int v = 0; v < 4; ++v)
+              dst[c * 4 + v] = make_uint4(
+                  pack2_bf16(__uint_as_float(a[8 * v + 0]), __uint_as_float(a[8 * v + 1])),
+                  pack2_bf16(__uint_as_float(a[8 * v + 2]), __uint_as_float(a[8 * v + 3])),
+                  pack2_bf16(__uint_as_float(a[8 * v + 4]), __uint_as_float(a[8 * v + 5])),
+                  pack2_bf16(__uint_as_float(a[8 * v + 6]), __uint_as_float(a[8 * v + 7])));
+          });
         } else {
           // SwiGLU backward of 32 columns f at a time: dh (unweighted) from
           // TMEM, g and u from the fp32 pre-activations (the clamp decisions
@@ -425,17 +515,27 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll 1
           for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
             const int f0 = col0 + c * 32;
+            const int gc0 = gate_col(f0, p.F, p.interleave);
+            const int uc0 = up_col(f0, p.F, p.interleave);
+            // all 64 pre-activations of the chunk in flight before the TMEM
+            // load: one memory round trip per chunk
+            float4 ga[8], ua[8];
+            if (row_ok) {
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4) {
+                ga[q4] = __ldg(arow + gc0 / 4 + q4);
+                ua[q4] = __ldg(arow + uc0 / 4 + q4);
+              }
+            }
             uint32_t d[32];
             tmem_ld_32x32b_x32(t_lane + c * 32, d);
             tmem_ld_wait();
             if (!row_ok) continue;
-            const int gc0 = gate_col(f0, p.F, p.interleave);
-            const int uc0 = up_col(f0, p.F, p.interleave);
             uint32_t dgp[16], dup[16], hp[16];
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {  // 4 columns per step
-              const float4 g4 = __ldg(arow + gc0 / 4 + q4);
-              const float4 u4 = __ldg(arow + uc0 / 4 + q4);
+              const float4 g4 = ga[q4];
+              const float4 u4 = ua[q4];
               const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
               const float us[4] = {u4.x, u4.y, u4.z, u4.w};
               float dg[4], du[4], hh[4];
@@ -479,6 +579,9 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
       tc_fence_before();
       mbar_arrive(&tempty[buf]);
     }
+    // the staged outputs must be written before the CTA's shared memory goes
+    if (kWeightGrad && lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -490,14 +593,15 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
 }
 
 template <BwdMode kMode>
-cudaError_t launch_bwd_impl(const CUtensorMap& ma, const CUtensorMap& mb, const BwdParams& kp,
-                            int grid, cudaStream_t s) {
+cudaError_t launch_bwd_impl(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                            const BwdParams& kp, int grid, cudaStream_t s) {
   auto kern = grouped_gemm_bwd_kernel<kMode>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytesB));
+                                         static_cast<int>(smem_bytes_of<static_cast<int>(kMode)>()));
   if (err != cudaSuccess) return err;
-  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsB), kSmemBytesB, s,
-                       1, ma, mb, kp);
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsB),
+                       smem_bytes_of<static_cast<int>(kMode)>(), s,
+                       1, ma, mb, mo, kp);
 }
 
 }  // namespace
@@ -527,6 +631,12 @@ cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s) {
                           static_cast<uint64_t>(g.N), 64u)) {
     return cudaErrorInvalidValue;
   }
+  // weight gradients: the output [E * M, N] in 64-column x 32-row boxes
+  // (128-byte swizzle) for the bulk-tensor stores; unused by other modes
+  CUtensorMap mo = ma;
+  if (weight && !make_map_2d(&mo, g.out, static_cast<uint64_t>(g.E) * static_cast<uint64_t>(g.M),
+                             static_cast<uint64_t>(g.N), 32u))
+    return cudaErrorInvalidValue;
   BwdParams kp{};
   kp.expert_offsets = g.expert_offsets;
   kp.mtile_prefix = g.mtile_prefix;
@@ -557,10 +667,15 @@ cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s) {
   }
   const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
   switch (g.mode) {
-    case kBwdDataPlain: return launch_bwd_impl<BwdMode::kDataPlain>(ma, mb, kp, grid, s);
-    case kBwdDataSwiGLU: return launch_bwd_impl<BwdMode::kDataSwiGLU>(ma, mb, kp, grid, s);
-    case kBwdWeight: return launch_bwd_impl<BwdMode::kWeight>(ma, mb, kp, grid, s);
-    case kBwdPreact: return launch_bwd_impl<BwdMode::kPreact>(ma, mb, kp, grid, s);
+    case kBwdDataPlain: return launch_bwd_impl<BwdMode::kDataPlain>(ma, mb, mo, kp, grid, s);
+    case kBwdDataSwiGLU: return launch_bwd_impl<BwdMode::kDataSwiGLU>(ma, mb, mo, kp, grid, s);
+    case kBwdWeight:
+      // experts averaging 512 rows or more: K loops long enough to want the
+      // fourth pipeline stage more than the wider output staging
+      return static_cast<long>(g.R) >= 512L * g.E
+                 ? launch_bwd_impl<BwdMode::kWeightLong>(ma, mb, mo, kp, grid, s)
+                 : launch_bwd_impl<BwdMode::kWeight>(ma, mb, mo, kp, grid, s);
+    case kBwdPreact: return launch_bwd_impl<BwdMode::kPreact>(ma, mb, mo, kp, grid, s);
   }
   return cudaErrorInvalidValue;
 }

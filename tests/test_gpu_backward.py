@@ -79,6 +79,8 @@ SMALL = [
     mi.MoEShape("il64", T=150, H=512, F=256, E=5, k=3, glu_interleave=64, swiglu_clamp=1.2),
     mi.MoEShape("il128", T=90, H=256, F=256, E=4, k=2, glu_interleave=128),
     mi.MoEShape("deep", T=700, H=256, F=256, E=2, k=1),
+    # >= 512 rows per expert on average: the 4-stage weight-gradient variant
+    mi.MoEShape("long", T=1100, H=256, F=384, E=2, k=1, glu_interleave=64, swiglu_clamp=1.0),
     mi.MoEShape("skew", T=160, H=256, F=256, E=16, k=2, zipf_s=1.5),
     mi.MoEShape("one", T=1, H=256, F=256, E=8, k=2),
 ]
