@@ -564,6 +564,22 @@ bool make_map_2d_plain(CUtensorMap* map, const void* base, uint64_t rows, uint64
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [rows, cols] map with 32-column x box_rows boxes (128 bytes wide) and
+// the 128-byte swizzle (fp32 tiles staged in shared memory for bulk stores).
+bool make_map_2d_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32u, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // uint8 [rows, cols] map with 32-byte x 128-row boxes and no swizzle (packed
 // E2M1 weight codes, two per byte).
 bool make_map_u8(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

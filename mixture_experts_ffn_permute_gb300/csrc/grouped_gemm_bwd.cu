@@ -47,8 +47,8 @@ namespace moe {
 // (grouped_gemm.cu).
 bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
-bool make_map_2d_plain(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                       uint32_t box_cols, uint32_t box_rows);
+bool make_map_2d_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows);
 
 namespace {
 
@@ -77,7 +77,8 @@ template <int kMode>
 __host__ __device__ constexpr uint32_t out_stage_bytes() {
   return (kMode == 2 || kMode == 4)
              ? 4 * out_buffers<kMode>() * (out_step_cols<kMode>() / 64) * kOutBoxBytes
-             : 0;
+         : kMode == 3 ? 4 * kOutBoxBytes  // fp32 pre-activations: 32 x 32 per warp
+                      : 0;
 }
 template <int kMode>
 constexpr size_t smem_bytes_of() {
@@ -86,7 +87,7 @@ constexpr size_t smem_bytes_of() {
 }
 static_assert((2 * 4 + 5) * 8 + 8 <= 256, "barrier area");
 static_assert(smem_bytes_of<0>() <= 232448 && smem_bytes_of<2>() <= 232448 &&
-                  smem_bytes_of<4>() <= 232448,
+                  smem_bytes_of<3>() <= 232448 && smem_bytes_of<4>() <= 232448,
               "shared memory budget");
 
 enum class BwdMode : int {
@@ -106,6 +107,7 @@ struct BwdParams {
   int n_tiles;  // ceil(N / 256)
   int M;        // weight gradients: output rows per expert
   int m_tiles;  // M / 128
+  int m_outer;  // weight gradients: 1 = the n-tiles of one m-tile adjacent
   uint4* out;   // data: [R, N] bf16; weight: [E, M, N] bf16; pre-activations [R, N] fp32
   int ldo_vec;  // N / 8 (bf16) or N / 4 (fp32)
   // SwiGLU backward
@@ -141,8 +143,15 @@ __device__ __forceinline__ BTile decode_btile(int tile, const int32_t* mtp, cons
     const int per = p.m_tiles * p.n_tiles;
     t.e = tile / per;
     const int local = tile - t.e * per;
-    t.n = local / p.m_tiles;  // m-tiles of one n-tile adjacent: B columns shared from L2
-    t.m = local - t.n * p.m_tiles;
+    // the larger operand's column blocks outermost, so each is streamed once
+    // while the smaller one stays in L2
+    if (p.m_outer) {
+      t.m = local / p.n_tiles;
+      t.n = local - t.m * p.n_tiles;
+    } else {
+      t.n = local / p.m_tiles;
+      t.m = local - t.n * p.m_tiles;
+    }
   } else {
     const int q = tile / p.n_tiles;
     t.e = find_expert_b(mtp, p.E, q);
@@ -239,7 +248,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&map_a);
     prefetch_tensormap(&map_b);
-    if (kWeightGrad) prefetch_tensormap(&map_out);
+    if (kWeightGrad || kMode == BwdMode::kPreact) prefetch_tensormap(&map_out);
   }
   if (warp == 1) tmem_alloc<kTmemColsB>(tmem_slot);
   tc_fence_before();
@@ -480,14 +489,36 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
         const bool row_ok = t.m * kBM + row_in_tile < rows_of(t.e);
         const long out_row = static_cast<long>(s_off[t.e]) + t.m * kBM + row_in_tile;
         if (kMode == BwdMode::kPreact) {
+          // a warp whose 32 rows all belong to the expert stages each 32 x 32
+          // fp32 chunk (128-byte swizzle) and bulk-stores it; a ragged warp
+          // stores its valid rows directly
+          const bool warp_full = t.m * kBM + quad * 32 + 32 <= rows_of(t.e);
+          uint8_t* stg = s_out + (warp - 2) * kOutBoxBytes;
+          const int rsw = lane & 7;
+          const long orow0 = static_cast<long>(s_off[t.e]) + t.m * kBM + quad * 32;
           float4* dst = reinterpret_cast<float4*>(p.out) + out_row * p.ldo_vec + col0 / 4;
           chunk_pairs(false, [&](int c, const uint32_t(&a)[32]) {
-            if (!row_ok) return;
+            if (warp_full) {
+              if (lane == 0) bulk_wait_group_read<0>();  // the buffer's last store read it
+              __syncwarp();
+              uint8_t* row = stg + lane * 128;
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[c * 8 + v] = make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
-                                           __uint_as_float(a[4 * v + 2]),
-                                           __uint_as_float(a[4 * v + 3]));
+              for (int v = 0; v < 8; ++v)
+                *reinterpret_cast<uint4*>(row + ((v ^ rsw) << 4)) =
+                    make_uint4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&map_out, stg, col0 + c * 32, static_cast<int>(orow0));
+                bulk_commit_group();
+              }
+            } else if (row_ok) {
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[c * 8 + v] = make_float4(__uint_as_float(a[4 * v]), __uint_as_float(a[4 * v + 1]),
+                                             __uint_as_float(a[4 * v + 2]),
+                                             __uint_as_float(a[4 * v + 3]));
+            }
           });
         } else if (kMode == BwdMode::kDataPlain) {
           uint4* dst = p.out + out_row * p.ldo_vec + col0 / 8;
@@ -580,7 +611,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
       mbar_arrive(&tempty[buf]);
     }
     // the staged outputs must be written before the CTA's shared memory goes
-    if (kWeightGrad && lane == 0) bulk_wait_group<0>();
+    if ((kWeightGrad || kMode == BwdMode::kPreact) && lane == 0) bulk_wait_group<0>();
     __syncwarp();
   }
 
@@ -637,6 +668,10 @@ cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s) {
   if (weight && !make_map_2d(&mo, g.out, static_cast<uint64_t>(g.E) * static_cast<uint64_t>(g.M),
                              static_cast<uint64_t>(g.N), 32u))
     return cudaErrorInvalidValue;
+  // pre-activations: the fp32 output [R, N] in 32 x 32 boxes (128-byte swizzle)
+  if (preact && !make_map_2d_f32(&mo, g.out, static_cast<uint64_t>(g.R),
+                                 static_cast<uint64_t>(g.N), 32u))
+    return cudaErrorInvalidValue;
   BwdParams kp{};
   kp.expert_offsets = g.expert_offsets;
   kp.mtile_prefix = g.mtile_prefix;
@@ -646,6 +681,7 @@ cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s) {
   kp.n_tiles = ceil_div(g.N, kBN);
   kp.M = g.M;
   kp.m_tiles = weight ? g.M / kBM : 0;
+  kp.m_outer = weight && g.M >= g.N ? 1 : 0;
   kp.out = static_cast<uint4*>(g.out);
   kp.ldo_vec = preact ? g.N / 4 : g.N / 8;
   kp.act = static_cast<const float4*>(g.act);
