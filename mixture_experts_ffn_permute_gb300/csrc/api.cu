@@ -132,7 +132,7 @@ BwdLayout bwd_layout_of(const moe_problem& p0) {
   B.act = take(sizeof(float) * R * 2 * F);
   B.dact = take(2 * R * 2 * F);
   B.w_perm = take(sizeof(float) * R);
-  B.dw_part = take(sizeof(float) * R * ((F + kBN - 1) / kBN));
+  B.dw_part = take(sizeof(float) * R * bwd_router_parts(static_cast<int>(F)));
   B.total = o;
   return B;
 }
@@ -656,7 +656,7 @@ int moe_backward(const moe_problem* p, const void* x, const float* logits, const
   void* dact = at<void>(ws, B.dact);  // [R, 2F] bf16 their gradient
   float* w_perm = at<float>(ws, B.w_perm);
   float* dw_part = at<float>(ws, B.dw_part);
-  const int n_parts = ceil_div(F, kBN);
+  const int n_parts = bwd_router_parts(F);
 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;

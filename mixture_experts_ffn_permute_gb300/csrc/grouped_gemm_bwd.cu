@@ -55,7 +55,12 @@ namespace {
 // pipeline depth: the weight gradients trade a stage for output staging
 template <int kMode>
 __host__ __device__ constexpr int stages_of() { return kMode == 2 ? 3 : 4; }
-constexpr int kThreadsB = 192;
+// threads: producer warp, MMA warp, then the epilogue warps -- one per TMEM
+// lane quadrant, kBwdSwiGLUSplit per quadrant for the SwiGLU backward
+template <int kMode>
+__host__ __device__ constexpr int epi_warps_of() { return kMode == 1 ? 4 * kBwdSwiGLUSplit : 4; }
+template <int kMode>
+__host__ __device__ constexpr int threads_of() { return 64 + 32 * epi_warps_of<kMode>(); }
 constexpr uint32_t kABytesB = kBM * kBK * 2;             // 16 KB
 constexpr uint32_t kBBytesB = kBN * kBK * 2;             // 32 KB
 constexpr uint32_t kStageBytesB = kABytesB + kBBytesB;   // 48 KB
@@ -201,7 +206,7 @@ __device__ __forceinline__ int up_col(int f, int F, int I) {
 }
 
 template <BwdMode kMode>
-__global__ void __launch_bounds__(kThreadsB, 1)
+__global__ void __launch_bounds__(threads_of<static_cast<int>(kMode)>(), 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_out, const BwdParams p) {
@@ -228,6 +233,8 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
   constexpr bool kBKMajor = kMode == BwdMode::kPreact;  // B = weight rows, K-major
   constexpr uint32_t kIdescB = idesc_bwd(kWeightGrad, !kBKMajor);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kThreadsB = threads_of<static_cast<int>(kMode)>();
+  constexpr int kEpiWarps = epi_warps_of<static_cast<int>(kMode)>();
   for (int i = threadIdx.x; i <= p.E; i += kThreadsB) {
     s_off[i] = p.expert_offsets[i];
     s_mtp[i] = kWeightGrad ? 0 : p.mtile_prefix[i];
@@ -239,7 +246,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 128);
+      mbar_init(&tempty[b], 32 * kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -543,8 +550,10 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
           uint4* drow = p.dact + out_row * p.dact_vec;
           uint4* hrow = p.hw + out_row * (p.F / 8);
           float dw_acc = 0.f;
+          // the two warps of a quadrant take alternate chunks
+          const int half = (warp - 2) / 4;
 #pragma unroll 1
-          for (int c = 0; c < kBN / 32 && col0 + c * 32 < p.N; ++c) {
+          for (int c = half; c < kBN / 32 && col0 + c * 32 < p.N; c += kEpiWarps / 4) {
             const int f0 = col0 + c * 32;
             const int gc0 = gate_col(f0, p.F, p.interleave);
             const int uc0 = up_col(f0, p.F, p.interleave);
@@ -604,7 +613,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
               hrow[f0 / 8 + v] = make_uint4(hp[4 * v], hp[4 * v + 1], hp[4 * v + 2], hp[4 * v + 3]);
             }
           }
-          if (row_ok) p.dw_part[out_row * p.n_tiles + t.n] = dw_acc;
+          if (row_ok) p.dw_part[(out_row * p.n_tiles + t.n) * (kEpiWarps / 4) + half] = dw_acc;
         }
       }
       tc_fence_before();
@@ -630,7 +639,8 @@ cudaError_t launch_bwd_impl(const CUtensorMap& ma, const CUtensorMap& mb, const 
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes_of<static_cast<int>(kMode)>()));
   if (err != cudaSuccess) return err;
-  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsB),
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)),
+                       dim3(threads_of<static_cast<int>(kMode)>()),
                        smem_bytes_of<static_cast<int>(kMode)>(), s,
                        1, ma, mb, mo, kp);
 }

@@ -210,7 +210,7 @@ struct BwdGemmArgs {
   const void* act = nullptr;      // [R, 2F] fp32 pre-activations
   void* dact = nullptr;           // [R, 2F] bf16 out: their gradient dA
   void* hw = nullptr;             // [R, F] bf16 out: w * h
-  float* dw_part = nullptr;       // [R, ceil(N / 256)] fp32 out
+  float* dw_part = nullptr;       // [R, bwd_router_parts(N)] fp32 out
   const float* w_perm = nullptr;  // [R] routing weight per permuted row
   int F = 0, interleave = 0;
   float clamp = 0.f;
@@ -218,6 +218,13 @@ struct BwdGemmArgs {
 };
 
 cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s);
+
+// Epilogue warps per TMEM lane quadrant in the SwiGLU-backward GEMM (they
+// split a tile's 32-column chunks), and the router-gradient partials it
+// writes per permuted row for N = F columns: one per tile and warp of a
+// quadrant.
+constexpr int kBwdSwiGLUSplit = 1;
+inline int bwd_router_parts(int F) { return kBwdSwiGLUSplit * ((F + kBN - 1) / kBN); }
 
 // w_perm[row_id_map[t][j]] = topk_w[t][j] for every valid route.
 cudaError_t launch_weights_to_rows(const int32_t* row_id_map, const float* topk_w, long routes,
