@@ -322,9 +322,27 @@ class MoEFFN:
                 res.get("topk_w"), res.get("tokens_per_expert"))
         return res
 
+    def backward(self, x: torch.Tensor, logits: torch.Tensor,
+                 d_out: torch.Tensor) -> Dict[str, torch.Tensor]:
+        """Gradients of the layer given d_out = dL/d out (moe_backward): dx, dlogits,
+        dw1, dw2.  The forward's intermediates are recomputed from x and logits."""
+        T = x.shape[0]
+        p = self.problem(T)
+        if getattr(self, "_bws", None) is None or T > self._bws_T:
+            self._bws = alloc_backward_workspace(p, device=x.device)
+            self._bws_T = T
+        res = {"dx": torch.empty_like(x),
+               "dlogits": torch.empty(T, self.E, dtype=torch.float32, device=x.device),
+               "dw1": torch.empty_like(self.w1), "dw2": torch.empty_like(self.w2)}
+        backward(p, x, logits, self.w1, self.w2, d_out, res["dx"], res["dw1"], res["dw2"],
+                 self._bws, d_logits=res["dlogits"])
+        return res
+
 
 __all__ = ["Problem", "MoEError", "MoEFFN", "load", "workspace_size", "alloc_workspace",
            "route_topk", "permute", "grouped_swiglu_mlp", "unpermute_combine", "forward",
            "get_device_status", "clear_device_status", "last_launch_count", "LIB_PATH",
            "stage_timing_begin", "stage_timing_end", "permute_noalloc",
-           "prepared_scales_size", "prepare_weights", "forward_fp8_nvfp4", "selected_kernel"]
+           "prepared_scales_size", "prepare_weights", "forward_fp8_nvfp4", "selected_kernel",
+           "forward_routed", "prepare_weights_mxfp4", "selftest_wait_timeout",
+           "backward_workspace_size", "alloc_backward_workspace", "backward"]
