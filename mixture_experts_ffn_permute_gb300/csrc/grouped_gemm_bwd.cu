@@ -36,9 +36,11 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 
 #include "../../include/moe_ffn.h"
 #include "internal.h"
+#include "pair_tiles.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -52,9 +54,11 @@ bool make_map_2d_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
 
 namespace {
 
-// pipeline depth: the weight gradients trade a stage for output staging
-template <int kMode>
-__host__ __device__ constexpr int stages_of() { return kMode == 2 ? 3 : 4; }
+// pipeline depth: 2-CTA pairs (32 KB per CTA and stage) keep 6 stages; 1-CTA
+// tiles (48 KB) 4, the weight gradients of small experts trade one for output
+// staging
+template <int kMode, bool kPair>
+__host__ __device__ constexpr int stages_of() { return kPair ? 6 : (kMode == 2 ? 3 : 4); }
 // threads: producer warp, MMA warp, then the epilogue warps -- one per TMEM
 // lane quadrant, kBwdSwiGLUSplit per quadrant for the SwiGLU backward
 template <int kMode>
@@ -63,7 +67,10 @@ template <int kMode>
 __host__ __device__ constexpr int threads_of() { return 64 + 32 * epi_warps_of<kMode>(); }
 constexpr uint32_t kABytesB = kBM * kBK * 2;             // 16 KB
 constexpr uint32_t kBBytesB = kBN * kBK * 2;             // 32 KB
-constexpr uint32_t kStageBytesB = kABytesB + kBBytesB;   // 48 KB
+// B bytes per stage in one CTA: the whole 256-column tile, or a pair's half
+__host__ __device__ constexpr uint32_t b_stage_bytes(bool pair) {
+  return pair ? kBBytesB / 2 : kBBytesB;
+}
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;              // one MN-major box, 8 KB
 constexpr uint32_t kStepBytesMN = 16 * 128;              // one K=16 step of an MN-major tile
 constexpr uint32_t kTmemColsB = 2 * kBN;
@@ -85,14 +92,16 @@ __host__ __device__ constexpr uint32_t out_stage_bytes() {
          : kMode == 3 ? 4 * kOutBoxBytes  // fp32 pre-activations: 32 x 32 per warp
                       : 0;
 }
-template <int kMode>
+template <int kMode, bool kPair>
 constexpr size_t smem_bytes_of() {
-  return 1024 + stages_of<kMode>() * kStageBytesB + out_stage_bytes<kMode>() + 256 +
-         2 * (kMaxEB + 1) * sizeof(int32_t);
+  return 1024 + stages_of<kMode, kPair>() * (kABytesB + b_stage_bytes(kPair)) +
+         out_stage_bytes<kMode>() + 256 + 3 * (kMaxEB + 1) * sizeof(int32_t);
 }
-static_assert((2 * 4 + 5) * 8 + 8 <= 256, "barrier area");
-static_assert(smem_bytes_of<0>() <= 232448 && smem_bytes_of<2>() <= 232448 &&
-                  smem_bytes_of<3>() <= 232448 && smem_bytes_of<4>() <= 232448,
+static_assert((2 * 6 + 5) * 8 + 8 <= 256, "barrier area");
+static_assert(smem_bytes_of<0, false>() <= 232448 && smem_bytes_of<2, false>() <= 232448 &&
+                  smem_bytes_of<3, false>() <= 232448 && smem_bytes_of<4, false>() <= 232448 &&
+                  smem_bytes_of<0, true>() <= 232448 && smem_bytes_of<1, true>() <= 232448 &&
+                  smem_bytes_of<3, true>() <= 232448,
               "shared memory budget");
 
 enum class BwdMode : int {
@@ -205,7 +214,15 @@ __device__ __forceinline__ int up_col(int f, int F, int I) {
   return I == 0 ? F + f : (f / I) * 2 * I + f % I + I;
 }
 
-template <BwdMode kMode>
+// kPair (data gradients only): 2-CTA clusters.  CTA r of a pair holds the 128
+// token rows of m-tile 2*mp + r and the 128 columns 128*r .. 128*r+127 of the
+// 256-column B tile; both load into their own shared memory and complete on
+// the leader's full barrier (.cta_group::2 loads); the leader (rank 0) issues
+// tcgen05.mma.cta_group::2 (M = 256 across the pair) and its commits arrive
+// on both CTAs' empty / TMEM-full barriers; every epilogue thread of the pair
+// arrives on the leader's TMEM-empty barrier.  Each SM then loads half the B
+// bytes per 256 x 256 MMA, which shared-memory bandwidth rewards.
+template <BwdMode kMode, bool kPair>
 __global__ void __launch_bounds__(threads_of<static_cast<int>(kMode)>(), 1)
 grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_b,
@@ -214,10 +231,12 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;
-  constexpr int kStagesB = stages_of<static_cast<int>(kMode)>();
+  constexpr int kStagesB = stages_of<static_cast<int>(kMode), kPair>();
   constexpr uint32_t kOutStageBytes = out_stage_bytes<static_cast<int>(kMode)>();
+  constexpr uint32_t kBStage = b_stage_bytes(kPair);     // B bytes per stage, this CTA
+  constexpr uint32_t kStageBytes = kABytesB + kBStage;   // bytes per stage, this CTA
   uint8_t* sB = smem + kStagesB * kABytesB;
-  uint8_t* s_out = sB + kStagesB * kBBytesB;  // kWeight: output staging (1024-aligned)
+  uint8_t* s_out = sB + kStagesB * kBStage;  // output staging (1024-aligned)
   uint64_t* full = reinterpret_cast<uint64_t*>(s_out + kOutStageBytes);
   uint64_t* empty = full + kStagesB;
   uint64_t* tfull = empty + kStagesB;
@@ -226,13 +245,19 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_off =
-      reinterpret_cast<int32_t*>(smem + kStagesB * kStageBytesB + kOutStageBytes + 256);
+      reinterpret_cast<int32_t*>(smem + kStagesB * kStageBytes + kOutStageBytes + 256);
   int32_t* s_mtp = s_off + (p.E + 1);
+  int32_t* s_ptp = s_mtp + (p.E + 1);  // kPair: prefix of ceil(m-tiles / 2)
 
   constexpr bool kWeightGrad = kMode == BwdMode::kWeight || kMode == BwdMode::kWeightLong;
   constexpr bool kBKMajor = kMode == BwdMode::kPreact;  // B = weight rows, K-major
-  constexpr uint32_t kIdescB = idesc_bwd(kWeightGrad, !kBKMajor);
+  static_assert(!(kPair && kWeightGrad), "pairs serve the data gradients");
+  constexpr uint32_t kIdescB =
+      kPair ? idesc_bf16_f32(2 * kBM, kBN) | (static_cast<uint32_t>(!kBKMajor) << 16)
+            : idesc_bwd(kWeightGrad, !kBKMajor);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0;
+  const bool leader = rank == 0;
   constexpr int kThreadsB = threads_of<static_cast<int>(kMode)>();
   constexpr int kEpiWarps = epi_warps_of<static_cast<int>(kMode)>();
   for (int i = threadIdx.x; i <= p.E; i += kThreadsB) {
@@ -246,7 +271,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 32 * kEpiWarps);
+      mbar_init(&tempty[b], (kPair ? 2 : 1) * 32 * kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -257,13 +282,54 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
     prefetch_tensormap(&map_b);
     if (kWeightGrad || kMode == BwdMode::kPreact) prefetch_tensormap(&map_out);
   }
-  if (warp == 1) tmem_alloc<kTmemColsB>(tmem_slot);
+  if (warp == 1) {
+    if (kPair) pair::tmem_alloc2<kTmemColsB>(tmem_slot);  // the pair's columns together
+    else tmem_alloc<kTmemColsB>(tmem_slot);
+  }
+  __syncthreads();
+  if (kPair) {  // prefix of ceil(m-tiles / 2) per expert
+    __shared__ int s_part[kThreadsB / 32];
+    const int per = (p.E + kThreadsB - 1) / kThreadsB;
+    const int e0 = min(p.E, static_cast<int>(threadIdx.x) * per), e1 = min(p.E, e0 + per);
+    int run = 0;
+    for (int e = e0; e < e1; ++e) run += (s_mtp[e + 1] - s_mtp[e] + 1) >> 1;
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) s_part[warp] = incl;
+    __syncthreads();
+    int acc = incl - run;
+    for (int w = 0; w < warp; ++w) acc += s_part[w];
+    for (int e = e0; e < e1; ++e) {
+      s_ptp[e] = acc;
+      acc += (s_mtp[e + 1] - s_mtp[e] + 1) >> 1;
+    }
+    if (threadIdx.x == kThreadsB - 1) {
+      int total = 0;
+      for (int w = 0; w < kThreadsB / 32; ++w) total += s_part[w];
+      s_ptp[p.E] = total;
+    }
+  }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();  // both CTAs' barriers exist before anything signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int total_tiles = kWeightGrad ? p.E * p.m_tiles * p.n_tiles : s_mtp[p.E] * p.n_tiles;
+  const int total_tiles = kWeightGrad ? p.E * p.m_tiles * p.n_tiles
+                          : kPair     ? s_ptp[p.E] * p.n_tiles
+                                      : s_mtp[p.E] * p.n_tiles;
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tstride = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  auto tile_at = [&](int tile) {
+    if (!kPair) return decode_btile<kMode>(tile, s_mtp, p);
+    BTile t = decode_btile<kMode>(tile, s_ptp, p);  // m = the pair index
+    t.m = 2 * t.m + static_cast<int>(rank);
+    return t;
+  };
   auto rows_of = [&](int e) { return s_off[e + 1] - s_off[e]; };
   auto ksteps = [&](const BTile& t) {
     return kWeightGrad ? (rows_of(t.e) + kBK - 1) / kBK : p.K / kBK;
@@ -276,40 +342,48 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
       int stage = 0;
       uint32_t phase = 0;
       long issued = 0;
-      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      // a pair's loads complete on the leader's barrier (its cluster address)
+      auto load = [&](void* dst, const CUtensorMap* map, int c0, int c1, int st) {
+        if (kPair) pair::tma_load(dst, map, c0, c1, pair::mapa(smem_u32(&full[st]), 0), pol);
+        else tma_load_2d(dst, map, c0, c1, &full[st], pol);
+      };
+      for (int tile = tile0; tile < total_tiles; tile += tstride) {
         if (*abort_flag) break;
-        const BTile t = decode_btile<kMode>(tile, s_mtp, p);
+        const BTile t = tile_at(tile);
         const int nk = ksteps(t);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], kStageBytesB);
+          if (leader) mbar_arrive_expect_tx(&full[stage], (kPair ? 2 : 1) * kStageBytes);
           uint8_t* a_dst = sA + stage * kABytesB;
-          uint8_t* b_dst = sB + stage * kBBytesB;
+          uint8_t* b_dst = sB + stage * kBStage;
           int brow;
           if (kWeightGrad) {
             brow = s_off[t.e] + kb * kBK;  // the expert's rows are the contraction
-            tma_load_2d(a_dst, &map_a, t.m * kBM, brow, &full[stage], pol);
-            tma_load_2d(a_dst + kBoxBytes, &map_a, t.m * kBM + 64, brow, &full[stage], pol);
+            load(a_dst, &map_a, t.m * kBM, brow, stage);
+            load(a_dst + kBoxBytes, &map_a, t.m * kBM + 64, brow, stage);
           } else {
-            tma_load_2d(a_dst, &map_a, kb * kBK, s_off[t.e] + t.m * kBM, &full[stage], pol);
+            load(a_dst, &map_a, kb * kBK, s_off[t.e] + t.m * kBM, stage);
             brow = t.e * p.K + kb * kBK;  // rows of the expert's weight matrix
           }
-          if (kBKMajor) {  // 256 weight rows x 64 K in one box
-            tma_load_2d(b_dst, &map_b, kb * kBK, t.e * p.N + t.n * kBN, &full[stage], pol);
+          // this CTA's B columns: all 256, or a pair member's 128
+          const int bcol0 = t.n * kBN + (kPair ? static_cast<int>(rank) * (kBN / 2) : 0);
+          if (kBKMajor) {  // weight rows x 64 K in one box
+            load(b_dst, &map_b, kb * kBK, t.e * p.N + bcol0, stage);
           } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tma_load_2d(b_dst + i * kBoxBytes, &map_b, t.n * kBN + 64 * i, brow, &full[stage],
-                          pol);
+            for (int i = 0; i < static_cast<int>(kBStage / kBoxBytes); ++i)
+              load(b_dst + i * kBoxBytes, &map_b, bcol0 + 64 * i, brow, stage);
           }
           ++issued;
           if (++stage == kStagesB) { stage = 0; phase ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
       }
-      // Leave no bulk copy in flight: wait for the last fill of every stage.
-      for (int i = 1; i <= kStagesB && i <= issued; ++i) {
+      // Leave no bulk copy in flight: wait for the last fill of every stage
+      // (a pair's copies all complete on the leader's barriers; the peer's
+      // shared memory outlives them through the final cluster barrier).
+      for (int i = 1; leader && i <= kStagesB && i <= issued; ++i) {
         int s = stage - i;
         uint32_t ph = phase;
         if (s < 0) { s += kStagesB; ph ^= 1; }
@@ -318,90 +392,99 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    int stage = 0;
-    uint32_t phase = 0;
-    int local = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
-      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      const int buf = local & 1;
-      const uint32_t tph = (local >> 1) & 1;
-      const BTile t = decode_btile<kMode>(tile, s_mtp, p);
-      const int nk = ksteps(t);
-      int ok = lane == 0 ? (mbar_wait(&tempty[buf], tph ^ 1, p.status) ? 1 : 0) : 1;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + buf * kBN;
-      for (int kb = 0; kb < nk; ++kb) {
-        ok = lane == 0 ? (mbar_wait(&full[stage], phase, p.status) ? 1 : 0) : 1;
+    // (only the leader's for a pair: one cta_group::2 MMA covers both CTAs)
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = tile0; tile < total_tiles; tile += tstride, ++local) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        const int buf = local & 1;
+        const uint32_t tph = (local >> 1) & 1;
+        const BTile t = tile_at(tile);
+        const int nk = ksteps(t);
+        int ok = lane == 0 ? (mbar_wait(&tempty[buf], tph ^ 1, p.status) ? 1 : 0) : 1;
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        int nkk = kBK / 16;  // K=16 MMA steps of this stage
-        if (kWeightGrad) {
-          const int valid = rows_of(t.e) - kb * kBK;
-          if (valid < kBK) {
-            // the MMAs read rows 0 .. 16*nkk-1; rows valid .. 16*nkk-1 of each
-            // of the six boxes are the next expert's (or past the matrix):
-            // zero them, then hand the writes to the async proxy the MMA reads
-            nkk = (valid + 15) / 16;
-            const int zrows = 16 * nkk - valid;
-            if (zrows > 0) {
-              __syncwarp();
-              const int per_box = zrows * 8;  // 16-byte vectors per box
-              for (int i = lane; i < 6 * per_box; i += 32) {
-                const int b = i / per_box, v = i - b * per_box;
-                uint8_t* box = b < 2 ? sA + stage * kABytesB + b * kBoxBytes
-                                     : sB + stage * kBBytesB + (b - 2) * kBoxBytes;
-                reinterpret_cast<uint4*>(box + valid * 128)[v] = make_uint4(0, 0, 0, 0);
+        if (!ok) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          ok = lane == 0 ? (mbar_wait(&full[stage], phase, p.status) ? 1 : 0) : 1;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          int nkk = kBK / 16;  // K=16 MMA steps of this stage
+          if (kWeightGrad) {
+            const int valid = rows_of(t.e) - kb * kBK;
+            if (valid < kBK) {
+              // the MMAs read rows 0 .. 16*nkk-1; rows valid .. 16*nkk-1 of each
+              // of the six boxes are the next expert's (or past the matrix):
+              // zero them, then hand the writes to the async proxy the MMA reads
+              nkk = (valid + 15) / 16;
+              const int zrows = 16 * nkk - valid;
+              if (zrows > 0) {
+                __syncwarp();
+                const int per_box = zrows * 8;  // 16-byte vectors per box
+                for (int i = lane; i < 6 * per_box; i += 32) {
+                  const int b = i / per_box, v = i - b * per_box;
+                  uint8_t* box = b < 2 ? sA + stage * kABytesB + b * kBoxBytes
+                                       : sB + stage * kBStage + (b - 2) * kBoxBytes;
+                  reinterpret_cast<uint4*>(box + valid * 128)[v] = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_shared();
               }
-              fence_proxy_async_shared();
             }
+            __syncwarp();
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + stage * kABytesB);
+            const uint32_t b_addr = smem_u32(sB + stage * kBStage);
+  #pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              if (kk >= nkk) break;
+              const uint64_t a_desc = kWeightGrad
+                                          ? sw128_mnmajor_desc(a_addr + kk * kStepBytesMN)
+                                          : sw128_kmajor_desc(a_addr) + 2 * kk;
+              const uint64_t b_desc = kBKMajor ? sw128_kmajor_desc(b_addr) + 2 * kk
+                                               : sw128_mnmajor_desc(b_addr + kk * kStepBytesMN);
+              if (kPair) pair::mma(d_tmem, a_desc, b_desc, kIdescB, (kb | kk) != 0);
+              else mma_bf16_ss(d_tmem, a_desc, b_desc, kIdescB, (kb | kk) != 0);
+            }
+            if (kPair) pair::commit_both(&empty[stage]);  // both CTAs' copies of the stage
+            else mma_commit(&empty[stage]);
           }
           __syncwarp();
+          if (++stage == kStagesB) { stage = 0; phase ^= 1; }
         }
+        if (!ok) {
+          if (lane == 0) *abort_flag = 1;
+          break;
+        }
+        // an expert without rows commits no MMA: the epilogue writes zeros
         if (lane == 0) {
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * kABytesB);
-          const uint32_t b_addr = smem_u32(sB + stage * kBBytesB);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            if (kk >= nkk) break;
-            const uint64_t a_desc = kWeightGrad
-                                        ? sw128_mnmajor_desc(a_addr + kk * kStepBytesMN)
-                                        : sw128_kmajor_desc(a_addr) + 2 * kk;
-            const uint64_t b_desc = kBKMajor ? sw128_kmajor_desc(b_addr) + 2 * kk
-                                             : sw128_mnmajor_desc(b_addr + kk * kStepBytesMN);
-            mma_bf16_ss(d_tmem, a_desc, b_desc, kIdescB, (kb | kk) != 0);
-          }
-          mma_commit(&empty[stage]);
+          if (kPair) pair::commit_both(&tfull[buf]);
+          else mma_commit(&tfull[buf]);
         }
         __syncwarp();
-        if (++stage == kStagesB) { stage = 0; phase ^= 1; }
       }
-      if (!ok) {
-        if (lane == 0) *abort_flag = 1;
-        break;
+      if (lane == 0) {
+        // All MMAs of this CTA (or pair) done before TMEM is released.
+        if (kPair) pair::commit_local(drain);
+        else mma_commit(drain);
+        mbar_wait(drain, 0, p.status);
       }
-      // an expert without rows commits no MMA: the epilogue writes zeros
-      if (lane == 0) mma_commit(&tfull[buf]);
       __syncwarp();
-    }
-    if (lane == 0) {
-      // All MMAs of this CTA done before TMEM is released.
-      mma_commit(drain);
-      mbar_wait(drain, 0, p.status);
-    }
-    __syncwarp();
+    }  // leader
   } else {
     // ---------------------------------------------------------------- epilogue
     const int quad = warp & 3;  // TMEM lanes this warp may access
     const int row_in_tile = quad * 32 + lane;
     int local = 0;
     int n_stores = 0;  // bulk-tensor stores this warp issued (kWeight)
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
+    for (int tile = tile0; tile < total_tiles; tile += tstride, ++local) {
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       const int buf = local & 1;
       const uint32_t tph = (local >> 1) & 1;
@@ -411,7 +494,7 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
         break;
       }
       tc_fence_after();
-      const BTile t = decode_btile<kMode>(tile, s_mtp, p);
+      const BTile t = tile_at(tile);
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + buf * kBN;
       const int col0 = t.n * kBN;
       // chunks of 32 columns, read from TMEM two at a time (one wait per pair)
@@ -617,7 +700,8 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[buf]);
+      if (kPair) pair::arrive_remote(pair::mapa(smem_u32(&tempty[buf]), 0));  // the leader's
+      else mbar_arrive(&tempty[buf]);
     }
     // the staged outputs must be written before the CTA's shared memory goes
     if ((kWeightGrad || kMode == BwdMode::kPreact) && lane == 0) bulk_wait_group<0>();
@@ -626,23 +710,34 @@ grouped_gemm_bwd_kernel(const __grid_constant__ CUtensorMap map_a,
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair frees TMEM or exits while the other may still signal
+  // its barriers or the leader's MMAs may still write its TMEM
+  if (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc<kTmemColsB>(tmem_base);
+    if (kPair) pair::tmem_dealloc2<kTmemColsB>(tmem_base);
+    else tmem_dealloc<kTmemColsB>(tmem_base);
   }
 }
 
-template <BwdMode kMode>
+template <BwdMode kMode, bool kPair>
 cudaError_t launch_bwd_impl(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                             const BwdParams& kp, int grid, cudaStream_t s) {
-  auto kern = grouped_gemm_bwd_kernel<kMode>;
+  auto kern = grouped_gemm_bwd_kernel<kMode, kPair>;
+  constexpr size_t smem = smem_bytes_of<static_cast<int>(kMode), kPair>();
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes_of<static_cast<int>(kMode)>()));
+                                         static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(static_cast<unsigned>(grid)),
-                       dim3(threads_of<static_cast<int>(kMode)>()),
-                       smem_bytes_of<static_cast<int>(kMode)>(), s,
-                       1, ma, mb, mo, kp);
+                       dim3(threads_of<static_cast<int>(kMode)>()), smem, s, kPair ? 2 : 1, ma,
+                       mb, mo, kp);
+}
+
+// The data gradients run on 2-CTA pairs unless MOE_BWD_1CTA is set (1-CTA
+// tiles, kept for comparison).
+bool bwd_pairs() {
+  static const bool on = std::getenv("MOE_BWD_1CTA") == nullptr;
+  return on;
 }
 
 }  // namespace
@@ -661,10 +756,11 @@ cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s) {
                    static_cast<uint64_t>(weight ? g.M : g.K), weight ? 64u : static_cast<uint32_t>(kBM)))
     return cudaErrorInvalidValue;
   const bool preact = g.mode == kBwdPreact;
-  if (preact) {  // the stacked weight rows [E * N, K], 256-row K-major boxes
+  const bool pair = !weight && bwd_pairs();
+  if (preact) {  // the stacked weight rows [E * N, K], K-major boxes of a CTA's rows
     if (g.N % kBN != 0 ||
         !make_map_2d(&mb, g.b, static_cast<uint64_t>(g.E) * static_cast<uint64_t>(g.N),
-                     static_cast<uint64_t>(g.K), static_cast<uint32_t>(kBN)))
+                     static_cast<uint64_t>(g.K), static_cast<uint32_t>(pair ? kBN / 2 : kBN)))
       return cudaErrorInvalidValue;
   } else if (!make_map_2d(&mb, g.b,
                           weight ? static_cast<uint64_t>(g.R)
@@ -711,17 +807,29 @@ cudaError_t launch_grouped_gemm_bwd(const BwdGemmArgs& g, cudaStream_t s) {
   } else {
     max_tiles = (ceil_div(g.R, kBM) + std::min(g.E, g.R)) * static_cast<long>(kp.n_tiles);
   }
+  if (pair) {  // clusters of two CTAs: an even grid, at most one CTA per SM
+    const long pairs = (ceil_div(g.R, 2 * kBM) + std::min(g.E, g.R)) * static_cast<long>(kp.n_tiles);
+    const int grid = static_cast<int>(2 * std::max(1L, std::min<long>(num_sms() / 2, pairs)));
+    switch (g.mode) {
+      case kBwdDataPlain: return launch_bwd_impl<BwdMode::kDataPlain, true>(ma, mb, mo, kp, grid, s);
+      case kBwdDataSwiGLU:
+        return launch_bwd_impl<BwdMode::kDataSwiGLU, true>(ma, mb, mo, kp, grid, s);
+      case kBwdPreact: return launch_bwd_impl<BwdMode::kPreact, true>(ma, mb, mo, kp, grid, s);
+    }
+    return cudaErrorInvalidValue;
+  }
   const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
   switch (g.mode) {
-    case kBwdDataPlain: return launch_bwd_impl<BwdMode::kDataPlain>(ma, mb, mo, kp, grid, s);
-    case kBwdDataSwiGLU: return launch_bwd_impl<BwdMode::kDataSwiGLU>(ma, mb, mo, kp, grid, s);
+    case kBwdDataPlain: return launch_bwd_impl<BwdMode::kDataPlain, false>(ma, mb, mo, kp, grid, s);
+    case kBwdDataSwiGLU:
+      return launch_bwd_impl<BwdMode::kDataSwiGLU, false>(ma, mb, mo, kp, grid, s);
     case kBwdWeight:
       // experts averaging 512 rows or more: K loops long enough to want the
       // fourth pipeline stage more than the wider output staging
       return static_cast<long>(g.R) >= 512L * g.E
-                 ? launch_bwd_impl<BwdMode::kWeightLong>(ma, mb, mo, kp, grid, s)
-                 : launch_bwd_impl<BwdMode::kWeight>(ma, mb, mo, kp, grid, s);
-    case kBwdPreact: return launch_bwd_impl<BwdMode::kPreact>(ma, mb, mo, kp, grid, s);
+                 ? launch_bwd_impl<BwdMode::kWeightLong, false>(ma, mb, mo, kp, grid, s)
+                 : launch_bwd_impl<BwdMode::kWeight, false>(ma, mb, mo, kp, grid, s);
+    case kBwdPreact: return launch_bwd_impl<BwdMode::kPreact, false>(ma, mb, mo, kp, grid, s);
   }
   return cudaErrorInvalidValue;
 }
