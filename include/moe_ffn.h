@@ -257,6 +257,21 @@ MOE_API int moe_backward(const moe_problem* p, const void* x, const float* logit
                          float* d_logits, void* dw1, void* dw2, void* ws, size_t ws_bytes,
                          void* stream);
 
+/* The backward of moe_forward_routed (routing supplied by the caller): the
+ * same gradients with topk_idx / topk_w as given (int32 [T, k], -1 = masked
+ * slot; fp32 [T, k]) and, instead of the logit gradient, the gradient of
+ * every routing weight:
+ *   d_topk_w [T, k] fp32 out (NULL to skip): dL/d topk_w[t][j] = <G_t, y_tj>,
+ *   the unweighted output of the slot's expert for token t; 0 for a masked
+ *   slot.
+ * Masked, out-of-range and repeated slots are handled and reported as in
+ * moe_forward_routed.  shared_experts must be 0; bf16 precision only;
+ * workspace of moe_backward_workspace_size(p) bytes. */
+MOE_API int moe_backward_routed(const moe_problem* p, const void* x, const int32_t* topk_idx,
+                                const float* topk_w, const void* w1, const void* w2,
+                                const void* d_out, void* dx, float* d_topk_w, void* dw1,
+                                void* dw2, void* ws, size_t ws_bytes, void* stream);
+
 /* Self-test of the bounded waits (the pages have no counterpart: this checks
  * the library's own failure detection).  Launches one CTA that waits on an
  * mbarrier nothing arrives on, through the same bounded wait every kernel

@@ -92,6 +92,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_selftest_wait_timeout": ([vp, ctypes.c_uint64, vp], ci),
         "moe_backward_workspace_size": ([pp], sz),
         "moe_backward": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_backward_routed": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_get_device_status": ([vp, vp], ci),
         "moe_clear_device_status": ([vp, vp], ci),
         "moe_last_launch_count": ([], ci),
@@ -251,6 +252,15 @@ def backward(p: Problem, x, logits, w1, w2, d_out, dx, dw1, dw2, ws, d_logits=No
           _stream(stream))
 
 
+def backward_routed(p: Problem, x, topk_idx, topk_w, w1, w2, d_out, dx, dw1, dw2, ws,
+                    d_topk_w=None, stream=None) -> None:
+    """Gradients of the layer with caller-supplied routing (int32 [T, k], -1 =
+    masked; fp32 [T, k]): dx, dw1, dw2 and, optionally, d_topk_w [T, k] fp32."""
+    _call("moe_backward_routed", ctypes.byref(p), _ptr(x), _ptr(topk_idx), _ptr(topk_w),
+          _ptr(w1), _ptr(w2), _ptr(d_out), _ptr(dx), _ptr(d_topk_w), _ptr(dw1), _ptr(dw2),
+          _ptr(ws), ws.numel(), _stream(stream))
+
+
 def selftest_wait_timeout(ws, limit_ns: int, stream=None) -> None:
     """Run the bounded-wait self-test: a wait that runs out after limit_ns and
     records MOE_ERR_DEVICE_TIMEOUT in ws's status word."""
@@ -345,4 +355,4 @@ __all__ = ["Problem", "MoEError", "MoEFFN", "load", "workspace_size", "alloc_wor
            "stage_timing_begin", "stage_timing_end", "permute_noalloc",
            "prepared_scales_size", "prepare_weights", "forward_fp8_nvfp4", "selected_kernel",
            "forward_routed", "prepare_weights_mxfp4", "selftest_wait_timeout",
-           "backward_workspace_size", "alloc_backward_workspace", "backward"]
+           "backward_workspace_size", "alloc_backward_workspace", "backward", "backward_routed"]

@@ -339,6 +339,147 @@ int run_permute(const moe_problem* p, const int32_t* topk_idx, int32_t* row_id_m
   return MOE_OK;
 }
 
+// Checks shared by moe_backward and moe_backward_routed; a non-zero return is
+// the status to give the caller.
+int check_backward(const moe_problem* p, const void* w1, const void* w2, void* dw1, void* dw2,
+                   void* ws, size_t ws_bytes) {
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < bwd_layout_of(*p).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  MOE_REQUIRE_PTR(w1);
+  MOE_REQUIRE_PTR(w2);
+  MOE_REQUIRE_PTR(dw1);
+  MOE_REQUIRE_PTR(dw2);
+  return MOE_OK;
+}
+
+// No routes: the weight gradients are zero.
+int backward_no_tokens(const moe_problem* q, void* dw1, void* dw2, cudaStream_t s) {
+  int launches = 0;
+  const size_t w1_bytes = sizeof(uint16_t) * q->E * 2 * static_cast<size_t>(q->F) * q->H;
+  const size_t w2_bytes = sizeof(uint16_t) * q->E * static_cast<size_t>(q->H) * q->F;
+  MOE_LAUNCH(cudaMemsetAsync(dw1, 0, w1_bytes, s));
+  MOE_LAUNCH(cudaMemsetAsync(dw2, 0, w2_bytes, s));
+  g_launches = launches;
+  return MOE_OK;
+}
+
+// The backward after routing and permutation (routes in the workspace's
+// row maps, weights in `wts` [T, q->k]): the row gathers, the pre-activation
+// recompute, dH with the SwiGLU backward, dW2, dXp, dW1 and the dx sum.
+// Leaves the per-row router partials in the workspace.
+int run_backward_core(const moe_problem* p, const moe_problem* q, const BwdLayout& B,
+                      const void* x, const void* d_out, const float* wts, const void* w1,
+                      const void* w2, void* dx, void* dw1, void* dw2, void* ws, cudaStream_t s,
+                      int& launches, StageTimer& tm, int call) {
+  const Layout& L = B.f;
+  const int R = q->T * q->k;
+  const int H = q->H, F = q->F;
+  int32_t* off = at<int32_t>(ws, L.expert_offsets);
+  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
+  int32_t* rmap = at<int32_t>(ws, L.row_id_map);
+  int32_t* ptok = at<int32_t>(ws, L.permuted_token);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* hw = at<void>(ws, L.h);      // [R, F] w * h
+  void* dy = at<void>(ws, L.y);      // [R, H] permuted output gradient, later dXp
+  float* act = at<float>(ws, B.act);  // [R, 2F] fp32 pre-activations
+  void* dact = at<void>(ws, B.dact);  // [R, 2F] bf16 their gradient
+  float* w_perm = at<float>(ws, B.w_perm);
+  float* dw_part = at<float>(ws, B.dw_part);
+  MOE_LAUNCH(launch_gather_rows(x, ptok, R, H, x_perm, s));
+  MOE_LAUNCH(launch_gather_rows(d_out, ptok, R, H, dy, s));
+  MOE_LAUNCH(launch_weights_to_rows(rmap, wts, R, w_perm, s));
+  tm.mark(call, 3, s);
+  // pre-activations a = x W1_e^T in fp32, recomputed rather than kept from
+  // the forward
+  BwdGemmArgs ga{};
+  ga.mode = kBwdPreact;
+  ga.a = x_perm;
+  ga.b = w1;
+  ga.R = R;
+  ga.E = q->E;
+  ga.K = H;
+  ga.N = 2 * F;
+  ga.expert_offsets = off;
+  ga.mtile_prefix = mtp;
+  ga.out = act;
+  ga.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(ga, s));
+  tm.mark(call, 4, s);
+  // dh = dY W2_e, then the SwiGLU backward: dA, w*h, router partials
+  BwdGemmArgs g{};
+  g.mode = kBwdDataSwiGLU;
+  g.a = dy;
+  g.b = w2;
+  g.R = R;
+  g.E = q->E;
+  g.K = H;
+  g.N = F;
+  g.expert_offsets = off;
+  g.mtile_prefix = mtp;
+  g.act = act;
+  g.dact = dact;
+  g.hw = hw;
+  g.dw_part = dw_part;
+  g.w_perm = w_perm;
+  g.F = F;
+  g.interleave = p->glu_interleave;
+  g.clamp = clamp_of(p);
+  g.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(g, s));
+  tm.mark(call, 5, s);
+  // dW2_e = dY_e^T (w h)_e
+  BwdGemmArgs gw2{};
+  gw2.mode = kBwdWeight;
+  gw2.a = dy;
+  gw2.b = hw;
+  gw2.R = R;
+  gw2.E = q->E;
+  gw2.M = H;
+  gw2.N = F;
+  gw2.expert_offsets = off;
+  gw2.out = dw2;
+  gw2.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(gw2, s));
+  tm.mark(call, 6, s);
+  // dXp = dA W1_e (into dY's region, no longer needed)
+  BwdGemmArgs gx{};
+  gx.mode = kBwdDataPlain;
+  gx.a = dact;
+  gx.b = w1;
+  gx.R = R;
+  gx.E = q->E;
+  gx.K = 2 * F;
+  gx.N = H;
+  gx.expert_offsets = off;
+  gx.mtile_prefix = mtp;
+  gx.out = dy;
+  gx.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(gx, s));
+  tm.mark(call, 7, s);
+  // dW1_e = dA_e^T x_e
+  BwdGemmArgs gw1{};
+  gw1.mode = kBwdWeight;
+  gw1.a = dact;
+  gw1.b = x_perm;
+  gw1.R = R;
+  gw1.E = q->E;
+  gw1.M = 2 * F;
+  gw1.N = H;
+  gw1.expert_offsets = off;
+  gw1.out = dw1;
+  gw1.status = status;
+  MOE_LAUNCH(launch_grouped_gemm_bwd(gw1, s));
+  tm.mark(call, 8, s);
+  // dx_t = sum over the token's routes of dXp (weights already applied)
+  MOE_LAUNCH(launch_combine(dy, rmap, nullptr, q->T, H, q->k, dx, s));
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -609,38 +750,21 @@ size_t moe_backward_workspace_size(const moe_problem* p) {
 int moe_backward(const moe_problem* p, const void* x, const float* logits, const void* w1,
                  const void* w2, const void* d_out, void* dx, float* d_logits, void* dw1,
                  void* dw2, void* ws, size_t ws_bytes, void* stream) {
-  int rc = check_full(p);
+  int rc = check_backward(p, w1, w2, dw1, dw2, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
-  if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
-  if (!ws) return MOE_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return MOE_ERR_MISALIGNED;
-  const BwdLayout B = bwd_layout_of(*p);
-  if (ws_bytes < B.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  MOE_REQUIRE_PTR(w1);
-  MOE_REQUIRE_PTR(w2);
-  MOE_REQUIRE_PTR(dw1);
-  MOE_REQUIRE_PTR(dw2);
   if (d_logits && !aligned16(d_logits)) return MOE_ERR_MISALIGNED;
+  const BwdLayout B = bwd_layout_of(*p);
   const Layout& L = B.f;
   const moe_problem pe = expanded(*p);  // after routing: E+S experts, k+S slots
   const moe_problem* q = &pe;
   const int S = p->shared_experts;
-  int launches = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t w1_bytes = sizeof(uint16_t) * q->E * 2 * static_cast<size_t>(q->F) * q->H;
-  const size_t w2_bytes = sizeof(uint16_t) * q->E * static_cast<size_t>(q->H) * q->F;
-  if (p->T == 0) {  // no routes: the weight gradients are zero
-    MOE_LAUNCH(cudaMemsetAsync(dw1, 0, w1_bytes, s));
-    MOE_LAUNCH(cudaMemsetAsync(dw2, 0, w2_bytes, s));
-    g_launches = launches;
-    return MOE_OK;
-  }
+  if (p->T == 0) return backward_no_tokens(q, dw1, dw2, s);
   MOE_REQUIRE_PTR(x);
   MOE_REQUIRE_PTR(logits);
   MOE_REQUIRE_PTR(d_out);
   MOE_REQUIRE_PTR(dx);
-  const int R = q->T * q->k;
-  const int H = q->H, F = q->F;
+  int launches = 0;
   int32_t* idx = at<int32_t>(ws, L.topk_idx);
   float* wts = at<float>(ws, L.topk_w);
   int32_t* tpe = at<int32_t>(ws, L.tokens_per_expert);
@@ -648,15 +772,6 @@ int moe_backward(const moe_problem* p, const void* x, const float* logits, const
   int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
   int32_t* rmap = at<int32_t>(ws, L.row_id_map);
   int32_t* ptok = at<int32_t>(ws, L.permuted_token);
-  uint32_t* status = at<uint32_t>(ws, L.status);
-  void* x_perm = at<void>(ws, L.x_perm);
-  void* hw = at<void>(ws, L.h);      // [R, F] w * h
-  void* dy = at<void>(ws, L.y);      // [R, H] permuted output gradient, later dXp
-  float* act = at<float>(ws, B.act);  // [R, 2F] fp32 pre-activations
-  void* dact = at<void>(ws, B.dact);  // [R, 2F] bf16 their gradient
-  float* w_perm = at<float>(ws, B.w_perm);
-  float* dw_part = at<float>(ws, B.dw_part);
-  const int n_parts = bwd_router_parts(F);
 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
@@ -672,97 +787,58 @@ int moe_backward(const moe_problem* p, const void* x, const float* logits, const
     if (rc != MOE_OK) return rc;
   }
   tm.mark(call, 2, s);
-  MOE_LAUNCH(launch_gather_rows(x, ptok, R, H, x_perm, s));
-  MOE_LAUNCH(launch_gather_rows(d_out, ptok, R, H, dy, s));
-  MOE_LAUNCH(launch_weights_to_rows(rmap, wts, R, w_perm, s));
-  tm.mark(call, 3, s);
-  // pre-activations a = x W1_e^T in fp32, recomputed rather than kept from
-  // the forward
-  BwdGemmArgs ga{};
-  ga.mode = kBwdPreact;
-  ga.a = x_perm;
-  ga.b = w1;
-  ga.R = R;
-  ga.E = q->E;
-  ga.K = H;
-  ga.N = 2 * F;
-  ga.expert_offsets = off;
-  ga.mtile_prefix = mtp;
-  ga.out = act;
-  ga.status = status;
-  MOE_LAUNCH(launch_grouped_gemm_bwd(ga, s));
-  tm.mark(call, 4, s);
-  // dh = dY W2_e, then the SwiGLU backward: dA, w*h, router partials
-  BwdGemmArgs g{};
-  g.mode = kBwdDataSwiGLU;
-  g.a = dy;
-  g.b = w2;
-  g.R = R;
-  g.E = q->E;
-  g.K = H;
-  g.N = F;
-  g.expert_offsets = off;
-  g.mtile_prefix = mtp;
-  g.act = act;
-  g.dact = dact;
-  g.hw = hw;
-  g.dw_part = dw_part;
-  g.w_perm = w_perm;
-  g.F = F;
-  g.interleave = p->glu_interleave;
-  g.clamp = clamp_of(p);
-  g.status = status;
-  MOE_LAUNCH(launch_grouped_gemm_bwd(g, s));
-  tm.mark(call, 5, s);
-  // dW2_e = dY_e^T (w h)_e
-  BwdGemmArgs gw2{};
-  gw2.mode = kBwdWeight;
-  gw2.a = dy;
-  gw2.b = hw;
-  gw2.R = R;
-  gw2.E = q->E;
-  gw2.M = H;
-  gw2.N = F;
-  gw2.expert_offsets = off;
-  gw2.out = dw2;
-  gw2.status = status;
-  MOE_LAUNCH(launch_grouped_gemm_bwd(gw2, s));
-  tm.mark(call, 6, s);
-  // dXp = dA W1_e (into dY's region, no longer needed)
-  BwdGemmArgs gx{};
-  gx.mode = kBwdDataPlain;
-  gx.a = dact;
-  gx.b = w1;
-  gx.R = R;
-  gx.E = q->E;
-  gx.K = 2 * F;
-  gx.N = H;
-  gx.expert_offsets = off;
-  gx.mtile_prefix = mtp;
-  gx.out = dy;
-  gx.status = status;
-  MOE_LAUNCH(launch_grouped_gemm_bwd(gx, s));
-  tm.mark(call, 7, s);
-  // dW1_e = dA_e^T x_e
-  BwdGemmArgs gw1{};
-  gw1.mode = kBwdWeight;
-  gw1.a = dact;
-  gw1.b = x_perm;
-  gw1.R = R;
-  gw1.E = q->E;
-  gw1.M = 2 * F;
-  gw1.N = H;
-  gw1.expert_offsets = off;
-  gw1.out = dw1;
-  gw1.status = status;
-  MOE_LAUNCH(launch_grouped_gemm_bwd(gw1, s));
-  tm.mark(call, 8, s);
-  // dx_t = sum over the token's routes of dXp (weights already applied)
-  MOE_LAUNCH(launch_combine(dy, rmap, nullptr, q->T, H, q->k, dx, s));
+  rc = run_backward_core(p, q, B, x, d_out, wts, w1, w2, dx, dw1, dw2, ws, s, launches, tm, call);
+  if (rc != MOE_OK) return rc;
   tm.mark(call, 9, s);
   if (d_logits)
-    MOE_LAUNCH(launch_router_backward(logits, idx, wts, rmap, dw_part, n_parts, p->T, p->E,
-                                      p->k, q->k, p->renormalize ? 1 : 0, d_logits, s));
+    MOE_LAUNCH(launch_router_backward(logits, idx, wts, rmap, at<float>(ws, B.dw_part),
+                                      bwd_router_parts(q->F), p->T, p->E, p->k, q->k,
+                                      p->renormalize ? 1 : 0, d_logits, s));
+  tm.mark(call, 10, s);
+  g_launches = launches;
+  return MOE_OK;
+}
+
+int moe_backward_routed(const moe_problem* p, const void* x, const int32_t* topk_idx,
+                        const float* topk_w, const void* w1, const void* w2, const void* d_out,
+                        void* dx, float* d_topk_w, void* dw1, void* dw2, void* ws,
+                        size_t ws_bytes, void* stream) {
+  int rc = check_backward(p, w1, w2, dw1, dw2, ws, ws_bytes);
+  if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_backward only
+  if (d_topk_w && !aligned16(d_topk_w)) return MOE_ERR_MISALIGNED;
+  const BwdLayout B = bwd_layout_of(*p);
+  const Layout& L = B.f;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p->T == 0) return backward_no_tokens(p, dw1, dw2, s);
+  MOE_REQUIRE_PTR(x);
+  MOE_REQUIRE_PTR(topk_idx);
+  MOE_REQUIRE_PTR(topk_w);
+  MOE_REQUIRE_PTR(d_out);
+  MOE_REQUIRE_PTR(dx);
+  int launches = 0;
+  int32_t* tpe = at<int32_t>(ws, L.tokens_per_expert);
+  int32_t* off = at<int32_t>(ws, L.expert_offsets);
+  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
+  int32_t* rmap = at<int32_t>(ws, L.row_id_map);
+  int32_t* ptok = at<int32_t>(ws, L.permuted_token);
+  const int call = g_timer.on ? g_timer.used++ : 0;
+  StageTimer& tm = g_timer;
+  if (tm.on) tm.kind = 1;
+  tm.mark(call, 0, s);
+  tm.mark(call, 1, s);
+  // the validating permutation: masked, out-of-range and repeated routes
+  rc = run_permute(p, topk_idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches);
+  if (rc != MOE_OK) return rc;
+  tm.mark(call, 2, s);
+  rc = run_backward_core(p, p, B, x, d_out, topk_w, w1, w2, dx, dw1, dw2, ws, s, launches, tm,
+                         call);
+  if (rc != MOE_OK) return rc;
+  tm.mark(call, 9, s);
+  if (d_topk_w)
+    MOE_LAUNCH(launch_route_weight_grad(rmap, at<float>(ws, B.dw_part),
+                                        bwd_router_parts(p->F),
+                                        static_cast<long>(p->T) * p->k, d_topk_w, s));
   tm.mark(call, 10, s);
   g_launches = launches;
   return MOE_OK;

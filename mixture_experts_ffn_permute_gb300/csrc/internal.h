@@ -230,6 +230,12 @@ inline int bwd_router_parts(int F) { return kBwdSwiGLUSplit * ((F + kBN - 1) / k
 cudaError_t launch_weights_to_rows(const int32_t* row_id_map, const float* topk_w, long routes,
                                    float* w_perm, cudaStream_t s);
 
+// d topk_w[t][j] = sum of the dw_part row of route (t, j) (fixed order), 0
+// for a masked slot: the routing-weight gradient of caller-supplied routes.
+cudaError_t launch_route_weight_grad(const int32_t* row_id_map, const float* dw_part,
+                                     int n_parts, long routes, float* d_topk_w,
+                                     cudaStream_t s);
+
 // Router backward, one warp per token: dw_j = sum of the dw_part row of the
 // route (fixed order), then the softmax backward over the first k slots of
 // the `slots` per token into dlogits [T, E] fp32.

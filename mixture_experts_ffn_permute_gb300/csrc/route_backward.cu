@@ -96,7 +96,35 @@ router_backward_kernel(const float* __restrict__ logits, const int32_t* __restri
   }
 }
 
+// d topk_w[t][j] = the route's <dOut_t, y>: the fixed-order sum of its
+// row's partials; 0 for a masked slot.  One thread per slot.
+__global__ void __launch_bounds__(256)
+route_weight_grad_kernel(const int32_t* __restrict__ row_id_map,
+                         const float* __restrict__ dw_part, int n_parts, long routes,
+                         float* __restrict__ d_topk_w) {
+  pdl_enter();
+  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < routes;
+       i += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int r = row_id_map[i];
+    float acc = 0.f;
+    if (r >= 0) {
+      const float* part = dw_part + static_cast<long>(r) * n_parts;
+      for (int q = 0; q < n_parts; ++q) acc += part[q];
+    }
+    d_topk_w[i] = acc;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_route_weight_grad(const int32_t* row_id_map, const float* dw_part,
+                                     int n_parts, long routes, float* d_topk_w,
+                                     cudaStream_t s) {
+  if (routes <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<long>((routes + 255) / 256, num_sms() * 8L));
+  return launch_kernel(route_weight_grad_kernel, dim3(blocks), dim3(256), 0, s, 1, row_id_map,
+                       dw_part, n_parts, routes, d_topk_w);
+}
 
 cudaError_t launch_weights_to_rows(const int32_t* row_id_map, const float* topk_w, long routes,
                                    float* w_perm, cudaStream_t s) {

@@ -204,3 +204,18 @@ def test_backward_validates(lib):
     # shared experts widen the workspace like the forward's
     ps = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, shared_experts=1)
     assert moe.backward_workspace_size(ps) > need
+
+
+def test_backward_routed_validates(lib):
+    p = P()
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    big = 1 << 40
+    f = lib.moe_backward_routed
+    need = moe.backward_workspace_size(p)
+    assert f(ctypes.byref(p), a, None, a, a, a, a, a, a, a, a, a, big, None) == 1    # topk_idx
+    assert f(ctypes.byref(p), a, a, None, a, a, a, a, a, a, a, a, big, None) == 1    # topk_w
+    assert f(ctypes.byref(p), a, a, a, a, a, a, a, mis, a, a, a, big, None) == 3     # d_topk_w
+    assert f(ctypes.byref(p), a, a, a, a, a, a, a, a, a, a, a, need - 1, None) == 4
+    ps = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, shared_experts=1)
+    assert f(ctypes.byref(ps), a, a, a, a, a, a, a, a, a, a, a, big, None) == 1      # no shared

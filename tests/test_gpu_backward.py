@@ -198,3 +198,69 @@ def test_backward_mixtral_full_size_sampled():
 
 def test_backward_skewed_full_size_sampled():
     sampled_backward(mi.SKEWED, n_tok=4)
+
+
+# ------------------------------------------------------------------ caller-supplied routing
+
+def run_backward_routed(shape, inp, idx, w, g):
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True,
+                         shape.glu_interleave, shape.swiglu_clamp)
+    ws = moe.alloc_backward_workspace(p)
+    moe.clear_device_status(ws)
+    nan = float("nan")
+    dx = torch.full((shape.T, shape.H), nan, dtype=torch.bfloat16, device=DEV)
+    dtw = torch.full((shape.T, shape.k), nan, dtype=torch.float32, device=DEV)
+    dw1 = torch.full_like(inp["w1"], nan)
+    dw2 = torch.full_like(inp["w2"], nan)
+    moe.backward_routed(p, inp["x"], idx.to(DEV), w.to(DEV), inp["w1"], inp["w2"], g, dx, dw1,
+                        dw2, ws, d_topk_w=dtw)
+    torch.cuda.synchronize()
+    return {"dx": dx, "dw_route": dtw, "dw1": dw1, "dw2": dw2}, moe.get_device_status(ws)
+
+
+ROUTED = [mi.MoEShape("routed", T=150, H=256, F=384, E=7, k=3, glu_interleave=32,
+                      swiglu_clamp=1.0),
+          mi.MoEShape("routed-big", T=900, H=512, F=256, E=4, k=2)]
+
+
+@pytest.mark.parametrize("shape", ROUTED, ids=[s.name for s in ROUTED])
+def test_backward_routed_matches_oracle(shape):
+    """Masked slots contribute nothing and get a zero weight gradient; a token
+    with every slot masked gets a zero dx row; the weights are used as given."""
+    inp, g = small_inputs(shape, seed=9)
+    idx = mi.random_topk_idx(shape.T, shape.E, shape.k, seed=9, mask_frac=0.25)
+    idx[5] = -1
+    w = mi.random_weights(shape.T, shape.k, seed=9)
+    kw = dict(interleave=shape.glu_interleave, clamp=shape.swiglu_clamp, mask_f32=True)
+    ref = oracle.expert_backward(inp["x"], idx, w, inp["w1"], inp["w2"], g, **kw)
+    mag = oracle.expert_backward(inp["x"], idx, w, inp["w1"], inp["w2"], g, magnitude=True, **kw)
+    res, st = run_backward_routed(shape, {k: v.to(DEV) for k, v in inp.items()}, idx, w,
+                                  g.to(DEV))
+    assert st == moe.MOE_OK, moe.STATUS_NAMES[st]
+    for name in ("dx", "dw1", "dw2", "dw_route"):
+        assert_grad_bound(res[name], ref[name], mag[name], f"{name}[{shape.name}]")
+    assert (res["dw_route"].cpu()[idx < 0] == 0).all()
+    assert not res["dx"][5].float().abs().sum().item()
+
+
+def test_backward_routed_invalid_indices_are_masked():
+    shape = ROUTED[0]
+    inp, g = small_inputs(shape, seed=4)
+    idx = mi.random_topk_idx(shape.T, shape.E, shape.k, seed=4)
+    w = mi.random_weights(shape.T, shape.k, seed=4)
+    idx[10, 1] = shape.E          # out of range
+    idx[11, 0] = -5               # out of range
+    idx[12, 2] = idx[12, 0]       # repeated: the later slot is dropped
+    clean = idx.clone()
+    clean[10, 1] = -1
+    clean[11, 0] = -1
+    clean[12, 2] = -1
+    kw = dict(interleave=shape.glu_interleave, clamp=shape.swiglu_clamp, mask_f32=True)
+    ref = oracle.expert_backward(inp["x"], clean, w, inp["w1"], inp["w2"], g, **kw)
+    mag = oracle.expert_backward(inp["x"], clean, w, inp["w1"], inp["w2"], g, magnitude=True,
+                                 **kw)
+    res, st = run_backward_routed(shape, {k: v.to(DEV) for k, v in inp.items()}, idx, w,
+                                  g.to(DEV))
+    assert moe.STATUS_NAMES[st] == "MOE_ERR_DEVICE_INDEX"
+    for name in ("dx", "dw1", "dw2", "dw_route"):
+        assert_grad_bound(res[name], ref[name], mag[name], f"{name} (invalid routes masked)")
