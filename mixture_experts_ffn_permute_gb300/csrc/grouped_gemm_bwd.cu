@@ -23,12 +23,17 @@
 // (8 KB) further (its leading offset).  One K=16 MMA step is 16 rows = 2 KB.
 //
 // Warp roles (192 threads, one CTA per SM, persistent over the tile list):
-//   warp 0      TMA producer, 4-stage ring of 48 KB (A 16 KB + B 32 KB)
-//   warp 1      TMEM allocation + MMA issue (lane 0); in the weight-gradient
-//               kernel the whole warp first zeroes the rows of a ragged last
-//               K step that belong to the next expert
+//   warp 0      TMA producer.  1-CTA tiles (weight gradients): a ring of 48 KB
+//               stages (A 16 KB + B 32 KB), 4 deep, 3 for the weight gradients
+//               of small experts; 2-CTA pairs (data gradients): 6 stages of
+//               32 KB per CTA (A 16 KB + half of B)
+//   warp 1      TMEM allocation + MMA issue (lane 0; the leader's for a pair);
+//               in the weight-gradient kernel the whole warp first zeroes the
+//               rows of a ragged last K step that belong to the next expert
 //   warps 2..5  epilogue (TMEM lanes 32*(warp%4) ..), two 256-column
-//               accumulators so a tile's epilogue overlaps the next mainloop
+//               accumulators so a tile's epilogue overlaps the next mainloop;
+//               weight gradients and fp32 pre-activations leave through
+//               swizzled shared-memory staging and bulk-tensor stores
 // Every wait is bounded (ptx.cuh).
 #include <cuda.h>
 #include <cuda_bf16.h>
