@@ -267,6 +267,72 @@ def cpu_baseline(shape, inp_host, target_s: float):
                       f"{dt:.1f} s)"}
 
 
+# ------------------------------------------------------------------ end to end
+
+E2E_HOW = ("every step: inputs host->device from pinned memory, the layer call, its result "
+           "device->host; the copies of step i+1 (in) and step i-1 (out) overlap step i's "
+           "call (two buffer sets, separate copy streams), as a serving loop runs")
+
+
+def timed_e2e(dev, stream, steps, warm, host_inputs, outs, run):
+    """Milliseconds per step of a pipelined loop through the public API.  Step
+    i's inputs go host->device on one stream while step i-1 computes, and its
+    outputs come back on another while step i+1 computes; every step's bytes
+    cross inside the timed region, which runs from an event before the first
+    copy to the completion of the last read-back.  ``outs`` holds two sets of
+    device output tensors; ``run(inputs, outs_set)`` enqueues one layer call on
+    ``stream``."""
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dins = [[torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_inputs]
+            for _ in range(2)]
+    houts = [[torch.empty(o.shape, dtype=o.dtype, device="cpu").pin_memory() for o in outs[0]]
+             for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    read = [torch.cuda.Event() for _ in range(2)]
+
+    def issue_h2d(i):
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(done[b])  # the call that read this buffer has finished
+            for hs, dd in zip(host_inputs, dins[b]):
+                dd.copy_(hs, non_blocking=True)
+            copied[b].record(h2d)
+
+    def step(i):
+        b = i % 2
+        stream.wait_event(copied[b])
+        if i >= 2:
+            stream.wait_event(read[b])  # this buffer's previous outputs are on the host
+        run(dins[b], outs[b])
+        done[b].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(done[b])
+            for o, ho in zip(outs[b], houts[b]):
+                ho.copy_(o, non_blocking=True)
+            read[b].record(d2h)
+
+    def loop(n, start=None):
+        if start is not None:
+            h2d.wait_event(start)
+        issue_h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                issue_h2d(i + 1)
+            step(i)
+        stream.wait_event(read[(n - 1) % 2])
+
+    loop(max(warm, 2))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    loop(steps, start=e0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 # ------------------------------------------------------------------ our arm
 
 def bench_ours(args, shape, desc):
@@ -375,32 +441,19 @@ def bench_ours(args, shape, desc):
     # host -> device each step; the weights are parameters and stay resident
     step_inputs = [x, logits] + ([xs] if shape.lowprec else [])
     hosts = [t.cpu().pin_memory() for t in step_inputs]
-    devs = [torch.empty_like(t) for t in step_inputs]
-    oh = torch.empty_like(out, device="cpu").pin_memory()
+    outs2 = [[out], [torch.empty_like(out)]]
 
-    def e2e_step():
-        for hsrc, ddst in zip(hosts, devs):
-            ddst.copy_(hsrc, non_blocking=True)
+    def e2e_run(ins, o):
         if shape.lowprec:
-            moe.forward_fp8_nvfp4(p, devs[0], devs[2], devs[1], lp["w1q"], lp["w1g"], lp["w2q"],
-                                  lp["w2g"], prepared, out, ws)
+            moe.forward_fp8_nvfp4(p, ins[0], ins[2], ins[1], lp["w1q"], lp["w1g"], lp["w2q"],
+                                  lp["w2g"], prepared, o[0], ws)
         else:
-            fwd(devs[0], devs[1])
-        oh.copy_(out, non_blocking=True)
+            moe.forward(p, ins[0], ins[1], w1, w2, o[0], ws)
 
-    for _ in range(2):
-        e2e_step()
     K2 = max(3, K // 2)
     barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K2):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    e2e_ms = reduce_max(timed_e2e(dev, stream, K2, 2, hosts, outs2, e2e_run), world, dev)
     barrier(world)
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / K2, world, dev)
 
     # experts that received tokens (untimed extra call): their weights are the
     # bytes GEMM1 must stream
@@ -466,7 +519,7 @@ def bench_ours(args, shape, desc):
         "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in step_inputs),
-                "d2h_bytes_per_step": out.numel() * 2},
+                "d2h_bytes_per_step": out.numel() * 2, "how": E2E_HOW},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
         "stages_ms": {k: round(v, 5) for k, v in stages.items() if not k.startswith("_")},
@@ -580,30 +633,16 @@ def bench_backward(args, shape, desc):
     # optimizer's input)
     step_inputs = [x, logits, g]
     hosts = [t.cpu().pin_memory() for t in step_inputs]
-    devs = [torch.empty_like(t) for t in step_inputs]
     outs = [dx, dl]
-    out_h = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    outs2 = [outs, [torch.empty_like(dx), torch.empty_like(dl)]]
 
-    def e2e_step():
-        for hsrc, ddst in zip(hosts, devs):
-            ddst.copy_(hsrc, non_blocking=True)
-        bwd(*devs)
-        for src, dst in zip(outs, out_h):
-            dst.copy_(src, non_blocking=True)
+    def e2e_run(ins, o):
+        moe.backward(p, ins[0], ins[1], w1, w2, ins[2], o[0], dw1, dw2, ws, d_logits=o[1])
 
-    for _ in range(2):
-        e2e_step()
     K2 = max(3, K // 2)
     barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K2):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    e2e_ms = reduce_max(timed_e2e(dev, stream, K2, 2, hosts, outs2, e2e_run), world, dev)
     barrier(world)
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / K2, world, dev)
 
     flops = bwd_flops(shape)
     rhf = float(shape.R) * shape.H * shape.F
@@ -642,7 +681,8 @@ def bench_backward(args, shape, desc):
         "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in step_inputs),
-                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs)},
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs),
+                "how": E2E_HOW},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
         "stages_ms": {k: round(v, 5) for k, v in stages.items() if not k.startswith("_")},
