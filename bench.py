@@ -53,7 +53,9 @@ KERNEL_NAMES = {1: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU> (GEMM1, 1-CT
                 4: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU,pair> (GEMM1, multicast pair)"),
                 5: ("grouped_gemm_2cta.cu", "grouped_gemm_2cta_kernel<SwiGLU> (GEMM1, cta_group::2)"),
                 6: ("grouped_gemm_swap2.cu",
-                    "grouped_gemm_swap2_kernel<SwiGLU> (GEMM1, weight rows on M, cta_group::2)")}
+                    "grouped_gemm_swap2_kernel<SwiGLU> (GEMM1, weight rows on M, cta_group::2)"),
+                7: ("grouped_mlp_decode.cu",
+                    "grouped_mlp_decode_kernel (GEMM1+SwiGLU, GEMM2 and combine in one launch)")}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 WORKLOADS = {
     "mixtral": (mi.MIXTRAL, "Mixtral-shaped MoE FFN layer: T=4096 H=4096 F=14336 E=8 top-2 bf16"),
@@ -110,6 +112,14 @@ def ncu_traffic(kernel_file: str, workload: str):
     return None
 
 
+def traffic_key(args) -> str:
+    """Workload key of the ncu traffic table: the workload name, with -T<T>
+    for a token-count override; other overrides have no entry."""
+    if args.E or args.k:
+        return "custom"
+    return f"{args.workload}-T{args.T}" if args.T else args.workload
+
+
 def gemm1_algorithmic_bytes(shape, used_experts: int, scale_block: int = 16) -> float:
     """HBM bytes GEMM1 cannot avoid: the gate/up weights of every expert that
     received tokens, the permuted activation rows read once and h written once.
@@ -121,6 +131,14 @@ def gemm1_algorithmic_bytes(shape, used_experts: int, scale_block: int = 16) -> 
     R, H, F = shape.R, shape.H, shape.F
     w = (2 * F * H / 2 + 2 * F * H / scale_block) if shape.lowprec else 2 * F * H * 2
     return used_experts * w + R * H * 2 + R * F * 2
+
+
+def decode_mlp_algorithmic_bytes(shape, used_experts: int) -> float:
+    """HBM bytes of the one-launch decode MLP: W1 (2F*H) and W2 (H*F) bf16 of
+    every expert that received tokens, the permuted rows read once (R*H*2)
+    and the combined output written once (T*H*2); h and y stay in L2."""
+    R, H, F = shape.R, shape.H, shape.F
+    return used_experts * 3 * F * H * 2 + R * H * 2 + shape.T * H * 2
 
 
 def load_peaks():
@@ -474,6 +492,11 @@ def bench_ours(args, shape, desc):
     gemm1_ms = stages.get("gemm1_swiglu", float("nan"))
     gemm1_flops = 4.0 * shape.R * shape.H * shape.F
     gemm1_bytes = gemm1_algorithmic_bytes(shape, used_experts, 32 if mx else 16)
+    if kid == 7 and not shape.lowprec:
+        # one launch holds both GEMMs and the combine (its time is the
+        # gemm1_swiglu stage; the gemm2 and combine stages read zero)
+        gemm1_flops = 6.0 * shape.R * shape.H * shape.F
+        gemm1_bytes = decode_mlp_algorithmic_bytes(shape, used_experts)
     peak_key = "bf16_tflops_sustained"
     gemm1_s = gemm1_ms / 1e3
     t_tensor = gemm1_flops / (peaks[peak_key] * 1e12)
@@ -509,8 +532,7 @@ def bench_ours(args, shape, desc):
         "roofline": {"kernel": kname, "bound": main["bound"],
                      "achieved": main["achieved"], "peak": main["peak"], "unit": main["unit"],
                      "frac": main["frac"],
-                     "traffic": ncu_traffic(kfile, args.workload if not args.T and not args.E
-                                            and not args.k else "custom"),
+                     "traffic": ncu_traffic(kfile, traffic_key(args)),
                      "peak_source": main["peak_source"],
                      "algorithmic": {"flops": gemm1_flops, "bytes": gemm1_bytes,
                                      "experts_with_tokens": used_experts},

@@ -90,8 +90,9 @@ typedef struct moe_problem {
   int32_t fusion;
   /* GEMM tiling (moe_problem.kernel):
        MOE_KERNEL_AUTO          T*k <= 2*E (at most two routes per expert on
-                                average): weight-row tiles; else 2-CTA
-                                weight-row tiles
+                                average): weight-row tiles (in moe_forward at
+                                T*k < E: the one-launch decode MLP below);
+                                else 2-CTA weight-row tiles
        MOE_KERNEL_TOKEN_TILES   128 permuted token rows x 256 weight rows per tile
        MOE_KERNEL_WEIGHT_TILES  128 weight rows x up to 32 token rows per tile
                                 (decode sizes: weights stream once at HBM speed)
@@ -111,6 +112,17 @@ typedef struct moe_problem {
                                 experts with one token tile (weight-streaming)
                                 interleaved with those of experts with more
                                 (MMA-bound)
+       MOE_KERNEL_DECODE_FUSED  moe_forward only (the other entry points run
+                                MOE_KERNEL_WEIGHT_TILES): the 32-token weight
+                                tiles of GEMM1 + SwiGLU and of GEMM2 and the
+                                weighted combine in ONE persistent launch.
+                                Tiles are claimed from a global counter,
+                                GEMM1's first; a GEMM2 tile streams its
+                                weights at once and waits for its expert's h
+                                rows on a per-expert count; the tile that
+                                completes a token's k routes of a 128-feature
+                                block sums them in slot order (bit-identical
+                                to the separate combine)
      The fusion options do not apply to the weight-row tilings. */
   int32_t kernel;
   /* Shared experts (moe_forward only; 0 elsewhere): S >= 0 experts, stored
@@ -131,6 +143,7 @@ typedef struct moe_problem {
 #define MOE_KERNEL_TOKEN_TILES_PAIR 4
 #define MOE_KERNEL_TOKEN_TILES_2CTA 5
 #define MOE_KERNEL_WEIGHT_TILES_2CTA 6
+#define MOE_KERNEL_DECODE_FUSED 7
 
 /* Limits checked by every entry point. */
 #define MOE_MAX_EXPERTS 1024

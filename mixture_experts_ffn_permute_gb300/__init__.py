@@ -36,6 +36,7 @@ KERNEL_WEIGHT_TILES_WIDE = 3  # 128 weight rows x up to 256 token rows, N fitted
 KERNEL_TOKEN_TILES_PAIR = 4   # token-row tiles by 2-CTA clusters multicasting the weight tile
 KERNEL_TOKEN_TILES_2CTA = 5   # 256x256 tiles per CTA pair, tcgen05.mma.cta_group::2
 KERNEL_WEIGHT_TILES_2CTA = 6  # 256 weight rows x up to 256 tokens per CTA pair, N fitted
+KERNEL_DECODE_FUSED = 7  # moe_forward: both GEMMs and the combine of 32-token tiles in one launch
 STATUS_NAMES = {
     0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
     3: "MOE_ERR_MISALIGNED", 4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_CUDA",

@@ -78,7 +78,7 @@ moe_problem expanded(const moe_problem& p) {
 
 struct Layout {
   size_t status, chunk_counts, tokens_per_expert, expert_offsets, mtile_prefix, topk_idx, topk_w,
-      row_id_map, permuted_token, counters, x_perm, h, y, total;
+      row_id_map, permuted_token, counters, dec_counters, x_perm, h, y, total;
 };
 
 Layout layout_of(const moe_problem& p0) {
@@ -102,6 +102,7 @@ Layout layout_of(const moe_problem& p0) {
   L.row_id_map = take(sizeof(int32_t) * R);
   L.permuted_token = take(sizeof(int32_t) * R);
   L.counters = take(sizeof(int32_t) * T * (p.H > 0 ? (static_cast<size_t>(p.H) + kBN - 1) / kBN : 0));
+  L.dec_counters = take(sizeof(int32_t) * static_cast<size_t>(decode_mlp_counters(p.T, p.E, p.H)));
   L.x_perm = take(2 * R * static_cast<size_t>(p.H));
   L.h = take(2 * R * static_cast<size_t>(p.F));
   L.y = take(2 * R * static_cast<size_t>(p.H));
@@ -162,7 +163,7 @@ int check_full(const moe_problem* p) {
   if (p->precision != MOE_PREC_BF16 && p->precision != MOE_PREC_FP8_NVFP4)
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
-  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_WEIGHT_TILES_2CTA)
+  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_DECODE_FUSED)
     return MOE_ERR_INVALID_ARG;
   // the FP8/NVFP4 GEMMs come in two tilings
   if (p->precision == MOE_PREC_FP8_NVFP4 && p->kernel != MOE_KERNEL_AUTO &&
@@ -206,6 +207,8 @@ int check_ws(const moe_problem* p, void* ws, size_t ws_bytes) {
 // (a ragged expert pads at most 31 rows) -- on GB300 they match or beat the
 // token-row tilings even for experts with thousands of rows.
 int gemm_tiling(const moe_problem* p) {
+  // the one-launch decode MLP is moe_forward's; elsewhere its tiles run as two GEMMs
+  if (p->kernel == MOE_KERNEL_DECODE_FUSED) return MOE_KERNEL_WEIGHT_TILES;
   if (p->kernel != MOE_KERNEL_AUTO) return p->kernel;
   const long long routes = static_cast<long long>(p->T) * p->k;
   if (routes <= 2LL * p->E) return MOE_KERNEL_WEIGHT_TILES;
@@ -220,6 +223,17 @@ int lowprec_tiling(const moe_problem* p) {
   if (p->kernel == MOE_KERNEL_WEIGHT_TILES_2CTA || p->kernel == MOE_KERNEL_WEIGHT_TILES_WIDE)
     return p->kernel;
   return MOE_KERNEL_TOKEN_TILES;
+}
+
+// moe_forward at decode sizes: GEMM1, GEMM2 and the combine in one launch
+// (grouped_mlp_decode.cu) below one route per expert on average.  From one
+// to two routes per expert the two-GEMM 32-token weight tiles measured as
+// fast or faster on GB300 (H=2048 F=768 E=128 top-8, CUDA-graph replay:
+// T=16 150 us against 147 us, T=32 217 us against 203 us; below: T=1 37.1
+// against 38.6 us, T=4 67.6 against 79.3 us, T=8 105.7 against 113.9 us).
+bool use_decode_fused(const moe_problem* p) {
+  if (p->kernel == MOE_KERNEL_DECODE_FUSED) return true;
+  return p->kernel == MOE_KERNEL_AUTO && static_cast<long long>(p->T) * p->k < p->E;
 }
 
 bool use_weight_tiles(const moe_problem* p) {
@@ -655,6 +669,9 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
                            gemm_tiling(q) == MOE_KERNEL_WEIGHT_TILES_2CTA;
   const bool fuse_gather = !plain_tiles && (p->fusion & MOE_FUSE_GATHER_A) != 0;
   const bool fuse_combine = !plain_tiles && (p->fusion & MOE_FUSE_COMBINE) != 0;
+  const bool decode_fused = use_decode_fused(q);
+  int32_t* dctr = decode_fused ? at<int32_t>(ws, L.dec_counters) : nullptr;
+  const int n_dctr = decode_fused ? decode_mlp_counters(q->T, q->E, q->H) : 0;
 
   const int call = g_timer.on ? g_timer.used++ : 0;
   StageTimer& tm = g_timer;
@@ -666,7 +683,8 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
     const bool gather_here = !fuse_gather && R <= kTinyGatherRoutes;
     MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, S, p->renormalize ? 1 : 0, idx,
                                          wts, tpe, off, mtp, rmap, ptok,
-                                         gather_here ? x : nullptr, p->H, x_perm, s));
+                                         gather_here ? x : nullptr, p->H, x_perm, s, dctr,
+                                         n_dctr));
     for (int i = 1; i <= 4; ++i) tm.mark(call, i, s);
     if (!fuse_gather && !gather_here) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   } else {
@@ -675,16 +693,46 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
     tm.mark(call, 1, s);
     if (!fuse_combine && permute_small_fits(q->T, q->E, q->k)) {
       // decode sizes: histogram + scan + scatter in one block
-      MOE_LAUNCH(launch_permute_small(idx, q->T, q->E, q->k, tpe, off, mtp, rmap, ptok, s));
+      MOE_LAUNCH(launch_permute_small(idx, q->T, q->E, q->k, tpe, off, mtp, rmap, ptok, s,
+                                      dctr, n_dctr));
       for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
     } else {
       rc = run_permute(q, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2,
                        fuse_combine ? counters : nullptr, p->H / kBN);
       if (rc != MOE_OK) return rc;
+      if (decode_fused)
+        MOE_LAUNCH(cudaMemsetAsync(dctr, 0, sizeof(int32_t) * static_cast<size_t>(n_dctr), s));
     }
     if (!fuse_gather) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   }
   tm.mark(call, 5, s);
+  if (decode_fused) {
+    // GEMM1, GEMM2 and the combine in one launch (timed as the GEMM1 stage)
+    DecodeMlpArgs a{};
+    a.x_perm = x_perm;
+    a.w1 = w1;
+    a.w2 = w2;
+    a.expert_offsets = off;
+    a.h = h;
+    a.y = y;
+    a.out = out;
+    a.permuted_token = ptok;
+    a.row_id_map = rmap;
+    a.topk_w = wts;
+    a.counters = dctr;
+    a.R = R;
+    a.E = q->E;
+    a.H = q->H;
+    a.F = q->F;
+    a.k = q->k;
+    a.interleave = q->glu_interleave;
+    a.clamp = clamp_of(q);
+    a.status = status;
+    MOE_LAUNCH(launch_grouped_mlp_decode(a, s));
+    for (int i = 6; i <= 8; ++i) tm.mark(call, i, s);
+    g_launches = launches;
+    return MOE_OK;
+  }
   const FusedIO fused{fuse_gather, fuse_combine, ptok, rmap, wts, counters, out};
   rc = run_mlp(q, fuse_gather ? x : x_perm, off, mtp, w1, w2, h, y, status, s, launches, &tm,
                call, 6, &fused);
@@ -1039,7 +1087,7 @@ int moe_selected_kernel(const moe_problem* p) {
   if (check_full(p) != MOE_OK) return -1;
   if (p->precision == MOE_PREC_FP8_NVFP4) return lowprec_tiling(p);
   const moe_problem q = expanded(*p);
-  return gemm_tiling(&q);
+  return use_decode_fused(&q) ? MOE_KERNEL_DECODE_FUSED : gemm_tiling(&q);
 }
 
 int moe_stage_timing_begin(int n_calls) {

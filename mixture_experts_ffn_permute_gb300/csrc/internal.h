@@ -84,18 +84,22 @@ constexpr int kTinyExperts = 256;   // staged logits: T * E floats of shared mem
 constexpr int kTinyRoutes = 256;
 constexpr int kTinyGatherRoutes = 64;  // rows one block gathers faster than a launch
 bool route_permute_tiny_fits(int T, int E, int k, int S);
+// Both single-block forms also zero zero_ints[0 .. n_zero) when given (the
+// counters of the one-launch decode MLP that follows them).
 cudaError_t launch_route_permute_tiny(const float* logits, int T, int E, int k, int S,
                                       int renormalize,
                                       int32_t* topk_idx, float* topk_w,
                                       int32_t* tokens_per_expert, int32_t* expert_offsets,
                                       int32_t* mtile_prefix, int32_t* row_id_map,
                                       int32_t* permuted_token, const void* x, int H,
-                                      void* x_perm, cudaStream_t s);
+                                      void* x_perm, cudaStream_t s,
+                                      int32_t* zero_ints = nullptr, int n_zero = 0);
 bool permute_small_fits(int T, int E, int k);
 cudaError_t launch_permute_small(const int32_t* topk_idx, int T, int E, int k,
                                  int32_t* tokens_per_expert, int32_t* expert_offsets,
                                  int32_t* mtile_prefix, int32_t* row_id_map,
-                                 int32_t* permuted_token, cudaStream_t s);
+                                 int32_t* permuted_token, cudaStream_t s,
+                                 int32_t* zero_ints = nullptr, int n_zero = 0);
 
 // Step 2c: stable scatter -> row_id_map and permuted_token.
 cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
@@ -155,6 +159,29 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s);
 // The same GEMMs with weight rows on the MMA's M side and up to 32 (wide:
 // 256) tokens on N (kSwiGLU and kPlain epilogues; no gather / combine fusion).
 cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaStream_t s);
+
+// Decode sizes in one launch: GEMM1 + SwiGLU, GEMM2 and (out != NULL) the
+// weighted combine, 128 weight rows x up to 32 token rows per tile
+// (grouped_mlp_decode.cu).  counters: decode_mlp_counters(T, E, H) int32,
+// zero at launch; with the combine every route of every token must be valid.
+struct DecodeMlpArgs {
+  const void* x_perm;             // [R, H] bf16
+  const void* w1;                 // [E * 2F, H] bf16
+  const void* w2;                 // [E * H, F] bf16
+  const int32_t* expert_offsets;  // [E + 1]
+  void* h;                        // [R, F] bf16 (scratch)
+  void* y;                        // [R, H] bf16 (the output without the combine)
+  void* out;                      // [T, H] bf16 or NULL
+  const int32_t* permuted_token;  // [R]
+  const int32_t* row_id_map;      // [T, k]
+  const float* topk_w;            // [T, k]
+  int32_t* counters;
+  int R, E, H, F, k, interleave;
+  float clamp;
+  uint32_t* status;
+};
+int decode_mlp_counters(int T, int E, int H);
+cudaError_t launch_grouped_mlp_decode(const DecodeMlpArgs& g, cudaStream_t s);
 
 // Token-row tiles on CTA pairs with tcgen05.mma.cta_group::2 (kSwiGLU, kPlain).
 cudaError_t launch_grouped_gemm_2cta(const GroupedGemmArgs& g, cudaStream_t s);

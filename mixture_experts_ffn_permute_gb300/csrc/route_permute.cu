@@ -423,8 +423,10 @@ __global__ void __launch_bounds__(1024)
 permute_small_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
                      int32_t* __restrict__ tokens_per_expert,
                      int32_t* __restrict__ expert_offsets, int32_t* __restrict__ mtile_prefix,
-                     int32_t* __restrict__ row_id_map, int32_t* __restrict__ permuted_token) {
+                     int32_t* __restrict__ row_id_map, int32_t* __restrict__ permuted_token,
+                     int32_t* __restrict__ zero_ints, int n_zero) {
   pdl_enter();
+  for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_ints[i] = 0;
   extern __shared__ int32_t s_small[];
   __shared__ int s_warp[32];
   const int R = T * k;
@@ -448,8 +450,10 @@ route_permute_tiny_kernel(const float* __restrict__ logits, int T, int E, int k,
                           int32_t* __restrict__ expert_offsets,
                           int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ row_id_map,
                           int32_t* __restrict__ permuted_token, const uint4* __restrict__ x,
-                          int vecs_per_row, uint4* __restrict__ x_perm) {
+                          int vecs_per_row, uint4* __restrict__ x_perm,
+                          int32_t* __restrict__ zero_ints, int n_zero) {
   pdl_enter();
+  for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_ints[i] = 0;
   extern __shared__ int32_t s_tiny[];
   __shared__ int s_warp[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -541,11 +545,12 @@ bool permute_small_fits(int T, int E, int k) {
 cudaError_t launch_permute_small(const int32_t* topk_idx, int T, int E, int k,
                                  int32_t* tokens_per_expert, int32_t* expert_offsets,
                                  int32_t* mtile_prefix, int32_t* row_id_map,
-                                 int32_t* permuted_token, cudaStream_t s) {
+                                 int32_t* permuted_token, cudaStream_t s, int32_t* zero_ints,
+                                 int n_zero) {
   const size_t smem = sizeof(int32_t) * (static_cast<size_t>(T) * k + E);
   return launch_kernel(permute_small_kernel, dim3(1), dim3(1024), smem, s, 1, topk_idx, T, E, k,
                        tokens_per_expert, expert_offsets, mtile_prefix, row_id_map,
-                       permuted_token);
+                       permuted_token, zero_ints, zero_ints ? n_zero : 0);
 }
 
 bool route_permute_tiny_fits(int T, int E, int k, int S) {
@@ -557,14 +562,15 @@ cudaError_t launch_route_permute_tiny(const float* logits, int T, int E, int k, 
                                       int32_t* tokens_per_expert, int32_t* expert_offsets,
                                       int32_t* mtile_prefix, int32_t* row_id_map,
                                       int32_t* permuted_token, const void* x, int H,
-                                      void* x_perm, cudaStream_t s) {
+                                      void* x_perm, cudaStream_t s, int32_t* zero_ints,
+                                      int n_zero) {
   const int R = T * (k + S);
   const size_t smem = sizeof(int32_t) * (2 * static_cast<size_t>(R) + E + S) +
                       sizeof(float) * static_cast<size_t>(T) * E;
   return launch_kernel(route_permute_tiny_kernel, dim3(1), dim3(1024), smem, s, 1, logits, T, E,
                        k, S, renormalize, topk_idx, topk_w, tokens_per_expert, expert_offsets,
                        mtile_prefix, row_id_map, permuted_token, static_cast<const uint4*>(x),
-                       H / 8, static_cast<uint4*>(x_perm));
+                       H / 8, static_cast<uint4*>(x_perm), zero_ints, zero_ints ? n_zero : 0);
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* row_id_map, const float* topk_w,

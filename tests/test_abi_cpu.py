@@ -105,9 +105,19 @@ def test_binding_raises_without_library(tmp_path):
 
 
 def test_auto_tiling_selection():
-    """Auto picks 32-token weight-row tiles at <= 2 routes per expert, else 2-CTA weight-row tiles."""
+    """Auto picks the one-launch decode MLP below 1 route per expert, the two-GEMM 32-token
+    weight-row tiles up to 2, else 2-CTA weight-row tiles."""
     lib = moe.load()
-    assert moe.selected_kernel(moe.Problem.make(T=1, H=2048, F=768, E=128, k=8)) == moe.KERNEL_WEIGHT_TILES
+    assert moe.selected_kernel(moe.Problem.make(T=1, H=2048, F=768, E=128, k=8)) == \
+        moe.KERNEL_DECODE_FUSED
+    assert moe.selected_kernel(moe.Problem.make(T=15, H=2048, F=768, E=128, k=8)) == \
+        moe.KERNEL_DECODE_FUSED
+    assert moe.selected_kernel(moe.Problem.make(T=16, H=2048, F=768, E=128, k=8)) == \
+        moe.KERNEL_WEIGHT_TILES
+    assert moe.selected_kernel(moe.Problem.make(T=32, H=2048, F=768, E=128, k=8)) == \
+        moe.KERNEL_WEIGHT_TILES
+    p = moe.Problem.make(T=8, H=2048, F=768, E=128, k=8, kernel=moe.KERNEL_WEIGHT_TILES)
+    assert moe.selected_kernel(p) == moe.KERNEL_WEIGHT_TILES
     assert moe.selected_kernel(moe.Problem.make(T=64, H=2048, F=768, E=128, k=8)) == \
         moe.KERNEL_WEIGHT_TILES_2CTA
     assert moe.selected_kernel(moe.Problem.make(T=4096, H=4096, F=14336, E=8, k=2)) == \
@@ -127,7 +137,8 @@ def test_lowprec_tiling_selection():
     assert moe.selected_kernel(mk(moe.KERNEL_WEIGHT_TILES_2CTA)) == moe.KERNEL_WEIGHT_TILES_2CTA
     assert moe.selected_kernel(mk(moe.KERNEL_TOKEN_TILES)) == moe.KERNEL_TOKEN_TILES
     assert moe.selected_kernel(mk(moe.KERNEL_WEIGHT_TILES_WIDE)) == moe.KERNEL_WEIGHT_TILES_WIDE
-    for k in (moe.KERNEL_WEIGHT_TILES, moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA):
+    for k in (moe.KERNEL_WEIGHT_TILES, moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA,
+              moe.KERNEL_DECODE_FUSED):
         assert moe.selected_kernel(mk(k)) == -1
 
 

@@ -56,9 +56,10 @@ SMALL = [
 
 
 KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE,
-           moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA, moe.KERNEL_WEIGHT_TILES_2CTA]
+           moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA, moe.KERNEL_WEIGHT_TILES_2CTA,
+           moe.KERNEL_DECODE_FUSED]
 KERNEL_IDS = ["token_tiles", "weight_tiles", "weight_tiles_wide", "token_tiles_pair",
-              "token_tiles_2cta", "weight_tiles_2cta"]
+              "token_tiles_2cta", "weight_tiles_2cta", "decode_fused"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
@@ -153,6 +154,39 @@ def test_forward_is_bitwise_deterministic_and_reuses_workspace():
     fresh = run_forward(shape, b)
     assert torch.equal(r2["out"].view(torch.int16), fresh["out"].view(torch.int16))
     assert moe.last_launch_count() >= 5
+
+
+# One launch for GEMM1, GEMM2 and the combine (decode sizes): the same MMA
+# shapes, K order and epilogue arithmetic as the two-GEMM 32-token weight
+# tiles followed by the separate combine kernel, so the outputs agree bit for
+# bit.  Shapes cover the single-block routing path, the one-block permutation
+# (E > 256), experts with several 32-token tiles, empty experts, and (T*k >
+# 4096) the multi-kernel permutation with the counters cleared by a memset.
+DECODE_FUSED_SHAPES = [mi.DECODE.with_T(1), mi.DECODE.with_T(8), mi.DECODE.with_T(32),
+                       mi.MoEShape("fused-e257", T=8, H=256, F=256, E=257, k=8),
+                       mi.MoEShape("fused-ragged", T=333, H=512, F=384, E=7, k=3),
+                       mi.MoEShape("fused-il32clamp", T=20, H=512, F=256, E=64, k=4,
+                                   glu_interleave=32, swiglu_clamp=7.0),
+                       mi.MoEShape("fused-multikernel-permute", T=1100, H=256, F=256, E=16, k=4)]
+
+
+@pytest.mark.parametrize("shape", DECODE_FUSED_SHAPES, ids=lambda s: s.name)
+def test_decode_fused_matches_two_gemm_path_bitwise(shape):
+    d = to_dev(mi.make_inputs(shape, seed=11))
+    fused = run_forward(shape, d, kernel=moe.KERNEL_DECODE_FUSED)
+    n_fused = moe.last_launch_count()
+    two = run_forward(shape, d, kernel=moe.KERNEL_WEIGHT_TILES)
+    assert n_fused < moe.last_launch_count()
+    assert torch.equal(fused["topk_idx"], two["topk_idx"])
+    assert torch.equal(fused["out"].view(torch.int16), two["out"].view(torch.int16)), \
+        f"decode-fused output differs from the two-GEMM path [{shape.name}]"
+    # the same workspace again, after a call with other routing: the counters
+    # the one-launch kernel depends on start from zero on every call
+    other = dict(d)
+    other["logits"] = mi.make_logits(shape, seed=12).to(DEV)
+    run_forward(shape, other, ws=fused["ws"], kernel=moe.KERNEL_DECODE_FUSED)
+    again = run_forward(shape, d, ws=fused["ws"], kernel=moe.KERNEL_DECODE_FUSED)
+    assert torch.equal(fused["out"].view(torch.int16), again["out"].view(torch.int16))
 
 
 # ------------------------------------------------------------------ full size, sampled
@@ -274,8 +308,8 @@ SHARED_CASES = [(mi.MoEShape("shared-tiny-path", T=4, H=256, F=256, E=16, k=4), 
 
 
 @pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_TOKEN_TILES,
-                                    moe.KERNEL_WEIGHT_TILES_2CTA],
-                         ids=["auto", "token_tiles", "weight_tiles_2cta"])
+                                    moe.KERNEL_WEIGHT_TILES_2CTA, moe.KERNEL_DECODE_FUSED],
+                         ids=["auto", "token_tiles", "weight_tiles_2cta", "decode_fused"])
 @pytest.mark.parametrize("case", SHARED_CASES, ids=lambda c: c[0].name)
 def test_forward_shared_experts(case, kernel):
     """S shared experts (the last S of w1/w2) join every token with weight 1."""
