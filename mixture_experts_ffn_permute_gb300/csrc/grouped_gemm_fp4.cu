@@ -276,9 +276,16 @@ grouped_gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
           ok = false;
           break;
         }
+        // The row's 32 code bytes as two 16-byte loads; rows with bit 2 set
+        // take the halves in the other order, so the eight threads of each
+        // load phase cover all 32 banks (rows 32 bytes apart otherwise put
+        // threads t and t+4 on the same banks).
         const uint8_t* raw = sRaw + sr * kRawBytes + row * 32;
-        const uint4 q0 = *reinterpret_cast<const uint4*>(raw);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 16);
+        const int h0 = (row & 4) ? 16 : 0;
+        const uint4 qa = *reinterpret_cast<const uint4*>(raw + h0);
+        const uint4 qb = *reinterpret_cast<const uint4*>(raw + (h0 ^ 16));
+        const uint4 q0 = h0 ? qb : qa;
+        const uint4 q1 = h0 ? qa : qb;
         const uint32_t sw = *reinterpret_cast<const uint32_t*>(sSc + sr * kScBytes + row * 4);
         mbar_arrive(&r_empty[sr]);  // codes and scales are in registers now
         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
