@@ -115,7 +115,9 @@ typedef struct moe_problem {
        MOE_KERNEL_DECODE_FUSED  moe_forward only (the other entry points run
                                 MOE_KERNEL_WEIGHT_TILES): the 32-token weight
                                 tiles of GEMM1 + SwiGLU and of GEMM2 and the
-                                weighted combine in ONE persistent launch.
+                                weighted combine in ONE persistent launch
+                                (GEMM1 gathers its token rows from x with
+                                TMA tile::gather4: no permuted copy of x).
                                 Tiles are claimed from a global counter,
                                 GEMM1's first; a GEMM2 tile streams its
                                 weights at once and waits for its expert's h

@@ -680,13 +680,15 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   if (!fuse_combine && route_permute_tiny_fits(p->T, p->E, p->k, S)) {
     // the smallest decode steps: routing, permutation and (few rows) the
     // gather in one block
-    const bool gather_here = !fuse_gather && R <= kTinyGatherRoutes;
+    // (the one-launch decode MLP gathers its rows itself)
+    const bool gather_here = !fuse_gather && !decode_fused && R <= kTinyGatherRoutes;
     MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, S, p->renormalize ? 1 : 0, idx,
                                          wts, tpe, off, mtp, rmap, ptok,
                                          gather_here ? x : nullptr, p->H, x_perm, s, dctr,
                                          n_dctr));
     for (int i = 1; i <= 4; ++i) tm.mark(call, i, s);
-    if (!fuse_gather && !gather_here) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
+    if (!fuse_gather && !decode_fused && !gather_here)
+      MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   } else {
     MOE_LAUNCH(
         launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s, S));
@@ -703,13 +705,13 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
       if (decode_fused)
         MOE_LAUNCH(cudaMemsetAsync(dctr, 0, sizeof(int32_t) * static_cast<size_t>(n_dctr), s));
     }
-    if (!fuse_gather) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
+    if (!fuse_gather && !decode_fused) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
   }
   tm.mark(call, 5, s);
   if (decode_fused) {
     // GEMM1, GEMM2 and the combine in one launch (timed as the GEMM1 stage)
     DecodeMlpArgs a{};
-    a.x_perm = x_perm;
+    a.x = x;
     a.w1 = w1;
     a.w2 = w2;
     a.expert_offsets = off;
@@ -721,6 +723,7 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
     a.topk_w = wts;
     a.counters = dctr;
     a.R = R;
+    a.T = q->T;
     a.E = q->E;
     a.H = q->H;
     a.F = q->F;

@@ -50,7 +50,11 @@
 //               weight TMA loads (10-stage ring of 16 KB)
 //   warp 1      TMEM allocation + single-thread tcgen05.mma issue
 //   warps 2..5  epilogue (tcgen05.ld -> SwiGLU / bf16 -> global stores)
-//   warp 6      token-row TMA loads (6-stage ring of 4 KB); waits on done[e]
+//   warp 6      token-row TMA loads (6-stage ring of 4 KB): GEMM1 gathers its
+//               rows straight from x by permuted_token (tile::gather4, four
+//               rows per copy, only as many copies as the tile has rows), so
+//               no permuted copy of x is made; GEMM2 loads 32-row boxes of h
+//               after waiting on done[e]
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -104,7 +108,7 @@ struct DParams {
   const float* topk_w;            // [T, k]
   int32_t* ctr;                   // [2 + E + T * (H / 128)], zero at launch
   const uint8_t* w2;              // bf16 [E, H, F] (L2 prefetch)
-  int E, H, F, k, R, interleave, w1t, w2t;
+  int E, H, F, k, R, T, interleave, w1t, w2t;
   float clamp;
   uint32_t* status;
 };
@@ -381,6 +385,14 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
         if (tile < 0) break;
         const DTile t = decode_dtile(tile, s_ntp, s_ntk, p.E, p.w1t, p.w2t);
         const int x_row = s_off[t.e] + t.n * kN;
+        const int nval = min(kN, s_off[t.e + 1] - x_row);
+        const int ng = (nval + 3) >> 2;  // GEMM1: four-row gathers
+        int tk[kN];  // GEMM1: token of each tile row (rows past nval read token 0)
+#pragma unroll
+        for (int i = 0; i < kN; ++i) {
+          const int v = (t.gemm == 0 && i < nval) ? __ldg(p.permuted_token + x_row + i) : 0;
+          tk[i] = min(max(v, 0), p.T - 1);
+        }
         if (t.gemm == 1 && !all_h) {
           // every GEMM1 tile of expert e has stored its h rows (once all
           // GEMM1 tiles have, no later tile needs to ask)
@@ -401,13 +413,24 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
           if (!ok) { *abort_flag = 1; break; }
           fence_proxy_async_global();
         }
-        const CUtensorMap* mx = t.gemm ? &map_h : &map_x;
         const int num_kb = (t.gemm ? p.F : p.H) / kBK;
+        // rows of the stage past those loaded keep older data: they only
+        // feed accumulator columns that are never stored
+        const uint32_t bytes = t.gemm ? kXBytesD : static_cast<uint32_t>(ng) * 512u;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&x_empty[sx], px ^ 1, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&x_full[sx], kXBytesD);
-          tma_load_2d(sX + sx * kXBytesD, mx, kb * kBK, x_row, &x_full[sx], pol_x);
+          mbar_arrive_expect_tx(&x_full[sx], bytes);
+          uint8_t* dst = sX + sx * kXBytesD;
+          if (t.gemm) {
+            tma_load_2d(dst, &map_h, kb * kBK, x_row, &x_full[sx], pol_x);
+          } else {
+#pragma unroll
+            for (int g = 0; g < kN / 4; ++g)
+              if (g < ng)
+                tma_gather4(dst + g * 512, &map_x, kb * kBK, tk[4 * g], tk[4 * g + 1],
+                            tk[4 * g + 2], tk[4 * g + 3], &x_full[sx], pol_x);
+          }
           ++issued;
           if (++sx == kXStagesD) { sx = 0; px ^= 1; }
         }
@@ -619,7 +642,7 @@ cudaError_t launch_grouped_mlp_decode(const DecodeMlpArgs& g, cudaStream_t s) {
   CUtensorMap mw1, mx, mw2, mh;
   if (!make_map_2d(&mw1, g.w1, static_cast<uint64_t>(g.E) * 2 * g.F, static_cast<uint64_t>(g.H),
                    kM / 2) ||
-      !make_map_2d(&mx, g.x_perm, static_cast<uint64_t>(g.R), static_cast<uint64_t>(g.H), kN) ||
+      !make_map_2d(&mx, g.x, static_cast<uint64_t>(g.T), static_cast<uint64_t>(g.H), 1) ||
       !make_map_2d(&mw2, g.w2, static_cast<uint64_t>(g.E) * g.H, static_cast<uint64_t>(g.F),
                    kM / 2) ||
       !make_map_2d(&mh, g.h, static_cast<uint64_t>(g.R), static_cast<uint64_t>(g.F), kN))
@@ -639,6 +662,7 @@ cudaError_t launch_grouped_mlp_decode(const DecodeMlpArgs& g, cudaStream_t s) {
   p.F = g.F;
   p.k = g.k;
   p.R = g.R;
+  p.T = g.T;
   p.interleave = g.interleave;
   p.w1t = g.F / (kM / 2);
   p.w2t = g.H / kM;

@@ -165,7 +165,7 @@ cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaSt
 // (grouped_mlp_decode.cu).  counters: decode_mlp_counters(T, E, H) int32,
 // zero at launch; with the combine every route of every token must be valid.
 struct DecodeMlpArgs {
-  const void* x_perm;             // [R, H] bf16
+  const void* x;                  // [T, H] bf16 token rows (gathered by permuted_token)
   const void* w1;                 // [E * 2F, H] bf16
   const void* w2;                 // [E * H, F] bf16
   const int32_t* expert_offsets;  // [E + 1]
@@ -176,7 +176,7 @@ struct DecodeMlpArgs {
   const int32_t* row_id_map;      // [T, k]
   const float* topk_w;            // [T, k]
   int32_t* counters;
-  int R, E, H, F, k, interleave;
+  int R, T, E, H, F, k, interleave;
   float clamp;
   uint32_t* status;
 };
