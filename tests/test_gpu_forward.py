@@ -167,7 +167,12 @@ DECODE_FUSED_SHAPES = [mi.DECODE.with_T(1), mi.DECODE.with_T(8), mi.DECODE.with_
                        mi.MoEShape("fused-ragged", T=333, H=512, F=384, E=7, k=3),
                        mi.MoEShape("fused-il32clamp", T=20, H=512, F=256, E=64, k=4,
                                    glu_interleave=32, swiglu_clamp=7.0),
-                       mi.MoEShape("fused-multikernel-permute", T=1100, H=256, F=256, E=16, k=4)]
+                       mi.MoEShape("fused-multikernel-permute", T=1100, H=256, F=256, E=16, k=4),
+                       mi.MoEShape("fused-il64", T=6, H=256, F=256, E=32, k=4, glu_interleave=64),
+                       mi.MoEShape("fused-il128", T=6, H=512, F=256, E=32, k=4,
+                                   glu_interleave=128, swiglu_clamp=7.0),
+                       mi.MoEShape("fused-e1024", T=4, H=256, F=128, E=1024, k=8),
+                       mi.MoEShape("fused-t1-k1", T=1, H=256, F=128, E=64, k=1)]
 
 
 @pytest.mark.parametrize("shape", DECODE_FUSED_SHAPES, ids=lambda s: s.name)
