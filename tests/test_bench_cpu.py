@@ -1,0 +1,69 @@
+"""CPU checks of bench.py's bookkeeping: the algorithmic bytes and FLOPs behind
+the roofline object, the key of the committed ncu traffic table and its
+source-hash guard, and the peak fallback.  No GPU."""
+import hashlib
+import os
+
+import moe_inputs as mi
+
+import bench
+
+
+def test_mixtral_gemm1_bytes_and_flops():
+    # 8 experts x W1 (2F x H bf16) + the permuted rows in + h out
+    s = mi.MIXTRAL
+    b = bench.gemm1_algorithmic_bytes(s, 8)
+    assert b == 8 * 2 * 14336 * 4096 * 2 + 8192 * 4096 * 2 + 8192 * 14336 * 2
+    assert b == 2181038080  # the figure the bench printed on the GPU for this workload
+    assert s.flops() == 6.0 * 8192 * 4096 * 14336
+
+
+def test_lowprec_gemm1_bytes_count_codes_and_scales():
+    s = mi.LOWPREC
+    per_expert = 2 * s.F * s.H / 2 + 2 * s.F * s.H / 16  # E2M1 codes + one E4M3 per 16
+    rows = s.R * s.H * 2 + s.R * s.F * 2                   # f16 rows in, f16 h out
+    assert bench.gemm1_algorithmic_bytes(s, 256) == 256 * per_expert + rows
+    # MXFP4: one E8M0 per 32 values
+    assert bench.gemm1_algorithmic_bytes(s, 256, 32) == \
+        256 * (2 * s.F * s.H / 2 + 2 * s.F * s.H / 32) + rows
+
+
+def test_decode_mlp_bytes_are_both_weights_rows_in_and_tokens_out():
+    s = mi.DECODE.with_T(8)
+    b = bench.decode_mlp_algorithmic_bytes(s, 54)
+    assert b == 54 * 3 * 768 * 2048 * 2 + 64 * 2048 * 2 + 8 * 2048 * 2
+    assert b == 509902848  # printed by the bench for T=8 (54 experts with tokens)
+
+
+def test_traffic_key_names_the_workload_and_token_override():
+    key = lambda argv: bench.traffic_key(bench.parse_args(argv))  # noqa: E731
+    assert key([]) == "mixtral"
+    assert key(["--workload", "decode"]) == "decode"
+    assert key(["--workload", "decode", "--T", "8"]) == "decode-T8"
+    assert key(["--workload", "lowprec", "--E", "32"]) == "custom"
+    assert key(["--workload", "skewed", "--k", "4"]) == "custom"
+
+
+def test_traffic_table_is_used_only_for_the_captured_source():
+    table = os.path.join(bench.ROOT, "profiles", "roofline_traffic.txt")
+    rows = [l.split() for l in open(table) if l.strip() and not l.startswith("#")]
+    csrc = os.path.join(bench.ROOT, "mixture_experts_ffn_permute_gb300", "csrc")
+    files = {"grouped_mlp_decode_kernel": "grouped_mlp_decode.cu",
+             "grouped_gemm_swap2_kernel": "grouped_gemm_swap2.cu",
+             "grouped_gemm_fp4_kernel": "grouped_gemm_fp4.cu",
+             "grouped_gemm_bwd_kernel": "grouped_gemm_bwd.cu"}
+    for sha, workload, kernel, rd, wr in rows:
+        src = files[kernel]
+        cur = hashlib.sha256(open(os.path.join(csrc, src), "rb").read()).hexdigest()[:16]
+        got = bench.ncu_traffic(src, workload)
+        if sha == cur:
+            assert got == float(rd) + float(wr)
+    # a workload without a row has no traffic figure
+    assert bench.ncu_traffic("grouped_mlp_decode.cu", "decode-T3") is None
+    assert bench.ncu_traffic("no_such_file.cu", "mixtral") is None
+
+
+def test_peaks_fall_back_without_the_measured_file(monkeypatch, tmp_path):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    peaks, src = bench.load_peaks()
+    assert src == "fallback" and peaks == bench.FALLBACK_PEAKS
