@@ -2,12 +2,19 @@
 
 One step = one moe_forward (route -> permute -> GEMM1+SwiGLU -> GEMM2 ->
 combine) over one batch of synthetic tokens already resident in HBM.  The
-default workload is the Mixtral-shaped layer (T=4096, H=4096, F=14336, E=8,
-top-2, bf16).  Its 2.8 GB of weights exceed the 129 MB L2, so no flush is
-needed between steps.
+default workload is the largest single-GPU one, the fine-grained skewed layer
+(T=8192, H=7168, F=2048, E=256, top-8, bf16, Zipf(1.1) expert bias).  Its
+22.5 GB of weights exceed the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload mixtral|skewed|decode|tiny] [--T T] [--backward]
+                  [--workload skewed|mixtral|decode|lowprec|tiny] [--T T] [--backward]
+
+Roofline: the dominant kernel (GEMM1) against the tensor peak or HBM
+bandwidth, whichever bounds it, and the whole layer against the slower of
+6*T*k*H*F FLOPs at the tensor peak and its algorithmic bytes at HBM
+bandwidth.  The tensor peak is the measured burst bf16 GEMM rate when the
+timed region is shorter than SUSTAINED_AFTER_S seconds, else the measured
+sustained rate; the fraction against the other peak is reported beside it.
 
 Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
 own batch of T tokens with the same weights (weak scaling, no data-path
@@ -49,14 +56,13 @@ BWD_KERNEL = ("grouped_gemm_bwd.cu", "grouped_gemm_bwd_kernel")
 # GEMM kernel (file and instance) behind each moe_problem.kernel value
 KERNEL_NAMES = {1: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU> (GEMM1, 1-CTA 128x256 tiles)"),
                 2: ("grouped_gemm_swap.cu", "grouped_gemm_swap_kernel<SwiGLU,32> (GEMM1)"),
-                3: ("grouped_gemm_swap.cu", "grouped_gemm_swap_kernel<SwiGLU,256> (GEMM1)"),
-                4: ("grouped_gemm.cu", "grouped_gemm_kernel<SwiGLU,pair> (GEMM1, multicast pair)"),
-                5: ("grouped_gemm_2cta.cu", "grouped_gemm_2cta_kernel<SwiGLU> (GEMM1, cta_group::2)"),
                 6: ("grouped_gemm_swap2.cu",
                     "grouped_gemm_swap2_kernel<SwiGLU> (GEMM1, weight rows on M, cta_group::2)"),
                 7: ("grouped_mlp_decode.cu",
                     "grouped_mlp_decode_kernel (GEMM1+SwiGLU, GEMM2 and combine in one launch)")}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# timed regions at least this long are compared with the sustained tensor peak
+SUSTAINED_AFTER_S = 2.0
 WORKLOADS = {
     "mixtral": (mi.MIXTRAL, "Mixtral-shaped MoE FFN layer: T=4096 H=4096 F=14336 E=8 top-2 bf16"),
     "skewed": (mi.SKEWED, "fine-grained skewed MoE FFN: T=8192 H=7168 F=2048 E=256 top-8 "
@@ -72,10 +78,10 @@ WORKLOADS = {
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="skewed")
     ap.add_argument("--T", type=int, default=0, help="override the token count")
     ap.add_argument("--E", type=int, default=0, help="override the expert count (profiling)")
     ap.add_argument("--k", type=int, default=0, help="override top-k (profiling)")
@@ -139,6 +145,30 @@ def decode_mlp_algorithmic_bytes(shape, used_experts: int) -> float:
     and the combined output written once (T*H*2); h and y stay in L2."""
     R, H, F = shape.R, shape.H, shape.F
     return used_experts * 3 * F * H * 2 + R * H * 2 + shape.T * H * 2
+
+
+def layer_algorithmic_bytes(shape, used_experts: int, scale_block: int = 16) -> float:
+    """HBM bytes the whole layer cannot avoid: W1 and W2 of every expert that
+    received tokens, x and the router logits read once, out written once.
+    bf16 weights 3F*H*2 per expert and x T*H*2; FP8/FP4: 3F*H/2 packed E2M1 +
+    3F*H/scale_block scale bytes + 2*4 bytes of expert scales per expert, x
+    as E4M3 codes T*H plus fp32 scales T*H/128*4."""
+    T, H, F, E = shape.T, shape.H, shape.F, shape.E
+    if shape.lowprec:
+        w = 3 * F * H / 2 + 3 * F * H / scale_block + 8
+        xb = T * H + T * (H // 128) * 4
+    else:
+        w = 3 * F * H * 2
+        xb = T * H * 2
+    return used_experts * w + xb + T * E * 4 + T * H * 2
+
+
+def tensor_peak(peaks, region_s: float):
+    """(peak TFLOP/s, its key, the other key) for a timed region of region_s
+    seconds: burst below SUSTAINED_AFTER_S, sustained from there on."""
+    if region_s < SUSTAINED_AFTER_S:
+        return peaks["bf16_tflops"], "bf16_tflops", "bf16_tflops_sustained"
+    return peaks["bf16_tflops_sustained"], "bf16_tflops_sustained", "bf16_tflops"
 
 
 def load_peaks():
@@ -497,18 +527,33 @@ def bench_ours(args, shape, desc):
         # gemm1_swiglu stage; the gemm2 and combine stages read zero)
         gemm1_flops = 6.0 * shape.R * shape.H * shape.F
         gemm1_bytes = decode_mlp_algorithmic_bytes(shape, used_experts)
-    peak_key = "bf16_tflops_sustained"
+    region_s = K * sec
+    peak_val, peak_key, other_key = tensor_peak(peaks, region_s)
     gemm1_s = gemm1_ms / 1e3
-    t_tensor = gemm1_flops / (peaks[peak_key] * 1e12)
+    t_tensor = gemm1_flops / (peak_val * 1e12)
     t_hbm = gemm1_bytes / (peaks["hbm_gbs"] * 1e9)
     tensor_roof = {"bound": "tensor", "achieved": gemm1_flops / gemm1_s / 1e12,
-                   "peak": peaks[peak_key], "unit": "TFLOP/s",
-                   "peak_source": f"{peak_key} ({peak_src})"}
+                   "peak": peak_val, "unit": "TFLOP/s",
+                   "peak_source": f"{peak_key} ({peak_src}; timed region {region_s:.2f} s)",
+                   "frac_vs_" + other_key: gemm1_flops / gemm1_s / 1e12 / peaks[other_key]}
     hbm_roof = {"bound": "hbm", "achieved": gemm1_bytes / gemm1_s / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "peak_source": f"hbm_gbs ({peak_src})"}
     for r in (tensor_roof, hbm_roof):
         r["frac"] = r["achieved"] / r["peak"]
     main, other = (hbm_roof, tensor_roof) if t_hbm > t_tensor else (tensor_roof, hbm_roof)
+    # the whole layer: the slower of its FLOPs at the tensor peak and its
+    # algorithmic bytes at HBM bandwidth, over the measured step time
+    layer_bytes = layer_algorithmic_bytes(shape, used_experts, 32 if mx else 16)
+    lt_tensor = flops / (peak_val * 1e12)
+    lt_hbm = layer_bytes / (peaks["hbm_gbs"] * 1e9)
+    layer_roof = {"bound": "tensor" if lt_tensor >= lt_hbm else "hbm",
+                  "roof_ms": max(lt_tensor, lt_hbm) * 1e3, "ms_per_step": ms,
+                  "frac": max(lt_tensor, lt_hbm) / sec,
+                  "flops": flops, "bytes": layer_bytes,
+                  "tensor_ms": lt_tensor * 1e3, "hbm_ms": lt_hbm * 1e3,
+                  "peaks": {"tensor_tflops": peak_val, "tensor_key": peak_key,
+                            "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
+                  "frac_vs_" + other_key: max(flops / (peaks[other_key] * 1e12), lt_hbm) / sec}
     line = {
         "metric": METRIC,
         "value": world * flops / sec / 1e12,
@@ -538,6 +583,7 @@ def bench_ours(args, shape, desc):
                                      "experts_with_tokens": used_experts},
                      "other_roof": {k: other[k] for k in ("bound", "achieved", "peak", "unit",
                                                          "frac")}},
+        "layer_roofline": layer_roof,
         "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in step_inputs),
@@ -671,7 +717,7 @@ def bench_backward(args, shape, desc):
     gemm_ms = {k: stages[k] for k in BWD_GEMMS if k in stages}
     top = max(gemm_ms, key=gemm_ms.get)
     top_flops = BWD_GEMMS[top] * rhf
-    peak_key = "bf16_tflops_sustained"
+    peak_val, peak_key, other_key = tensor_peak(peaks, K * sec)
     achieved = top_flops / (gemm_ms[top] / 1e3) / 1e12
     wl = ("backward-" + args.workload) if not args.T and not args.E and not args.k else "custom"
     line = {
@@ -695,8 +741,9 @@ def bench_backward(args, shape, desc):
                    "flops": "12*R*H*F (dH 2, dX 4, dW2 2, dW1 4); the 4*R*H*F recompute of "
                             "the pre-activations is timed but not counted"},
         "roofline": {"kernel": f"{BWD_KERNEL[1]} ({top})", "bound": "tensor",
-                     "achieved": achieved, "peak": peaks[peak_key], "unit": "TFLOP/s",
-                     "frac": achieved / peaks[peak_key],
+                     "achieved": achieved, "peak": peak_val, "unit": "TFLOP/s",
+                     "frac": achieved / peak_val,
+                     "frac_vs_" + other_key: achieved / peaks[other_key],
                      "traffic": ncu_traffic(BWD_KERNEL[0], wl + ":" + top),
                      "peak_source": f"{peak_key} ({peak_src})",
                      "algorithmic": {"flops": top_flops}},

@@ -94,18 +94,9 @@ typedef struct moe_problem {
                                 T*k < E: the one-launch decode MLP below);
                                 else 2-CTA weight-row tiles
        MOE_KERNEL_TOKEN_TILES   128 permuted token rows x 256 weight rows per tile
+                                (the tiling the fusion options apply to)
        MOE_KERNEL_WEIGHT_TILES  128 weight rows x up to 32 token rows per tile
                                 (decode sizes: weights stream once at HBM speed)
-       MOE_KERNEL_WEIGHT_TILES_WIDE  128 weight rows x up to 256 token rows per
-                                tile, N fitted to the expert's rows (ragged
-                                experts pad at most 15 rows)
-       MOE_KERNEL_TOKEN_TILES_PAIR  token-row tiles run by 2-CTA clusters that
-                                take two m-tiles of one weight tile and
-                                multicast the weight tile's halves to each
-                                other (each weight byte read once per pair)
-       MOE_KERNEL_TOKEN_TILES_2CTA  256 token rows x 256 weight rows per CTA
-                                pair with tcgen05.mma.cta_group::2 (each CTA
-                                loads half of both operands)
        MOE_KERNEL_WEIGHT_TILES_2CTA  256 weight rows x up to 256 token rows per
                                 CTA pair (cta_group::2), N fitted to the
                                 expert's rows (pads at most 31 rows); tiles of
@@ -125,7 +116,8 @@ typedef struct moe_problem {
                                 completes a token's k routes of a 128-feature
                                 block sums them in slot order (bit-identical
                                 to the separate combine)
-     The fusion options do not apply to the weight-row tilings. */
+     The fusion options do not apply to the weight-row tilings.  Any other
+     value is MOE_ERR_INVALID_ARG. */
   int32_t kernel;
   /* Shared experts (moe_forward only; 0 elsewhere): S >= 0 experts, stored
      after the E routed ones in w1/w2 (experts E .. E+S-1, same shapes), that
@@ -141,9 +133,7 @@ typedef struct moe_problem {
 #define MOE_KERNEL_AUTO 0
 #define MOE_KERNEL_TOKEN_TILES 1
 #define MOE_KERNEL_WEIGHT_TILES 2
-#define MOE_KERNEL_WEIGHT_TILES_WIDE 3
-#define MOE_KERNEL_TOKEN_TILES_PAIR 4
-#define MOE_KERNEL_TOKEN_TILES_2CTA 5
+/* 3, 4 and 5 named tilings that are no longer built */
 #define MOE_KERNEL_WEIGHT_TILES_2CTA 6
 #define MOE_KERNEL_DECODE_FUSED 7
 
@@ -312,8 +302,10 @@ MOE_API int moe_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream)
  * loading this library keeps until the process exits; nothing is allocated
  * or freed, by this call or by anything it calls.
  *   - The first call on a device looks the array's device address up
- *     (cudaGetSymbolAddress, with that device current); make that first
- *     call before any stream capture on the device.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for
+ *     every later call; make that first call before any stream capture on
+ *     the device.  Resetting the device (cudaDeviceReset) after it is not
+ *     supported: the kept address may no longer be the array's.
  *   - Every call on a device shares the one array.  Calls whose work can
  *     overlap on the GPU (different streams without ordering between them)
  *     race on it and give wrong results; serialise them.  Each call
@@ -339,10 +331,7 @@ MOE_API int moe_permute_noalloc(const moe_problem* p, const int32_t* topk_idx, c
  * E4M3 with one fp32 scale (amax / 448) per 128 values of a row before
  * GEMM2, as that page's split GEMM1 does.  Output bf16.  Tilings
  * (moe_problem.kernel): MOE_KERNEL_AUTO or MOE_KERNEL_TOKEN_TILES run 1-CTA
- * 128-token x 256-weight-row tiles; MOE_KERNEL_WEIGHT_TILES_WIDE runs 1-CTA
- * 128-weight-row x up to 192-token tiles fitted per expert, the weights
- * expanded straight into tensor memory (the MMA's A operand) and the token
- * rows shared by CTA pairs; MOE_KERNEL_WEIGHT_TILES_2CTA runs 2-CTA
+ * 128-token x 256-weight-row tiles; MOE_KERNEL_WEIGHT_TILES_2CTA runs 2-CTA
  * weight-row tiles (each CTA expands its 128 weight rows; the 1x128
  * re-quantisation block of h spans both CTAs of a pair, whose per-token
  * maxima are exchanged through distributed shared memory); any other value

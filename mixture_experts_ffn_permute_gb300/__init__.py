@@ -32,9 +32,6 @@ FUSE_COMBINE = 2    # weighted top-k reduction in GEMM2's epilogue
 KERNEL_AUTO = 0
 KERNEL_TOKEN_TILES = 1   # 128 token rows x 256 weight rows per tile
 KERNEL_WEIGHT_TILES = 2  # 128 weight rows x up to 32 token rows per tile (decode sizes)
-KERNEL_WEIGHT_TILES_WIDE = 3  # 128 weight rows x up to 256 token rows, N fitted per tile
-KERNEL_TOKEN_TILES_PAIR = 4   # token-row tiles by 2-CTA clusters multicasting the weight tile
-KERNEL_TOKEN_TILES_2CTA = 5   # 256x256 tiles per CTA pair, tcgen05.mma.cta_group::2
 KERNEL_WEIGHT_TILES_2CTA = 6  # 256 weight rows x up to 256 tokens per CTA pair, N fitted
 KERNEL_DECODE_FUSED = 7  # moe_forward: both GEMMs and the combine of 32-token tiles in one launch
 STATUS_NAMES = {

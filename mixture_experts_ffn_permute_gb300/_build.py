@@ -18,9 +18,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoeffn.so")
-SOURCES = ["api.cu", "route_permute.cu", "grouped_gemm.cu", "grouped_gemm_swap.cu", "grouped_gemm_fp4.cu",
-           "grouped_gemm_2cta.cu", "grouped_gemm_swap2.cu", "grouped_gemm_fp4_pair.cu",
-           "grouped_gemm_fp4_tmem.cu", "grouped_gemm_bwd.cu", "grouped_mlp_decode.cu", "route_backward.cu", "noalloc.cu",
+SOURCES = ["api.cu", "route_permute.cu", "grouped_gemm.cu", "grouped_gemm_swap.cu",
+           "grouped_gemm_fp4.cu", "grouped_gemm_swap2.cu", "grouped_gemm_fp4_pair.cu",
+           "grouped_gemm_bwd.cu", "grouped_mlp_decode.cu", "route_backward.cu", "noalloc.cu",
            "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -4,7 +4,6 @@
 
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 
 #include "../../include/moe_ffn.h"
@@ -12,10 +11,6 @@
 
 namespace moe {
 
-bool pdl_enabled() {
-  static const bool on = std::getenv("MOE_DISABLE_PDL") == nullptr;
-  return on;
-}
 
 int num_sms() {
   static int cache[64] = {0};
@@ -32,8 +27,12 @@ int num_sms() {
 }
 
 namespace {
-
 thread_local int g_launches = 0;
+}  // namespace
+
+void set_last_launch_count(int n) { g_launches = n; }
+
+namespace {
 
 // Stage names of moe_forward and moe_backward, in launch order.
 constexpr int kFwdStages = 8;
@@ -163,12 +162,13 @@ int check_full(const moe_problem* p) {
   if (p->precision != MOE_PREC_BF16 && p->precision != MOE_PREC_FP8_NVFP4)
     return MOE_ERR_UNSUPPORTED_SHAPE;
   if (p->fusion & ~(MOE_FUSE_GATHER_A | MOE_FUSE_COMBINE)) return MOE_ERR_INVALID_ARG;
-  if (p->kernel < MOE_KERNEL_AUTO || p->kernel > MOE_KERNEL_DECODE_FUSED)
+  if (p->kernel != MOE_KERNEL_AUTO && p->kernel != MOE_KERNEL_TOKEN_TILES &&
+      p->kernel != MOE_KERNEL_WEIGHT_TILES && p->kernel != MOE_KERNEL_WEIGHT_TILES_2CTA &&
+      p->kernel != MOE_KERNEL_DECODE_FUSED)
     return MOE_ERR_INVALID_ARG;
   // the FP8/NVFP4 GEMMs come in two tilings
   if (p->precision == MOE_PREC_FP8_NVFP4 && p->kernel != MOE_KERNEL_AUTO &&
-      p->kernel != MOE_KERNEL_TOKEN_TILES && p->kernel != MOE_KERNEL_WEIGHT_TILES_WIDE &&
-      p->kernel != MOE_KERNEL_WEIGHT_TILES_2CTA)
+      p->kernel != MOE_KERNEL_TOKEN_TILES && p->kernel != MOE_KERNEL_WEIGHT_TILES_2CTA)
     return MOE_ERR_INVALID_ARG;
   // hidden a multiple of 256, intermediate a multiple of 128 (the tile sizes)
   if (p->H % 256 != 0 || p->F % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -220,8 +220,7 @@ int gemm_tiling(const moe_problem* p) {
 // fitting N to ragged experts saves no tensor time; the token-row tiles are
 // faster on GB300).
 int lowprec_tiling(const moe_problem* p) {
-  if (p->kernel == MOE_KERNEL_WEIGHT_TILES_2CTA || p->kernel == MOE_KERNEL_WEIGHT_TILES_WIDE)
-    return p->kernel;
+  if (p->kernel == MOE_KERNEL_WEIGHT_TILES_2CTA) return p->kernel;
   return MOE_KERNEL_TOKEN_TILES;
 }
 
@@ -236,10 +235,7 @@ bool use_decode_fused(const moe_problem* p) {
   return p->kernel == MOE_KERNEL_AUTO && static_cast<long long>(p->T) * p->k < p->E;
 }
 
-bool use_weight_tiles(const moe_problem* p) {
-  const int t = gemm_tiling(p);
-  return t == MOE_KERNEL_WEIGHT_TILES || t == MOE_KERNEL_WEIGHT_TILES_WIDE;
-}
+bool use_weight_tiles(const moe_problem* p) { return gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES; }
 
 float clamp_of(const moe_problem* p) {
   const float c = p->swiglu_clamp;
@@ -286,13 +282,9 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
     g1.permuted_token = fused->permuted_token;
     g1.x_rows = p->T;
   }
-  g1.pair = gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_PAIR;
-  const bool wide = gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES_WIDE;
-  const bool cta2 = gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_2CTA;
   const bool swap2 = gemm_tiling(p) == MOE_KERNEL_WEIGHT_TILES_2CTA;
-  if (cta2 || swap2) g1.permuted_token = nullptr;  // no gathered-A form
-  MOE_LAUNCH(swap    ? launch_grouped_gemm_swap(g1, wide, s)
-             : cta2  ? launch_grouped_gemm_2cta(g1, s)
+  if (swap2) g1.permuted_token = nullptr;  // no gathered-A form
+  MOE_LAUNCH(swap    ? launch_grouped_gemm_swap(g1, s)
              : swap2 ? launch_grouped_gemm_swap2(g1, s)
                      : launch_grouped_gemm(g1, s));
   if (tm) tm->mark(call, mark, s);
@@ -312,8 +304,7 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
   g2.out_rows = R;
   g2.F = p->F;
   g2.status = status;
-  g2.pair = gemm_tiling(p) == MOE_KERNEL_TOKEN_TILES_PAIR;
-  if (fused && fused->combine && !swap && !cta2 && !swap2) {
+  if (fused && fused->combine && !swap && !swap2) {
     g2.epi = Epi::kCombine;
     g2.out = fused->out;
     g2.partials = y;
@@ -323,8 +314,7 @@ int run_mlp(const moe_problem* p, const void* x_perm, const int32_t* offsets,
     g2.counters = fused->counters;
     g2.k = p->k;
   }
-  MOE_LAUNCH(swap    ? launch_grouped_gemm_swap(g2, wide, s)
-             : cta2  ? launch_grouped_gemm_2cta(g2, s)
+  MOE_LAUNCH(swap    ? launch_grouped_gemm_swap(g2, s)
              : swap2 ? launch_grouped_gemm_swap2(g2, s)
                      : launch_grouped_gemm(g2, s));
   if (tm) tm->mark(call, mark + 1, s);
@@ -665,8 +655,7 @@ int moe_forward(const moe_problem* p, const void* x, const float* logits, const 
   void* h = at<void>(ws, L.h);
   void* y = at<void>(ws, L.y);
   int32_t* counters = at<int32_t>(ws, L.counters);
-  const bool plain_tiles = use_weight_tiles(q) || gemm_tiling(q) == MOE_KERNEL_TOKEN_TILES_2CTA ||
-                           gemm_tiling(q) == MOE_KERNEL_WEIGHT_TILES_2CTA;
+  const bool plain_tiles = use_weight_tiles(q) || gemm_tiling(q) == MOE_KERNEL_WEIGHT_TILES_2CTA;
   const bool fuse_gather = !plain_tiles && (p->fusion & MOE_FUSE_GATHER_A) != 0;
   const bool fuse_combine = !plain_tiles && (p->fusion & MOE_FUSE_COMBINE) != 0;
   const bool decode_fused = use_decode_fused(q);
@@ -1034,9 +1023,7 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
   g1.status = status;
   const int lt = lowprec_tiling(p);
   MOE_LAUNCH(lt == MOE_KERNEL_WEIGHT_TILES_2CTA ? launch_grouped_gemm_fp4_pair(g1, sc1, w1_gscale, s)
-             : lt == MOE_KERNEL_WEIGHT_TILES_WIDE
-                 ? launch_grouped_gemm_fp4_tmem(g1, sc1, w1_gscale, s)
-                 : launch_grouped_gemm_fp4(g1, sc1, w1_gscale, s));
+                                                : launch_grouped_gemm_fp4(g1, sc1, w1_gscale, s));
   tm.mark(call, 6, s);
   GroupedGemmArgs g2{};
   g2.epi = Epi::kPlain;
@@ -1055,9 +1042,7 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
   g2.F = p->F;
   g2.status = status;
   MOE_LAUNCH(lt == MOE_KERNEL_WEIGHT_TILES_2CTA ? launch_grouped_gemm_fp4_pair(g2, sc2, w2_gscale, s)
-             : lt == MOE_KERNEL_WEIGHT_TILES_WIDE
-                 ? launch_grouped_gemm_fp4_tmem(g2, sc2, w2_gscale, s)
-                 : launch_grouped_gemm_fp4(g2, sc2, w2_gscale, s));
+                                                : launch_grouped_gemm_fp4(g2, sc2, w2_gscale, s));
   tm.mark(call, 7, s);
   MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
   tm.mark(call, 8, s);

@@ -55,7 +55,7 @@ constexpr int kMaxE = 1024;
 static_assert((2 * kStages + 5) * 8 + 8 <= 256, "barrier area");
 constexpr size_t kSmemBytes =
     1024 /*alignment slack*/ + kStages * kStageBytes + 256 /*barriers*/ +
-    3 * (kMaxE + 1) * sizeof(int32_t) /*offsets, m-tile prefix, m-tile-pair prefix*/;
+    2 * (kMaxE + 1) * sizeof(int32_t) /*offsets, m-tile prefix*/;
 
 struct KParams {
   const int32_t* expert_offsets;
@@ -117,14 +117,7 @@ __device__ __forceinline__ void add_bf16x8(const uint4& v, float (&acc)[8]) {
   }
 }
 
-// With kPair the kernel runs as clusters of two CTAs that take the two
-// m-tiles of one (expert, n-tile) pair together: each CTA TMA-loads one half
-// of the shared weight tile and multicasts it into both CTAs' shared memory,
-// so every weight byte leaves L2 once per pair instead of once per CTA.  A
-// stage is reloaded only after both CTAs' MMAs released it (each MMA commit
-// arrives on both CTAs' empty barrier).  An odd m-tile count leaves the
-// second CTA an empty tile, whose rows are all masked.
-template <Epi kEpi, bool kGatherA, bool kPair>
+template <Epi kEpi, bool kGatherA>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, const KParams p) {
@@ -144,10 +137,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
   int32_t* s_mtp = s_off + (p.E + 1);
-  int32_t* s_pmtp = s_mtp + (p.E + 1);  // prefix of ceil(m-tiles / 2) (kPair)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = kPair ? cluster_ctarank() : 0;
   for (int i = threadIdx.x; i <= p.E; i += kThreads) {
     s_off[i] = p.expert_offsets[i];
     s_mtp[i] = p.mtile_prefix[i];
@@ -155,7 +146,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kPair ? 2 : 1);
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -170,52 +161,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     prefetch_tensormap(&map_b);
   }
   if (warp == 1) tmem_alloc<kTmemCols>(tmem_slot);
-  __syncthreads();
-  if (kPair) {
-    // prefix of ceil(m-tiles / 2): thread i scans a run of ceil(E / 192)
-    // experts, runs are offset by a scan over the threads
-    __shared__ int s_part[kThreads / 32];
-    const int per = (p.E + kThreads - 1) / kThreads;
-    const int e0 = min(p.E, static_cast<int>(threadIdx.x) * per), e1 = min(p.E, e0 + per);
-    int run = 0;
-    for (int e = e0; e < e1; ++e) run += (s_mtp[e + 1] - s_mtp[e] + 1) >> 1;
-    int incl = run;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    if (lane == 31) s_part[warp] = incl;
-    __syncthreads();
-    int acc = incl - run;
-    for (int w = 0; w < warp; ++w) acc += s_part[w];
-    for (int e = e0; e < e1; ++e) {
-      s_pmtp[e] = acc;
-      acc += (s_mtp[e + 1] - s_mtp[e] + 1) >> 1;
-    }
-    if (threadIdx.x == kThreads - 1) {
-      int total = 0;
-      for (int w = 0; w < kThreads / 32; ++w) total += s_part[w];
-      s_pmtp[p.E] = total;
-    }
-  }
   tc_fence_before();
   __syncthreads();
-  // the peer's barriers must be initialised before anything is multicast to them
-  if (kPair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // tile list: (expert, n-tile, m-tile) or, paired, (expert, n-tile, m-tile pair)
-  const int32_t* s_tp = kPair ? s_pmtp : s_mtp;
-  const int total_tiles = s_tp[p.E] * p.n_tiles;
-  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int tstride = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  auto tile_at = [&](int tile) {
-    Tile t = decode_tile(tile, s_tp, p.E, p.n_tiles);
-    if (kPair) t.m = 2 * t.m + static_cast<int>(rank);
-    return t;
-  };
+  // tile list: (expert, n-tile, m-tile)
+  const int total_tiles = s_mtp[p.E] * p.n_tiles;
+  const int tile0 = static_cast<int>(blockIdx.x);
+  const int tstride = static_cast<int>(gridDim.x);
+  auto tile_at = [&](int tile) { return decode_tile(tile, s_mtp, p.E, p.n_tiles); };
   const int num_kb = p.K / kBK;
 
   if (warp == 0) {
@@ -286,13 +241,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         if (lane == 0) {
           if (!kGatherA) tma_load_2d(sA + stage * kABytes, &map_a, kx, a_row, &full[stage], pol_a);
           uint8_t* b_dst = sB + stage * kBBytes;
-          if (kPair) {  // this CTA's half of the weight tile, into both CTAs
-            tma_load_2d_multicast(b_dst + rank * (kBBytes / 2), &map_b, kx,
-                                  rank ? b_row1 : b_row0, &full[stage], 0x3, pol_b);
-          } else {
-            tma_load_2d(b_dst, &map_b, kx, b_row0, &full[stage], pol_b);
-            tma_load_2d(b_dst + kBBytes / 2, &map_b, kx, b_row1, &full[stage], pol_b);
-          }
+          tma_load_2d(b_dst, &map_b, kx, b_row0, &full[stage], pol_b);
+          tma_load_2d(b_dst + kBBytes / 2, &map_b, kx, b_row1, &full[stage], pol_b);
         }
         ++issued;
         if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -331,8 +281,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             // descriptor's 16-byte address units
             mma_bf16_ss(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, kIdesc, (kb | kk) != 0);
           }
-          if (kPair) mma_commit_multicast(&empty[stage], 0x3);  // both CTAs' copies
-          else mma_commit(&empty[stage]);
+          mma_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
@@ -485,27 +434,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
   tc_fence_before();
   __syncthreads();
-  // neither CTA leaves while its peer may still write into its shared memory
-  // or arrive on its barriers
-  if (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<kTmemCols>(tmem_base);
   }
 }
 
-template <Epi kEpi, bool kGatherA, bool kPair>
+template <Epi kEpi, bool kGatherA>
 cudaError_t launch_impl(const CUtensorMap& ma, const CUtensorMap& mb, const KParams& kp,
                         int grid, cudaStream_t s) {
-  auto kern = grouped_gemm_kernel<kEpi, kGatherA, kPair>;
+  auto kern = grouped_gemm_kernel<kEpi, kGatherA>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
   if (err != cudaSuccess) return err;
-  if (!kPair)
-    return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s,
-                         1, ma, mb, kp);
-  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s, 2,
-                       ma, mb, kp);
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, s,
+                       1, ma, mb, kp);
 }
 
 }  // namespace
@@ -630,26 +573,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s) {
   // Upper bound on tiles: every expert may add one ragged m-tile.
   const long max_mtiles = ceil_div(g.a_rows, kBM) + std::min(g.E, g.a_rows);
   const long max_tiles = max_mtiles * g.n_tiles;
-  const bool pair = g.pair && !gather;
-  if (pair) {  // clusters of two CTAs: an even grid, at most one CTA per SM
-    const long want = std::min<long>(num_sms() & ~1, 2 * max_tiles);
-    const int grid = static_cast<int>(std::max(2L, want & ~1L));
-    switch (g.epi) {
-      case Epi::kSwiGLU: return launch_impl<Epi::kSwiGLU, false, true>(ma, mb, kp, grid, s);
-      case Epi::kPlain: return launch_impl<Epi::kPlain, false, true>(ma, mb, kp, grid, s);
-      case Epi::kCombine: return launch_impl<Epi::kCombine, false, true>(ma, mb, kp, grid, s);
-    }
-    return cudaErrorInvalidValue;
-  }
   const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
   switch (g.epi) {
     case Epi::kSwiGLU:
-      return gather ? launch_impl<Epi::kSwiGLU, true, false>(ma, mb, kp, grid, s)
-                    : launch_impl<Epi::kSwiGLU, false, false>(ma, mb, kp, grid, s);
+      return gather ? launch_impl<Epi::kSwiGLU, true>(ma, mb, kp, grid, s)
+                    : launch_impl<Epi::kSwiGLU, false>(ma, mb, kp, grid, s);
     case Epi::kPlain:
-      return launch_impl<Epi::kPlain, false, false>(ma, mb, kp, grid, s);
+      return launch_impl<Epi::kPlain, false>(ma, mb, kp, grid, s);
     case Epi::kCombine:
-      return launch_impl<Epi::kCombine, false, false>(ma, mb, kp, grid, s);
+      return launch_impl<Epi::kCombine, false>(ma, mb, kp, grid, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -738,11 +738,14 @@ cudaError_t launch_bwd_impl(const CUtensorMap& ma, const CUtensorMap& mb, const 
                        mb, mo, kp);
 }
 
-// The data gradients run on 2-CTA pairs unless MOE_BWD_1CTA is set (1-CTA
-// tiles, kept for comparison).
-bool bwd_pairs() {
-  static const bool on = std::getenv("MOE_BWD_1CTA") == nullptr;
-  return on;
+// The data gradients run on 2-CTA pairs; building with -DMOE_BWD_1CTA keeps
+// the 1-CTA tiles instead (for comparison timings only).
+constexpr bool bwd_pairs() {
+#ifdef MOE_BWD_1CTA
+  return false;
+#else
+  return true;
+#endif
 }
 
 }  // namespace

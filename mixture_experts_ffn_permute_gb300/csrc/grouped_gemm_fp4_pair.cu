@@ -334,9 +334,16 @@ grouped_gemm_fp4_pair_kernel(const __grid_constant__ CUtensorMap map_q,
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int row = r * 32 + lane;
+        // the row's 32 code bytes as two 16-byte loads; rows with bit 2 set
+        // take the halves in the other order, so the eight lanes of each
+        // load phase cover all 32 banks (rows 32 bytes apart would otherwise
+        // put lanes t and t+4 on the same banks)
         const uint8_t* code = sCode + sr * kCodeBytesQ + row * 32;
-        q[r][0] = *reinterpret_cast<const uint4*>(code);
-        q[r][1] = *reinterpret_cast<const uint4*>(code + 16);
+        const int h0 = (row & 4) ? 16 : 0;
+        const uint4 qa = *reinterpret_cast<const uint4*>(code + h0);
+        const uint4 qb = *reinterpret_cast<const uint4*>(code + (h0 ^ 16));
+        q[r][0] = h0 ? qb : qa;
+        q[r][1] = h0 ? qa : qb;
         sc4[r] = *reinterpret_cast<const uint32_t*>(sSc + sr * kScBytesQ + row * 4);
       }
       __syncwarp();

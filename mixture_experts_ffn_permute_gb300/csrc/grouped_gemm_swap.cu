@@ -1,18 +1,13 @@
 // Decode-sized grouped GEMMs: the weight rows are the MMA's M side and the
 // few tokens of each expert its N side ("swap-AB").
 //
-// A tile is 128 weight rows x up to kNmax token rows of one expert:
+// A tile is 128 weight rows x up to kNmax = 32 token rows of one expert:
 //   D[128 x N] = W[128 weight rows of e, K] * X[N token rows of e, K]^T
-// with N = the expert's remaining rows rounded up to 16 (at most kNmax), set
-// per tile in the instruction descriptor.  Two instances:
-//   kNmax = 32,  8 stages: decode sizes, where an expert sees a handful of
-//     tokens: a K step moves 16 KB of weights and 4 KB of activations, so
-//     the weights stream once at HBM speed;
-//   kNmax = 256, 4 stages: ragged experts of tens to hundreds of rows: a
-//     token tile pads at most 15 rows, where a 128-row token tile pads up to
-//     127 (the full MMA shape 128 x 256 when the expert has the rows).
-// Tokens are loaded in 32-row boxes, only as many as the tile needs.  The
-// tile count is (expert, weight-row tile, token tile), token tiles fastest so
+// with N = the expert's remaining rows rounded up to 16, set per tile in the
+// instruction descriptor.  At decode sizes an expert sees a handful of
+// tokens: a K step moves 16 KB of weights and 4 KB of activations, so the
+// weights stream once at HBM speed (10 weight stages, 6 token stages).
+// Tokens are loaded in one 32-row box.  The tile count is (expert, weight-row tile, token tile), token tiles fastest so
 // that CTAs sharing a weight tile run together and the second read hits L2.
 //
 // Epilogues:
@@ -42,22 +37,14 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 namespace {
 
 constexpr int kM = 128;                                // weight rows per tile
-constexpr int kXBox = 32;                              // token rows per small TMA box
-constexpr int kXBoxWide = 128;                         // token rows per large TMA box
+constexpr int kXBox = 32;                              // token rows per TMA box
 constexpr int kThreadsS = 192;
 constexpr uint32_t kWBytes = kM * kBK * 2;             // 16 KB
 constexpr int kMaxES = 1024;
 constexpr int kDPitch = 33;                            // padded fp32 row of the exchange chunk
-// wide instance: token tiles of up to kWideN rows, kWideStages-deep ring
-constexpr int kWideN = 256;
-#ifndef MOE_WIDE_W
-#define MOE_WIDE_W 4
-#endif
-#ifndef MOE_WIDE_X
-#define MOE_WIDE_X 4
-#endif
-constexpr int kWideW = MOE_WIDE_W;   // weight-ring depth (HBM)
-constexpr int kWideX = MOE_WIDE_X;   // token-ring depth (L2)
+constexpr int kNmaxS = 32;                             // token rows per tile
+constexpr int kWStagesS = 10;                          // weight-ring depth (HBM)
+constexpr int kXStagesS = 6;                           // token-ring depth (L2)
 
 // Separate rings for the weight tiles (from HBM: deep) and the token tiles
 // (from L2).
@@ -110,8 +97,7 @@ __device__ __forceinline__ float silu_s(float z) { return z / (1.0f + expf(-z));
 template <Epi kEpi, int kNmax, int kWStages, int kXStages>
 __global__ void __launch_bounds__(kThreadsS, 1)
 grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
-                         const __grid_constant__ CUtensorMap map_x,
-                         const __grid_constant__ CUtensorMap map_xw, const SParams p) {
+                         const __grid_constant__ CUtensorMap map_x, const SParams p) {
   using Cfg = SwapCfg<kNmax, kWStages, kXStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, kept as a shared-array pointer so that accesses
@@ -154,7 +140,6 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&map_w);
     prefetch_tensormap(&map_x);
-    if (kNmax > kXBox) prefetch_tensormap(&map_xw);
   }
   if (warp == 1) tmem_alloc<Cfg::kTmemCols>(tmem_slot);
   // Everything above touches only this CTA's shared memory and tensor memory
@@ -216,11 +201,9 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
         const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
         const int tok0 = t.n * kNmax;
         const int nval = min(kNmax, s_off[t.e + 1] - s_off[t.e] - tok0);
-        // few TMA ops per stage: one 32-row box, or 128-row boxes
-        const bool wide_box = kNmax > kXBox && nval > kXBox;
-        const int box_rows = wide_box ? kXBoxWide : kXBox;
-        const int nbox = (nval + box_rows - 1) / box_rows;
-        const uint32_t x_bytes = static_cast<uint32_t>(nbox * box_rows * kBK * 2);
+        // few TMA ops per stage: 32-row boxes, as many as the tile needs
+        const int nbox = (nval + kXBox - 1) / kXBox;
+        const uint32_t x_bytes = static_cast<uint32_t>(nbox * kXBox * kBK * 2);
         const int x_row = s_off[t.e] + tok0;
         int w_row0, w_row1;
         if (kEpi == Epi::kSwiGLU) {
@@ -252,8 +235,8 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
           mbar_arrive_expect_tx(&x_full[sx], x_bytes);
           uint8_t* x_dst = sX + sx * Cfg::kXBytes;
           for (int b = 0; b < nbox; ++b)
-            tma_load_2d(x_dst + b * box_rows * kBK * 2, wide_box ? &map_xw : &map_x, kx,
-                        x_row + b * box_rows, &x_full[sx], pol_x);
+            tma_load_2d(x_dst + b * kXBox * kBK * 2, &map_x, kx, x_row + b * kXBox,
+                        &x_full[sx], pol_x);
           ++issued;
           if (++sw == kWStages) { sw = 0; pw ^= 1; }
           if (++sx == kXStages) { sx = 0; px ^= 1; }
@@ -398,32 +381,28 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
 }
 
 template <Epi kEpi, int kNmax, int kWStages, int kXStages>
-cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx,
-                             const CUtensorMap& mxw, const SParams& sp, int grid,
-                             cudaStream_t s) {
+cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx, const SParams& sp,
+                             int grid, cudaStream_t s) {
   using Cfg = SwapCfg<kNmax, kWStages, kXStages>;
   auto kern = grouped_gemm_swap_kernel<kEpi, kNmax, kWStages, kXStages>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::kSmem));
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreadsS), Cfg::kSmem, s, 1,
-                       mw, mx, mxw, sp);
+                       mw, mx, sp);
 }
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaStream_t s) {
+cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s) {
   if (g.a_rows == 0) return cudaSuccess;
   if (g.E > kMaxES) return cudaErrorInvalidValue;
-  CUtensorMap mw, mx, mxw;
-  // weights: 64-row boxes; tokens: 32-row and 128-row boxes
+  CUtensorMap mw, mx;
+  // weights: 64-row boxes; tokens: 32-row boxes
   if (!make_map_2d(&mw, g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
                    static_cast<uint64_t>(g.K), kM / 2))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&mx, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K), kXBox))
-    return cudaErrorInvalidValue;
-  if (!make_map_2d(&mxw, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K),
-                   kXBoxWide))
     return cudaErrorInvalidValue;
   SParams sp;
   sp.expert_offsets = g.expert_offsets;
@@ -438,17 +417,14 @@ cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaSt
   sp.clamp = g.clamp;
   sp.status = g.status;
   sp.w_tiles = (g.epi == Epi::kSwiGLU) ? g.F / (kM / 2) : g.ldo / kM;
-  const int nmax = wide ? kWideN : 32;
   // every expert may add one ragged token tile
   const long max_tiles =
-      (static_cast<long>(ceil_div(g.a_rows, nmax)) + std::min(g.E, g.a_rows)) * sp.w_tiles;
+      (static_cast<long>(ceil_div(g.a_rows, kNmaxS)) + std::min(g.E, g.a_rows)) * sp.w_tiles;
   const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
   if (g.epi == Epi::kSwiGLU)
-    return wide ? launch_swap_impl<Epi::kSwiGLU, kWideN, kWideW, kWideX>(mw, mx, mxw, sp, grid, s)
-                : launch_swap_impl<Epi::kSwiGLU, 32, 10, 6>(mw, mx, mxw, sp, grid, s);
+    return launch_swap_impl<Epi::kSwiGLU, kNmaxS, kWStagesS, kXStagesS>(mw, mx, sp, grid, s);
   if (g.epi == Epi::kPlain)
-    return wide ? launch_swap_impl<Epi::kPlain, kWideN, kWideW, kWideX>(mw, mx, mxw, sp, grid, s)
-                : launch_swap_impl<Epi::kPlain, 32, 10, 6>(mw, mx, mxw, sp, grid, s);
+    return launch_swap_impl<Epi::kPlain, kNmaxS, kWStagesS, kXStagesS>(mw, mx, sp, grid, s);
   return cudaErrorInvalidValue;
 }
 

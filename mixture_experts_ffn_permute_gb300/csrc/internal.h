@@ -21,8 +21,19 @@ inline int ceil_div(long a, long b) { return static_cast<int>((a + b - 1) / b); 
 
 int num_sms();
 
-// False when MOE_DISABLE_PDL is set in the environment (for A/B timing).
-bool pdl_enabled();
+// Records the number of kernel launches of the entry point that just
+// succeeded on this thread (read back by moe_last_launch_count).
+void set_last_launch_count(int n);
+
+// Programmatic dependent launch for every kernel; building with
+// -DMOE_NO_PDL turns it off (for comparison timings only).
+constexpr bool pdl_enabled() {
+#ifdef MOE_NO_PDL
+  return false;
+#else
+  return true;
+#endif
+}
 
 // cudaLaunchKernelEx with programmatic stream serialization allowed (the
 // kernels wait with griddepcontrol.wait before touching global memory) and an
@@ -150,15 +161,13 @@ struct GroupedGemmArgs {
   int32_t* counters = nullptr;  // [T, n_tiles], zero before the launch
   void* partials = nullptr;     // [R, ldo] bf16
   int k = 0;
-  // token-row tiles as 2-CTA clusters sharing (multicasting) the weight tile
-  bool pair = false;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& g, cudaStream_t s);
 
-// The same GEMMs with weight rows on the MMA's M side and up to 32 (wide:
-// 256) tokens on N (kSwiGLU and kPlain epilogues; no gather / combine fusion).
-cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, bool wide, cudaStream_t s);
+// The same GEMMs with weight rows on the MMA's M side and up to 32 tokens on
+// N (kSwiGLU and kPlain epilogues; no gather / combine fusion).
+cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s);
 
 // Decode sizes in one launch: GEMM1 + SwiGLU, GEMM2 and (out != NULL) the
 // weighted combine, 128 weight rows x up to 32 token rows per tile
@@ -183,9 +192,6 @@ struct DecodeMlpArgs {
 int decode_mlp_counters(int T, int E, int H);
 cudaError_t launch_grouped_mlp_decode(const DecodeMlpArgs& g, cudaStream_t s);
 
-// Token-row tiles on CTA pairs with tcgen05.mma.cta_group::2 (kSwiGLU, kPlain).
-cudaError_t launch_grouped_gemm_2cta(const GroupedGemmArgs& g, cudaStream_t s);
-
 // Weight-row tiles on CTA pairs (cta_group::2), tokens on N fitted per tile.
 cudaError_t launch_grouped_gemm_swap2(const GroupedGemmArgs& g, cudaStream_t s);
 
@@ -197,11 +203,6 @@ cudaError_t launch_grouped_gemm_fp4(const GroupedGemmArgs& g, const uint8_t* sca
 // The same GEMMs with weight-row tiles on CTA pairs (cta_group::2, N fitted per
 // expert); needs rows per expert a multiple of 128.
 cudaError_t launch_grouped_gemm_fp4_pair(const GroupedGemmArgs& g, const uint8_t* scales,
-                                         const float* gscale, cudaStream_t s);
-// The same GEMMs with 1-CTA weight-row tiles (128 weight rows x N <= 192
-// tokens fitted per expert), the weights expanded into tensor memory; CTA
-// pairs share token rows by multicast.
-cudaError_t launch_grouped_gemm_fp4_tmem(const GroupedGemmArgs& g, const uint8_t* scales,
                                          const float* gscale, cudaStream_t s);
 // [E][N][K/16] E4M3 scales -> [E][N/128][K/64][128][4]
 cudaError_t launch_prepare_scales(const uint8_t* src, uint8_t* dst, int E, int N, int K,

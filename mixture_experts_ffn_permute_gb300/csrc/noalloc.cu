@@ -23,7 +23,8 @@ std::mutex g_scratch_mu;
 
 // Device address of g_noalloc_scratch on the current device.  Host code only
 // sees a host-side stand-in under the array's name, so the address is looked
-// up once per device with that device current.
+// up once per device with that device current and kept for later calls (a
+// device reset after that first call is therefore not supported).
 int scratch_on_current_device(int32_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
@@ -75,19 +76,30 @@ extern "C" int moe_permute_noalloc(const moe_problem* p, const int32_t* topk_idx
   int32_t* mtile_prefix = scratch + nchunks * p->E;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int R = p->T * p->k;
+  int launches = 0;
   // Every chunk's histogram row is written in full before the scan reads it,
   // and the scan writes the whole m-tile prefix: nothing needs clearing.
-  if (nchunks > 0 &&
-      launch_chunk_histogram(topk_idx, p->T, p->E, p->k, chunk_counts, nullptr, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (nchunks > 0) {
+    if (launch_chunk_histogram(topk_idx, p->T, p->E, p->k, chunk_counts, nullptr, s) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    ++launches;
+  }
   if (launch_scan(chunk_counts, static_cast<int>(nchunks), p->E, R, tokens_per_expert,
                   expert_offsets, mtile_prefix, permuted_token, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (nchunks > 0 && launch_scatter(topk_idx, p->T, p->E, p->k, chunk_counts, row_id_map,
-                                    permuted_token, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (x_perm && p->T > 0 &&
-      launch_gather_rows(x, permuted_token, R, p->H, x_perm, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  ++launches;
+  if (nchunks > 0) {
+    if (launch_scatter(topk_idx, p->T, p->E, p->k, chunk_counts, row_id_map, permuted_token,
+                       s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    ++launches;
+  }
+  if (x_perm && p->T > 0) {
+    if (launch_gather_rows(x, permuted_token, R, p->H, x_perm, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    ++launches;
+  }
+  set_last_launch_count(launches);
   return MOE_OK;
 }

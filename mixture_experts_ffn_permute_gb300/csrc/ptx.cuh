@@ -136,21 +136,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// The same box delivered to the same shared-memory offset of every CTA in
-// `cta_mask` (this cluster), completion counted on the mbarrier at the same
-// offset in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map,
-                                                      int32_t c0, int32_t c1, uint64_t* bar,
-                                                      uint16_t cta_mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask),
-      "l"(policy)
-      : "memory");
-}
-
 // Four rows (r0..r3) of `map`, each a box of the map's inner width starting
 // at column c0, gathered into consecutive rows of shared memory.
 __device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, int32_t c0,
@@ -275,16 +260,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at the same offset in every CTA of
-// `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 

@@ -86,3 +86,24 @@ def assert_grad_bound(gpu, ref, mag, what: str = "", rms: float = RMS_BF16, tau:
     e = rms_rel(g, r)
     assert e <= rms, f"{what}: RMS relative error {e:.3e} > {rms:.1e}"
     return e
+
+
+def tile_sample_tokens(perm, tile_rows: int = 256) -> np.ndarray:
+    """Tokens whose outputs a full-size parity test compares, chosen from the
+    oracle's permutation (never from the GPU's) so that every tile kind the
+    kernels run at full size is reached: for every expert with rows, the
+    token at its first permuted row and at the last row of each of its
+    tile_rows-row token tiles (the last one being the expert's ragged tail).
+    Sorted, without repeats."""
+    off = np.asarray(perm["expert_offsets"])
+    ptok = np.asarray(perm["permuted_token"])
+    rows = []
+    for e in range(len(off) - 1):
+        a, b = int(off[e]), int(off[e + 1])
+        if b <= a:
+            continue
+        rows.append(a)
+        for t0 in range(a, b, tile_rows):
+            rows.append(min(b, t0 + tile_rows) - 1)
+    toks = ptok[np.asarray(rows, np.int64)]
+    return np.unique(toks[toks >= 0]).astype(np.int64)

@@ -122,13 +122,16 @@ def test_auto_tiling_selection():
         moe.KERNEL_WEIGHT_TILES_2CTA
     assert moe.selected_kernel(moe.Problem.make(T=4096, H=4096, F=14336, E=8, k=2)) == \
         moe.KERNEL_WEIGHT_TILES_2CTA
-    p = moe.Problem.make(T=4096, H=4096, F=14336, E=8, k=2, kernel=moe.KERNEL_TOKEN_TILES_2CTA)
-    assert moe.selected_kernel(p) == moe.KERNEL_TOKEN_TILES_2CTA
+    p = moe.Problem.make(T=4096, H=4096, F=14336, E=8, k=2, kernel=moe.KERNEL_TOKEN_TILES)
+    assert moe.selected_kernel(p) == moe.KERNEL_TOKEN_TILES
+    for dropped in (3, 4, 5, 8):  # tiling numbers that are not built
+        p = moe.Problem.make(T=4096, H=4096, F=14336, E=8, k=2, kernel=dropped)
+        assert moe.selected_kernel(p) == -1
     assert lib is not None
 
 
 def test_lowprec_tiling_selection():
-    """FP8/NVFP4: token-row tiles by default; 1-CTA or 2-CTA weight-row tiles on request; no others."""
+    """FP8/NVFP4: token-row tiles by default; 2-CTA weight-row tiles on request; no others."""
     moe.load()
     mk = lambda kernel: moe.Problem.make(T=4096, H=7168, F=2048, E=256, k=8, glu_interleave=32,  # noqa: E731
                                          swiglu_clamp=7.0, precision=moe.PREC_FP8_NVFP4,
@@ -136,9 +139,7 @@ def test_lowprec_tiling_selection():
     assert moe.selected_kernel(mk(moe.KERNEL_AUTO)) == moe.KERNEL_TOKEN_TILES
     assert moe.selected_kernel(mk(moe.KERNEL_WEIGHT_TILES_2CTA)) == moe.KERNEL_WEIGHT_TILES_2CTA
     assert moe.selected_kernel(mk(moe.KERNEL_TOKEN_TILES)) == moe.KERNEL_TOKEN_TILES
-    assert moe.selected_kernel(mk(moe.KERNEL_WEIGHT_TILES_WIDE)) == moe.KERNEL_WEIGHT_TILES_WIDE
-    for k in (moe.KERNEL_WEIGHT_TILES, moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA,
-              moe.KERNEL_DECODE_FUSED):
+    for k in (moe.KERNEL_WEIGHT_TILES, 3, 4, 5, moe.KERNEL_DECODE_FUSED):
         assert moe.selected_kernel(mk(k)) == -1
 
 

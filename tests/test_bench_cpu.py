@@ -37,7 +37,8 @@ def test_decode_mlp_bytes_are_both_weights_rows_in_and_tokens_out():
 
 def test_traffic_key_names_the_workload_and_token_override():
     key = lambda argv: bench.traffic_key(bench.parse_args(argv))  # noqa: E731
-    assert key([]) == "mixtral"
+    assert key([]) == "skewed"
+    assert key(["--workload", "mixtral"]) == "mixtral"
     assert key(["--workload", "decode"]) == "decode"
     assert key(["--workload", "decode", "--T", "8"]) == "decode-T8"
     assert key(["--workload", "lowprec", "--E", "32"]) == "custom"
@@ -67,3 +68,27 @@ def test_peaks_fall_back_without_the_measured_file(monkeypatch, tmp_path):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     peaks, src = bench.load_peaks()
     assert src == "fallback" and peaks == bench.FALLBACK_PEAKS
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    a = bench.parse_args([])
+    shape, _ = bench.WORKLOADS[a.workload]
+    assert (shape.T, shape.H, shape.F, shape.E, shape.k) == (8192, 7168, 2048, 256, 8)
+
+
+def test_layer_bytes_are_active_weights_x_logits_and_out():
+    s = mi.SKEWED
+    b = bench.layer_algorithmic_bytes(s, 196)
+    assert b == 196 * 3 * 2048 * 7168 * 2 + 8192 * 7168 * 2 + 8192 * 256 * 4 + 8192 * 7168 * 2
+    lp = mi.LOWPREC
+    per = 3 * lp.F * lp.H / 2 + 3 * lp.F * lp.H / 16 + 8
+    xin = lp.T * lp.H + lp.T * (lp.H // 128) * 4
+    assert bench.layer_algorithmic_bytes(lp, 256) == 256 * per + xin + lp.T * 256 * 4 + \
+        lp.T * lp.H * 2
+
+
+def test_tensor_peak_is_burst_for_short_regions_and_sustained_for_long():
+    peaks = {"hbm_gbs": 6775.6, "bf16_tflops": 1916.9, "bf16_tflops_sustained": 1719.2}
+    assert bench.tensor_peak(peaks, 1.1)[:2] == (1916.9, "bf16_tflops")
+    assert bench.tensor_peak(peaks, bench.SUSTAINED_AFTER_S)[:2] == \
+        (1719.2, "bf16_tflops_sustained")

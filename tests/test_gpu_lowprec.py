@@ -10,7 +10,7 @@ import moe_inputs as mi
 import oracle
 import mixture_experts_ffn_permute_gb300 as moe
 from mixture_experts_ffn_permute_gb300 import _build
-from parity import assert_equal, rms_rel, to_f64
+from parity import assert_equal, rms_rel, tile_sample_tokens, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -24,10 +24,9 @@ def built():
     moe.load()
 
 
-# token-row tiles (the default), weight-row tiles with the weights in tensor
-# memory, and 2-CTA weight-row tiles
-KERNELS = [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_WIDE, moe.KERNEL_WEIGHT_TILES_2CTA]
-KERNEL_IDS = ["token_tiles", "weight_tiles_tmem", "weight_tiles_2cta"]
+# token-row tiles (the default) and 2-CTA weight-row tiles
+KERNELS = [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_2CTA]
+KERNEL_IDS = ["token_tiles", "weight_tiles_2cta"]
 
 
 def run_lowprec(shape, inp, kernel=moe.KERNEL_AUTO):
@@ -105,8 +104,10 @@ def test_lowprec_full_size_sampled(kernel):
     logits_h = inp["logits"].cpu()
     idx_ref, _ = oracle.route_topk(logits_h, shape.k)
     assert_equal(res["topk_idx"], idx_ref, "topk_idx")
-    g = np.random.default_rng(7)
-    toks = np.sort(g.choice(shape.T, size=4, replace=False))
+    # first row of every expert and last row of each 128-row token tile, from
+    # the oracle's permutation
+    toks = tile_sample_tokens(oracle.permute(idx_ref, shape.E), tile_rows=128)
+    assert len(toks) >= 256
     used = sorted(set(idx_ref[toks].ravel().tolist()))
     lists = {n: [None] * shape.E for n in ("w1q", "w1s", "w2q", "w2s")}
     for e in used:
@@ -141,8 +142,8 @@ def run_lowprec_mx(shape, inp, kernel=moe.KERNEL_AUTO):
     return {"out": out, "topk_idx": idx, "prepared": prepared, "g1": g1, "g2": g2}
 
 
-@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_WIDE],
-                         ids=["token_tiles", "weight_tiles_tmem"])
+@pytest.mark.parametrize("kernel", [moe.KERNEL_AUTO, moe.KERNEL_WEIGHT_TILES_2CTA],
+                         ids=["token_tiles", "weight_tiles_2cta"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
 def test_mxfp4_forward_small(shape, kernel):
     inp = mi.make_lowprec_inputs(shape, seed=0, wfmt="mxfp4")
@@ -199,8 +200,8 @@ def test_mxfp4_full_size_sampled():
     logits_h = inp["logits"].cpu()
     idx_ref, _ = oracle.route_topk(logits_h, shape.k)
     assert_equal(res["topk_idx"], idx_ref, "topk_idx")
-    g = np.random.default_rng(8)
-    toks = np.sort(g.choice(shape.T, size=4, replace=False))
+    toks = tile_sample_tokens(oracle.permute(idx_ref, shape.E), tile_rows=128)
+    assert len(toks) >= 256
     used = sorted(set(idx_ref[toks].ravel().tolist()))
     lists = {n: [None] * shape.E for n in ("w1q", "w1s", "w2q", "w2s")}
     for e in used:

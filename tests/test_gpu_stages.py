@@ -150,12 +150,10 @@ def _routed_inputs(shape, seed=0, mask=0.0):
     return inp, idx, w, perm, xp
 
 
-KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_WIDE,
-           moe.KERNEL_TOKEN_TILES_PAIR, moe.KERNEL_TOKEN_TILES_2CTA, moe.KERNEL_WEIGHT_TILES_2CTA]
+KERNELS = [moe.KERNEL_TOKEN_TILES, moe.KERNEL_WEIGHT_TILES, moe.KERNEL_WEIGHT_TILES_2CTA]
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_wide",
-                                                "token_tiles_pair", "token_tiles_2cta", "weight_tiles_2cta"])
+@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_2cta"])
 @pytest.mark.parametrize("shape", MLP_CASES, ids=lambda s: s.name)
 def test_grouped_swiglu_mlp(shape, kernel):
     inp, idx, w, perm, xp = _routed_inputs(shape, seed=1)
@@ -175,8 +173,7 @@ def test_grouped_swiglu_mlp(shape, kernel):
     assert_bf16_close(y, y_ref, f"y_perm[{shape.name}]")
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_wide",
-                                                "token_tiles_pair", "token_tiles_2cta", "weight_tiles_2cta"])
+@pytest.mark.parametrize("kernel", KERNELS, ids=["token_tiles", "weight_tiles", "weight_tiles_2cta"])
 def test_grouped_mlp_masked_tail_rows_are_zero(kernel):
     shape = mi.MoEShape("masked", T=100, H=256, F=256, E=6, k=2)
     inp, idx, w, perm, xp = _routed_inputs(shape, seed=4, mask=0.25)

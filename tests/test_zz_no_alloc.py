@@ -57,7 +57,14 @@ def test_noalloc_permute_matches_workspace_permute_on_consecutive_calls():
         x = mi.make_x(mi.MoEShape("x", T=T, H=H, F=128, E=E, k=k), seed=seed).to(DEV)
         p = moe.Problem.make(T, H, 128, E, k)
         want = _with_workspace(p, idx, x)
+        # a one-launch call in between, so the count below is the no-alloc call's
+        moe.unpermute_combine(p, want["x_perm"], want["row_id_map"],
+                              torch.ones(T, k, dtype=torch.float32, device=DEV),
+                              torch.empty(T, H, dtype=torch.bfloat16, device=DEV))
+        assert moe.last_launch_count() == 1
         got = _without_workspace(p, idx, x)
+        # histogram, scan, scatter and the row gather
+        assert moe.last_launch_count() == 4
         torch.cuda.synchronize()
         for key in KEYS:  # integer outputs: bit for bit
             assert torch.equal(got[key], want[key]), (T, key)
