@@ -177,19 +177,57 @@ MOE_API int moe_permute(const moe_problem* p, const int32_t* topk_idx, const voi
                         int32_t* tokens_per_expert, int32_t* expert_offsets, void* ws,
                         size_t ws_bytes, void* stream);
 
+/* Scales of NVFP4 weights as the low-precision entry points take them
+ * ("[SM90] Add W4A8 MegaMoE support", Usage: E4M3 scales per 16 values,
+ * transformed before the call, and one fp32 scale per expert tensor).  A
+ * HOST struct holding DEVICE pointers:
+ *   prepared   the block scales of W1 and W2 as moe_prepare_weights (or
+ *              moe_prepare_weights_mxfp4) wrote them
+ *   w1_gscale  [E] fp32 per-expert scale of W1
+ *   w2_gscale  [E] fp32 per-expert scale of W2 */
+typedef struct moe_fp4_scales {
+  const void* prepared;
+  const float* w1_gscale;
+  const float* w2_gscale;
+} moe_fp4_scales;
+
 /* Steps 3-5 -- grouped expert MLP on permuted rows ("Support GEMM + Swiglu
  * fused MLP"; MegaMoE description: two expert GEMMs and clamped SwiGLU).
+ *   expert_offsets [E + 1] int32 (device), non-decreasing, offsets[E] <= R
+ *   y_perm         [R, H] bf16 out: y = silu-glu(x W1^T) W2^T per row, NOT
+ *                  weighted; rows >= expert_offsets[E] are set to zero.
+ * precision = MOE_PREC_BF16:
  *   x_perm         [R, H] bf16, rows of expert e at
  *                  [expert_offsets[e], expert_offsets[e+1])
- *   expert_offsets [E + 1] int32 (device), non-decreasing, offsets[E] <= R
+ *   x_perm_scale   must be NULL
  *   w1             [E, 2F, H] bf16 (gate/up rows per glu_interleave)
  *   w2             [E, H, F] bf16
- *   y_perm         [R, H] bf16 out: y = silu-glu(x W1^T) W2^T per row, NOT
- *                  weighted; rows >= expert_offsets[E] are set to zero. */
+ *   wscales        must be NULL
+ * precision = MOE_PREC_FP8_NVFP4 (the MegaMoE page's W4A8 formats; see the
+ * low-precision section below):
+ *   x_perm         [R, H] E4M3 codes (one byte each), permuted rows
+ *   x_perm_scale   [R, H/128] fp32 scale of every 128 values of a row
+ *   w1, w2         packed E2M1 codes [E, 2F, H/2] and [E, H, F/2]
+ *   wscales        const moe_fp4_scales* (host struct of device pointers)
+ *   GEMM1's SwiGLU output is re-quantised to E4M3 per 1x128 before GEMM2, as
+ *   in moe_forward_fp8_nvfp4.  H a multiple of 256, F of 128. */
 MOE_API int moe_grouped_swiglu_mlp(const moe_problem* p, const void* x_perm,
-                                   const int32_t* expert_offsets, const void* w1,
-                                   const void* w2, void* y_perm, void* ws, size_t ws_bytes,
-                                   void* stream);
+                                   const float* x_perm_scale, const int32_t* expert_offsets,
+                                   const void* w1, const void* w2, const void* wscales,
+                                   void* y_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* Row gather for payloads other than bf16 hidden rows (the permute of "add
+ * permute fusion into hybrid ep", PR description, applied to any fixed-width
+ * row): dst[r] = src[permuted_token[r]] for r < T*k, a zero row where
+ * permuted_token[r] is -1.  For the low-precision layer's staged form: the
+ * E4M3 code rows (row_bytes = H) and their fp32 scale rows (row_bytes =
+ * 4*H/128) of x, gathered with the permuted_token moe_permute wrote.
+ *   permuted_token [T*k] int32 (device), values in [-1, T)
+ *   src [T, row_bytes] bytes, dst [T*k, row_bytes] bytes out (device)
+ *   row_bytes a positive multiple of 4 (pointers 16-byte aligned).
+ * A token index outside [-1, T) gives a zero row (not reported). */
+MOE_API int moe_permute_rows(const moe_problem* p, const int32_t* permuted_token,
+                             const void* src, int32_t row_bytes, void* dst, void* stream);
 
 /* Step 6 -- weighted unpermute/combine (MegaMoE description: top-k
  * reduction):  out[t] = sum_{j=0..k-1, row_id_map[t][j] >= 0}
@@ -203,13 +241,19 @@ MOE_API int moe_unpermute_combine(const moe_problem* p, const void* y_perm,
                                   void* stream);
 
 /* The whole layer, steps 1-6, enqueued on `stream` with no host round trip.
- *   x [T, H] bf16, logits [T, E] fp32, w1 [E, 2F, H] bf16, w2 [E, H, F] bf16
- *   out [T, H] bf16 out
+ *   logits [T, E] fp32, out [T, H] bf16 out
  *   topk_idx_out [T, k] int32, topk_w_out [T, k] fp32,
  *   tokens_per_expert_out [E] int32: optional copies of the routing (NULL to
- *   skip). */
-MOE_API int moe_forward(const moe_problem* p, const void* x, const float* logits,
-                        const void* w1, const void* w2, void* out, int32_t* topk_idx_out,
+ *   skip).
+ * precision = MOE_PREC_BF16: x [T, H] bf16, x_scale NULL, w1 [E, 2F, H] and
+ *   w2 [E, H, F] bf16, wscales NULL.
+ * precision = MOE_PREC_FP8_NVFP4: x [T, H] E4M3 codes, x_scale [T, H/128]
+ *   fp32, w1 / w2 packed E2M1 codes, wscales a const moe_fp4_scales* -- the
+ *   same layer as moe_forward_fp8_nvfp4 (bit-identical results); shared
+ *   experts are bf16 only. */
+MOE_API int moe_forward(const moe_problem* p, const void* x, const float* x_scale,
+                        const float* logits, const void* w1, const void* w2,
+                        const void* wscales, void* out, int32_t* topk_idx_out,
                         float* topk_w_out, int32_t* tokens_per_expert_out, void* ws,
                         size_t ws_bytes, void* stream);
 

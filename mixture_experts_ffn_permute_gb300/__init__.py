@@ -6,6 +6,7 @@ function names mirror the C entry points of ``include/moe_ffn.h``:
 
     route_topk            -> moe_route_topk
     permute               -> moe_permute
+    permute_rows          -> moe_permute_rows
     grouped_swiglu_mlp    -> moe_grouped_swiglu_mlp
     unpermute_combine     -> moe_unpermute_combine
     forward               -> moe_forward
@@ -83,9 +84,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_workspace_size": ([pp], sz),
         "moe_route_topk": ([pp, vp, vp, vp, vp, sz, vp], ci),
         "moe_permute": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
-        "moe_grouped_swiglu_mlp": ([pp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_grouped_swiglu_mlp": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_permute_rows": ([pp, vp, vp, ctypes.c_int32, vp, vp], ci),
         "moe_unpermute_combine": ([pp, vp, vp, vp, vp, vp], ci),
-        "moe_forward": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
+        "moe_forward": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_forward_routed": ([pp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ci),
         "moe_selftest_wait_timeout": ([vp, ctypes.c_uint64, vp], ci),
         "moe_backward_workspace_size": ([pp], sz),
@@ -202,10 +204,44 @@ def permute_noalloc(p: Problem, topk_idx, x, x_perm, row_id_map, permuted_token,
           _ptr(expert_offsets), _stream(stream))
 
 
+class FP4Scales(ctypes.Structure):
+    """Mirror of ``moe_fp4_scales``: device pointers to the prepared block
+    scales and the per-expert fp32 scales of W1 and W2."""
+    _fields_ = [("prepared", ctypes.c_void_p), ("w1_gscale", ctypes.c_void_p),
+                ("w2_gscale", ctypes.c_void_p)]
+
+    @classmethod
+    def of(cls, prepared, w1_gscale, w2_gscale):
+        return cls(prepared.data_ptr(), w1_gscale.data_ptr(), w2_gscale.data_ptr())
+
+
+def _scales_ref(wscales):
+    if wscales is None:
+        return None
+    if isinstance(wscales, (tuple, list)):
+        wscales = FP4Scales.of(*wscales)
+    return ctypes.byref(wscales)
+
+
 def grouped_swiglu_mlp(p: Problem, x_perm, expert_offsets, w1, w2, y_perm, ws,
-                       stream=None) -> None:
-    _call("moe_grouped_swiglu_mlp", ctypes.byref(p), _ptr(x_perm), _ptr(expert_offsets),
-          _ptr(w1), _ptr(w2), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream))
+                       stream=None, x_perm_scale=None, wscales=None) -> None:
+    """Steps 3-5 on permuted rows.  bf16: x_perm [R, H] bf16, w1/w2 bf16.
+    FP8/NVFP4 (p.precision = PREC_FP8_NVFP4): x_perm [R, H] E4M3 codes (uint8),
+    x_perm_scale [R, H/128] fp32, w1/w2 packed E2M1 codes and wscales =
+    (prepared, w1_gscale, w2_gscale) tensors or an FP4Scales."""
+    _call("moe_grouped_swiglu_mlp", ctypes.byref(p), _ptr(x_perm), _ptr(x_perm_scale),
+          _ptr(expert_offsets), _ptr(w1), _ptr(w2), _scales_ref(wscales), _ptr(y_perm), _ptr(ws),
+          ws.numel(), _stream(stream))
+
+
+def permute_rows(p: Problem, permuted_token, src, dst, stream=None) -> None:
+    """dst[r] = src[permuted_token[r]] for rows of any width (a multiple of 4
+    bytes); zero rows for -1.  src [T, ...], dst [T*k, ...] of one dtype."""
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else 0
+    if dst.shape[0] != p.T * p.k or dst[0].numel() * dst.element_size() != row_bytes:
+        raise ValueError("dst must hold T*k rows of src's row width")
+    _call("moe_permute_rows", ctypes.byref(p), _ptr(permuted_token), _ptr(src),
+          int(row_bytes), _ptr(dst), _stream(stream))
 
 
 def unpermute_combine(p: Problem, y_perm, row_id_map, topk_w, out, stream=None) -> None:
@@ -214,10 +250,13 @@ def unpermute_combine(p: Problem, y_perm, row_id_map, topk_w, out, stream=None) 
 
 
 def forward(p: Problem, x, logits, w1, w2, out, ws, topk_idx=None, topk_w=None,
-            tokens_per_expert=None, stream=None) -> None:
-    _call("moe_forward", ctypes.byref(p), _ptr(x), _ptr(logits), _ptr(w1), _ptr(w2),
-          _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(tokens_per_expert), _ptr(ws),
-          ws.numel(), _stream(stream))
+            tokens_per_expert=None, stream=None, x_scale=None, wscales=None) -> None:
+    """The whole layer.  bf16: x bf16, w1/w2 bf16.  FP8/NVFP4 (p.precision =
+    PREC_FP8_NVFP4): x E4M3 codes, x_scale [T, H/128] fp32, w1/w2 packed E2M1
+    codes, wscales = (prepared, w1_gscale, w2_gscale) or an FP4Scales."""
+    _call("moe_forward", ctypes.byref(p), _ptr(x), _ptr(x_scale), _ptr(logits), _ptr(w1),
+          _ptr(w2), _scales_ref(wscales), _ptr(out), _ptr(topk_idx), _ptr(topk_w),
+          _ptr(tokens_per_expert), _ptr(ws), ws.numel(), _stream(stream))
 
 
 def forward_routed(p: Problem, x, topk_idx, topk_w, w1, w2, out, ws, tokens_per_expert=None,
@@ -348,7 +387,8 @@ class MoEFFN:
 
 
 __all__ = ["Problem", "MoEError", "MoEFFN", "load", "workspace_size", "alloc_workspace",
-           "route_topk", "permute", "grouped_swiglu_mlp", "unpermute_combine", "forward",
+           "route_topk", "permute", "permute_rows", "grouped_swiglu_mlp", "unpermute_combine",
+           "forward", "FP4Scales",
            "get_device_status", "clear_device_status", "last_launch_count", "LIB_PATH",
            "stage_timing_begin", "stage_timing_end", "permute_noalloc",
            "prepared_scales_size", "prepare_weights", "forward_fp8_nvfp4", "selected_kernel",

@@ -484,6 +484,149 @@ int run_backward_core(const moe_problem* p, const moe_problem* q, const BwdLayou
   return MOE_OK;
 }
 
+// GEMM1 + SwiGLU (+ the 1x128 E4M3 re-quantisation of h) and GEMM2 of the
+// FP8-activation / NVFP4-weight layer on f16 rows x_perm (dequantised
+// activations), into h (workspace) and y.
+int run_mlp_lowprec(const moe_problem* p, const void* x_perm, const int32_t* off,
+                    const int32_t* mtp, const void* w1q, const void* w2q,
+                    const moe_fp4_scales& sc, void* h, void* y, uint32_t* status, cudaStream_t s,
+                    int& launches, StageTimer* tm = nullptr, int call = 0, int mark = 0) {
+  const int R = p->T * p->k;
+  const uint8_t* sc1 = static_cast<const uint8_t*>(sc.prepared);
+  const uint8_t* sc2 = sc1 + static_cast<size_t>(p->E) * 2 * p->F * p->H / 16;
+  GroupedGemmArgs g1{};
+  g1.epi = Epi::kSwiGLU;
+  g1.a = x_perm;
+  g1.a_rows = R;
+  g1.b = w1q;
+  g1.b_rows_per_expert = 2 * p->F;
+  g1.E = p->E;
+  g1.K = p->H;
+  g1.n_tiles = p->F / (kBN / 2);
+  g1.expert_offsets = off;
+  g1.mtile_prefix = mtp;
+  g1.out = h;
+  g1.ldo = p->F;
+  g1.out_rows = R;
+  g1.F = p->F;
+  g1.interleave = p->glu_interleave;
+  g1.clamp = clamp_of(p);
+  g1.status = status;
+  const int lt = lowprec_tiling(p);
+  MOE_LAUNCH(lt == MOE_KERNEL_WEIGHT_TILES_2CTA
+                 ? launch_grouped_gemm_fp4_pair(g1, sc1, sc.w1_gscale, s)
+                 : launch_grouped_gemm_fp4(g1, sc1, sc.w1_gscale, s));
+  if (tm) tm->mark(call, mark, s);
+  GroupedGemmArgs g2{};
+  g2.epi = Epi::kPlain;
+  g2.a = h;
+  g2.a_rows = R;
+  g2.b = w2q;
+  g2.b_rows_per_expert = p->H;
+  g2.E = p->E;
+  g2.K = p->F;
+  g2.n_tiles = p->H / kBN;
+  g2.expert_offsets = off;
+  g2.mtile_prefix = mtp;
+  g2.out = y;
+  g2.ldo = p->H;
+  g2.out_rows = R;
+  g2.F = p->F;
+  g2.status = status;
+  MOE_LAUNCH(lt == MOE_KERNEL_WEIGHT_TILES_2CTA
+                 ? launch_grouped_gemm_fp4_pair(g2, sc2, sc.w2_gscale, s)
+                 : launch_grouped_gemm_fp4(g2, sc2, sc.w2_gscale, s));
+  if (tm) tm->mark(call, mark + 1, s);
+  return MOE_OK;
+}
+
+// Validation of the FP4 weight scales struct (host) and its device pointers.
+int check_fp4_scales(const void* wscales) {
+  if (!wscales) return MOE_ERR_INVALID_ARG;
+  const moe_fp4_scales* sc = static_cast<const moe_fp4_scales*>(wscales);
+  MOE_REQUIRE_PTR(sc->prepared);
+  MOE_REQUIRE_PTR(sc->w1_gscale);
+  MOE_REQUIRE_PTR(sc->w2_gscale);
+  return MOE_OK;
+}
+
+// The FP8-activation / NVFP4-weight layer (moe_forward at that precision and
+// moe_forward_fp8_nvfp4).
+int forward_lowprec(const moe_problem* p, const void* xq_v, const float* xs, const float* logits,
+                    const void* w1q, const void* w2q, const moe_fp4_scales* scp, void* out,
+                    int32_t* topk_idx_out, float* topk_w_out, int32_t* tokens_per_expert_out,
+                    void* ws, size_t ws_bytes, cudaStream_t s) {
+  const uint8_t* xq = static_cast<const uint8_t*>(xq_v);
+  int rc = check_full(p);
+  if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // bf16 moe_forward only
+  if (p->precision != MOE_PREC_FP8_NVFP4) return MOE_ERR_INVALID_ARG;
+  rc = check_ws(p, ws, ws_bytes);
+  if (rc != MOE_OK) return rc;
+  MOE_REQUIRE_PTR(w1q);
+  MOE_REQUIRE_PTR(w2q);
+  rc = check_fp4_scales(scp);
+  if (rc != MOE_OK) return rc;
+  const moe_fp4_scales& sc = *scp;
+  if (topk_idx_out && !aligned16(topk_idx_out)) return MOE_ERR_MISALIGNED;
+  if (topk_w_out && !aligned16(topk_w_out)) return MOE_ERR_MISALIGNED;
+  if (tokens_per_expert_out && !aligned16(tokens_per_expert_out)) return MOE_ERR_MISALIGNED;
+  const Layout L = layout_of(*p);
+  int launches = 0;
+  int32_t* tpe = tokens_per_expert_out ? tokens_per_expert_out
+                                       : at<int32_t>(ws, L.tokens_per_expert);
+  if (p->T == 0) {
+    if (tokens_per_expert_out)
+      MOE_LAUNCH(cudaMemsetAsync(tokens_per_expert_out, 0, sizeof(int32_t) * p->E, s));
+    g_launches = launches;
+    return MOE_OK;
+  }
+  MOE_REQUIRE_PTR(xq);
+  MOE_REQUIRE_PTR(xs);
+  MOE_REQUIRE_PTR(logits);
+  MOE_REQUIRE_PTR(out);
+  const int R = p->T * p->k;
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.topk_idx);
+  float* wts = topk_w_out ? topk_w_out : at<float>(ws, L.topk_w);
+  int32_t* off = at<int32_t>(ws, L.expert_offsets);
+  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
+  int32_t* rmap = at<int32_t>(ws, L.row_id_map);
+  int32_t* ptok = at<int32_t>(ws, L.permuted_token);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h = at<void>(ws, L.h);
+  void* y = at<void>(ws, L.y);
+
+  const int call = g_timer.on ? g_timer.used++ : 0;
+  StageTimer& tm = g_timer;
+  if (tm.on) tm.kind = 0;
+  tm.mark(call, 0, s);
+  if (route_permute_tiny_fits(p->T, p->E, p->k, 0)) {
+    MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, 0, p->renormalize ? 1 : 0, idx,
+                                         wts, tpe, off, mtp, rmap, ptok, nullptr, p->H, nullptr,
+                                         s));
+    for (int i = 1; i <= 4; ++i) tm.mark(call, i, s);
+  } else {
+    MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
+    tm.mark(call, 1, s);
+    if (permute_small_fits(p->T, p->E, p->k)) {
+      MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
+      for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
+    } else {
+      rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2);
+      if (rc != MOE_OK) return rc;
+    }
+  }
+  MOE_LAUNCH(launch_gather_dequant_fp8(xq, xs, ptok, R, p->H, x_perm, s));
+  tm.mark(call, 5, s);
+  rc = run_mlp_lowprec(p, x_perm, off, mtp, w1q, w2q, sc, h, y, status, s, launches, &tm, call, 6);
+  if (rc != MOE_OK) return rc;
+  MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
+  tm.mark(call, 8, s);
+  g_launches = launches;
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -567,13 +710,20 @@ int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, vo
   return MOE_OK;
 }
 
-int moe_grouped_swiglu_mlp(const moe_problem* p, const void* x_perm,
+int moe_grouped_swiglu_mlp(const moe_problem* p, const void* x_perm, const float* x_perm_scale,
                            const int32_t* expert_offsets, const void* w1, const void* w2,
-                           void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+                           const void* wscales, void* y_perm, void* ws, size_t ws_bytes,
+                           void* stream) {
   int rc = check_full(p);
   if (rc != MOE_OK) return rc;
   if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
-  if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
+  const bool lowprec = p->precision == MOE_PREC_FP8_NVFP4;
+  if (lowprec) {
+    rc = check_fp4_scales(wscales);
+    if (rc != MOE_OK) return rc;
+  } else if (x_perm_scale || wscales) {
+    return MOE_ERR_INVALID_ARG;  // bf16 rows carry no scales
+  }
   rc = check_ws(p, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
   MOE_REQUIRE_PTR(expert_offsets);
@@ -582,15 +732,45 @@ int moe_grouped_swiglu_mlp(const moe_problem* p, const void* x_perm,
   if (p->T == 0) { g_launches = 0; return MOE_OK; }
   MOE_REQUIRE_PTR(x_perm);
   MOE_REQUIRE_PTR(y_perm);
+  if (lowprec) MOE_REQUIRE_PTR(x_perm_scale);
   const Layout L = layout_of(*p);
   int launches = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t* status = at<uint32_t>(ws, L.status);
   int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
-  MOE_LAUNCH(launch_mtile_prefix_from_offsets(expert_offsets, p->E, p->T * p->k, mtp, status, s));
-  rc = run_mlp(p, x_perm, expert_offsets, mtp, w1, w2, at<void>(ws, L.h), y_perm, status, s,
-               launches);
+  const int R = p->T * p->k;
+  MOE_LAUNCH(launch_mtile_prefix_from_offsets(expert_offsets, p->E, R, mtp, status, s));
+  if (lowprec) {
+    // the E4M3 rows with their per-128 scales -> f16 rows in the workspace
+    // (in place: row r from row r), then the FP4 GEMMs
+    void* xf = at<void>(ws, L.x_perm);
+    MOE_LAUNCH(launch_gather_dequant_fp8(static_cast<const uint8_t*>(x_perm), x_perm_scale,
+                                         nullptr, R, p->H, xf, s));
+    rc = run_mlp_lowprec(p, xf, expert_offsets, mtp, w1, w2,
+                         *static_cast<const moe_fp4_scales*>(wscales), at<void>(ws, L.h), y_perm,
+                         status, s, launches);
+  } else {
+    rc = run_mlp(p, x_perm, expert_offsets, mtp, w1, w2, at<void>(ws, L.h), y_perm, status, s,
+                 launches);
+  }
   if (rc != MOE_OK) return rc;
+  g_launches = launches;
+  return MOE_OK;
+}
+
+int moe_permute_rows(const moe_problem* p, const int32_t* permuted_token, const void* src,
+                     int32_t row_bytes, void* dst, void* stream) {
+  int rc = check_routing(p);
+  if (rc != MOE_OK) return rc;
+  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
+  if (row_bytes <= 0 || row_bytes % 4 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (p->T == 0) { g_launches = 0; return MOE_OK; }
+  MOE_REQUIRE_PTR(permuted_token);
+  MOE_REQUIRE_PTR(src);
+  MOE_REQUIRE_PTR(dst);
+  int launches = 0;
+  MOE_LAUNCH(launch_gather_row_bytes(src, permuted_token, p->T * p->k, p->T, row_bytes, dst,
+                                     static_cast<cudaStream_t>(stream)));
   g_launches = launches;
   return MOE_OK;
 }
@@ -613,12 +793,19 @@ int moe_unpermute_combine(const moe_problem* p, const void* y_perm, const int32_
   return MOE_OK;
 }
 
-int moe_forward(const moe_problem* p, const void* x, const float* logits, const void* w1,
-                const void* w2, void* out, int32_t* topk_idx_out, float* topk_w_out,
-                int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes, void* stream) {
+int moe_forward(const moe_problem* p, const void* x, const float* x_scale, const float* logits,
+                const void* w1, const void* w2, const void* wscales, void* out,
+                int32_t* topk_idx_out, float* topk_w_out, int32_t* tokens_per_expert_out,
+                void* ws, size_t ws_bytes, void* stream) {
   int rc = check_full(p);
   if (rc != MOE_OK) return rc;
+  if (p->precision == MOE_PREC_FP8_NVFP4)
+    return forward_lowprec(p, x, x_scale, logits, w1, w2,
+                           static_cast<const moe_fp4_scales*>(wscales), out, topk_idx_out,
+                           topk_w_out, tokens_per_expert_out, ws, ws_bytes,
+                           static_cast<cudaStream_t>(stream));
   if (p->precision != MOE_PREC_BF16) return MOE_ERR_INVALID_ARG;
+  if (x_scale || wscales) return MOE_ERR_INVALID_ARG;  // bf16 rows carry no scales
   rc = check_ws(p, ws, ws_bytes);
   if (rc != MOE_OK) return rc;
   MOE_REQUIRE_PTR(w1);
@@ -939,115 +1126,9 @@ int moe_forward_fp8_nvfp4(const moe_problem* p, const uint8_t* xq, const float* 
                           void* out, int32_t* topk_idx_out, float* topk_w_out,
                           int32_t* tokens_per_expert_out, void* ws, size_t ws_bytes,
                           void* stream) {
-  int rc = check_full(p);
-  if (rc != MOE_OK) return rc;
-  if (p->shared_experts != 0) return MOE_ERR_INVALID_ARG;  // moe_forward only
-  if (p->precision != MOE_PREC_FP8_NVFP4) return MOE_ERR_INVALID_ARG;
-  rc = check_ws(p, ws, ws_bytes);
-  if (rc != MOE_OK) return rc;
-  MOE_REQUIRE_PTR(w1q);
-  MOE_REQUIRE_PTR(w2q);
-  MOE_REQUIRE_PTR(w1_gscale);
-  MOE_REQUIRE_PTR(w2_gscale);
-  MOE_REQUIRE_PTR(prepared_scales);
-  if (topk_idx_out && !aligned16(topk_idx_out)) return MOE_ERR_MISALIGNED;
-  if (topk_w_out && !aligned16(topk_w_out)) return MOE_ERR_MISALIGNED;
-  if (tokens_per_expert_out && !aligned16(tokens_per_expert_out)) return MOE_ERR_MISALIGNED;
-  const Layout L = layout_of(*p);
-  int launches = 0;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t* tpe = tokens_per_expert_out ? tokens_per_expert_out
-                                       : at<int32_t>(ws, L.tokens_per_expert);
-  if (p->T == 0) {
-    if (tokens_per_expert_out)
-      MOE_LAUNCH(cudaMemsetAsync(tokens_per_expert_out, 0, sizeof(int32_t) * p->E, s));
-    g_launches = launches;
-    return MOE_OK;
-  }
-  MOE_REQUIRE_PTR(xq);
-  MOE_REQUIRE_PTR(xs);
-  MOE_REQUIRE_PTR(logits);
-  MOE_REQUIRE_PTR(out);
-  const int R = p->T * p->k;
-  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.topk_idx);
-  float* wts = topk_w_out ? topk_w_out : at<float>(ws, L.topk_w);
-  int32_t* off = at<int32_t>(ws, L.expert_offsets);
-  int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
-  int32_t* rmap = at<int32_t>(ws, L.row_id_map);
-  int32_t* ptok = at<int32_t>(ws, L.permuted_token);
-  uint32_t* status = at<uint32_t>(ws, L.status);
-  void* x_perm = at<void>(ws, L.x_perm);
-  void* h = at<void>(ws, L.h);
-  void* y = at<void>(ws, L.y);
-  const uint8_t* sc1 = static_cast<const uint8_t*>(prepared_scales);
-  const uint8_t* sc2 = sc1 + static_cast<size_t>(p->E) * 2 * p->F * p->H / 16;
-
-  const int call = g_timer.on ? g_timer.used++ : 0;
-  StageTimer& tm = g_timer;
-  tm.mark(call, 0, s);
-  if (route_permute_tiny_fits(p->T, p->E, p->k, 0)) {
-    MOE_LAUNCH(launch_route_permute_tiny(logits, p->T, p->E, p->k, 0, p->renormalize ? 1 : 0, idx,
-                                         wts, tpe, off, mtp, rmap, ptok, nullptr, p->H, nullptr,
-                                         s));
-    for (int i = 1; i <= 4; ++i) tm.mark(call, i, s);
-  } else {
-    MOE_LAUNCH(launch_route_topk(logits, p->T, p->E, p->k, p->renormalize ? 1 : 0, idx, wts, s));
-    tm.mark(call, 1, s);
-    if (permute_small_fits(p->T, p->E, p->k)) {
-      MOE_LAUNCH(launch_permute_small(idx, p->T, p->E, p->k, tpe, off, mtp, rmap, ptok, s));
-      for (int i = 2; i <= 4; ++i) tm.mark(call, i, s);
-    } else {
-      rc = run_permute(p, idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches, &tm, call, 2);
-      if (rc != MOE_OK) return rc;
-    }
-  }
-  MOE_LAUNCH(launch_gather_dequant_fp8(xq, xs, ptok, R, p->H, x_perm, s));
-  tm.mark(call, 5, s);
-  GroupedGemmArgs g1{};
-  g1.epi = Epi::kSwiGLU;
-  g1.a = x_perm;
-  g1.a_rows = R;
-  g1.b = w1q;
-  g1.b_rows_per_expert = 2 * p->F;
-  g1.E = p->E;
-  g1.K = p->H;
-  g1.n_tiles = p->F / (kBN / 2);
-  g1.expert_offsets = off;
-  g1.mtile_prefix = mtp;
-  g1.out = h;
-  g1.ldo = p->F;
-  g1.out_rows = R;
-  g1.F = p->F;
-  g1.interleave = p->glu_interleave;
-  g1.clamp = clamp_of(p);
-  g1.status = status;
-  const int lt = lowprec_tiling(p);
-  MOE_LAUNCH(lt == MOE_KERNEL_WEIGHT_TILES_2CTA ? launch_grouped_gemm_fp4_pair(g1, sc1, w1_gscale, s)
-                                                : launch_grouped_gemm_fp4(g1, sc1, w1_gscale, s));
-  tm.mark(call, 6, s);
-  GroupedGemmArgs g2{};
-  g2.epi = Epi::kPlain;
-  g2.a = h;
-  g2.a_rows = R;
-  g2.b = w2q;
-  g2.b_rows_per_expert = p->H;
-  g2.E = p->E;
-  g2.K = p->F;
-  g2.n_tiles = p->H / kBN;
-  g2.expert_offsets = off;
-  g2.mtile_prefix = mtp;
-  g2.out = y;
-  g2.ldo = p->H;
-  g2.out_rows = R;
-  g2.F = p->F;
-  g2.status = status;
-  MOE_LAUNCH(lt == MOE_KERNEL_WEIGHT_TILES_2CTA ? launch_grouped_gemm_fp4_pair(g2, sc2, w2_gscale, s)
-                                                : launch_grouped_gemm_fp4(g2, sc2, w2_gscale, s));
-  tm.mark(call, 7, s);
-  MOE_LAUNCH(launch_combine(y, rmap, wts, p->T, p->H, p->k, out, s));
-  tm.mark(call, 8, s);
-  g_launches = launches;
-  return MOE_OK;
+  const moe_fp4_scales sc{prepared_scales, w1_gscale, w2_gscale};
+  return forward_lowprec(p, xq, xs, logits, w1q, w2q, &sc, out, topk_idx_out, topk_w_out,
+                         tokens_per_expert_out, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int moe_get_device_status(void* ws, void* stream) {

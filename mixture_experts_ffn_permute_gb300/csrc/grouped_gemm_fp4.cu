@@ -513,7 +513,7 @@ gather_dequant_fp8_kernel(const uint8_t* __restrict__ xq, const float* __restric
   pdl_enter();
   const int vecs = H / 8;
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    const int t = permuted_token[r];
+    const int t = permuted_token ? permuted_token[r] : r;
     uint4* dst = x_perm + static_cast<size_t>(r) * vecs;
     for (int v = threadIdx.x; v < vecs; v += blockDim.x) {
       if (t < 0) {

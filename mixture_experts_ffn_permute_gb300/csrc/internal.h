@@ -121,6 +121,11 @@ cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
 cudaError_t launch_gather_rows(const void* x, const int32_t* permuted_token, int R, int H,
                                void* x_perm, cudaStream_t s);
 
+// dst[r] = src[permuted_token[r]] for rows of row_bytes bytes (a multiple of
+// 4); zero row for -1 or a token outside [0, T).
+cudaError_t launch_gather_row_bytes(const void* src, const int32_t* permuted_token, int R, int T,
+                                    int row_bytes, void* dst, cudaStream_t s);
+
 // m-tile prefix from caller-supplied expert offsets (validated on device).
 cudaError_t launch_mtile_prefix_from_offsets(const int32_t* expert_offsets, int E, int R,
                                              int32_t* mtile_prefix, uint32_t* status,
@@ -272,7 +277,8 @@ cudaError_t launch_router_backward(const float* logits, const int32_t* topk_idx,
                                    const float* dw_part, int n_parts, int T, int E, int k,
                                    int slots, int renormalize, float* dlogits, cudaStream_t s);
 
-// FP8 rows (E4M3 codes + fp32 scales per 128) gathered by permuted_token into f16.
+// FP8 rows (E4M3 codes + fp32 scales per 128) gathered by permuted_token into
+// f16 (permuted_token NULL: row r from row r).
 cudaError_t launch_gather_dequant_fp8(const uint8_t* xq, const float* xs,
                                       const int32_t* permuted_token, int R, int H, void* x_perm,
                                       cudaStream_t s);

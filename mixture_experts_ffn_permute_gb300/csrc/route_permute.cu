@@ -288,6 +288,26 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
   }
 }
 
+// The same for rows of any width that is a multiple of 4 bytes: 16-byte
+// copies when the width allows, 4-byte copies otherwise; token indices
+// outside [0, T) give zero rows.
+template <typename V>
+__global__ void __launch_bounds__(256)
+gather_row_bytes_kernel(const V* __restrict__ src, const int32_t* __restrict__ permuted_token,
+                        int R, int T, int vecs_per_row, V* __restrict__ dst) {
+  pdl_enter();
+  for (int r = blockIdx.x; r < R; r += gridDim.x) {
+    const int t = permuted_token[r];
+    V* d = dst + static_cast<size_t>(r) * vecs_per_row;
+    if (t < 0 || t >= T) {
+      for (int v = threadIdx.x; v < vecs_per_row; v += blockDim.x) d[v] = V{};
+    } else {
+      const V* sp = src + static_cast<size_t>(t) * vecs_per_row;
+      for (int v = threadIdx.x; v < vecs_per_row; v += blockDim.x) d[v] = __ldg(sp + v);
+    }
+  }
+}
+
 // Validates caller-supplied offsets (non-decreasing, offsets[0] == 0,
 // offsets[E] <= R) and builds the m-tile prefix.  Bad offsets are recorded
 // and replaced by an empty problem.
@@ -529,6 +549,19 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* permuted_token, int
   return launch_kernel(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, 1,
                        static_cast<const uint4*>(x), permuted_token, R, vecs,
                        static_cast<uint4*>(x_perm));
+}
+
+cudaError_t launch_gather_row_bytes(const void* src, const int32_t* permuted_token, int R, int T,
+                                    int row_bytes, void* dst, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const int blocks = min(R, num_sms() * 8);
+  if (row_bytes % 16 == 0)
+    return launch_kernel(gather_row_bytes_kernel<uint4>, dim3(blocks), dim3(256), 0, s, 1,
+                         static_cast<const uint4*>(src), permuted_token, R, T, row_bytes / 16,
+                         static_cast<uint4*>(dst));
+  return launch_kernel(gather_row_bytes_kernel<uint32_t>, dim3(blocks), dim3(256), 0, s, 1,
+                       static_cast<const uint32_t*>(src), permuted_token, R, T, row_bytes / 4,
+                       static_cast<uint32_t*>(dst));
 }
 
 cudaError_t launch_mtile_prefix_from_offsets(const int32_t* expert_offsets, int E, int R,

@@ -40,6 +40,12 @@ def test_status_strings(lib):
         assert lib.moe_status_string(code).decode() == name
 
 
+def fwd(lib, p, x, lg, w1, w2, out, ws, nbytes, x_scale=None, wscales=None):
+    """moe_forward with no routing copies and the default stream."""
+    return lib.moe_forward(p, x, x_scale, lg, w1, w2, wscales, out, None, None, None, ws, nbytes,
+                           None)
+
+
 def P(**kw):
     base = dict(T=64, H=256, F=512, E=8, k=2)
     base.update(kw)
@@ -64,8 +70,7 @@ def test_workspace_size_grows_with_tokens(lib):
 def test_forward_rejects_bad_problems(lib, kw, code):
     p = P(**kw)
     fake = ctypes.c_void_p(1 << 20)
-    rc = lib.moe_forward(ctypes.byref(p), fake, fake, fake, fake, fake, None, None, None, fake,
-                         1 << 40, None)
+    rc = fwd(lib, ctypes.byref(p), fake, fake, fake, fake, fake, fake, 1 << 40)
     assert rc == code
 
 
@@ -75,15 +80,13 @@ def test_forward_rejects_bad_pointers_and_workspace(lib):
     mis = ctypes.c_void_p((1 << 20) + 8)
     big = 1 << 40
     ws_need = moe.workspace_size(p)
-    assert lib.moe_forward(ctypes.byref(p), None, a, a, a, a, None, None, None, a, big, None) == 1
-    assert lib.moe_forward(ctypes.byref(p), mis, a, a, a, a, None, None, None, a, big, None) == 3
+    assert fwd(lib, ctypes.byref(p), None, a, a, a, a, a, big) == 1
+    assert fwd(lib, ctypes.byref(p), mis, a, a, a, a, a, big) == 3
     # workspace must be 256-byte aligned and large enough
     ws_mis = ctypes.c_void_p((1 << 20) + 16)
-    assert lib.moe_forward(ctypes.byref(p), a, a, a, a, a, None, None, None, ws_mis, big,
-                           None) == 3
-    assert lib.moe_forward(ctypes.byref(p), a, a, a, a, a, None, None, None, a, ws_need - 1,
-                           None) == 4
-    assert lib.moe_forward(None, a, a, a, a, a, None, None, None, a, big, None) == 1
+    assert fwd(lib, ctypes.byref(p), a, a, a, a, a, ws_mis, big) == 3
+    assert fwd(lib, ctypes.byref(p), a, a, a, a, a, a, ws_need - 1) == 4
+    assert fwd(lib, None, a, a, a, a, a, a, big) == 1
 
 
 def test_other_entry_points_validate(lib):
@@ -93,8 +96,8 @@ def test_other_entry_points_validate(lib):
     assert lib.moe_route_topk(ctypes.byref(P(k=9)), a, a, a, None, 0, None) == 1
     assert lib.moe_route_topk(ctypes.byref(p), mis, a, a, None, 0, None) == 3
     assert lib.moe_permute(ctypes.byref(p), a, None, None, a, a, None, a, a, 1 << 30, None) == 1
-    assert lib.moe_grouped_swiglu_mlp(ctypes.byref(P(F=96)), a, a, a, a, a, a, 1 << 40,
-                                      None) == 2
+    assert lib.moe_grouped_swiglu_mlp(ctypes.byref(P(F=96)), a, None, a, a, a, None, a, a,
+                                      1 << 40, None) == 2
     assert lib.moe_unpermute_combine(ctypes.byref(P(H=12)), a, a, a, a, None) == 2
     assert lib.moe_get_device_status(None, None) == 1
 
@@ -171,8 +174,7 @@ def test_shared_experts_validation_and_workspace():
     bad = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, shared_experts=-1)
     assert moe.workspace_size(bad) == 0
     too_many = moe.Problem.make(T=64, H=256, F=512, E=8, k=8, shared_experts=25)
-    assert lib.moe_forward(ctypes.byref(too_many), a, a, a, a, a, None, None, None, a, big,
-                           None) == 2
+    assert fwd(lib, ctypes.byref(too_many), a, a, a, a, a, a, big) == 2
 
 
 def test_selftest_wait_timeout_validates(lib):
@@ -231,3 +233,37 @@ def test_backward_routed_validates(lib):
     assert f(ctypes.byref(p), a, a, a, a, a, a, a, a, a, a, a, need - 1, None) == 4
     ps = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, shared_experts=1)
     assert f(ctypes.byref(ps), a, a, a, a, a, a, a, a, a, a, a, big, None) == 1      # no shared
+
+
+def test_lowprec_stage_forms_validate(lib):
+    """moe_grouped_swiglu_mlp and moe_forward take FP8/NVFP4 operands with their
+    scales; bf16 calls must pass no scales; moe_permute_rows checks its width."""
+    a = ctypes.c_void_p(1 << 20)
+    big = 1 << 40
+    lp = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, precision=moe.PREC_FP8_NVFP4)
+    bf = P()
+    sc = moe.FP4Scales(1 << 20, 1 << 20, 1 << 20)
+    bad_sc = moe.FP4Scales(1 << 20, None, 1 << 20)
+    mlp = lib.moe_grouped_swiglu_mlp
+    # FP8: the scales struct is required and checked
+    assert mlp(ctypes.byref(lp), a, a, a, a, a, None, a, a, big, None) == 1
+    assert mlp(ctypes.byref(lp), a, a, a, a, a, ctypes.byref(bad_sc), a, a, big, None) == 1
+    assert mlp(ctypes.byref(lp), a, None, a, a, a, ctypes.byref(sc), a, a, big, None) == 1
+    ws_need = moe.workspace_size(lp)
+    assert mlp(ctypes.byref(lp), a, a, a, a, a, ctypes.byref(sc), a, a, ws_need - 1, None) == 4
+    # bf16: no scales
+    assert mlp(ctypes.byref(bf), a, a, a, a, a, None, a, a, big, None) == 1
+    assert mlp(ctypes.byref(bf), a, None, a, a, a, ctypes.byref(sc), a, a, big, None) == 1
+    # the whole layer
+    assert fwd(lib, ctypes.byref(lp), a, a, a, a, a, a, big) == 1           # no wscales
+    assert fwd(lib, ctypes.byref(lp), a, a, a, a, a, a, big, None, ctypes.byref(sc)) == 1
+    assert fwd(lib, ctypes.byref(bf), a, a, a, a, a, a, big, a) == 1        # bf16 with x_scale
+    shared = moe.Problem.make(T=64, H=256, F=512, E=8, k=2, shared_experts=1,
+                              precision=moe.PREC_FP8_NVFP4)
+    assert fwd(lib, ctypes.byref(shared), a, a, a, a, a, a, big, a, ctypes.byref(sc)) == 1
+    # row gather: a positive multiple of 4 bytes
+    rows = lib.moe_permute_rows
+    assert rows(ctypes.byref(bf), a, a, 6, a, None) == 2
+    assert rows(ctypes.byref(bf), a, a, 0, a, None) == 2
+    assert rows(ctypes.byref(bf), None, a, 8, a, None) == 1
+    assert rows(ctypes.byref(bf), a, a, 8, ctypes.c_void_p((1 << 20) + 4), None) == 3

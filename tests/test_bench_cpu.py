@@ -92,3 +92,9 @@ def test_tensor_peak_is_burst_for_short_regions_and_sustained_for_long():
     assert bench.tensor_peak(peaks, 1.1)[:2] == (1916.9, "bf16_tflops")
     assert bench.tensor_peak(peaks, bench.SUSTAINED_AFTER_S)[:2] == \
         (1719.2, "bf16_tflops_sustained")
+
+
+def test_fp8_layer_takes_the_fp8_tensor_peak():
+    peaks = {"hbm_gbs": 6775.6, "bf16_tflops": 1916.9, "bf16_tflops_sustained": 1719.2}
+    v, key, other = bench.tensor_peak(peaks, 1.0, fp8=True)
+    assert v == 2 * 1916.9 and bench.peak_of(peaks, other) == 2 * 1719.2

@@ -215,3 +215,105 @@ def test_mxfp4_full_size_sampled():
                                      interleave=shape.glu_interleave, clamp=shape.swiglu_clamp,
                                      wfmt=oracle.WFMT_MXFP4)
     check(res["out"][ti], ref["out"], "MXFP4 sampled")
+
+
+# ---------------------------------------------------------------- staged form
+
+def _prepared(shape, inp):
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True, shape.glu_interleave,
+                         shape.swiglu_clamp, precision=moe.PREC_FP8_NVFP4)
+    prepared = torch.empty(moe.prepared_scales_size(p), dtype=torch.uint8, device=DEV)
+    moe.prepare_weights(p, inp["w1s"], inp["w2s"], prepared)
+    return prepared
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KERNEL_IDS)
+@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[1], SHAPES[3]], ids=lambda s: s.name)
+def test_lowprec_stages_match_oracle_stages(shape, kernel):
+    """The staged low-precision path -- moe_permute (row maps), moe_permute_rows
+    (E4M3 code rows and their fp32 scale rows), moe_grouped_swiglu_mlp with
+    x_perm_scale and the FP4 scales, moe_unpermute_combine -- against the
+    oracle's GEMM1+SwiGLU (with the 1x128 E4M3 re-quantisation of h) and
+    GEMM2 on the oracle's own permutation."""
+    inp = mi.make_lowprec_inputs(shape, seed=3)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    idx, w = oracle.route_topk(inp["logits"], shape.k)
+    perm = oracle.permute(idx, shape.E)
+    ptok = torch.from_numpy(perm["permuted_token"]).to(torch.int64)
+    xq_perm_ref = inp["xq"][ptok.clamp(min=0)]
+    xs_perm_ref = inp["xs"][ptok.clamp(min=0)]
+    h = oracle.gemm1_swiglu_lowprec(xq_perm_ref, xs_perm_ref, perm["expert_offsets"], inp["w1q"],
+                                    inp["w1s"], inp["w1g"], shape.F, shape.glu_interleave,
+                                    shape.swiglu_clamp)
+    y_ref = oracle.gemm2_lowprec(h, perm["expert_offsets"], inp["w2q"], inp["w2s"], inp["w2g"],
+                                 shape.H)
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True, shape.glu_interleave,
+                         shape.swiglu_clamp, precision=moe.PREC_FP8_NVFP4, kernel=kernel)
+    ws = moe.alloc_workspace(p)
+    moe.clear_device_status(ws)
+    R = shape.R
+    rmap = torch.empty(shape.T, shape.k, dtype=torch.int32, device=DEV)
+    ptok_d = torch.empty(R, dtype=torch.int32, device=DEV)
+    tpe = torch.empty(shape.E, dtype=torch.int32, device=DEV)
+    off = torch.empty(shape.E + 1, dtype=torch.int32, device=DEV)
+    moe.permute(p, torch.from_numpy(idx).to(DEV), None, None, rmap, ptok_d, tpe, off, ws)
+    xq_perm = torch.full((R, shape.H), 0x7F, dtype=torch.uint8, device=DEV)
+    xs_perm = torch.full((R, shape.H // 128), float("nan"), dtype=torch.float32, device=DEV)
+    moe.permute_rows(p, ptok_d, d["xq"], xq_perm)
+    moe.permute_rows(p, ptok_d, d["xs"], xs_perm)
+    assert torch.equal(xq_perm.cpu(), xq_perm_ref)
+    assert torch.equal(xs_perm.cpu().view(torch.int32), xs_perm_ref.view(torch.int32))
+    y = torch.full((R, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    scales = (_prepared(shape, d), d["w1g"], d["w2g"])
+    moe.grouped_swiglu_mlp(p, xq_perm, off, d["w1q"], d["w2q"], y, ws, x_perm_scale=xs_perm,
+                           wscales=scales)
+    assert moe.get_device_status(ws) == 0
+    check(y, y_ref, f"lowprec y_perm[{shape.name}]")
+    out = torch.empty(shape.T, shape.H, dtype=torch.bfloat16, device=DEV)
+    moe.unpermute_combine(p, y, rmap, torch.from_numpy(w.astype(np.float32)).to(DEV), out)
+    ref = oracle.moe_forward_lowprec(inp["xq"], inp["xs"], inp["logits"], inp["w1q"], inp["w1s"],
+                                     inp["w1g"], inp["w2q"], inp["w2s"], inp["w2g"], shape.k,
+                                     interleave=shape.glu_interleave, clamp=shape.swiglu_clamp)
+    check(out, ref["out"], f"lowprec staged out[{shape.name}]")
+
+
+@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[2]], ids=lambda s: s.name)
+def test_moe_forward_at_fp8_precision_is_the_fp8_entry_point(shape):
+    """moe_forward with precision FP8_NVFP4 (x_scale and the FP4 scales) gives the
+    bits moe_forward_fp8_nvfp4 gives."""
+    inp = {k: v.to(DEV) for k, v in mi.make_lowprec_inputs(shape, seed=5).items()}
+    ref = run_lowprec(shape, inp)
+    p = moe.Problem.make(shape.T, shape.H, shape.F, shape.E, shape.k, True, shape.glu_interleave,
+                         shape.swiglu_clamp, precision=moe.PREC_FP8_NVFP4)
+    ws = moe.alloc_workspace(p)
+    out = torch.full((shape.T, shape.H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty(shape.T, shape.k, dtype=torch.int32, device=DEV)
+    moe.forward(p, inp["xq"], inp["logits"], inp["w1q"], inp["w2q"], out, ws, topk_idx=idx,
+                x_scale=inp["xs"], wscales=(ref["prepared"], inp["w1g"], inp["w2g"]))
+    torch.cuda.synchronize()
+    assert torch.equal(idx, ref["topk_idx"])
+    assert torch.equal(out.view(torch.int16), ref["out"].view(torch.int16))
+
+
+@pytest.mark.parametrize("cols,dtype", [(256, torch.uint8), (2, torch.float32),
+                                        (7168, torch.uint8), (56, torch.float32)],
+                         ids=["codes-256", "scales-8B", "codes-7168", "scales-224B"])
+def test_permute_rows_is_the_row_gather(cols, dtype):
+    """moe_permute_rows on 16-byte-multiple and 4-byte-multiple rows, with masked
+    routes: bit for bit the rows torch indexing picks by the oracle's
+    permutation, zero rows for the masked tail."""
+    T, E, k = 300, 16, 4
+    idx = mi.random_topk_idx(T, E, k, seed=9, mask_frac=0.2)
+    perm = oracle.permute(idx.numpy(), E)
+    g = torch.Generator().manual_seed(2)
+    src = torch.randint(0, 256, (T, cols * (4 if dtype == torch.float32 else 1)), generator=g,
+                        dtype=torch.uint8).view(dtype)
+    ptok = torch.from_numpy(perm["permuted_token"])
+    want = torch.zeros((T * k,) + src.shape[1:], dtype=dtype)
+    ok = ptok >= 0
+    want[ok] = src[ptok[ok].to(torch.int64)]
+    p = moe.Problem.make(T, 256, 128, E, k)
+    dst = torch.full_like(want, 7).to(DEV)
+    moe.permute_rows(p, ptok.to(DEV), src.to(DEV), dst)
+    torch.cuda.synchronize()
+    assert torch.equal(dst.cpu().view(torch.uint8), want.view(torch.uint8))
