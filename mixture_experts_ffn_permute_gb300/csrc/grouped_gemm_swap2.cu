@@ -11,7 +11,9 @@
 //   receives its 128 weight rows x N tokens.
 // So each CTA's epilogue is the 1-CTA weight-row epilogue (GEMM1 exchanges
 // gate and up rows through shared memory, 32 tokens at a time).  Tile order
-// and the cluster-scope helpers are in pair_tiles.cuh.
+// and the cluster-scope helpers are in pair_tiles.cuh; every role walks the
+// order with its own incremental iterator (no per-tile division or search
+// between K steps).
 // Synchronisation as in grouped_gemm_2cta.cu; every wait bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -133,8 +135,10 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
       int stage = 0;
       uint32_t phase = 0;
       long issued = 0;
-      for (int tile = tile0; tile < total_tiles && !*abort_flag; tile += tstride) {
-        const pair::Tile t = pair::decode(tile, sched);
+      pair::TileIter it;
+      it.init(tile0, tstride, sched);
+      for (int tile = tile0; tile < total_tiles && !*abort_flag; tile += tstride, it.next()) {
+        const pair::Tile t = it.get(sched);
         const int tok0 = t.n * kNmaxP;
         const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - tok0);
         const int half = pair::half_rows(nval);
@@ -177,10 +181,13 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
-      for (int tile = tile0; tile < total_tiles && !*abort_flag; tile += tstride, ++local) {
+      pair::TileIter it;
+      it.init(tile0, tstride, sched);
+      for (int tile = tile0; tile < total_tiles && !*abort_flag;
+           tile += tstride, ++local, it.next()) {
         const int buf = local & 1;
         const uint32_t tph = (local >> 1) & 1;
-        const pair::Tile t = pair::decode(tile, sched);
+        const pair::Tile t = it.get(sched);
         const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - t.n * kNmaxP);
         const uint32_t nmma = static_cast<uint32_t>(2 * pair::half_rows(nval));
         const uint32_t idesc = idesc_bf16_f32(2 * kMP, nmma);
@@ -218,7 +225,9 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
     const uint32_t tempty_leader0 = pair::mapa(smem_u32(&tempty[0]), 0);
     const uint32_t tempty_leader1 = pair::mapa(smem_u32(&tempty[1]), 0);
     int local = 0;
-    for (int tile = tile0; tile < total_tiles; tile += tstride, ++local) {
+    pair::TileIter it;
+    it.init(tile0, tstride, sched);
+    for (int tile = tile0; tile < total_tiles; tile += tstride, ++local, it.next()) {
       const int buf = local & 1;
       const uint32_t tph = (local >> 1) & 1;
       const bool ok = mbar_wait(&tfull[buf], tph, p.status);
@@ -227,7 +236,7 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
         break;
       }
       tc_fence_after();
-      const pair::Tile t = pair::decode(tile, sched);
+      const pair::Tile t = it.get(sched);
       const int tok0 = t.n * kNmaxP;
       const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - tok0);
       const int nchunk = (nval + 31) / 32;

@@ -49,10 +49,28 @@ struct Sched {
   const int32_t* cold_prefix;  // [E+1] tiles of cold experts before e
   const int32_t* ntk;          // [E] token tiles of e
   int E, w_tiles, nh, nc;
-  __device__ __forceinline__ int total() const { return nh + nc; }
+  __host__ __device__ __forceinline__ int total() const { return nh + nc; }
 };
 
-__device__ __forceinline__ Tile decode(int tile, const Sched& s) {
+// (m, n) of the tile at position `local` inside expert e's list.
+__host__ __device__ __forceinline__ Tile tile_in_expert(int e, bool hot, int local, int nt,
+                                                       int w_tiles) {
+  const int per_group = kGroup * w_tiles;
+  const int g = local / per_group;
+  const int within = local - g * per_group;
+  const int left = nt - g * kGroup;
+  const int gsz = left < kGroup ? left : kGroup;
+  Tile t;
+  t.e = e;
+  t.hot = hot;
+  t.m = within / gsz;
+  t.n = g * kGroup + (within - t.m * gsz);
+  return t;
+}
+
+// The tile at position `tile` of the merged order, from scratch (two 64-bit
+// divisions and a binary search over the experts).
+__host__ __device__ __forceinline__ Tile decode(int tile, const Sched& s) {
   const long long n = static_cast<long long>(s.nh) + s.nc;
   const int hb = static_cast<int>(static_cast<long long>(tile) * s.nh / n);
   const int ha = static_cast<int>(static_cast<long long>(tile + 1) * s.nh / n);
@@ -64,19 +82,64 @@ __device__ __forceinline__ Tile decode(int tile, const Sched& s) {
     const int mid = (lo + hi + 1) >> 1;
     if (pf[mid] <= idx) lo = mid; else hi = mid - 1;
   }
-  Tile t;
-  t.e = lo;
-  t.hot = hot;
-  const int local = idx - pf[lo];
-  const int nt = s.ntk[lo];
-  const int per_group = kGroup * s.w_tiles;
-  const int g = local / per_group;
-  const int within = local - g * per_group;
-  const int gsz = min(kGroup, nt - g * kGroup);
-  t.m = within / gsz;
-  t.n = g * kGroup + (within - t.m * gsz);
-  return t;
+  return tile_in_expert(lo, hot, idx - pf[lo], s.ntk[lo], s.w_tiles);
 }
+
+// The tiles one CTA pair visits -- first, first + stride, first + 2 stride,
+// ... -- each exactly as decode() gives it, but in O(1) amortised per tile,
+// which matters because the producer, the MMA issuer and the epilogue each
+// walk the sequence between their K steps.  The merge position is kept as a
+// running quotient hb = floor(tile nh / N) and remainder r = tile nh mod N
+// (tile is hot iff r + nh >= N), and each list's expert by a forward scan: a
+// list's index never decreases along the sequence (hb grows by
+// floor(stride nh / N) or one more, the cold index tile - hb by the rest).
+struct TileIter {
+  int tile, stride;
+  long long n;        // nh + nc
+  int nh, hb, q_s;    // floor(stride nh / N)
+  long long r, r_s;   // tile nh mod N, stride nh mod N
+  int e_hot, e_cold;  // expert cursors of the two lists
+
+  __host__ __device__ __forceinline__ void init(int first, int step, const Sched& s) {
+    tile = first;
+    stride = step;
+    nh = s.nh;
+    n = static_cast<long long>(s.nh) + s.nc;
+    e_hot = 0;
+    e_cold = 0;
+    if (n == 0) {
+      hb = q_s = 0;
+      r = r_s = 0;
+      return;
+    }
+    const long long a = static_cast<long long>(first) * s.nh;
+    const long long b = static_cast<long long>(step) * s.nh;
+    hb = static_cast<int>(a / n);
+    r = a - static_cast<long long>(hb) * n;
+    q_s = static_cast<int>(b / n);
+    r_s = b - static_cast<long long>(q_s) * n;
+  }
+
+  __host__ __device__ __forceinline__ Tile get(const Sched& s) {
+    const bool hot = r + nh >= n;
+    const int idx = hot ? hb : tile - hb;
+    const int32_t* pf = hot ? s.hot_prefix : s.cold_prefix;
+    int e = hot ? e_hot : e_cold;
+    while (e + 1 < s.E && pf[e + 1] <= idx) ++e;
+    if (hot) e_hot = e; else e_cold = e;
+    return tile_in_expert(e, hot, idx - pf[e], s.ntk[e], s.w_tiles);
+  }
+
+  __host__ __device__ __forceinline__ void next() {
+    tile += stride;
+    hb += q_s;
+    r += r_s;
+    if (r >= n) {
+      r -= n;
+      ++hb;
+    }
+  }
+};
 
 // Fills ntk[E], hot_prefix[E+1], cold_prefix[E+1] (shared memory) from the
 // expert offsets off[E+1] (shared memory); every thread of the block calls it.
