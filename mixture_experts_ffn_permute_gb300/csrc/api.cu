@@ -394,8 +394,8 @@ int run_backward_core(const moe_problem* p, const moe_problem* q, const BwdLayou
   void* dact = at<void>(ws, B.dact);  // [R, 2F] bf16 their gradient
   float* w_perm = at<float>(ws, B.w_perm);
   float* dw_part = at<float>(ws, B.dw_part);
-  MOE_LAUNCH(launch_gather_rows(x, ptok, R, H, x_perm, s));
-  MOE_LAUNCH(launch_gather_rows(d_out, ptok, R, H, dy, s));
+  MOE_LAUNCH(launch_scatter_rows(x, rmap, off, q->T, q->k, q->E, H, x_perm, s));
+  MOE_LAUNCH(launch_scatter_rows(d_out, rmap, off, q->T, q->k, q->E, H, dy, s));
   MOE_LAUNCH(launch_weights_to_rows(rmap, wts, R, w_perm, s));
   tm.mark(call, 3, s);
   // pre-activations a = x W1_e^T in fp32, recomputed rather than kept from
@@ -705,7 +705,8 @@ int moe_permute(const moe_problem* p, const int32_t* topk_idx, const void* x, vo
                    at<int32_t>(ws, L.mtile_prefix), ws, L, s, launches);
   if (rc != MOE_OK) return rc;
   if (x_perm && p->T > 0)
-    MOE_LAUNCH(launch_gather_rows(x, permuted_token, p->T * p->k, p->H, x_perm, s));
+    MOE_LAUNCH(launch_scatter_rows(x, row_id_map, expert_offsets, p->T, p->k, p->E, p->H, x_perm,
+                                   s));
   g_launches = launches;
   return MOE_OK;
 }
@@ -881,7 +882,8 @@ int moe_forward(const moe_problem* p, const void* x, const float* x_scale, const
       if (decode_fused)
         MOE_LAUNCH(cudaMemsetAsync(dctr, 0, sizeof(int32_t) * static_cast<size_t>(n_dctr), s));
     }
-    if (!fuse_gather && !decode_fused) MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
+    if (!fuse_gather && !decode_fused)
+      MOE_LAUNCH(launch_scatter_rows(x, rmap, off, q->T, q->k, q->E, q->H, x_perm, s));
   }
   tm.mark(call, 5, s);
   if (decode_fused) {
@@ -961,7 +963,7 @@ int moe_forward_routed(const moe_problem* p, const void* x, const int32_t* topk_
   // the validating permutation: masked, out-of-range and repeated routes
   rc = run_permute(p, topk_idx, rmap, ptok, tpe, off, mtp, ws, L, s, launches);
   if (rc != MOE_OK) return rc;
-  MOE_LAUNCH(launch_gather_rows(x, ptok, R, p->H, x_perm, s));
+  MOE_LAUNCH(launch_scatter_rows(x, rmap, off, p->T, p->k, p->E, p->H, x_perm, s));
   rc = run_mlp(p, x_perm, off, mtp, w1, w2, h, y, status, s, launches);
   if (rc != MOE_OK) return rc;
   MOE_LAUNCH(launch_combine(y, rmap, topk_w, p->T, p->H, p->k, out, s));

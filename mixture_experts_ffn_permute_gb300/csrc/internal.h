@@ -121,6 +121,12 @@ cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
 cudaError_t launch_gather_rows(const void* x, const int32_t* permuted_token, int R, int H,
                                void* x_perm, cudaStream_t s);
 
+// The same rows written from the source side: x_perm[row_id_map[t][j]] =
+// x[t] (each token row read once), zero rows for [expert_offsets[E], T*k).
+cudaError_t launch_scatter_rows(const void* x, const int32_t* row_id_map,
+                                const int32_t* expert_offsets, int T, int k, int E, int H,
+                                void* x_perm, cudaStream_t s);
+
 // dst[r] = src[permuted_token[r]] for rows of row_bytes bytes (a multiple of
 // 4); zero row for -1 or a token outside [0, T).
 cudaError_t launch_gather_row_bytes(const void* src, const int32_t* permuted_token, int R, int T,

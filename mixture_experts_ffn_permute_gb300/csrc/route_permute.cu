@@ -12,6 +12,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "../../include/moe_ffn.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -288,6 +289,42 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
   }
 }
 
+// x_perm[row_id_map[t][j]] = x[t] for every valid route, driven by the
+// source: each token row is read once and written to its (up to k) permuted
+// rows, so the copy reads T rows instead of T * k (one HBM read of x rather
+// than k).  Rows from expert_offsets[E] to R (the masked tail, no token) are
+// zeroed.  One CTA per token at a time; the token's row indices are staged in
+// shared memory.
+__global__ void __launch_bounds__(256)
+scatter_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_id_map,
+                    const int32_t* __restrict__ expert_offsets, int T, int k, int E, int R,
+                    int vecs_per_row, uint4* __restrict__ x_perm) {
+  pdl_enter();
+  __shared__ int32_t s_rows[MOE_MAX_TOPK];
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    if (threadIdx.x < k) {
+      const int32_t r = row_id_map[static_cast<size_t>(t) * k + threadIdx.x];
+      s_rows[threadIdx.x] = (r >= 0 && r < R) ? r : -1;
+    }
+    __syncthreads();
+    const uint4* src = x + static_cast<size_t>(t) * vecs_per_row;
+    for (int v = threadIdx.x; v < vecs_per_row; v += blockDim.x) {
+      const uint4 val = __ldcs(src + v);  // read once: streaming
+      for (int j = 0; j < k; ++j) {
+        const int32_t r = s_rows[j];
+        if (r >= 0) x_perm[static_cast<size_t>(r) * vecs_per_row + v] = val;
+      }
+    }
+    __syncthreads();
+  }
+  const int first = min(max(expert_offsets[E], 0), R);
+  const size_t n = static_cast<size_t>(R - first) * vecs_per_row;
+  uint4* tail = x_perm + static_cast<size_t>(first) * vecs_per_row;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    tail[i] = make_uint4(0, 0, 0, 0);
+}
+
 // The same for rows of any width that is a multiple of 4 bytes: 16-byte
 // copies when the width allows, 4-byte copies otherwise; token indices
 // outside [0, T) give zero rows.
@@ -549,6 +586,16 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* permuted_token, int
   return launch_kernel(gather_rows_kernel, dim3(blocks), dim3(256), 0, s, 1,
                        static_cast<const uint4*>(x), permuted_token, R, vecs,
                        static_cast<uint4*>(x_perm));
+}
+
+cudaError_t launch_scatter_rows(const void* x, const int32_t* row_id_map,
+                                const int32_t* expert_offsets, int T, int k, int E, int H,
+                                void* x_perm, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = min(T, num_sms() * 8);
+  return launch_kernel(scatter_rows_kernel, dim3(blocks), dim3(256), 0, s, 1,
+                       static_cast<const uint4*>(x), row_id_map, expert_offsets, T, k, E, T * k,
+                       H / 8, static_cast<uint4*>(x_perm));
 }
 
 cudaError_t launch_gather_row_bytes(const void* src, const int32_t* permuted_token, int R, int T,
