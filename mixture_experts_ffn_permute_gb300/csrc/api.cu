@@ -39,10 +39,10 @@ constexpr int kFwdStages = 8;
 constexpr int kBwdStages = 10;
 constexpr int kMaxStages = 10;
 const char* const kStageNames[kFwdStages] = {"route_topk", "chunk_histogram", "scan",
-                                             "scatter",    "gather_rows",     "gemm1_swiglu",
+                                             "scatter",    "permute_rows",    "gemm1_swiglu",
                                              "gemm2",      "combine"};
 const char* const kBwdStageNames[kBwdStages] = {
-    "route_topk",    "permute", "gather_rows", "gemm1_recompute", "dgrad_h_swiglu",
+    "route_topk",    "permute", "permute_rows", "gemm1_recompute", "dgrad_h_swiglu",
     "wgrad_w2",      "dgrad_x", "wgrad_w1",    "combine_dx",      "router_backward"};
 
 // Event ring for moe_stage_timing_begin/end (one row of kMaxStages+1 events
