@@ -951,7 +951,6 @@ int moe_forward_routed(const moe_problem* p, const void* x, const int32_t* topk_
   MOE_REQUIRE_PTR(topk_idx);
   MOE_REQUIRE_PTR(topk_w);
   MOE_REQUIRE_PTR(out);
-  const int R = p->T * p->k;
   int32_t* off = at<int32_t>(ws, L.expert_offsets);
   int32_t* mtp = at<int32_t>(ws, L.mtile_prefix);
   int32_t* rmap = at<int32_t>(ws, L.row_id_map);

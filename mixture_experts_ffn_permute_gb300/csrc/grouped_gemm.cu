@@ -491,6 +491,41 @@ bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 }
 
 
+// bf16 [rows, cols] viewed as 64-column planes {64, rows, cols / 64}: a box
+// of box_rows rows x 2 planes (two 64-deep K steps) lands as two consecutive
+// 128-byte-swizzled K-major tiles, and every row of it is one 256-byte
+// segment of global memory.
+bool make_map_kplanes(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc || cols % 128 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same planes for two 64-row blocks `gap` rows apart (a GLU's gate and up
+// rows): {64, rows - gap, 2, cols / 64} with boxes of 64 rows x both blocks
+// x 2 planes, so each plane holds the 64 + 64 rows as one 128-row tile.
+bool make_map_kplanes_pair(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint64_t gap) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc || cols % 128 != 0 || gap == 0 || gap >= rows) return false;
+  cuuint64_t dims[4] = {64, rows - gap, 2, cols / 64};
+  cuuint64_t strides[3] = {cols * 2, gap * cols * 2, 128};
+  cuuint32_t box[4] = {64, 64, 2, 2};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 [rows, cols] map with box_cols x box_rows boxes and no swizzle (tiles
 // staged row-major in shared memory, e.g. for bulk-tensor stores).
 bool make_map_2d_plain(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,

@@ -14,7 +14,20 @@
 // and the cluster-scope helpers are in pair_tiles.cuh; every role walks the
 // order with its own incremental iterator (no per-tile division or search
 // between K steps).
-// Synchronisation as in grouped_gemm_2cta.cu; every wait bounded.
+//
+// Operands move in stages of two 64-deep K steps (three stages of 32 KB of
+// weights + up to 32 KB of tokens per CTA): one 4-D bulk-tensor copy brings a
+// CTA's 128 weight rows (two 64-row blocks a fixed gap apart) for both K
+// steps and one 3-D copy its token rows, each row a 256-byte segment of
+// global memory.  A TMA unit keeps a bounded number of row requests in
+// flight, so 256-byte rows stream about twice as fast per SM as the 128-byte
+// rows of a 64-column box, and the producer issues a third of the copies.
+//
+// Synchronisation: both CTAs' copies complete on the leader's full barrier
+// (the leader's producer expects both CTAs' bytes); the leader's MMA commits
+// release the stage on both CTAs' empty barriers and the accumulator on both
+// CTAs' tfull barriers; every epilogue thread of both CTAs arrives on the
+// leader's tempty barrier.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -28,17 +41,23 @@
 
 namespace moe {
 
-bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                 uint32_t box_rows);  // grouped_gemm.cu
+bool make_map_kplanes(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows);  // grouped_gemm.cu
+bool make_map_kplanes_pair(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint64_t gap);  // grouped_gemm.cu
 
 namespace {
 
 constexpr int kThreadsP = 192;
 constexpr int kMP = pair::kM;                  // weight rows per CTA
 constexpr int kNmaxP = pair::kNmax;            // token rows per pair tile
-constexpr int kStagesP = 6;
-constexpr uint32_t kWBytesP = kMP * kBK * 2;   // 16 KB
-constexpr uint32_t kXBytesP = (kNmaxP / 2) * kBK * 2;  // 16 KB: this CTA's token half
+// A stage is two 64-deep K steps: every weight and token row of it is one
+// 256-byte segment of global memory, so one bulk-tensor copy moves twice the
+// bytes of a 64-column box for the same number of row requests.
+constexpr int kBKS = 2 * kBK;
+constexpr int kStagesP = 3;
+constexpr uint32_t kWBytesP = kMP * kBKS * 2;   // 32 KB
+constexpr uint32_t kXBytesP = (kNmaxP / 2) * kBKS * 2;  // 32 KB: this CTA's token half
 constexpr uint32_t kStageP = kWBytesP + kXBytesP;
 constexpr uint32_t kTmemColsP = 2 * kNmaxP;
 constexpr int kMaxEP = 1024;
@@ -124,7 +143,7 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
   const int total_tiles = sched.total();
   const int tile0 = static_cast<int>(blockIdx.x >> 1);
   const int tstride = static_cast<int>(gridDim.x >> 1);
-  const int num_kb = p.K / kBK;
+  const int num_kb = p.K / kBKS;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer (both CTAs)
@@ -147,21 +166,18 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
         const CUtensorMap* mx = bi == 0 ? &map_x16 : bi == 1 ? &map_x32 : bi == 2 ? &map_x64
                                                                                   : &map_x128;
         const int x_row = s_off[t.e] + tok0 + static_cast<int>(rank) * half;
-        int w_row0, w_row1;
+        int w_row0, w_row1;  // the second block is the map's fixed gap further
         pair::weight_rows(kEpi == Epi::kSwiGLU, t.m, rank, p.F, p.interleave, w_row0, w_row1);
         w_row0 += t.e * p.w_rows_per_expert;
-        w_row1 += t.e * p.w_rows_per_expert;
-        const uint32_t bytes = kWBytesP + static_cast<uint32_t>(box) * kBK * 2;
+        const uint32_t bytes = kWBytesP + static_cast<uint32_t>(box) * kBKS * 2;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) { *abort_flag = 1; break; }
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
           const uint32_t bar = pair::mapa(smem_u32(&full[stage]), 0);
-          const int kx = kb * kBK;
-          uint8_t* w_dst = sW + stage * kWBytesP;
+          const int plane = 2 * kb;
           const uint64_t pw = t.hot ? pol_w : pol_w_once;
-          pair::tma_load(w_dst, &map_w, kx, w_row0, bar, pw);
-          pair::tma_load(w_dst + kWBytesP / 2, &map_w, kx, w_row1, bar, pw);
-          pair::tma_load(sX + stage * kXBytesP, mx, kx, x_row, bar, pol_x);
+          pair::tma_load_4d(sW + stage * kWBytesP, &map_w, 0, w_row0, 0, plane, bar, pw);
+          pair::tma_load_3d(sX + stage * kXBytesP, mx, 0, x_row, plane, bar, pol_x);
           ++issued;
           if (++stage == kStagesP) { stage = 0; phase ^= 1; }
         }
@@ -189,8 +205,11 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
         const uint32_t tph = (local >> 1) & 1;
         const pair::Tile t = it.get(sched);
         const int nval = min(kNmaxP, s_off[t.e + 1] - s_off[t.e] - t.n * kNmaxP);
-        const uint32_t nmma = static_cast<uint32_t>(2 * pair::half_rows(nval));
+        const int half = pair::half_rows(nval);
+        const uint32_t nmma = static_cast<uint32_t>(2 * half);
         const uint32_t idesc = idesc_bf16_f32(2 * kMP, nmma);
+        // the token box's second plane follows its first (box rows x 128 B)
+        const uint32_t x_plane = (16u << pair::box_index(half)) * kBK * 2;
         if (!mbar_wait(&tempty[buf], tph ^ 1, p.status)) { *abort_flag = 1; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kNmaxP;
@@ -198,11 +217,16 @@ grouped_gemm_swap2_kernel(const __grid_constant__ CUtensorMap map_w,
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t w_desc = sw128_kmajor_desc(smem_u32(sW + stage * kWBytesP));
-          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + stage * kXBytesP));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            pair::mma(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
+          for (int pl = 0; pl < 2; ++pl) {
+            const uint64_t w_desc =
+                sw128_kmajor_desc(smem_u32(sW + stage * kWBytesP + pl * (kWBytesP / 2)));
+            const uint64_t x_desc =
+                sw128_kmajor_desc(smem_u32(sX + stage * kXBytesP + pl * x_plane));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              pair::mma(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | pl | kk) != 0);
+          }
           pair::commit_both(&empty[stage]);
           if (++stage == kStagesP) { stage = 0; phase ^= 1; }
         }
@@ -314,15 +338,19 @@ cudaError_t launch_swap2_impl(const CUtensorMap* maps, const PParams& pp, int gr
 
 cudaError_t launch_grouped_gemm_swap2(const GroupedGemmArgs& g, cudaStream_t s) {
   if (g.a_rows == 0) return cudaSuccess;
-  if (g.E > kMaxEP) return cudaErrorInvalidValue;
+  if (g.E > kMaxEP || g.K % kBKS != 0) return cudaErrorInvalidValue;
+  // rows between a CTA's two 64-row weight blocks (pair::weight_rows)
+  uint64_t gap = 64;
+  if (g.epi == Epi::kSwiGLU && g.interleave == 0) gap = static_cast<uint64_t>(g.F);
+  else if (g.epi == Epi::kSwiGLU && g.interleave > 64) gap = static_cast<uint64_t>(g.interleave);
   CUtensorMap maps[5];
-  if (!make_map_2d(&maps[0], g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
-                   static_cast<uint64_t>(g.K), 64))
+  if (!make_map_kplanes_pair(&maps[0], g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
+                             static_cast<uint64_t>(g.K), gap))
     return cudaErrorInvalidValue;
   const uint32_t boxes[4] = {16, 32, 64, 128};
   for (int i = 0; i < 4; ++i)
-    if (!make_map_2d(&maps[1 + i], g.a, static_cast<uint64_t>(g.a_rows),
-                     static_cast<uint64_t>(g.K), boxes[i]))
+    if (!make_map_kplanes(&maps[1 + i], g.a, static_cast<uint64_t>(g.a_rows),
+                          static_cast<uint64_t>(g.K), boxes[i]))
       return cudaErrorInvalidValue;
   PParams pp;
   pp.expert_offsets = g.expert_offsets;
