@@ -47,7 +47,10 @@
 //
 // Warp roles (224 threads, one CTA per SM):
 //   warp 0      tile claims (a 4-deep tile queue in shared memory) and the
-//               weight TMA loads (10-stage ring of 16 KB)
+//               weight TMA loads (5-stage ring of 32 KB, two 64-deep K steps
+//               per stage: one 4-D copy of the tile's two 64-row blocks, each
+//               row a 256-byte segment, so the SM's copy path -- which counts
+//               row requests -- streams twice the bytes of 64-column boxes)
 //   warp 1      TMEM allocation + single-thread tcgen05.mma issue
 //   warps 2..5  epilogue (tcgen05.ld -> SwiGLU / bf16 -> global stores)
 //   warp 6      token-row TMA loads (6-stage ring of 4 KB): GEMM1 gathers its
@@ -67,6 +70,8 @@
 
 namespace moe {
 
+bool make_map_kplanes_pair(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint64_t gap);  // grouped_gemm.cu
 bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);  // grouped_gemm.cu
 
@@ -75,11 +80,11 @@ namespace {
 constexpr int kM = 128;              // weight rows per tile
 constexpr int kN = 32;               // token rows per tile (max)
 constexpr int kThreadsD = 224;
-constexpr int kWStagesD = 10;
+constexpr int kWStagesD = 5;         // x 2 K steps
 constexpr int kXStagesD = 6;
 constexpr int kQueue = 4;
 constexpr int kClaimLead = 2;        // stages before a tile's last load that the next is claimed
-constexpr uint32_t kWBytesD = kM * kBK * 2;   // 16 KB
+constexpr uint32_t kWBytesD = 2 * kM * kBK * 2;   // 32 KB: two K steps
 constexpr uint32_t kXBytesD = kN * kBK * 2;   // 4 KB
 constexpr uint32_t kRingBytesD = kWStagesD * kWBytesD + kXStagesD * kXBytesD;
 constexpr uint32_t kTmemColsD = 2 * kN;
@@ -345,19 +350,19 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
           w_row0 = t.e * p.H + t.m * kM;
           w_row1 = w_row0 + kM / 2;
         }
-        const int claim_at = max(num_kb - kClaimLead, kWStagesD);
+        (void)w_row1;  // the map's second block is its fixed gap further
+        const int num_ks = num_kb / 2;  // stages of two K steps
+        const int claim_at = max(num_ks - kClaimLead, kWStagesD);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int ks = 0; ks < num_ks; ++ks) {
           if (!mbar_wait(&w_empty[sw], pw ^ 1, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&w_full[sw], kWBytesD);
-          uint8_t* dst = sW + sw * kWBytesD;
-          tma_load_2d(dst, mw, kb * kBK, w_row0, &w_full[sw], pol_w);
-          tma_load_2d(dst + kWBytesD / 2, mw, kb * kBK, w_row1, &w_full[sw], pol_w);
+          tma_load_4d(sW + sw * kWBytesD, mw, 0, w_row0, 0, 2 * ks, &w_full[sw], pol_w);
           ++issued;
           if (++sw == kWStagesD) { sw = 0; pw ^= 1; }
-          if (kb == claim_at) claimed = atomicAdd(next_tile, 1);
+          if (ks == claim_at) claimed = atomicAdd(next_tile, 1);
         }
-        if (ok && claim_at >= num_kb) claimed = atomicAdd(next_tile, 1);
+        if (ok && claim_at >= num_ks) claimed = atomicAdd(next_tile, 1);
         if (!ok) { *abort_flag = 1; break; }
       }
       // no bulk copy may still be writing this CTA's shared memory at exit
@@ -467,19 +472,24 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
         const uint32_t d_tmem = tmem_base + buf * kN;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&w_full[sw], pw, p.status) || !mbar_wait(&x_full[sx], px, p.status)) {
+          const int plane = kb & 1;  // K step inside the weight stage
+          if ((plane == 0 && !mbar_wait(&w_full[sw], pw, p.status)) ||
+              !mbar_wait(&x_full[sx], px, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t w_desc = sw128_kmajor_desc(smem_u32(sW + sw * kWBytesD));
+          const uint64_t w_desc =
+              sw128_kmajor_desc(smem_u32(sW + sw * kWBytesD + plane * (kWBytesD / 2)));
           const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + sx * kXBytesD));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
-          mma_commit(&w_empty[sw]);
+          if (plane == 1) {
+            mma_commit(&w_empty[sw]);
+            if (++sw == kWStagesD) { sw = 0; pw ^= 1; }
+          }
           mma_commit(&x_empty[sx]);
-          if (++sw == kWStagesD) { sw = 0; pw ^= 1; }
           if (++sx == kXStagesD) { sx = 0; px ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
@@ -638,13 +648,18 @@ int decode_mlp_counters(int T, int E, int H) { return 2 + E + T * (H / kM); }
 
 cudaError_t launch_grouped_mlp_decode(const DecodeMlpArgs& g, cudaStream_t s) {
   if (g.R == 0) return cudaSuccess;
-  if (g.E > kMaxED || g.H % kM != 0 || g.F % (kM / 2) != 0) return cudaErrorInvalidValue;
+  // weight stages hold two 64-deep K steps: H and F are multiples of 128
+  if (g.E > kMaxED || g.H % kM != 0 || g.F % kM != 0) return cudaErrorInvalidValue;
+  // rows between a GEMM1 tile's 64 gate and 64 up rows (the producer's w_row1 - w_row0)
+  uint64_t gap1 = kM / 2;
+  if (g.interleave == 0) gap1 = static_cast<uint64_t>(g.F);
+  else if (g.interleave != 32) gap1 = static_cast<uint64_t>(g.interleave);
   CUtensorMap mw1, mx, mw2, mh;
-  if (!make_map_2d(&mw1, g.w1, static_cast<uint64_t>(g.E) * 2 * g.F, static_cast<uint64_t>(g.H),
-                   kM / 2) ||
+  if (!make_map_kplanes_pair(&mw1, g.w1, static_cast<uint64_t>(g.E) * 2 * g.F,
+                             static_cast<uint64_t>(g.H), gap1) ||
       !make_map_2d(&mx, g.x, static_cast<uint64_t>(g.T), static_cast<uint64_t>(g.H), 1) ||
-      !make_map_2d(&mw2, g.w2, static_cast<uint64_t>(g.E) * g.H, static_cast<uint64_t>(g.F),
-                   kM / 2) ||
+      !make_map_kplanes_pair(&mw2, g.w2, static_cast<uint64_t>(g.E) * g.H,
+                             static_cast<uint64_t>(g.F), kM / 2) ||
       !make_map_2d(&mh, g.h, static_cast<uint64_t>(g.R), static_cast<uint64_t>(g.F), kN))
     return cudaErrorInvalidValue;
   DParams p;
