@@ -22,27 +22,14 @@ namespace {
 
 constexpr int kRouteWarps = 8;
 
-struct Cand {
-  float v;
-  int id;  // INT_MAX = none
-};
-
-// (value descending, id ascending); "none" loses to everything.
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-  if (b.id == INT_MAX) return a.id != INT_MAX;
-  if (a.id == INT_MAX) return false;
-  return a.v > b.v || (a.v == b.v && a.id < b.id);
-}
-
-__device__ __forceinline__ Cand warp_best(Cand c) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    Cand o;
-    o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
-    o.id = __shfl_xor_sync(0xffffffffu, c.id, off);
-    if (better(o, c)) c = o;
-  }
-  return c;
+// Selection key of expert e with logit v: larger logit first, ties to the
+// lower id.  The high word is the logit's bits mapped to an unsigned order
+// (-0 counted as +0, so the two compare equal); the low word is ~e.  Two warp
+// max-reductions (high word, then low word among the lanes holding that
+// high word) find the best key of the warp.  NaN logits are not supported.
+__device__ __forceinline__ uint32_t order_bits(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -61,27 +48,55 @@ __device__ __forceinline__ void route_token(const float* __restrict__ src, float
                                             int32_t* __restrict__ idx_out,
                                             float* __restrict__ w_out, int32_t* s_idx) {
   const int per_lane = (E + 31) >> 5;
-  for (int e = lane; e < E; e += 32) row[e] = __ldg(src + e);
+  // stage the logits: eight independent loads per lane before any store, so
+  // a token costs one memory round trip per 256 experts, not one per 32
+  for (int e0 = 0; e0 < E; e0 += 256) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + lane + 32 * i;
+      v[i] = e < E ? __ldg(src + e) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + lane + 32 * i;
+      if (e < E) row[e] = v[i];
+    }
+  }
   __syncwarp();
-  uint32_t taken = 0;
-  Cand mine{0.f, INT_MAX};
+  // each lane's best remaining expert (hi = 0: none left)
+  uint32_t taken = 0, hi = 0, lo = 0;
+  for (int i = 0; i < per_lane; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const uint32_t h = order_bits(row[e]), l = ~static_cast<uint32_t>(e);
+      if (h > hi || (h == hi && l > lo)) { hi = h; lo = l; }
+    }
+  }
+  int mine_id = -1;
   float top = 0.f;
   for (int j = 0; j < k; ++j) {
-    Cand c{0.f, INT_MAX};
-    for (int i = 0; i < per_lane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !(taken & (1u << i))) {
-        Cand o{row[e], e};
-        if (better(o, c)) c = o;
+    const uint32_t best_hi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t best_lo = __reduce_max_sync(0xffffffffu, hi == best_hi ? lo : 0u);
+    const int id = static_cast<int>(~best_lo);
+    if (lane == j) mine_id = id;
+    if (j == 0) top = row[id];
+    if ((id & 31) == lane) {  // the winner's lane takes the next of its experts
+      taken |= 1u << (id >> 5);
+      hi = 0;
+      lo = 0;
+      for (int i = 0; i < per_lane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !(taken & (1u << i))) {
+          const uint32_t h = order_bits(row[e]), l = ~static_cast<uint32_t>(e);
+          if (h > hi || (h == hi && l > lo)) { hi = h; lo = l; }
+        }
       }
     }
-    c = warp_best(c);
-    if (c.id != INT_MAX && (c.id & 31) == lane) taken |= 1u << (c.id >> 5);
-    if (lane == j) mine = c;
-    if (j == 0) top = c.v;
   }
+  const float mine_v = lane < k ? row[mine_id] : 0.f;
   // weights: exp(l - l_top) normalised over the selected (or all) experts
-  float ex = (lane < k) ? expf(mine.v - top) : 0.f;
+  float ex = (lane < k) ? expf(mine_v - top) : 0.f;
   float denom;
   if (renormalize) {
     denom = warp_sum(ex);
@@ -91,9 +106,9 @@ __device__ __forceinline__ void route_token(const float* __restrict__ src, float
     denom = warp_sum(part);
   }
   if (lane < k) {
-    idx_out[lane] = mine.id;
+    idx_out[lane] = mine_id;
     w_out[lane] = ex / denom;
-    if (s_idx) s_idx[lane] = mine.id;
+    if (s_idx) s_idx[lane] = mine_id;
   }
   if (lane < S) {
     idx_out[k + lane] = E + lane;
@@ -187,39 +202,80 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
   return excl;
 }
 
-// One CTA of 1024 threads; thread e owns expert e.
+// One CTA of 1024 threads.  Thread (g, e) = (tid / E, tid % E) owns expert e
+// in the g-th of G = 1024 / E runs of chunks: pass 1 sums its run (loads
+// batched 16 at a time, so a run costs a few memory round trips), the runs
+// and then the experts are scanned in shared memory, and pass 2 rewrites the
+// run's counts as global row bases (expert offset + rows of earlier chunks).
+constexpr int kScanBatch = 16;
 __global__ void __launch_bounds__(1024)
 scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E, int R,
             int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ expert_offsets,
             int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ permuted_token) {
   pdl_enter();
   __shared__ int s_warp[32];
-  const int e = threadIdx.x;
-  int count = 0;
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      int32_t* p = chunk_counts + static_cast<size_t>(c) * E + e;
-      const int v = *p;
-      *p = count;  // exclusive within the expert
-      count += v;
+  __shared__ int s_run[1024];   // [g][e]: the run's count, then its exclusive prefix
+  __shared__ int s_eoff[1024];  // [e]: the expert's first row
+  const int tid = threadIdx.x;
+  const int G = max(1, 1024 / max(E, 1));
+  const int g = tid / max(E, 1), e = tid - g * max(E, 1);
+  const bool active = E > 0 && g < G;
+  const int per = (nchunks + G - 1) / G;
+  const int c0 = min(nchunks, g * per), c1 = min(nchunks, c0 + per);
+  int run = 0;
+  if (active) {
+    for (int c = c0; c < c1; c += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int i = 0; i < kScanBatch; ++i)
+        v[i] = c + i < c1 ? chunk_counts[static_cast<size_t>(c + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < kScanBatch; ++i) run += v[i];
+    }
+    s_run[tid] = run;
+  }
+  __syncthreads();
+  int count = 0;  // the expert's total (threads of run 0)
+  if (active && g == 0) {
+    for (int q = 0; q < G; ++q) {
+      const int r = s_run[q * E + e];
+      s_run[q * E + e] = count;
+      count += r;
     }
   }
   int total = 0;
-  const int off = block_exclusive_scan(e < E ? count : 0, s_warp, &total);
+  const bool owner = active && g == 0;
+  const int off = block_exclusive_scan(owner ? count : 0, s_warp, &total);
   const int mt = (count + kBM - 1) / kBM;
   int mt_total = 0;
-  const int mt_off = block_exclusive_scan(e < E ? mt : 0, s_warp, &mt_total);
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) chunk_counts[static_cast<size_t>(c) * E + e] += off;
+  const int mt_off = block_exclusive_scan(owner ? mt : 0, s_warp, &mt_total);
+  if (owner) {
     tokens_per_expert[e] = count;
     expert_offsets[e] = off;
     mtile_prefix[e] = mt_off;
+    s_eoff[e] = off;
   }
-  if (e == 0) {
+  if (tid == 0) {
     expert_offsets[E] = total;
     mtile_prefix[E] = mt_total;
   }
-  for (int r = total + e; r < R; r += blockDim.x) permuted_token[r] = -1;
+  __syncthreads();
+  if (active) {
+    // the run's first row: the expert's offset plus the earlier runs' rows
+    int base = s_eoff[e] + s_run[g * E + e];
+    for (int c = c0; c < c1; c += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int i = 0; i < kScanBatch; ++i)
+        v[i] = c + i < c1 ? chunk_counts[static_cast<size_t>(c + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < kScanBatch; ++i) {
+        if (c + i < c1) chunk_counts[static_cast<size_t>(c + i) * E + e] = base;
+        base += v[i];
+      }
+    }
+  }
+  for (int r = total + tid; r < R; r += blockDim.x) permuted_token[r] = -1;
 }
 
 // One warp per chunk.  Routes are visited in (token, slot) order, 32 at a
@@ -233,21 +289,35 @@ scatter_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
                int32_t* __restrict__ permuted_token) {
   pdl_enter();
   extern __shared__ int32_t s_next[];
+  int32_t* s_idx = s_next + E;  // the chunk's routes, staged once
   const int chunk = blockIdx.x, lane = threadIdx.x;
   const int t0 = chunk * kChunkTokens;
   const int nt = min(kChunkTokens, T - t0);
-  for (int e = lane; e < E; e += 32) s_next[e] = chunk_base[static_cast<size_t>(chunk) * E + e];
-  __syncwarp();
   const int nr = nt * k;
   const size_t base = static_cast<size_t>(t0) * k;
+  for (int e = lane; e < E; e += 32) s_next[e] = chunk_base[static_cast<size_t>(chunk) * E + e];
+  for (int r0 = 0; r0 < nr; r0 += 8 * 32) {  // eight independent loads per lane at a time
+    int v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = r0 + lane + 32 * i;
+      v[i] = r < nr ? topk_idx[base + r] : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = r0 + lane + 32 * i;
+      if (r < nr) s_idx[r] = v[i];
+    }
+  }
+  __syncwarp();
   for (int r0 = 0; r0 < nr; r0 += 32) {
     const int r = r0 + lane;
     int e = -1;
     if (r < nr) {
-      e = topk_idx[base + r];
+      e = s_idx[r];
       const int t = r / k, j = r - t * k;
       bool dup = false;
-      for (int jj = 0; jj < j; ++jj) dup |= (topk_idx[base + t * k + jj] == e);
+      for (int jj = 0; jj < j; ++jj) dup |= (s_idx[t * k + jj] == e);
       if (e < 0 || e >= E || dup) e = -1;
     }
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
@@ -574,7 +644,8 @@ cudaError_t launch_scatter(const int32_t* topk_idx, int T, int E, int k,
                            int32_t* permuted_token, cudaStream_t s) {
   const int nchunks = ceil_div(T, kChunkTokens);
   if (nchunks == 0) return cudaSuccess;
-  return launch_kernel(scatter_kernel, dim3(nchunks), dim3(32), sizeof(int32_t) * E, s, 1,
+  return launch_kernel(scatter_kernel, dim3(nchunks), dim3(32),
+                       sizeof(int32_t) * (E + static_cast<size_t>(kChunkTokens) * k), s, 1,
                        topk_idx, T, E, k, chunk_base, row_id_map, permuted_token);
 }
 
