@@ -274,7 +274,7 @@ class ClockSampler:
                 self.thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, power = [], None, set(), []
         names = ["sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -285,13 +285,20 @@ class ClockSampler:
                 mx = float(parts[1])
             except ValueError:
                 continue
+            try:
+                power.append(float(parts[2]))
+            except ValueError:
+                pass
             for name, val in zip(names, parts[3:7]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+               "samples": len(sm)}
+        if power:
+            out["power_w"] = round(statistics.median(power), 1)
+        return out
 
 
 # ------------------------------------------------------------------ CPU oracle

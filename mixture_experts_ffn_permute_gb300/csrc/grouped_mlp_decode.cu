@@ -47,13 +47,14 @@
 //
 // Warp roles (224 threads, one CTA per SM):
 //   warp 0      tile claims (a 4-deep tile queue in shared memory) and the
-//               weight TMA loads (5-stage ring of 32 KB, two 64-deep K steps
-//               per stage: one 4-D copy of the tile's two 64-row blocks, each
-//               row a 256-byte segment, so the SM's copy path -- which counts
-//               row requests -- streams twice the bytes of 64-column boxes)
-//   warp 1      TMEM allocation + single-thread tcgen05.mma issue
+//               weight TMA loads: one 4-D copy per stage of the tile's two
+//               64-row blocks for both K steps (32 KB), each row a 256-byte
+//               segment, so the SM's copy path -- which counts row requests --
+//               streams twice the bytes of 64-column boxes
+//   warp 1      TMEM allocation + single-thread tcgen05.mma issue, one commit
+//               per stage
 //   warps 2..5  epilogue (tcgen05.ld -> SwiGLU / bf16 -> global stores)
-//   warp 6      token-row TMA loads (6-stage ring of 4 KB): GEMM1 gathers its
+//   warp 6      token-row TMA loads (8 KB per stage): GEMM1 gathers its
 //               rows straight from x by permuted_token (tile::gather4, four
 //               rows per copy, only as many copies as the tile has rows), so
 //               no permuted copy of x is made; GEMM2 loads 32-row boxes of h
@@ -80,13 +81,16 @@ namespace {
 constexpr int kM = 128;              // weight rows per tile
 constexpr int kN = 32;               // token rows per tile (max)
 constexpr int kThreadsD = 224;
-constexpr int kWStagesD = 5;         // x 2 K steps
-constexpr int kXStagesD = 6;
+// One ring of stages of two 64-deep K steps: weights and token rows land on
+// their own full barriers and the MMA releases both with one commit (a
+// tcgen05.commit costs about as much as the four MMAs of a small-N K step).
+constexpr int kStagesD = 4;
 constexpr int kQueue = 4;
 constexpr int kClaimLead = 2;        // stages before a tile's last load that the next is claimed
 constexpr uint32_t kWBytesD = 2 * kM * kBK * 2;   // 32 KB: two K steps
-constexpr uint32_t kXBytesD = kN * kBK * 2;   // 4 KB
-constexpr uint32_t kRingBytesD = kWStagesD * kWBytesD + kXStagesD * kXBytesD;
+constexpr uint32_t kXPlaneD = kN * kBK * 2;       // 4 KB: one K step of token rows
+constexpr uint32_t kXBytesD = 2 * kXPlaneD;        // 8 KB: two K steps
+constexpr uint32_t kRingBytesD = kStagesD * (kWBytesD + kXBytesD);
 constexpr uint32_t kTmemColsD = 2 * kN;
 constexpr int kMaxED = 1024;
 constexpr int kDPitchD = 33;
@@ -95,7 +99,7 @@ constexpr uint32_t kQueueConsumers = 6;
 // mbarriers: full/empty per ring stage, 2 + 2 accumulator, drain, queue
 // full/empty; then the queue slots, the TMEM address word and the abort flag
 constexpr uint32_t kBarBytesD = 512;
-static_assert((2 * (kWStagesD + kXStagesD) + 5 + 2 * kQueue) * 8 + (kQueue + 2) * 4 <=
+static_assert((3 * kStagesD + 5 + 2 * kQueue) * 8 + (kQueue + 2) * 4 <=
                   kBarBytesD,
               "barrier area");
 constexpr size_t kSmemD = 1024 + kRingBytesD + kBarBytesD +
@@ -190,12 +194,11 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sW = smem;
-  uint8_t* sX = smem + kWStagesD * kWBytesD;
+  uint8_t* sX = smem + kStagesD * kWBytesD;
   uint64_t* w_full = reinterpret_cast<uint64_t*>(smem + kRingBytesD);
-  uint64_t* w_empty = w_full + kWStagesD;
-  uint64_t* x_full = w_empty + kWStagesD;
-  uint64_t* x_empty = x_full + kXStagesD;
-  uint64_t* tfull = x_empty + kXStagesD;
+  uint64_t* x_full = w_full + kStagesD;
+  uint64_t* empty = x_full + kStagesD;  // stage consumed: weights and token rows
+  uint64_t* tfull = empty + kStagesD;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* q_full = drain + 1;
@@ -211,13 +214,12 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kWStagesD; ++s) {
+    for (int s = 0; s < kStagesD; ++s) {
       mbar_init(&w_full[s], 1);
-      mbar_init(&w_empty[s], 1);
+      mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kXStagesD; ++s) {
+    for (int s = 0; s < kStagesD; ++s) {
       mbar_init(&x_full[s], 1);
-      mbar_init(&x_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -352,24 +354,24 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
         }
         (void)w_row1;  // the map's second block is its fixed gap further
         const int num_ks = num_kb / 2;  // stages of two K steps
-        const int claim_at = max(num_ks - kClaimLead, kWStagesD);
+        const int claim_at = max(num_ks - kClaimLead, kStagesD);
         bool ok = true;
         for (int ks = 0; ks < num_ks; ++ks) {
-          if (!mbar_wait(&w_empty[sw], pw ^ 1, p.status)) { ok = false; break; }
+          if (!mbar_wait(&empty[sw], pw ^ 1, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&w_full[sw], kWBytesD);
           tma_load_4d(sW + sw * kWBytesD, mw, 0, w_row0, 0, 2 * ks, &w_full[sw], pol_w);
           ++issued;
-          if (++sw == kWStagesD) { sw = 0; pw ^= 1; }
+          if (++sw == kStagesD) { sw = 0; pw ^= 1; }
           if (ks == claim_at) claimed = atomicAdd(next_tile, 1);
         }
         if (ok && claim_at >= num_ks) claimed = atomicAdd(next_tile, 1);
         if (!ok) { *abort_flag = 1; break; }
       }
       // no bulk copy may still be writing this CTA's shared memory at exit
-      for (int i = 1; i <= kWStagesD && i <= issued; ++i) {
+      for (int i = 1; i <= kStagesD && i <= issued; ++i) {
         int s = sw - i;
         uint32_t ph = pw;
-        if (s < 0) { s += kWStagesD; ph ^= 1; }
+        if (s < 0) { s += kStagesD; ph ^= 1; }
         mbar_wait(&w_full[s], ph, p.status);
       }
     }
@@ -421,38 +423,41 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
         const int num_kb = (t.gemm ? p.F : p.H) / kBK;
         // rows of the stage past those loaded keep older data: they only
         // feed accumulator columns that are never stored
-        const uint32_t bytes = t.gemm ? kXBytesD : static_cast<uint32_t>(ng) * 512u;
+        const uint32_t bytes = 2 * (t.gemm ? kXPlaneD : static_cast<uint32_t>(ng) * 512u);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&x_empty[sx], px ^ 1, p.status)) { ok = false; break; }
+        for (int kb = 0; kb < num_kb; kb += 2) {  // stages of two K steps
+          if (!mbar_wait(&empty[sx], px ^ 1, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&x_full[sx], bytes);
-          uint8_t* dst = sX + sx * kXBytesD;
-          if (t.gemm) {
-            tma_load_2d(dst, &map_h, kb * kBK, x_row, &x_full[sx], pol_x);
-          } else {
 #pragma unroll
-            for (int g = 0; g < kN / 4; ++g)
-              if (g < ng)
-                tma_gather4(dst + g * 512, &map_x, kb * kBK, tk[4 * g], tk[4 * g + 1],
-                            tk[4 * g + 2], tk[4 * g + 3], &x_full[sx], pol_x);
+          for (int pl = 0; pl < 2; ++pl) {
+            uint8_t* dst = sX + sx * kXBytesD + pl * kXPlaneD;
+            if (t.gemm) {
+              tma_load_2d(dst, &map_h, (kb + pl) * kBK, x_row, &x_full[sx], pol_x);
+            } else {
+#pragma unroll
+              for (int g = 0; g < kN / 4; ++g)
+                if (g < ng)
+                  tma_gather4(dst + g * 512, &map_x, (kb + pl) * kBK, tk[4 * g], tk[4 * g + 1],
+                              tk[4 * g + 2], tk[4 * g + 3], &x_full[sx], pol_x);
+            }
           }
           ++issued;
-          if (++sx == kXStagesD) { sx = 0; px ^= 1; }
+          if (++sx == kStagesD) { sx = 0; px ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
       }
-      for (int i = 1; i <= kXStagesD && i <= issued; ++i) {
+      for (int i = 1; i <= kStagesD && i <= issued; ++i) {
         int s = sx - i;
         uint32_t ph = px;
-        if (s < 0) { s += kXStagesD; ph ^= 1; }
+        if (s < 0) { s += kStagesD; ph ^= 1; }
         mbar_wait(&x_full[s], ph, p.status);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int qs = 0, sw = 0, sx = 0;
-      uint32_t qp = 0, pw = 0, px = 0;
+      int qs = 0, sw = 0;
+      uint32_t qp = 0, pw = 0;
       int local = 0;
       while (true) {
         if (!mbar_wait(&q_full[qs], qp, p.status)) { *abort_flag = 1; break; }
@@ -471,26 +476,23 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kN;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          const int plane = kb & 1;  // K step inside the weight stage
-          if ((plane == 0 && !mbar_wait(&w_full[sw], pw, p.status)) ||
-              !mbar_wait(&x_full[sx], px, p.status)) {
+        for (int kb = 0; kb < num_kb; kb += 2) {  // stages of two K steps
+          if (!mbar_wait(&w_full[sw], pw, p.status) || !mbar_wait(&x_full[sw], pw, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t w_desc =
-              sw128_kmajor_desc(smem_u32(sW + sw * kWBytesD + plane * (kWBytesD / 2)));
-          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + sx * kXBytesD));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
-          if (plane == 1) {
-            mma_commit(&w_empty[sw]);
-            if (++sw == kWStagesD) { sw = 0; pw ^= 1; }
+          for (int pl = 0; pl < 2; ++pl) {
+            const uint64_t w_desc =
+                sw128_kmajor_desc(smem_u32(sW + sw * kWBytesD + pl * (kWBytesD / 2)));
+            const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + sw * kXBytesD + pl * kXPlaneD));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | pl | kk) != 0);
           }
-          mma_commit(&x_empty[sx]);
-          if (++sx == kXStagesD) { sx = 0; px ^= 1; }
+          mma_commit(&empty[sw]);  // releases the stage's weights and token rows
+          if (++sw == kStagesD) { sw = 0; pw ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
         mma_commit(&tfull[buf]);
