@@ -6,9 +6,14 @@
 // with N = the expert's remaining rows rounded up to 16, set per tile in the
 // instruction descriptor.  At decode sizes an expert sees a handful of
 // tokens: a K step moves 16 KB of weights and 4 KB of activations, so the
-// weights stream once at HBM speed (10 weight stages, 6 token stages).
-// Tokens are loaded in one 32-row box.  The tile count is (expert, weight-row tile, token tile), token tiles fastest so
-// that CTAs sharing a weight tile run together and the second read hits L2.
+// weights stream once at HBM speed.  One ring of four stages of two 64-deep
+// K steps holds both: one 4-D copy brings the tile's weight rows for both K
+// steps (each row a 256-byte segment: the copy path counts row requests) and
+// one 3-D copy its 32 token rows; the MMA issuer releases a stage with one
+// commit (at this N a tcgen05.commit costs about as much as a K step's four
+// MMAs).  The tile count is (expert, weight-row tile, token tile), token
+// tiles fastest so that CTAs sharing a weight tile run together and the
+// second read hits L2.
 //
 // Epilogues:
 //   GEMM1 (kSwiGLU): the 128 weight rows are 64 gate rows and the matching
@@ -31,32 +36,32 @@
 
 namespace moe {
 
-bool make_map_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                 uint32_t box_rows);  // grouped_gemm.cu
+bool make_map_kplanes(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                      uint32_t box_rows);  // grouped_gemm.cu
+bool make_map_kplanes_pair(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint64_t gap);  // grouped_gemm.cu
 
 namespace {
 
 constexpr int kM = 128;                                // weight rows per tile
 constexpr int kXBox = 32;                              // token rows per TMA box
 constexpr int kThreadsS = 192;
-constexpr uint32_t kWBytes = kM * kBK * 2;             // 16 KB
+constexpr uint32_t kWBytes = 2 * kM * kBK * 2;         // 32 KB: two K steps
 constexpr int kMaxES = 1024;
 constexpr int kDPitch = 33;                            // padded fp32 row of the exchange chunk
 constexpr int kNmaxS = 32;                             // token rows per tile
-constexpr int kWStagesS = 10;                          // weight-ring depth (HBM)
-constexpr int kXStagesS = 6;                           // token-ring depth (L2)
+constexpr int kStagesS = 4;                            // x 2 K steps
 
-// Separate rings for the weight tiles (from HBM: deep) and the token tiles
-// (from L2).
-template <int kNmax, int kWStages, int kXStages>
+template <int kNmax, int kStages>
 struct SwapCfg {
-  static constexpr uint32_t kXBytes = kNmax * kBK * 2;
-  static constexpr uint32_t kRingBytes = kWStages * kWBytes + kXStages * kXBytes;
+  static constexpr uint32_t kXPlane = kNmax * kBK * 2;  // one K step of token rows
+  static constexpr uint32_t kXBytes = 2 * kXPlane;
+  static constexpr uint32_t kRingBytes = kStages * (kWBytes + kXBytes);
   static constexpr uint32_t kTmemCols = 2 * kNmax;     // two accumulators
-  // mbarriers (full/empty per stage of both rings, 2 + 2 accumulator, drain)
-  // plus the TMEM address word and the abort flag
+  // mbarriers (full/empty per stage, 2 + 2 accumulator, drain) plus the TMEM
+  // address word and the abort flag
   static constexpr uint32_t kBarBytes = 512;
-  static_assert((2 * (kWStages + kXStages) + 5) * 8 + 8 <= kBarBytes, "barrier area");
+  static_assert((2 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
   static constexpr size_t kSmem = 1024 + kRingBytes + kBarBytes +
                                   3 * (kMaxES + 1) * sizeof(int32_t) +
                                   kM * kDPitch * sizeof(float);
@@ -94,22 +99,20 @@ __device__ __forceinline__ STile decode_stile(int tile, const int32_t* tp, const
 
 __device__ __forceinline__ float silu_s(float z) { return z / (1.0f + expf(-z)); }
 
-template <Epi kEpi, int kNmax, int kWStages, int kXStages>
+template <Epi kEpi, int kNmax, int kStages>
 __global__ void __launch_bounds__(kThreadsS, 1)
 grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
                          const __grid_constant__ CUtensorMap map_x, const SParams p) {
-  using Cfg = SwapCfg<kNmax, kWStages, kXStages>;
+  using Cfg = SwapCfg<kNmax, kStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, kept as a shared-array pointer so that accesses
   // compile to shared-memory instructions
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sW = smem;
-  uint8_t* sX = smem + kWStages * kWBytes;
-  uint64_t* w_full = reinterpret_cast<uint64_t*>(smem + Cfg::kRingBytes);
-  uint64_t* w_empty = w_full + kWStages;
-  uint64_t* x_full = w_empty + kWStages;
-  uint64_t* x_empty = x_full + kXStages;
-  uint64_t* tfull = x_empty + kXStages;
+  uint8_t* sX = smem + kStages * kWBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kRingBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -121,13 +124,9 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kWStages; ++s) {
-      mbar_init(&w_full[s], 1);
-      mbar_init(&w_empty[s], 1);
-    }
-    for (int s = 0; s < kXStages; ++s) {
-      mbar_init(&x_full[s], 1);
-      mbar_init(&x_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -187,23 +186,22 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = s_tp[p.E];
-  const int num_kb = p.K / kBK;
+  const int num_kb = p.K / kBK;  // even: stages hold two K steps
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_normal();
       const uint64_t pol_x = policy_evict_last();
-      int sw = 0, sx = 0;
-      uint32_t pw = 0, px = 0;
+      int st = 0;
+      uint32_t ph = 0;
       long issued = 0;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
         const STile t = decode_stile(tile, s_tp, s_ntk, p.E, p.w_tiles);
         const int tok0 = t.n * kNmax;
         const int nval = min(kNmax, s_off[t.e + 1] - s_off[t.e] - tok0);
-        // few TMA ops per stage: 32-row boxes, as many as the tile needs
-        const int nbox = (nval + kXBox - 1) / kXBox;
-        const uint32_t x_bytes = static_cast<uint32_t>(nbox * kXBox * kBK * 2);
+        static_assert(kNmax == kXBox, "one token box per tile");
+        (void)nval;
         const int x_row = s_off[t.e] + tok0;
         int w_row0, w_row1;
         if (kEpi == Epi::kSwiGLU) {
@@ -223,43 +221,28 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
           w_row1 = w_row0 + kM / 2;
         }
         w_row0 += t.e * p.w_rows_per_expert;
-        w_row1 += t.e * p.w_rows_per_expert;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          const int kx = kb * kBK;
-          if (!mbar_wait(&w_empty[sw], pw ^ 1, p.status)) { *abort_flag = 1; break; }
-          mbar_arrive_expect_tx(&w_full[sw], kWBytes);
-          uint8_t* w_dst = sW + sw * kWBytes;
-          tma_load_2d(w_dst, &map_w, kx, w_row0, &w_full[sw], pol_w);
-          tma_load_2d(w_dst + kWBytes / 2, &map_w, kx, w_row1, &w_full[sw], pol_w);
-          if (!mbar_wait(&x_empty[sx], px ^ 1, p.status)) { *abort_flag = 1; break; }
-          mbar_arrive_expect_tx(&x_full[sx], x_bytes);
-          uint8_t* x_dst = sX + sx * Cfg::kXBytes;
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d(x_dst + b * kXBox * kBK * 2, &map_x, kx, x_row + b * kXBox,
-                        &x_full[sx], pol_x);
+        (void)w_row1;  // the weight map's second block is its fixed gap further
+        for (int kb = 0; kb < num_kb; kb += 2) {
+          if (!mbar_wait(&empty[st], ph ^ 1, p.status)) { *abort_flag = 1; break; }
+          mbar_arrive_expect_tx(&full[st], kWBytes + Cfg::kXBytes);
+          tma_load_4d(sW + st * kWBytes, &map_w, 0, w_row0, 0, kb, &full[st], pol_w);
+          tma_load_3d(sX + st * Cfg::kXBytes, &map_x, 0, x_row, kb, &full[st], pol_x);
           ++issued;
-          if (++sw == kWStages) { sw = 0; pw ^= 1; }
-          if (++sx == kXStages) { sx = 0; px ^= 1; }
+          if (++st == kStages) { st = 0; ph ^= 1; }
         }
       }
-      for (int i = 1; i <= kWStages && i <= issued; ++i) {
-        int s = sw - i;
-        uint32_t ph = pw;
-        if (s < 0) { s += kWStages; ph ^= 1; }
-        mbar_wait(&w_full[s], ph, p.status);
-      }
-      for (int i = 1; i <= kXStages && i <= issued; ++i) {
-        int s = sx - i;
-        uint32_t ph = px;
-        if (s < 0) { s += kXStages; ph ^= 1; }
-        mbar_wait(&x_full[s], ph, p.status);
+      for (int i = 1; i <= kStages && i <= issued; ++i) {
+        int s = st - i;
+        uint32_t q = ph;
+        if (s < 0) { s += kStages; q ^= 1; }
+        mbar_wait(&full[s], q, p.status);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int sw = 0, sx = 0;
-      uint32_t pw = 0, px = 0;
+      int st = 0;
+      uint32_t ph = 0;
       int local = 0;
       for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x, ++local) {
         const int buf = local & 1;
@@ -272,21 +255,21 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kNmax;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&w_full[sw], pw, p.status) || !mbar_wait(&x_full[sx], px, p.status)) {
-            ok = false;
-            break;
-          }
+        for (int kb = 0; kb < num_kb; kb += 2) {
+          if (!mbar_wait(&full[st], ph, p.status)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t w_desc = sw128_kmajor_desc(smem_u32(sW + sw * kWBytes));
-          const uint64_t x_desc = sw128_kmajor_desc(smem_u32(sX + sx * Cfg::kXBytes));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | kk) != 0);
-          mma_commit(&w_empty[sw]);
-          mma_commit(&x_empty[sx]);
-          if (++sw == kWStages) { sw = 0; pw ^= 1; }
-          if (++sx == kXStages) { sx = 0; px ^= 1; }
+          for (int pl = 0; pl < 2; ++pl) {
+            const uint64_t w_desc =
+                sw128_kmajor_desc(smem_u32(sW + st * kWBytes + pl * (kWBytes / 2)));
+            const uint64_t x_desc =
+                sw128_kmajor_desc(smem_u32(sX + st * Cfg::kXBytes + pl * Cfg::kXPlane));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_ss(d_tmem, w_desc + 2 * kk, x_desc + 2 * kk, idesc, (kb | pl | kk) != 0);
+          }
+          mma_commit(&empty[st]);  // one commit releases the stage
+          if (++st == kStages) { st = 0; ph ^= 1; }
         }
         if (!ok) { *abort_flag = 1; break; }
         mma_commit(&tfull[buf]);
@@ -380,11 +363,11 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap map_w,
   }
 }
 
-template <Epi kEpi, int kNmax, int kWStages, int kXStages>
+template <Epi kEpi, int kNmax, int kStages>
 cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx, const SParams& sp,
                              int grid, cudaStream_t s) {
-  using Cfg = SwapCfg<kNmax, kWStages, kXStages>;
-  auto kern = grouped_gemm_swap_kernel<kEpi, kNmax, kWStages, kXStages>;
+  using Cfg = SwapCfg<kNmax, kStages>;
+  auto kern = grouped_gemm_swap_kernel<kEpi, kNmax, kStages>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::kSmem));
   if (err != cudaSuccess) return err;
@@ -396,13 +379,18 @@ cudaError_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mx, const
 
 cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s) {
   if (g.a_rows == 0) return cudaSuccess;
-  if (g.E > kMaxES) return cudaErrorInvalidValue;
+  if (g.E > kMaxES || g.K % (2 * kBK) != 0) return cudaErrorInvalidValue;
+  // rows between a tile's two 64-row weight blocks (the producer's w_row1 - w_row0)
+  uint64_t gap = kM / 2;
+  if (g.epi == Epi::kSwiGLU && g.interleave == 0) gap = static_cast<uint64_t>(g.F);
+  else if (g.epi == Epi::kSwiGLU && g.interleave != 32) gap = static_cast<uint64_t>(g.interleave);
   CUtensorMap mw, mx;
-  // weights: 64-row boxes; tokens: 32-row boxes
-  if (!make_map_2d(&mw, g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
-                   static_cast<uint64_t>(g.K), kM / 2))
+  // weights: two 64-row blocks x two planes; tokens: 32-row boxes x two planes
+  if (!make_map_kplanes_pair(&mw, g.b, static_cast<uint64_t>(g.E) * g.b_rows_per_expert,
+                             static_cast<uint64_t>(g.K), gap))
     return cudaErrorInvalidValue;
-  if (!make_map_2d(&mx, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K), kXBox))
+  if (!make_map_kplanes(&mx, g.a, static_cast<uint64_t>(g.a_rows), static_cast<uint64_t>(g.K),
+                        kXBox))
     return cudaErrorInvalidValue;
   SParams sp;
   sp.expert_offsets = g.expert_offsets;
@@ -422,9 +410,9 @@ cudaError_t launch_grouped_gemm_swap(const GroupedGemmArgs& g, cudaStream_t s) {
       (static_cast<long>(ceil_div(g.a_rows, kNmaxS)) + std::min(g.E, g.a_rows)) * sp.w_tiles;
   const int grid = static_cast<int>(std::max(1L, std::min<long>(num_sms(), max_tiles)));
   if (g.epi == Epi::kSwiGLU)
-    return launch_swap_impl<Epi::kSwiGLU, kNmaxS, kWStagesS, kXStagesS>(mw, mx, sp, grid, s);
+    return launch_swap_impl<Epi::kSwiGLU, kNmaxS, kStagesS>(mw, mx, sp, grid, s);
   if (g.epi == Epi::kPlain)
-    return launch_swap_impl<Epi::kPlain, kNmaxS, kWStagesS, kXStagesS>(mw, mx, sp, grid, s);
+    return launch_swap_impl<Epi::kPlain, kNmaxS, kStagesS>(mw, mx, sp, grid, s);
   return cudaErrorInvalidValue;
 }
 
