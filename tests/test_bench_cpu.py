@@ -51,6 +51,7 @@ def test_traffic_table_is_used_only_for_the_captured_source():
     csrc = os.path.join(bench.ROOT, "mixture_experts_ffn_permute_gb300", "csrc")
     files = {"grouped_mlp_decode_kernel": "grouped_mlp_decode.cu",
              "grouped_gemm_swap2_kernel": "grouped_gemm_swap2.cu",
+             "grouped_gemm_swap_kernel": "grouped_gemm_swap.cu",
              "grouped_gemm_fp4_kernel": "grouped_gemm_fp4.cu",
              "grouped_gemm_bwd_kernel": "grouped_gemm_bwd.cu"}
     for sha, workload, kernel, rd, wr in rows:
