@@ -370,22 +370,27 @@ scatter_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row
                     const int32_t* __restrict__ expert_offsets, int T, int k, int E, int R,
                     int vecs_per_row, uint4* __restrict__ x_perm) {
   pdl_enter();
-  __shared__ int32_t s_rows[MOE_MAX_TOPK];
+  constexpr int kVecs = 4;  // 16-byte vectors per thread loaded before any store
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
-    if (threadIdx.x < k) {
-      const int32_t r = row_id_map[static_cast<size_t>(t) * k + threadIdx.x];
-      s_rows[threadIdx.x] = (r >= 0 && r < R) ? r : -1;
-    }
-    __syncthreads();
     const uint4* src = x + static_cast<size_t>(t) * vecs_per_row;
-    for (int v = threadIdx.x; v < vecs_per_row; v += blockDim.x) {
-      const uint4 val = __ldcs(src + v);  // read once: streaming
-      for (int j = 0; j < k; ++j) {
-        const int32_t r = s_rows[j];
-        if (r >= 0) x_perm[static_cast<size_t>(r) * vecs_per_row + v] = val;
+    for (int v0 = 0; v0 < vecs_per_row; v0 += kVecs * blockDim.x) {
+      uint4 val[kVecs];
+#pragma unroll
+      for (int i = 0; i < kVecs; ++i) {
+        const int v = v0 + i * blockDim.x + threadIdx.x;
+        if (v < vecs_per_row) val[i] = __ldcs(src + v);  // read once: streaming
+      }
+      for (int j = 0; j < k; ++j) {  // the token's rows (the same words for every thread)
+        const int32_t r = __ldg(row_id_map + static_cast<size_t>(t) * k + j);
+        if (r < 0 || r >= R) continue;
+        uint4* dst = x_perm + static_cast<size_t>(r) * vecs_per_row;
+#pragma unroll
+        for (int i = 0; i < kVecs; ++i) {
+          const int v = v0 + i * blockDim.x + threadIdx.x;
+          if (v < vecs_per_row) dst[v] = val[i];
+        }
       }
     }
-    __syncthreads();
   }
   const int first = min(max(expert_offsets[E], 0), R);
   const size_t n = static_cast<size_t>(R - first) * vecs_per_row;
@@ -468,14 +473,30 @@ combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ row_id_m
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const int row = __ldg(row_id_map + static_cast<size_t>(t) * k + j);
-    if (row < 0) continue;
-    const float w = topk_w ? __ldg(topk_w + static_cast<size_t>(t) * k + j) : 1.f;
-    float f[8];
-    bf16x8_to_f32(__ldg(y + static_cast<size_t>(row) * vecs_per_row + v), f);
+  // up to eight routes at a time: their rows, weights and y vectors are
+  // loaded independently, then summed in slot order
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    int row[8];
+    float w[8];
+    uint4 yv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+    for (int i = 0; i < 8; ++i) {
+      const int j = j0 + i;
+      row[i] = j < k ? __ldg(row_id_map + static_cast<size_t>(t) * k + j) : -1;
+      w[i] = (j < k && topk_w) ? __ldg(topk_w + static_cast<size_t>(t) * k + j) : 1.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      yv[i] = row[i] >= 0 ? __ldcs(y + static_cast<size_t>(row[i]) * vecs_per_row + v)
+                          : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (row[i] < 0) continue;
+      float f[8];
+      bf16x8_to_f32(yv[i], f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(w[i], f[q], acc[q]);
+    }
   }
   uint4 o;
   __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
