@@ -295,7 +295,19 @@ scatter_kernel(const int32_t* __restrict__ topk_idx, int T, int E, int k,
   const int nt = min(kChunkTokens, T - t0);
   const int nr = nt * k;
   const size_t base = static_cast<size_t>(t0) * k;
-  for (int e = lane; e < E; e += 32) s_next[e] = chunk_base[static_cast<size_t>(chunk) * E + e];
+  for (int e0 = 0; e0 < E; e0 += 8 * 32) {  // eight independent loads per lane at a time
+    int v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + lane + 32 * i;
+      v[i] = e < E ? chunk_base[static_cast<size_t>(chunk) * E + e] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = e0 + lane + 32 * i;
+      if (e < E) s_next[e] = v[i];
+    }
+  }
   for (int r0 = 0; r0 < nr; r0 += 8 * 32) {  // eight independent loads per lane at a time
     int v[8];
 #pragma unroll
