@@ -50,6 +50,9 @@ SMALL = [
     mi.TINY,
     mi.MoEShape("ragged", T=333, H=512, F=384, E=7, k=3),
     mi.MoEShape("il32clamp", T=128, H=256, F=256, E=8, k=2, glu_interleave=32, swiglu_clamp=7.0),
+    # gate/up blocks 64 and 128 rows apart (the weight loads' block gap)
+    mi.MoEShape("il64", T=200, H=256, F=256, E=6, k=2, glu_interleave=64, swiglu_clamp=3.0),
+    mi.MoEShape("il128", T=150, H=512, F=256, E=5, k=3, glu_interleave=128),
     mi.MoEShape("skew-small", T=512, H=256, F=256, E=64, k=8, zipf_s=1.1),
     mi.MoEShape("t1", T=1, H=256, F=128, E=8, k=2),
 ]
