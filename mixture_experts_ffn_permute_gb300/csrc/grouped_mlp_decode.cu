@@ -39,12 +39,6 @@
 // The counters (next tile, GEMM1 tiles finished, done[E], arrivals[T][H/128])
 // are zeroed by the routing/permutation kernel of the same call.
 //
-// When the W2 matrices of the experts with tokens fit in a quarter of L2
-// (the smallest decode steps, where fewer weight tiles than SMs stream at
-// once and HBM has bandwidth to spare), the otherwise idle lanes of warp 0
-// prefetch them into L2 at the start, so GEMM2 tiles claimed after the GEMM1
-// tiles read their weights from L2.
-//
 // Warp roles (224 threads, one CTA per SM):
 //   warp 0      tile claims (a 4-deep tile queue in shared memory) and the
 //               weight TMA loads: one 4-D copy per stage of the tile's two
@@ -116,7 +110,6 @@ struct DParams {
   const int32_t* row_id_map;      // [T, k]
   const float* topk_w;            // [T, k]
   int32_t* ctr;                   // [2 + E + T * (H / 128)], zero at launch
-  const uint8_t* w2;              // bf16 [E, H, F] (L2 prefetch)
   int E, H, F, k, R, T, interleave, w1t, w2t;
   float clamp;
   uint32_t* status;
@@ -169,16 +162,6 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
   return old;
 }
 
-// Bulk prefetch of [ptr, ptr + bytes) into L2 (a hint: no data moves to the SM).
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes, uint64_t policy) {
-  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(ptr),
-               "r"(bytes), "l"(policy)
-               : "memory");
-}
-
-// W2 bytes of the experts with tokens up to which warp 0 prefetches them.
-constexpr long kW2PrefetchMax = 32l << 20;
-constexpr uint32_t kPrefetchPiece = 64u << 10;
 
 // Orders this thread's generic-proxy global accesses with its later (or the
 // earlier ones with others') bulk-tensor accesses.
@@ -288,28 +271,6 @@ grouped_mlp_decode_kernel(const __grid_constant__ CUtensorMap map_w1,
 
   if (warp == 0) {
     // ------------------------------------------------- tile claims + weights
-    const long w2_bytes = static_cast<long>(p.H) * p.F * 2;
-    if (lane > 0 && static_cast<long>(s_ntp[p.E]) * w2_bytes <= kW2PrefetchMax) {
-      // pieces of W2 per token tile (an expert with several token tiles is
-      // prefetched again: harmless); lanes 1..31 of every CTA share them
-      const uint64_t pol = policy_evict_last();
-      const long ppe = (w2_bytes + kPrefetchPiece - 1) / kPrefetchPiece;
-      const long n = static_cast<long>(s_ntp[p.E]) * ppe;
-      for (long g = static_cast<long>(blockIdx.x) * 31 + (lane - 1); g < n;
-           g += static_cast<long>(gridDim.x) * 31) {
-        const int j = static_cast<int>(g / ppe);  // token tile
-        const long q = g - static_cast<long>(j) * ppe;
-        int lo = 0, hi = p.E - 1;  // its expert: largest e with ntp[e] <= j
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (s_ntp[mid] <= j) lo = mid; else hi = mid - 1;
-        }
-        const long off = q * kPrefetchPiece;
-        const long len = min(static_cast<long>(kPrefetchPiece), w2_bytes - off);
-        prefetch_l2(p.w2 + static_cast<long>(lo) * w2_bytes + off, static_cast<uint32_t>(len),
-                    pol);
-      }
-    }
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_normal();
       int qs = 0, sw = 0;
@@ -673,7 +634,6 @@ cudaError_t launch_grouped_mlp_decode(const DecodeMlpArgs& g, cudaStream_t s) {
   p.row_id_map = g.row_id_map;
   p.topk_w = g.topk_w;
   p.ctr = g.counters;
-  p.w2 = static_cast<const uint8_t*>(g.w2);
   p.E = g.E;
   p.H = g.H;
   p.F = g.F;
