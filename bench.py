@@ -237,7 +237,7 @@ class ClockSampler:
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown")
+              "clocks_event_reasons.sw_thermal_slowdown,power.limit")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -274,7 +274,7 @@ class ClockSampler:
                 self.thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons, power = [], None, set(), []
+        sm, mx, reasons, power, limit = [], None, set(), [], None
         names = ["sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -292,12 +292,19 @@ class ClockSampler:
             for name, val in zip(names, parts[3:7]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+            if len(parts) > 7:
+                try:
+                    limit = float(parts[7])
+                except ValueError:
+                    pass
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
         out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                "samples": len(sm)}
         if power:
             out["power_w"] = round(statistics.median(power), 1)
+        if limit is not None:
+            out["power_limit_w"] = limit  # the board's enforced limit (sw_power_cap's bound)
         return out
 
 

@@ -99,3 +99,16 @@ def test_fp8_layer_takes_the_fp8_tensor_peak():
     peaks = {"hbm_gbs": 6775.6, "bf16_tflops": 1916.9, "bf16_tflops_sustained": 1719.2}
     v, key, other = bench.tensor_peak(peaks, 1.0, fp8=True)
     assert v == 2 * 1916.9 and bench.peak_of(peaks, other) == 2 * 1719.2
+
+
+def test_clock_summary_parses_nvidia_smi_lines():
+    c = bench.ClockSampler(0)
+    c.lines = ["1695, 2070, 702.3, Active, Not Active, Not Active, Not Active, 720.00",
+               "1710, 2070, 698.1, Not Active, Not Active, Not Active, Not Active, 720.00",
+               "1680, 2070, [N/A], Active, Not Active, Not Active, Not Active, 720.00",
+               "garbage"]
+    s = c.summary()
+    assert s["sm_mhz"] == 1695.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+    assert s["power_w"] == 700.2 and s["power_limit_w"] == 720.0
+    assert bench.ClockSampler(0).summary()["samples"] == 0
